@@ -1,0 +1,426 @@
+"""Benchmark: forward tokens/s and fraction of the GB300 roofline for the
+chunkwise gated delta rule, gated DeltaNet at B=4, H=16, T=2048, d=128, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one dn_chunk_fwd call over the whole workload (all chunk steps of
+the path in one launch).  Inputs are resident in HBM before the timed region;
+L2 is flushed (a 256 MiB write) before every timed step, outside the events
+that time the step.  Each rank runs its own copy of the workload (independent
+sequences, no exchange between GPUs), so scaling is weak and `value` is the
+tokens all ranks processed per second of the slowest rank.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead (on a
+bounded sample of the same workload per step); under torchrun only rank 0
+runs it.  One JSON line is printed by rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "fwd tokens/s & % of roofline, gated delta rule H=16 d=128 T=2048 (1 GB300)"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = os.path.join(ROOT, "chunkwise_gated_delta_chunk_gb300", "csrc")
+
+
+# --------------------------------------------------------------------------
+# Algorithmic work of one forward (full C x C tiles; solve and elementwise
+# terms excluded), per token and per state.
+# --------------------------------------------------------------------------
+def algorithmic(inp: dict) -> dict:
+    B, T, Nk, dk = inp["q"].shape
+    Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
+    C = 64
+    tok = B * T
+    e = inp["q"].element_size()
+    has_g = inp["g"] is not None
+    has_h0 = inp["h0"] is not None
+    has_ht = True
+    N = inp["N"]
+    flops = tok * (Nv * (6 * dk * dv + 2 * C * (dk + 2 * dv)) + Nk * (4 * C * dk))
+    bytes_ = (tok * (2 * Nk * dk * e + 2 * Nv * dv * e + Nv * 4 * (1 + has_g))
+              + N * Nv * dk * dv * 4 * (has_h0 + has_ht))
+    return dict(flops=flops, bytes=bytes_, tokens=tok)
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm_gbs=float(pk["hbm_gbs"]), bf16_tflops=float(pk["bf16_tflops"]),
+                    bf16_tflops_sustained=float(pk.get("bf16_tflops_sustained",
+                                                       pk["bf16_tflops"]))), "measured"
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0), "fallback"
+
+
+def sources_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(KERNEL_SOURCES)):
+        with open(os.path.join(KERNEL_SOURCES, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("sources") != sources_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "20", "-i", self.gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in load),
+                    sm_max_mhz=max(r["smax"] for r in rows), reasons=sorted(reasons),
+                    samples=len(rows), samples_under_load=len(load),
+                    power_w_max=max(r["power"] for r in rows))
+
+
+def smi_gpu_id(dev, local: int) -> str:
+    """nvidia-smi id (UUID) of the CUDA device, matched by UUID."""
+    try:
+        want = str(torch.cuda.get_device_properties(dev).uuid).lower().replace("gpu-", "")
+        out = subprocess.run(["nvidia-smi", "--query-gpu=uuid", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout
+        for line in out.splitlines():
+            u = line.strip()
+            if u.lower().replace("gpu-", "") == want:
+                return u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis:
+        return vis.split(",")[local].strip()
+    return str(local)
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm).
+# --------------------------------------------------------------------------
+def oracle_time(inp: dict, units, threads: int = 0) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
+                     inp["cu_seqlens"], inp["scale"], units=units, threads=threads)
+    return time.perf_counter() - t0
+
+
+def oracle_sample(inp: dict, budget_s: float):
+    """Units of the workload whose oracle run takes about `budget_s` seconds
+    on all host cores.  Returns (units, tokens, seconds, cores)."""
+    import oracle
+    cores = oracle.default_threads()
+    Nv = inp["v"].shape[2]
+    n_units = inp["N"] * Nv
+    per_unit_tokens = workloads.tokens(inp) / max(inp["N"], 1)
+    # one unit on one core to size the sample
+    t1 = oracle_time(inp, [0], threads=1)
+    want = max(1, min(n_units, int(budget_s * cores / max(t1, 1e-6))))
+    # whole waves of `cores` units keep every core busy
+    if want >= cores:
+        want = (want // cores) * cores
+    units = list(range(want))
+    return units, int(per_unit_tokens * want / Nv), cores
+
+
+def reference_arm(args, inp, wl_name, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.default_threads()
+    steps, warm = args.steps, args.warmup
+    # size each step so that (warmup + steps) finishes in about two minutes
+    t1 = oracle_time(inp, [0], threads=1)
+    Nv = inp["v"].shape[2]
+    budget = 120.0 / max(steps + warm, 1)
+    n_units = max(1, min(inp["N"] * Nv, int(budget * cores / max(t1, 1e-6))))
+    units = list(range(n_units))
+    tok_step = workloads.tokens(inp) * n_units / (inp["N"] * Nv)
+    for _ in range(warm):
+        oracle_time(inp, units)
+    times = [oracle_time(inp, units) for _ in range(steps)]
+    sec = sum(times)
+    value = tok_step * steps / sec
+    sample = "%d of %d (sequence, v-head) units per step (%.0f token-heads of %d)" % (
+        n_units, inp["N"] * Nv, tok_step * Nv, workloads.tokens(inp) * Nv)
+    line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=steps, warmup=warm,
+                ms_per_step=1e3 * sec / steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
+                config=config_of(wl_name, inp, l2="n/a (CPU)"),
+                cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl_name, inp, l2):
+    B, T, Nk, dk = inp["q"].shape
+    Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
+    return dict(workload=wl_name, B=B, T=T, Nk=Nk, Nv=Nv, dk=dk, dv=dv, chunk=64,
+                global_batch=B, seq_len=T, gate=inp["g"] is not None,
+                h0=inp["h0"] is not None, l2=l2)
+
+
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+
+    wl_name = args.workload
+    inp = workloads.workload_inputs(wl_name)
+
+    if args.impl == "reference":
+        reference_arm(args, inp, wl_name, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    dn.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    d = workloads.to_device(inp, dev)
+    B, T, Nk, dk = d["q"].shape
+    Nv, dv = d["v"].shape[2], d["v"].shape[3]
+    N = inp["N"]
+    o = torch.empty(B, T, Nv, dv, dtype=d["q"].dtype, device=dev)
+    ht = torch.empty(N, Nv, dk, dv, dtype=torch.float32, device=dev)
+    dt = dn.dtype_code(d["q"].dtype)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(q=d["q"], k=d["k"], v=d["v"], beta=d["beta"], g=d["g"], h0=d["h0"],
+               cu=d["cu_seqlens"], o=o, ht=ht):
+        st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
+                             inp["scale"], 64, o, ht, stream)
+        if st != dn.DN_OK:
+            raise dn.DnError(st)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    st = dn.dn_check(stream)
+    if st != dn.DN_OK:
+        raise dn.DnError(st, "warm-up")
+    kernel = dn.dn_last_kernel()
+
+    # ---------------- device-timed region --------------------------------
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    gpu_id = smi_gpu_id(dev, local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_id) as clk:
+        w0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev0[i].record(stream)
+            launch()
+            ev1[i].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - w0
+    if dist is not None:
+        dist.barrier()
+    per = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms = sum(per) / K
+    st = dn.dn_check(stream)
+    if st != dn.DN_OK:
+        raise dn.DnError(st, "timed region")
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # ---------------- end to end through the public API -------------------
+    # per step: pinned host -> device copies of the inputs, the call, and the
+    # device -> host read of o and ht
+    host = {}
+    for key in ("q", "k", "v", "beta", "g", "h0", "cu_seqlens"):
+        if inp[key] is not None:
+            host[key] = inp[key].contiguous().pin_memory()
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    ht_host = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+    dbuf = {key: torch.empty_like(val, device=dev) for key, val in host.items()}
+    h2d = sum(val.numel() * val.element_size() for val in host.values())
+    d2h = o.numel() * o.element_size() + ht.numel() * ht.element_size()
+
+    def e2e_step():
+        for key, val in host.items():
+            dbuf[key].copy_(val, non_blocking=True)
+        launch(q=dbuf["q"], k=dbuf["k"], v=dbuf["v"], beta=dbuf["beta"], g=dbuf.get("g"),
+               h0=dbuf.get("h0"), cu=dbuf.get("cu_seqlens"))
+        o_host.copy_(o, non_blocking=True)
+        ht_host.copy_(ht, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    E = args.e2e_steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / E
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    # ---------------- roofline --------------------------------------------
+    alg = algorithmic(inp)
+    peaks, peak_src = load_peaks()
+    sec = ms / 1e3
+    achieved_gbs = alg["bytes"] / sec / 1e9
+    tflops = alg["flops"] / sec / 1e12
+    t_hbm = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        roof = dict(bound="hbm", achieved=achieved_gbs, peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=achieved_gbs / peaks["hbm_gbs"])
+    else:
+        roof = dict(bound="tensor", achieved=tflops, peak=peaks["bf16_tflops"],
+                    unit="TFLOP/s", frac=tflops / peaks["bf16_tflops"])
+    roof["traffic"] = measured_traffic(kernel, wl_name)
+    roof["peak_source"] = peak_src
+    roof["roofline_time_us"] = 1e6 * max(t_hbm, t_tc)
+    roof["algorithmic_bytes"] = alg["bytes"]
+    roof["algorithmic_flops"] = alg["flops"]
+    roof["tflops"] = tflops
+    roof["kernel"] = kernel
+
+    line = dict(metric=METRIC, value=alg["tokens"] * world / (ms_max / 1e3), unit=UNIT,
+                n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16"
+                if d["q"].dtype == torch.bfloat16 else "f32", data="synthetic",
+                config=config_of(wl_name, inp, l2="flushed before every timed step "
+                                 "(256 MiB write, outside the step's events)"),
+                parallelism="dp%d (independent sequences per GPU, no collective)" % world,
+                gpu_launches=K, roofline=roof,
+                e2e=dict(value=alg["tokens"] * world / (e2e_ms / 1e3), unit=UNIT,
+                         h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                         ms_per_step=e2e_ms),
+                wall_ms_timed_loop=1e3 * wall)
+    clocks = clk.summary()
+    line["clocks"] = clocks
+    if not args.no_cpu_baseline and world == 1:
+        units, toks, cores = oracle_sample(inp, budget_s=15.0)
+        secs = oracle_time(inp, units)
+        line["cpu_baseline"] = dict(
+            value=toks / secs, unit=UNIT, cores=cores, kind="oracle",
+            sample="%d of %d (sequence, v-head) units of the workload, one pass (%.1f s)" % (
+                len(units), inp["N"] * Nv, secs))
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+"""GB300 chunkwise gated delta rule forward -- Python binding of the C ABI.
+
+The binding only marshals arguments: every step of the forward runs in the
+CUDA kernels of ``libdnchunk.so`` (declared in ``include/dn_chunk_fwd.h``).
+There is no CPU path: if the library is missing, :func:`load` raises.
+PyTorch supplies device memory and streams.
+
+Names follow the C ABI: :func:`dn_chunk_fwd`, :func:`dn_check`,
+:func:`dn_status_str`, :func:`dn_last_kernel`.  :func:`chunk_fwd` is a
+convenience that allocates ``o`` and ``ht`` with torch and calls
+:func:`dn_chunk_fwd`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdnchunk.so")
+
+DN_OK = 0
+DN_ERR_INVALID_ARG = 1
+DN_ERR_UNSUPPORTED = 2
+DN_ERR_CUDA = 3
+DN_ERR_TIMEOUT = 4
+DN_ERR_DEVICE_ARG = 5
+
+DN_BF16 = 0
+DN_F32 = 1
+
+# Every symbol the public header declares.
+ABI_SYMBOLS = ("dn_chunk_fwd", "dn_check", "dn_status_str", "dn_last_kernel")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DnError(RuntimeError):
+    def __init__(self, status: int, what: str = "dn_chunk_fwd"):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, dn_status_str(status)))
+
+
+def load(path: str | None = None):
+    """Load ``libdnchunk.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                "libdnchunk.so is not built (%s); run `python -c \"import __graft_entry__ as g; "
+                "g.build()\"` -- there is no fallback path" % p)
+        lib = ctypes.CDLL(p)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.dn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P]
+        lib.dn_chunk_fwd.restype = I
+        lib.dn_check.argtypes = [P]
+        lib.dn_check.restype = I
+        lib.dn_status_str.argtypes = [I]
+        lib.dn_status_str.restype = ctypes.c_char_p
+        lib.dn_last_kernel.argtypes = []
+        lib.dn_last_kernel.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(x):
+    """Device pointer of a tensor (or an int address, or None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    if not x.is_contiguous():
+        raise ValueError("tensors passed to dn_chunk_fwd must be contiguous")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
+                 scale, chunk, o, ht, stream=None) -> int:
+    """Call the C entry point as is; returns its status code."""
+    lib = load()
+    return lib.dn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                            _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
+                            int(dk), int(dv), int(dtype), float(scale), int(chunk), _ptr(o),
+                            _ptr(ht), _stream(stream))
+
+
+def dn_check(stream=None) -> int:
+    return load().dn_check(_stream(stream))
+
+
+def dn_status_str(status: int) -> str:
+    try:
+        return load().dn_status_str(int(status)).decode()
+    except RuntimeError:
+        return "status %d" % status
+
+
+def dn_last_kernel() -> str:
+    return load().dn_last_kernel().decode()
+
+
+def dtype_code(dtype) -> int:
+    import torch
+    if dtype == torch.bfloat16:
+        return DN_BF16
+    if dtype == torch.float32:
+        return DN_F32
+    raise ValueError("unsupported dtype %s (bf16 or fp32)" % dtype)
+
+
+def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
+              output_final_state=True, chunk=64, stream=None, o=None, ht=None):
+    """Allocate ``o`` (and ``ht``) and run :func:`dn_chunk_fwd`.
+
+    q, k ``[B, T, Nk, dk]``; v ``[B, T, Nv, dv]``; beta, g ``[B, T, Nv]`` fp32;
+    h0 ``[N, Nv, dk, dv]`` fp32; cu_seqlens int64 ``[N+1]`` on the device.
+    Returns ``(o, ht)`` (``ht`` is None unless ``output_final_state``).
+    """
+    import torch
+    B, T, Nk, dk = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if o is None:
+        o = torch.empty(B, T, Nv, dv, dtype=q.dtype, device=q.device)
+    if ht is None and output_final_state:
+        ht = torch.empty(N, Nv, dk, dv, dtype=torch.float32, device=q.device)
+    st = dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
+                      dtype_code(q.dtype), 0.0 if scale is None else scale, chunk, o,
+                      ht if output_final_state else None, stream)
+    if st != DN_OK:
+        raise DnError(st)
+    return o, (ht if output_final_state else None)

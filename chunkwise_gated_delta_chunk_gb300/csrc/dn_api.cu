@@ -1,0 +1,118 @@
+// C-ABI front end: argument validation, kernel selection and launch.
+//
+// Everything here runs on the host.  Validation happens before any CUDA call,
+// so argument errors return without touching the device.
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "dn_chunk_fwd.h"
+#include "dn_internal.h"
+
+#define DN_EXPORT extern "C" __attribute__((visibility("default")))
+
+// Per-device status word: kernels OR error bits into it; dn_check reads and
+// clears it.  Module-scope device memory, so no allocation is ever needed.
+__device__ unsigned g_dn_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices];
+
+thread_local const char *t_last_kernel = "";
+
+// Device address of g_dn_status on the current device (looked up once per
+// device; the lookup is a host call that allocates nothing).
+cudaError_t status_ptr(unsigned **out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_dn_status);
+        if (err != cudaSuccess) return err;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
+
+}  // namespace
+
+DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
+                                 const float *beta, const float *g, const float *h0,
+                                 const int64_t *cu_seqlens, int n_seqs,
+                                 int B, int T, int Nk, int Nv, int dk, int dv,
+                                 dn_dtype dtype, float scale, int chunk,
+                                 void *o, float *ht, dn_stream_t stream) {
+    // ---- arguments that are wrong whatever is built ----------------------
+    if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
+    if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
+        return DN_ERR_INVALID_ARG;
+    if (Nv % Nk != 0) return DN_ERR_INVALID_ARG;
+    if (cu_seqlens ? B != 1 : n_seqs != B) return DN_ERR_INVALID_ARG;
+    if (isnan(scale) || isinf(scale)) return DN_ERR_INVALID_ARG;
+    if (chunk <= 0) return DN_ERR_INVALID_ARG;
+    const long long tokens = (long long)B * T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, g, h0, cu_seqlens, o, ht};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
+    // ---- valid, but not built --------------------------------------------
+    if (chunk != dn::kChunk) return DN_ERR_UNSUPPORTED;
+    if (!dim_ok(dk) || !dim_ok(dv)) return DN_ERR_UNSUPPORTED;
+    if (dtype == DN_F32 && dk > 128) return DN_ERR_UNSUPPORTED;
+    if (n_seqs == 0) return DN_OK;
+
+    dn::Params p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.cu = cu_seqlens;
+    p.o = o; p.ht = ht;
+    p.N = n_seqs; p.B = B; p.T = T; p.Nk = Nk; p.Nv = Nv; p.dk = dk; p.dv = dv;
+    p.tokens = tokens;
+    p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
+    if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
+
+    const char *name = "";
+    cudaError_t err = dn::simt_launch(p, dtype == DN_BF16, (cudaStream_t)stream, &name);
+    if (err != cudaSuccess) return DN_ERR_CUDA;
+    t_last_kernel = name;
+    return DN_OK;
+}
+
+DN_EXPORT dn_status dn_check(dn_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DN_ERR_CUDA;
+    unsigned *dptr = nullptr;
+    if (status_ptr(&dptr) != cudaSuccess) return DN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, dptr, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DN_ERR_CUDA;
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(dptr, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DN_ERR_CUDA;
+    }
+    if (word & dn::kStatusTimeout) return DN_ERR_TIMEOUT;
+    if (word & dn::kStatusBadSeq) return DN_ERR_DEVICE_ARG;
+    return DN_OK;
+}
+
+DN_EXPORT const char *dn_status_str(dn_status status) {
+    switch (status) {
+        case DN_OK: return "DN_OK";
+        case DN_ERR_INVALID_ARG: return "DN_ERR_INVALID_ARG";
+        case DN_ERR_UNSUPPORTED: return "DN_ERR_UNSUPPORTED";
+        case DN_ERR_CUDA: return "DN_ERR_CUDA";
+        case DN_ERR_TIMEOUT: return "DN_ERR_TIMEOUT";
+        case DN_ERR_DEVICE_ARG: return "DN_ERR_DEVICE_ARG";
+    }
+    return "DN_ERR_UNKNOWN";
+}
+
+DN_EXPORT const char *dn_last_kernel(void) { return t_last_kernel; }

@@ -1,0 +1,33 @@
+// Internal declarations shared by the C-ABI front end and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dn {
+
+constexpr int kChunk = 64;  // C: tokens per chunk
+
+// Bits of the per-device status word (see dn_check in the public header).
+constexpr unsigned kStatusTimeout = 1u;   // a bounded mbarrier wait ran out
+constexpr unsigned kStatusBadSeq = 2u;    // cu_seqlens out of order / out of range
+
+struct Params {
+    const void *q, *k, *v;     // [tokens, Nk, dk], [tokens, Nk, dk], [tokens, Nv, dv]
+    const float *beta, *g;     // [tokens, Nv]; g may be null
+    const float *h0;           // [N, Nv, dk, dv] or null
+    const int64_t *cu;         // [N+1] or null
+    void *o;                   // [tokens, Nv, dv]
+    float *ht;                 // [N, Nv, dk, dv] or null
+    int N, B, T, Nk, Nv, dk, dv;
+    long long tokens;          // B*T
+    float scale;
+    unsigned *status;          // per-device status word
+};
+
+// CUDA-core kernel: fp32 arithmetic for every product; any supported shape.
+// `bf16` selects bf16 q/k/v/o, else fp32.  Returns the launch error.
+cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
+size_t simt_smem_bytes(int dk, bool bf16);
+
+}  // namespace dn

@@ -1,0 +1,355 @@
+// CUDA-core kernel of the chunkwise gated delta rule forward.
+//
+// Every product is an fp32 FMA (no TF32), so this kernel serves fp32 inputs,
+// whose tolerance leaves no room for reduced-precision tensor-core products,
+// and every shape the tensor-core kernel does not take.
+//
+// Sources: [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1-§3.3;
+//          [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §2.3-§2.4.
+//
+// One CTA owns one (sequence, value head, 32-column value tile) and walks the
+// sequence's chunks in order, keeping its fp32 state tile S[dk][32] in shared
+// memory.  Per chunk of L <= 64 tokens:
+//   a1  G = inclusive prefix sum of g (warp scan), e^{G_i}, e^{G_L - G_i}
+//   a2  A_ij = -beta_i (k_i.k_j) e^{G_i-G_j} (j < i),
+//       P_ij = scale (q_i.k_j) e^{G_i-G_j} (j <= i)
+//   a3  T = (I - A)^-1 by forward substitution, one column per 4 lanes
+//   a4+a5  v_new = U - W S_in = T diag(beta) (V - diag(e^G) K S_in)
+//       (the same product as T diag(beta) V - T diag(beta e^G) K S_in, grouped
+//        so that W = T diag(beta e^G) K is never formed: K S_in is 64 x 32,
+//        cheaper than the 64 x dk matrix W on CUDA cores)
+//   a6  o = scale e^{G} (Q S_in) + P v_new
+//   a5  S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "dn_internal.h"
+
+namespace dn {
+namespace {
+
+constexpr int C = kChunk;
+constexpr int BV = 32;   // value columns per CTA
+constexpr int NT = 256;  // threads per CTA (8 warps)
+constexpr int LDC = C + 1;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void put(float *p, float x) { *p = x; }
+__device__ __forceinline__ void put(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Row stride (elements) of the shared K/Q copies: odd in 4-byte words, so
+// lanes reading one column of 32 different rows hit 32 different banks.
+template <typename Tin>
+__host__ __device__ constexpr int kq_ld(int dk) { return sizeof(Tin) == 2 ? dk + 2 : dk + 1; }
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+struct Layout {
+    size_t k, q, s, a, t, p, v, r, vn, g, eg, dec, beta, end;
+};
+
+template <typename Tin>
+__host__ __device__ inline Layout layout(int dk) {
+    Layout L{};
+    size_t off = 0;
+    const size_t kq = align16(size_t(C) * kq_ld<Tin>(dk) * sizeof(Tin));
+    L.k = off; off += kq;
+    L.q = off; off += kq;
+    L.s = off; off += align16(size_t(dk) * BV * 4);
+    L.a = off; off += align16(size_t(C) * LDC * 4);
+    L.t = off; off += align16(size_t(C) * LDC * 4);
+    L.p = off; off += align16(size_t(C) * LDC * 4);
+    L.v = off; off += size_t(C) * BV * 4;
+    L.r = off; off += size_t(C) * BV * 4;
+    L.vn = off; off += size_t(C) * BV * 4;
+    L.g = off; off += C * 4;
+    L.eg = off; off += C * 4;
+    L.dec = off; off += C * 4;
+    L.beta = off; off += C * 4;
+    off += 16;  // G_L and spare
+    L.end = off;
+    return L;
+}
+
+// Copy L rows of a [tokens, H, d] tensor (head `hh`, tokens from t0) into a
+// padded shared tile, zero-filling rows L..C-1.
+template <typename Tin>
+__device__ __forceinline__ void load_rows(Tin *dst, const Tin *src, long long t0, int L, int H,
+                                          int hh, int d, int tid) {
+    constexpr int VEC = 16 / sizeof(Tin);
+    const int ld = kq_ld<Tin>(d);
+    const int per_row = d / VEC;
+    for (int idx = tid; idx < L * per_row; idx += NT) {
+        const int i = idx / per_row, cv = idx - i * per_row;
+        const uint4 w = *reinterpret_cast<const uint4 *>(src + ((t0 + i) * H + hh) * (long long)d + cv * VEC);
+        const Tin *e = reinterpret_cast<const Tin *>(&w);
+#pragma unroll
+        for (int x = 0; x < VEC; ++x) dst[i * ld + cv * VEC + x] = e[x];
+    }
+    for (int idx = L * ld + tid; idx < C * ld; idx += NT) dst[idx] = Tin(0.0f);
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT) simt_fwd(Params p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
+    const int nvt = (dv + BV - 1) / BV;
+    const int unit = blockIdx.x;
+    const int vt = unit % nvt;
+    const int h = (unit / nvt) % Nv;
+    const int n = unit / (nvt * Nv);
+    const int hk = h / (Nv / Nk);
+    const int v0 = vt * BV;
+    const int bvw = min(BV, dv - v0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    const Layout lay = layout<Tin>(dk);
+    Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);
+    Tin *sQ = reinterpret_cast<Tin *>(smem + lay.q);
+    float *sS = reinterpret_cast<float *>(smem + lay.s);
+    float *sA = reinterpret_cast<float *>(smem + lay.a);
+    float *sT = reinterpret_cast<float *>(smem + lay.t);
+    float *sP = reinterpret_cast<float *>(smem + lay.p);
+    float *sV = reinterpret_cast<float *>(smem + lay.v);
+    float *sR = reinterpret_cast<float *>(smem + lay.r);
+    float *sVn = reinterpret_cast<float *>(smem + lay.vn);
+    float *sG = reinterpret_cast<float *>(smem + lay.g);
+    float *sEG = reinterpret_cast<float *>(smem + lay.eg);
+    float *sDec = reinterpret_cast<float *>(smem + lay.dec);
+    float *sBeta = reinterpret_cast<float *>(smem + lay.beta);
+    float *sGL = reinterpret_cast<float *>(smem + lay.beta + C * 4);
+    const int ldkq = kq_ld<Tin>(dk);
+
+    const Tin *q = static_cast<const Tin *>(p.q);
+    const Tin *k = static_cast<const Tin *>(p.k);
+    const Tin *v = static_cast<const Tin *>(p.v);
+    Tin *o = static_cast<Tin *>(p.o);
+
+    long long bos, eos;
+    if (p.cu) {
+        bos = p.cu[n];
+        eos = p.cu[n + 1];
+        if (bos < 0 || eos < bos || eos > p.tokens) {
+            if (tid == 0) atomicOr(p.status, kStatusBadSeq);
+            bos = eos = 0;
+        }
+    } else {
+        bos = (long long)n * p.T;
+        eos = bos + p.T;
+    }
+
+    // S <- h0 tile (or 0)
+    const size_t sbase = ((size_t)n * Nv + h) * dk * dv;
+    for (int idx = tid; idx < dk * BV; idx += NT) {
+        const int d = idx / BV, c = idx - d * BV;
+        sS[idx] = (p.h0 && c < bvw) ? p.h0[sbase + (size_t)d * dv + v0 + c] : 0.0f;
+    }
+
+    for (long long t0 = bos; t0 < eos; t0 += C) {
+        const int L = (eos - t0) < C ? (int)(eos - t0) : C;
+        __syncthreads();  // previous chunk fully consumed
+
+        // ---- load the chunk --------------------------------------------
+        load_rows<Tin>(sK, k, t0, L, Nk, hk, dk, tid);
+        load_rows<Tin>(sQ, q, t0, L, Nk, hk, dk, tid);
+        for (int idx = tid; idx < C * BV; idx += NT) {
+            const int i = idx / BV, c = idx - i * BV;
+            sV[idx] = (i < L && c < bvw) ? to_f(v[((t0 + i) * Nv + h) * (long long)dv + v0 + c]) : 0.0f;
+        }
+        if (tid < C) {
+            sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
+            sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
+        }
+        __syncthreads();
+
+        // ---- a1: gate prefix sum ----------------------------------------
+        if (warp == 0) {
+            float a = sG[lane], b = sG[lane + 32];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float ta = __shfl_up_sync(0xffffffffu, a, off);
+                const float tb = __shfl_up_sync(0xffffffffu, b, off);
+                if (lane >= off) { a += ta; b += tb; }
+            }
+            b += __shfl_sync(0xffffffffu, a, 31);
+            const float ga = __shfl_sync(0xffffffffu, a, (L - 1) & 31);
+            const float gb = __shfl_sync(0xffffffffu, b, (L - 1) & 31);
+            const float GL = (L - 1) < 32 ? ga : gb;
+            sG[lane] = a;
+            sG[lane + 32] = b;
+            sEG[lane] = lane < L ? expf(a) : 0.0f;
+            sEG[lane + 32] = lane + 32 < L ? expf(b) : 0.0f;
+            sDec[lane] = lane < L ? expf(GL - a) : 0.0f;
+            sDec[lane + 32] = lane + 32 < L ? expf(GL - b) : 0.0f;
+            if (lane == 0) sGL[0] = GL;
+        }
+        __syncthreads();
+
+        // ---- a2: A (strictly lower) and P (lower incl. diagonal) ---------
+        for (int idx = tid; idx < C * C; idx += NT) {
+            const int i = idx >> 6, j = idx & 63;
+            float a = 0.0f, pv = 0.0f;
+            if (i < L && j <= i) {
+                const Tin *ki = sK + i * ldkq, *kj = sK + j * ldkq, *qi = sQ + i * ldkq;
+                float sk = 0.0f, sq = 0.0f;
+                for (int d = 0; d < dk; ++d) {
+                    const float kjd = to_f(kj[d]);
+                    sk = fmaf(to_f(ki[d]), kjd, sk);
+                    sq = fmaf(to_f(qi[d]), kjd, sq);
+                }
+                const float dec = expf(sG[i] - sG[j]);
+                if (j < i) a = -sBeta[i] * dec * sk;
+                pv = p.scale * dec * sq;
+            }
+            sA[i * LDC + j] = a;
+            sP[i * LDC + j] = pv;
+        }
+        __syncthreads();
+
+        // ---- a3: T = (I - A)^-1, column j by the 4 lanes 4j..4j+3 ---------
+        // Column j of T solves (I - A) x = e_j:  x_j = 1 and
+        // x_i = sum_{j <= m < i} A_im x_m for i > j.  Lane p sums the terms
+        // with m = j + p (mod 4) and keeps those x_m itself.
+        {
+            const int j = tid >> 2, pl = tid & 3;
+            for (int i = pl; i < C; i += 4) sT[i * LDC + j] = (i == j) ? 1.0f : 0.0f;
+            __syncwarp();  // the solve below reads rows other lanes initialised
+            for (int i = 1; i < L; ++i) {
+                float part = 0.0f;
+                if (i > j) {
+                    for (int m = j + pl; m < i; m += 4) part = fmaf(sA[i * LDC + m], sT[m * LDC + j], part);
+                }
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                if (i > j && ((i - j) & 3) == pl) sT[i * LDC + j] = part;
+            }
+        }
+        __syncthreads();
+
+        // ---- a4/a5: R = diag(beta)(V - diag(e^G) K S_in); also Q S_in -----
+        const int c = lane;
+        float qs[8];
+        {
+            float ks[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) { ks[r] = 0.0f; qs[r] = 0.0f; }
+            for (int d = 0; d < dk; ++d) {
+                const float s = sS[d * BV + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int i = warp + 8 * r;
+                    ks[r] = fmaf(to_f(sK[i * ldkq + d]), s, ks[r]);
+                    qs[r] = fmaf(to_f(sQ[i * ldkq + d]), s, qs[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = warp + 8 * r;
+                sR[i * BV + c] = i < L ? sBeta[i] * (sV[i * BV + c] - sEG[i] * ks[r]) : 0.0f;
+            }
+        }
+        __syncthreads();
+
+        // ---- a5: v_new = T R --------------------------------------------
+        {
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+            for (int j = 0; j < L; ++j) {
+                const float rj = sR[j * BV + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[r] = fmaf(sT[(warp + 8 * r) * LDC + j], rj, acc[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = warp + 8 * r;
+                sVn[i * BV + c] = i < L ? acc[r] : 0.0f;
+            }
+        }
+        __syncthreads();
+
+        // ---- a6: o = scale e^G (Q S_in) + P v_new ------------------------
+        {
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+            for (int j = 0; j < L; ++j) {
+                const float vj = sVn[j * BV + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) acc[r] = fmaf(sP[(warp + 8 * r) * LDC + j], vj, acc[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int i = warp + 8 * r;
+                if (i < L && c < bvw) {
+                    const float out = fmaf(p.scale * sEG[i], qs[r], acc[r]);
+                    put(o + ((t0 + i) * Nv + h) * (long long)dv + v0 + c, out);
+                }
+            }
+        }
+
+        // ---- a5: S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T ----
+        {
+            const float eGL = expf(sGL[0]);
+            for (int d0 = warp; d0 < dk; d0 += 8 * 8) {
+                float acc[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int d = d0 + 8 * r;
+                    acc[r] = d < dk ? eGL * sS[d * BV + c] : 0.0f;
+                }
+                for (int i = 0; i < L; ++i) {
+                    const float w = sDec[i] * sVn[i * BV + c];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int d = d0 + 8 * r;
+                        if (d < dk) acc[r] = fmaf(to_f(sK[i * ldkq + d]), w, acc[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int d = d0 + 8 * r;
+                    if (d < dk) sS[d * BV + c] = acc[r];
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (p.ht) {
+        for (int idx = tid; idx < dk * BV; idx += NT) {
+            const int d = idx / BV, c = idx - d * BV;
+            if (c < bvw) p.ht[sbase + (size_t)d * dv + v0 + c] = sS[idx];
+        }
+    }
+}
+
+}  // namespace
+
+size_t simt_smem_bytes(int dk, bool bf16) {
+    return bf16 ? layout<__nv_bfloat16>(dk).end : layout<float>(dk).end;
+}
+
+cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name) {
+    const int nvt = (p.dv + BV - 1) / BV;
+    const long long grid = (long long)p.N * p.Nv * nvt;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const size_t smem = simt_smem_bytes(p.dk, bf16);
+    cudaError_t err;
+    if (bf16) {
+        err = cudaFuncSetAttribute(simt_fwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        simt_fwd<__nv_bfloat16><<<(unsigned)grid, NT, smem, stream>>>(p);
+        *name = "simt_fwd<bf16>";
+    } else {
+        err = cudaFuncSetAttribute(simt_fwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        simt_fwd<float><<<(unsigned)grid, NT, smem, stream>>>(p);
+        *name = "simt_fwd<f32>";
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dn

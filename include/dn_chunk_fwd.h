@@ -1,0 +1,123 @@
+/*
+ * dn_chunk_fwd.h -- C ABI of the chunkwise gated delta rule forward for GB300.
+ *
+ * Sources (web pages on the method, cited by title and section):
+ *   [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现"
+ *   [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么"
+ *
+ * Operation ([CGDR] §1 recurrence, evaluated per chunk as in [CGDR] §3 and
+ * [WY] §2.4): for every sequence n and value head h (query/key head
+ * h / (Nv/Nk), [CGDR] §1), starting from S = h0[n,h] (or 0),
+ *
+ *     S_t = e^{g_t} S_{t-1} + beta_t k_t (v_t - k_t^T e^{g_t} S_{t-1})^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * and ht[n,h] = S after the sequence's last token.  The state is decayed
+ * before the delta read ("forget first, then write", [CGDR] §1); o_t reads
+ * the state after token t's own write.  The library computes it per 64-token
+ * chunk: gate prefix sum, WY matrix and T = (I - A)^-1 by forward
+ * substitution, W and U, the cross-chunk state pass and the causal output.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major
+ *     and contiguous, 16-byte aligned.  The library keeps no reference to
+ *     them after the call and allocates no device memory per call.
+ *   - Calls are asynchronous and ordered on `stream` (NULL = legacy default
+ *     stream).  Outputs are valid once the stream reaches the call.
+ *   - Errors are returned as a dn_status, never thrown or aborted.  Argument
+ *     errors are found on the host before anything is launched; nothing is
+ *     written then.  A launch failure returns DN_ERR_CUDA.  Errors found on
+ *     the device (a bounded wait that ran out, a malformed cu_seqlens) are
+ *     recorded in a per-device status word and reported by dn_check().
+ */
+#ifndef DN_CHUNK_FWD_H
+#define DN_CHUNK_FWD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; declared here so that this header
+ * needs no CUDA header. */
+typedef struct CUstream_st *dn_stream_t;
+
+typedef enum {
+    DN_OK = 0,
+    DN_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or combination */
+    DN_ERR_UNSUPPORTED = 2,  /* valid per the method but not built here (e.g. chunk != 64) */
+    DN_ERR_CUDA = 3,         /* the CUDA runtime reported an error */
+    DN_ERR_TIMEOUT = 4,      /* a device-side bounded wait ran out (dn_check) */
+    DN_ERR_DEVICE_ARG = 5    /* the device found a malformed cu_seqlens (dn_check) */
+} dn_status;
+
+/* Element type of q, k, v and o (one dtype for all four, as in [WY] §5). */
+typedef enum {
+    DN_BF16 = 0,
+    DN_F32 = 1
+} dn_dtype;
+
+/*
+ * dn_chunk_fwd -- forward pass of the chunkwise gated delta rule.
+ *
+ * Arguments (all shapes row-major; "tokens" = B*T, flattened over the batch):
+ *   q, k        [B, T, Nk, dk]  dtype       queries, keys ([CGDR] §1 table)
+ *   v           [B, T, Nv, dv]  dtype       values
+ *   beta        [B, T, Nv]      float32     write strength beta_t
+ *   g           [B, T, Nv]      float32     log-domain decay g_t; NULL means
+ *                                           g = 0 (plain DeltaNet, [WY] §1)
+ *   h0          [N, Nv, dk, dv] float32     initial state; NULL means zero
+ *   cu_seqlens  [N+1]           int64       packed sequence offsets
+ *                                           ([WY] §5 varlen); NULL means N = B
+ *                                           sequences of length T.  Non-NULL
+ *                                           requires B == 1.  Must be
+ *                                           non-decreasing with cu[0] = 0 and
+ *                                           cu[N] <= T (checked on the device:
+ *                                           a bad sequence is skipped and
+ *                                           dn_check returns DN_ERR_DEVICE_ARG).
+ *   n_seqs      N; must equal B when cu_seqlens is NULL.  N = 0 is a no-op.
+ *   B, T        batch and tokens per batch row; T may be 0.
+ *   Nk, Nv      key/value head counts; Nv % Nk == 0 (GQA, nvPerNk = Nv/Nk).
+ *   dk, dv      head dims, each one of 16, 32, 64, 128, 256.
+ *   dtype       DN_BF16 or DN_F32.  With DN_F32 every product is computed in
+ *               fp32 on CUDA cores (no TF32), and dk must be <= 128.
+ *   scale       multiplies q in the output; scale <= 0 selects 1/sqrt(dk).
+ *   chunk       chunk length C; only 64 is built (others: DN_ERR_UNSUPPORTED).
+ *   o           [B, T, Nv, dv]  dtype       output, written for every token of
+ *                                           every sequence (rounded to nearest
+ *                                           even from fp32 for DN_BF16).
+ *   ht          [N, Nv, dk, dv] float32     final state; NULL: not written.
+ *   stream      CUDA stream for the launch.
+ *
+ * Returns DN_OK once the work is enqueued.  One kernel launch per call.
+ */
+dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
+                       const float *beta, const float *g, const float *h0,
+                       const int64_t *cu_seqlens, int n_seqs,
+                       int B, int T, int Nk, int Nv, int dk, int dv,
+                       dn_dtype dtype, float scale, int chunk,
+                       void *o, float *ht, dn_stream_t stream);
+
+/*
+ * dn_check -- wait for `stream`, then read and clear the device status word
+ * of the current device.  Returns DN_ERR_TIMEOUT or DN_ERR_DEVICE_ARG if a
+ * kernel of this library recorded one since the last check, DN_ERR_CUDA if
+ * the stream reports an error, else DN_OK.
+ */
+dn_status dn_check(dn_stream_t stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *dn_status_str(dn_status status);
+
+/*
+ * dn_last_kernel -- name of the kernel the last successful dn_chunk_fwd call
+ * on this host thread launched ("" before any call).  Static storage.
+ */
+const char *dn_last_kernel(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DN_CHUNK_FWD_H */

@@ -1,0 +1,105 @@
+"""Boundary tests that need no GPU: the library loads, exports exactly the
+entry points its headers declare, and rejects bad arguments on the host
+before anything reaches the device."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import chunkwise_gated_delta_chunk_gb300 as dn
+from chunkwise_gated_delta_chunk_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    _build.build()
+    return dn.load()
+
+
+def declared_symbols():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dn_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_abi():
+    assert set(dn.ABI_SYMBOLS) <= declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in declared_symbols():
+        assert getattr(clib, name) is not None
+
+
+def test_library_exports_nothing_else():
+    _build.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", dn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    ours = {line.split()[-1] for line in out.splitlines()
+            if line.split() and line.split()[-1].startswith("dn_")}
+    assert ours == declared_symbols()
+
+
+def test_status_strings(clib):
+    for code, name in [(0, "DN_OK"), (1, "DN_ERR_INVALID_ARG"), (2, "DN_ERR_UNSUPPORTED"),
+                       (3, "DN_ERR_CUDA"), (4, "DN_ERR_TIMEOUT"), (5, "DN_ERR_DEVICE_ARG")]:
+        assert clib.dn_status_str(code).decode() == name
+    assert clib.dn_status_str(99).decode() == "DN_ERR_UNKNOWN"
+
+
+# Fake, 16-byte aligned "device" addresses: validation rejects the call before
+# any pointer could be used, so nothing is ever dereferenced.
+A = 1 << 20
+
+
+def call(clib, **over):
+    args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, chunk=64, o=A, ht=None)
+    args.update(over)
+    return clib.dn_chunk_fwd(args["q"], args["k"], args["v"], args["beta"], args["g"], args["h0"],
+                             args["cu"], args["n"], args["B"], args["T"], args["Nk"], args["Nv"],
+                             args["dk"], args["dv"], args["dtype"], args["scale"], args["chunk"],
+                             args["o"], args["ht"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Nv=3), dn.DN_ERR_INVALID_ARG),                 # Nv % Nk != 0
+    (dict(Nk=0), dn.DN_ERR_INVALID_ARG),
+    (dict(n=3), dn.DN_ERR_INVALID_ARG),                  # N != B without cu_seqlens
+    (dict(cu=A, n=2, B=2), dn.DN_ERR_INVALID_ARG),       # cu_seqlens needs B == 1
+    (dict(q=None), dn.DN_ERR_INVALID_ARG),
+    (dict(beta=None), dn.DN_ERR_INVALID_ARG),
+    (dict(o=None), dn.DN_ERR_INVALID_ARG),
+    (dict(q=A + 8), dn.DN_ERR_INVALID_ARG),              # misaligned
+    (dict(ht=A + 4), dn.DN_ERR_INVALID_ARG),
+    (dict(T=-1), dn.DN_ERR_INVALID_ARG),
+    (dict(dtype=7), dn.DN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), dn.DN_ERR_INVALID_ARG),
+    (dict(chunk=0), dn.DN_ERR_INVALID_ARG),
+    (dict(chunk=32), dn.DN_ERR_UNSUPPORTED),             # only C = 64 is built
+    (dict(dk=96), dn.DN_ERR_UNSUPPORTED),
+    (dict(dv=512), dn.DN_ERR_UNSUPPORTED),
+    (dict(dtype=dn.DN_F32, dk=256), dn.DN_ERR_UNSUPPORTED),
+])
+def test_invalid_arguments_rejected_on_host(clib, over, code):
+    assert call(clib, **over) == code
+
+
+def test_zero_sequences_is_a_noop(clib):
+    assert call(clib, n=0, B=0, T=0, q=None, k=None, v=None, beta=None, o=None) == dn.DN_OK
+    assert call(clib, n=0, B=1, T=5, cu=A) == dn.DN_OK
+
+
+def test_product_path_has_no_fallback(tmp_path):
+    """The binding refuses to run without the CUDA library (no CPU path)."""
+    with pytest.raises(RuntimeError, match="no fallback"):
+        dn.load(str(tmp_path / "missing.so"))

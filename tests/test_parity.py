@@ -1,0 +1,186 @@
+"""GPU parity: the CUDA path (called through the C ABI) against the fp64 oracle,
+element by element on the same seeded inputs.
+
+Small cases compare every output and span several chunks plus a ragged tail;
+the named full-size workloads compare every output of sampled (sequence,
+value-head) units, which the oracle computes one by one, in the same launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from conftest import cuda_ok
+from parity_util import TOL, check, run_gpu
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA GPU")]
+
+
+def inputs(B=2, T=130, Nk=2, Nv=2, dk=64, dv=64, dtype=torch.bfloat16, gate=3.0, h0=True,
+           seed=0, lengths=None, **kw):
+    return workloads.make_inputs(B, T, Nk, Nv, dk, dv, dtype=dtype, gate_mu=gate, h0=h0,
+                                 seed=seed, lengths=lengths, **kw)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 64), (64, 128), (128, 64),
+                                   (128, 128), (256, 128), (128, 256), (256, 256)])
+def test_dims_bf16(lib, dk, dv):
+    inp = inputs(dk=dk, dv=dv, seed=dk + dv)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="bf16 %dx%d" % (dk, dv))
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (64, 32), (64, 64), (128, 128)])
+def test_dims_fp32(lib, dk, dv):
+    inp = inputs(dk=dk, dv=dv, dtype=torch.float32, seed=7 + dk)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="f32 %dx%d" % (dk, dv))
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 129, 200])
+def test_lengths(lib, T):
+    inp = inputs(B=3, T=T, dk=128, dv=128, seed=100 + T)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="T=%d" % T)
+
+
+@pytest.mark.parametrize("nv_per_nk", [1, 2, 4])
+def test_varlen_gqa(lib, nv_per_nk):
+    lengths = [1, 63, 64, 65, 0, 200, 128, 3]
+    inp = inputs(B=1, Nk=2, Nv=2 * nv_per_nk, dk=128, dv=128, lengths=lengths,
+                 seed=200 + nv_per_nk)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="varlen r=%d" % nv_per_nk)
+
+
+@pytest.mark.parametrize("gate,h0,final", [(None, False, True), (None, True, True),
+                                           (3.0, False, True), (3.0, True, False)])
+def test_optional_inputs(lib, gate, h0, final):
+    inp = inputs(dk=128, dv=128, gate=gate, h0=h0, seed=300)
+    o, ht = run_gpu(inp, output_final_state=final)
+    assert (ht is None) == (not final)
+    check(inp, o, ht, label="gate=%s h0=%s" % (gate, h0))
+
+
+def test_custom_scale(lib):
+    inp = inputs(dk=128, dv=128, seed=301)
+    inp["scale"] = 0.37
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="scale")
+
+
+def test_extreme_gates(lib):
+    """Very strong decay (e^g ~ 1e-13 per token), no decay, and beta = 1."""
+    inp = inputs(dk=128, dv=128, seed=302, T=150)
+    inp["g"] = torch.full_like(inp["g"], -30.0)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="g=-30")
+    inp = inputs(dk=128, dv=128, seed=303, T=150)
+    inp["g"] = torch.zeros_like(inp["g"])
+    inp["beta"] = torch.ones_like(inp["beta"])
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="g=0 beta=1")
+    inp = inputs(dk=128, dv=128, seed=304, T=150)
+    inp["g"] = -torch.rand(inp["g"].shape, generator=torch.Generator().manual_seed(9)) * 4.0
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="g~U(-4,0)")
+
+
+def test_state_carry(lib):
+    """Second call from the first call's ht equals one call on the whole."""
+    inp = inputs(B=2, T=300, dk=128, dv=128, seed=305)
+    o, ht = run_gpu(inp)
+    cut = 100
+    p1, p2 = dict(inp), dict(inp)
+    for key in ("q", "k", "v", "beta", "g"):
+        p1[key] = inp[key][:, :cut].contiguous()
+        p2[key] = inp[key][:, cut:].contiguous()
+    o1, h1 = run_gpu(p1)
+    p2["h0"] = h1.cpu()
+    o2, h2 = run_gpu(p2)
+    both = torch.cat([o1, o2], dim=1).float()
+    tol = TOL[torch.bfloat16]
+    assert (both - o.float()).abs().max().item() <= tol["max_abs"]
+    assert (h2 - ht).abs().max().item() <= tol["max_abs"]
+
+
+def test_deterministic(lib):
+    inp = inputs(dk=128, dv=128, seed=306, T=257)
+    o1, h1 = run_gpu(inp)
+    o2, h2 = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_guard_regions_untouched(lib):
+    """The kernel writes exactly o and ht: sentinels around them survive."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = inputs(B=2, T=70, dk=128, dv=128, seed=307)
+    d = workloads.to_device(inp, "cuda")
+    n_o = d["v"].numel()
+    n_h = 2 * 2 * 128 * 128
+    o_buf = torch.full((n_o + 4096,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    h_buf = torch.full((n_h + 4096,), -777.0, dtype=torch.float32, device="cuda")
+    o = o_buf[:n_o].view_as(d["v"])
+    ht = h_buf[:n_h].view(2, 2, 128, 128)
+    dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], None, o=o, ht=ht,
+                 scale=inp["scale"])
+    torch.cuda.synchronize()
+    assert bool((o_buf[n_o:] == 12345.0).all()) and bool((h_buf[n_h:] == -777.0).all())
+    check(inp, o, ht, label="guards")
+
+
+def test_empty_sequences_keep_h0(lib):
+    inp = inputs(B=1, dk=128, dv=128, lengths=[0, 5, 0], seed=308)
+    o, ht = run_gpu(inp)
+    assert torch.equal(ht[0].cpu(), inp["h0"][0]) and torch.equal(ht[2].cpu(), inp["h0"][2])
+    check(inp, o, ht, label="empty")
+
+
+def test_zero_tokens(lib):
+    inp = inputs(B=2, T=0, dk=64, dv=64, seed=309)
+    o, ht = run_gpu(inp)
+    assert o.numel() == 0 and torch.equal(ht.cpu(), inp["h0"])
+
+
+def test_malformed_cu_seqlens_reported(lib):
+    """A decreasing cu_seqlens is caught by the kernel's own bounds check and
+    reported by dn_check; the bad sequence is skipped, the others computed."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = inputs(B=1, dk=64, dv=64, lengths=[10, 20, 30], seed=310)
+    d = workloads.to_device(inp, "cuda")
+    cu = torch.tensor([0, 10, 5, 60], dtype=torch.int64, device="cuda")
+    o, ht = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], cu,
+                         scale=inp["scale"])
+    assert dn.dn_check() == dn.DN_ERR_DEVICE_ARG
+    assert dn.dn_check() == dn.DN_OK  # the status word was cleared
+
+
+# ---------------------------------------------------------------------------
+# The named workloads at full size, sampled units.
+# ---------------------------------------------------------------------------
+SAMPLES = {
+    "deltanet_fp32_h2_t256_d64": None,
+    "gdn_bf16_b4_h16_t2048_d128": [0, 17, 40, 63],
+    "gdn_gqa_varlen_bf16_n8_nk8_nv32_d128": "longest_shortest",
+    "gdn_long_bf16_b1_h32_t32768_d128": [0, 31],
+    "gdn_wide_bf16_b8_h8_t8192_d256": [0, 63],
+}
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_workload_full_size(lib, name):
+    inp = workloads.workload_inputs(name)
+    o, ht = run_gpu(inp)
+    units = SAMPLES[name]
+    if units == "longest_shortest":
+        cu = inp["cu_seqlens"]
+        lens = (cu[1:] - cu[:-1]).tolist()
+        Nv = inp["v"].shape[2]
+        nl, ns = int(np.argmax(lens)), int(np.argmin(lens))
+        units = [nl * Nv, nl * Nv + Nv - 1, ns * Nv + 1]
+    res = check(inp, o, ht, units=units, label=name)
+    # every output of every unit is finite
+    assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
+    print(name, res)
