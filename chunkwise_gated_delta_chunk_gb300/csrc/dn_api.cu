@@ -9,6 +9,7 @@
 
 #include "dn_chunk_fwd.h"
 #include "dn_internal.h"
+#include "dn_tc.h"
 
 #define DN_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -82,7 +83,12 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
 
     const char *name = "";
-    cudaError_t err = dn::simt_launch(p, dtype == DN_BF16, (cudaStream_t)stream, &name);
+    const bool bf16 = dtype == DN_BF16;
+    cudaError_t err;
+    if (tokens > 0 && dn::tc_supported(dk, dv, bf16))
+        err = dn::tc_launch(p, (cudaStream_t)stream, &name);
+    else
+        err = dn::simt_launch(p, bf16, (cudaStream_t)stream, &name);
     if (err != cudaSuccess) return DN_ERR_CUDA;
     t_last_kernel = name;
     return DN_OK;

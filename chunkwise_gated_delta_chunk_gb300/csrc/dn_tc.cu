@@ -1,0 +1,862 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernel of the chunkwise gated delta rule
+// forward, bf16 q/k/v/o, dk = 128, 128 value columns per CTA.
+//
+// Sources: [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1-§3.3;
+//          [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §2.3-§3.4.
+//
+// One persistent CTA per (sequence, value head, 128-column value tile) walks
+// the sequence's 64-token chunks in order.  The fp32 state lives in tensor
+// memory, transposed (lane = value column v, column = key index d), for the
+// whole sequence.  Every contraction is a tcgen05 MMA with M = 128:
+//
+//   KQ  [K;Q] K^T        -> KK^T and QK^T        (a2, a6)
+//   W   K^T T'^T         -> W^T, T' = T diag(beta e^G)          (a4)
+//   U   V^T T''^T        -> U^T, T'' = T diag(beta)             (a4)
+//   VN  U^T - S^T W^T    -> v_new^T (S^T as a bf16 TMEM operand) (a5)
+//   O   S^T Q^T          -> inter-chunk output                   (a6)
+//   DS  S^T += v~^T K    -> state update, v~ = e^{G_L-G} v_new   (a5)
+//   PV  v_new^T P^T      -> intra-chunk output, P = tril(QK^T.D) (a6)
+//
+// Warp roles (14 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
+// group of four consecutive warps covers all 128 lanes):
+//   0      loader: TMA for the K, Q, V tiles of a chunk and the gate scalars
+//          (prefix sum G, e^G, decays) computed with warp shuffles;
+//   1      MMA issuer (one thread) and TMEM owner;
+//   2-5    prep: A and P from KK^T / QK^T, T = (I - A)^-1 (16x16 diagonal
+//          blocks by forward substitution, then block rows with TF32 mma.sync),
+//          T' and T'', then W^T from TMEM to a bf16 operand.  Runs up to one
+//          chunk ahead of the state scan;
+//   6-9    state: v_new and v~ operands, the fp32 state update, ht;
+//   10-13  output: o = scale e^{G} (S^T Q^T) + P v_new, stored as bf16.
+//
+// Every wait is bounded: after kTimeoutNs a CTA records kStatusTimeout in the
+// status word, raises a shared abort flag so the other roles stop too, drains
+// its own outstanding TMA and MMA work and frees its tensor memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "dn_internal.h"
+#include "dn_tc.h"
+#include "dn_tmap.h"
+#include "tc_ptx.cuh"
+
+namespace dn {
+namespace {
+
+using namespace ptx;
+
+constexpr int C = kChunk;      // 64
+constexpr int DK = 128;
+constexpr int BVT = 128;       // value columns per CTA
+constexpr int NS = 3;          // pipeline stages of K/Q/V tiles
+constexpr int NTHREADS = 448;
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+
+// ---- shared memory map (offsets from a 1024-byte aligned base) -------------
+constexpr uint32_t STAGE_BYTES = 49152;  // K0 Q0 K1 Q1 V0 V1, 8 KB each
+constexpr uint32_t OFF_STAGE = 0;
+constexpr uint32_t OFF_P = OFF_STAGE + NS * STAGE_BYTES;  // 2 x 8 KB (double buffered)
+constexpr uint32_t OFF_TP = OFF_P + 2 * 8192;              // T'  8 KB
+constexpr uint32_t OFF_TPP = OFF_TP + 8192;                // T'' 8 KB
+constexpr uint32_t OFF_WT = OFF_TPP + 8192;                // -W^T 16 KB
+constexpr int LDA = 68;                                    // fp32 row stride of A / T
+constexpr uint32_t OFF_A = OFF_WT + 16384;                 // 64 x 68 fp32
+constexpr int LDX = 56;
+constexpr uint32_t OFF_X = OFF_A + 64 * LDA * 4;           // 16 x 56 fp32
+constexpr int SCAL_FLOATS = 640;
+constexpr uint32_t OFF_SCAL = OFF_X + 16 * LDX * 4;        // NS x 2560 B
+constexpr uint32_t OFF_BAR = OFF_SCAL + NS * SCAL_FLOATS * 4;
+constexpr int NBARS = 32;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;         // TMEM base, abort flag
+constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;          // alignment slack
+
+static_assert(OFF_P % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_TPP % 1024 == 0 && OFF_WT % 1024 == 0,
+              "MMA operands need 1024-byte aligned swizzle atoms");
+static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB of shared memory per CTA");
+
+// Scalars of one chunk (floats within a stage's scalar block).
+constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, SC_F = 320,
+              SC_H = 384 /* 3 x 64 */, SC_ALPHA = 576, SC_L = 577;
+
+// Barrier indices.
+enum {
+    B_FULL = 0,                 // NS: TMA bytes + loader scalars
+    B_EMPTY = B_FULL + NS,      // NS: every reader of the stage is done
+    B_KQ_FULL = B_EMPTY + NS,
+    B_KQ_EMPTY,
+    B_T_FULL,
+    B_W_FULL,
+    B_W_EMPTY,
+    B_WSM_FULL,
+    B_S_FULL,
+    B_V_FULL,
+    B_VSM_FULL,
+    B_D_FULL,
+    B_O_EMPTY,
+    B_DRAIN,
+    B_COUNT
+};
+static_assert(B_COUNT <= NBARS, "barrier space");
+
+// Tensor memory columns (fp32 accumulators; SB holds bf16 pairs).
+constexpr uint32_t TM_KQ = 0, TM_W = 64, TM_V = 128, TM_S = 192, TM_SB = 320, TM_O = 384,
+                   TM_P = 448, TM_COLS = 512;
+
+// Instruction descriptors.
+constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);   // A, B K-major
+constexpr uint32_t ID_W = idesc_bf16(128, 64, 1, 0);    // A MN-major (K^T), B K-major
+constexpr uint32_t ID_U = idesc_bf16(128, 64, 1, 0);
+constexpr uint32_t ID_VN = idesc_bf16(128, 64, 0, 1);   // A TMEM, B MN-major (-W^T rows d)
+constexpr uint32_t ID_O = idesc_bf16(128, 64, 0, 0);    // A TMEM, B K-major (Q rows)
+constexpr uint32_t ID_DS = idesc_bf16(128, 128, 0, 1);  // A TMEM, B MN-major (K rows)
+constexpr uint32_t ID_PV = idesc_bf16(128, 64, 0, 0);   // A TMEM, B K-major (P rows)
+
+struct Ctx {
+    uint32_t base;     // shared address of the aligned base
+    uint8_t *gbase;    // generic pointer to the same
+    volatile int *abort_flag;
+    unsigned *status;
+};
+
+__device__ __forceinline__ uint32_t bar(const Ctx &x, int i) { return x.base + OFF_BAR + 8u * i; }
+__device__ __forceinline__ float *scal(const Ctx &x, int s) {
+    return reinterpret_cast<float *>(x.gbase + OFF_SCAL + s * SCAL_FLOATS * 4);
+}
+
+// Bounded wait.  Returns false once the CTA is aborting.
+__device__ __noinline__ bool wait_slow(const Ctx &x, uint32_t b, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(b, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*x.abort_flag) return false;
+            if (globaltimer() - t0 > kTimeoutNs) {
+                *x.abort_flag = 1;
+                atomicOr(x.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait(const Ctx &x, uint32_t b, uint32_t parity) {
+    if (mbar_try_wait(b, parity)) return true;
+    return wait_slow(x, b, parity);
+}
+
+// Wait that ignores the abort flag (used while draining); bounded by time.
+__device__ __noinline__ void wait_drain(uint32_t b, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(b, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return;
+}
+
+// Warp-uniform wait: every lane gets the same answer, so lanes never diverge
+// around the .sync.aligned tcgen05 instructions and warp syncs that follow.
+__device__ __forceinline__ bool wwait(const Ctx &x, uint32_t b, uint32_t parity) {
+    const bool ok = wait(x, b, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// OR of `pred` over the `n` threads of named barrier `id` (also a barrier).
+__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
+    return tmem + ((uint32_t)((warp & 3) * 32) << 16);
+}
+
+__device__ __forceinline__ void warp_arrive(uint32_t b) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(b);
+}
+
+struct Unit {
+    long long bos, eos;
+    int n, h, hk, v0, nc;
+};
+
+__device__ __forceinline__ Unit unit_of(const Params &p) {
+    Unit u;
+    const int nvt = p.dv / BVT;
+    const int idx = blockIdx.x;
+    const int vt = idx % nvt;
+    u.h = (idx / nvt) % p.Nv;
+    u.n = idx / (nvt * p.Nv);
+    u.hk = u.h / (p.Nv / p.Nk);
+    u.v0 = vt * BVT;
+    if (p.cu) {
+        u.bos = p.cu[u.n];
+        u.eos = p.cu[u.n + 1];
+        if (u.bos < 0 || u.eos < u.bos || u.eos > p.tokens) {
+            if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeq);
+            u.bos = u.eos = 0;
+        }
+    } else {
+        u.bos = (long long)u.n * p.T;
+        u.eos = u.bos + p.T;
+    }
+    u.nc = (int)((u.eos - u.bos + C - 1) / C);
+    return u;
+}
+
+// ---------------------------------------------------------------------------
+// Loader warp: TMA tiles + gate scalars of each chunk.
+// ---------------------------------------------------------------------------
+__device__ void loader_role(const Ctx &x, const Params &p, const Unit &u, const CUtensorMap *mK,
+                            const CUtensorMap *mQ, const CUtensorMap *mV, int &armed_last) {
+    const int lane = threadIdx.x & 31;
+    armed_last = -1;
+    for (int c = 0; c < u.nc; ++c) {
+        const int s = c % NS;
+        if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
+        const long long t0 = u.bos + (long long)c * C;
+        const int L = (int)min((long long)C, u.eos - t0);
+        const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
+        if (lane == 0) {
+            const uint32_t fb = bar(x, B_FULL + s);
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const int tt = (int)t0;
+            tma_load_3d(st + 0, mK, fb, 0, u.hk, tt);
+            tma_load_3d(st + 8192, mQ, fb, 0, u.hk, tt);
+            tma_load_3d(st + 16384, mK, fb, 64, u.hk, tt);
+            tma_load_3d(st + 24576, mQ, fb, 64, u.hk, tt);
+            tma_load_3d(st + 32768, mV, fb, u.v0, u.h, tt);
+            tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
+        }
+        armed_last = c;
+        // gate scalars: lane owns tokens lane and lane + 32 of the chunk
+        float ga = 0.f, gb = 0.f, ba = 0.f, bb = 0.f;
+        if (lane < L) {
+            ba = p.beta[(t0 + lane) * p.Nv + u.h];
+            if (p.g) ga = p.g[(t0 + lane) * p.Nv + u.h];
+        }
+        if (lane + 32 < L) {
+            bb = p.beta[(t0 + lane + 32) * p.Nv + u.h];
+            if (p.g) gb = p.g[(t0 + lane + 32) * p.Nv + u.h];
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float ta = __shfl_up_sync(0xffffffffu, ga, off);
+            const float tb = __shfl_up_sync(0xffffffffu, gb, off);
+            if (lane >= off) { ga += ta; gb += tb; }
+        }
+        gb += __shfl_sync(0xffffffffu, ga, 31);
+        const float GLa = __shfl_sync(0xffffffffu, ga, (L - 1) & 31);
+        const float GLb = __shfl_sync(0xffffffffu, gb, (L - 1) & 31);
+        const float GL = (L - 1) < 32 ? GLa : GLb;
+        // block-start prefix values G_0, G_16, G_32, G_48
+        const float Gb0 = __shfl_sync(0xffffffffu, ga, 0);
+        const float Gb1 = __shfl_sync(0xffffffffu, ga, 16);
+        const float Gb2 = __shfl_sync(0xffffffffu, gb, 0);
+        const float Gb3 = __shfl_sync(0xffffffffu, gb, 16);
+        float *sc = scal(x, s);
+        const int ia = lane, ib = lane + 32;
+        sc[SC_G + ia] = ga;
+        sc[SC_G + ib] = gb;
+        sc[SC_BETA + ia] = ba;
+        sc[SC_BETA + ib] = bb;
+        sc[SC_BEG + ia] = ba * __expf(ga);
+        sc[SC_BEG + ib] = bb * __expf(gb);
+        sc[SC_DEC + ia] = ia < L ? __expf(GL - ga) : 0.f;
+        sc[SC_DEC + ib] = ib < L ? __expf(GL - gb) : 0.f;
+        sc[SC_OSC + ia] = p.scale * __expf(ga);
+        sc[SC_OSC + ib] = p.scale * __expf(gb);
+        sc[SC_F + ia] = __expf(ga - (lane < 16 ? Gb0 : Gb1));
+        sc[SC_F + ib] = __expf(gb - (lane < 16 ? Gb2 : Gb3));
+        // H[blk][j] = e^{G_{16 blk} - G_j} for j <= 16 blk (blk = 1..3)
+        sc[SC_H + 0 * 64 + ia] = ia <= 16 ? __expf(Gb1 - ga) : 0.f;
+        sc[SC_H + 0 * 64 + ib] = 0.f;
+        sc[SC_H + 1 * 64 + ia] = __expf(Gb2 - ga);
+        sc[SC_H + 1 * 64 + ib] = ib <= 32 ? __expf(Gb2 - gb) : 0.f;
+        sc[SC_H + 2 * 64 + ia] = __expf(Gb3 - ga);
+        sc[SC_H + 2 * 64 + ib] = ib <= 48 ? __expf(Gb3 - gb) : 0.f;
+        if (lane == 0) {
+            sc[SC_ALPHA] = __expf(GL);
+            sc[SC_L] = __int_as_float(L);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void issue_kq(const Ctx &x, uint32_t tm, int c) {
+    const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t a = st + kb * 16384 + kk * 32;
+            mma_ss(tm + TM_KQ, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
+        }
+}
+
+__device__ __forceinline__ void issue_w(const Ctx &x, uint32_t tm, int c) {
+    const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tm + TM_W, sdesc(st + kk * 2048, 16384, 1024), sdesc(x.base + OFF_TP + kk * 32, 16, 1024),
+               ID_W, kk != 0);
+}
+
+__device__ __forceinline__ void issue_u(const Ctx &x, uint32_t tm, int c) {
+    const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES + 32768;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tm + TM_V, sdesc(st + kk * 2048, 8192, 1024), sdesc(x.base + OFF_TPP + kk * 32, 16, 1024),
+               ID_U, kk != 0);
+}
+
+__device__ void mma_role(const Ctx &x, const Unit &u, uint32_t tm) {
+    const int nc = u.nc;
+    if (nc == 0) return;
+    // prologue: KQ(0), W(0), U(0)
+    if (!wait(x, bar(x, B_FULL + 0), 0)) goto drain;
+    tc_fence_after();
+    issue_kq(x, tm, 0);
+    mma_commit(bar(x, B_KQ_FULL));
+    if (!wait(x, bar(x, B_T_FULL), 0)) goto drain;
+    tc_fence_after();
+    issue_w(x, tm, 0);
+    mma_commit(bar(x, B_W_FULL));
+    issue_u(x, tm, 0);
+    for (int c = 0; c < nc; ++c) {
+        const int s = c % NS;
+        const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
+        const uint32_t par = c & 1;
+        // [A] v_new^T = U^T + S^T (-W^T)
+        if (!wait(x, bar(x, B_WSM_FULL), par)) goto drain;
+        if (!wait(x, bar(x, B_S_FULL), par)) goto drain;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tm + TM_V, tm + TM_SB + kk * 8, sdesc(x.base + OFF_WT + kk * 2048, 8192, 1024), ID_VN, 1);
+        mma_commit(bar(x, B_V_FULL));
+        // [B] inter-chunk output S^T Q^T
+        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) goto drain;
+        tc_fence_after();
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tm + TM_O, tm + TM_SB + kb * 32 + kk * 8,
+                       sdesc(st + 8192 + kb * 16384 + kk * 32, 16, 1024), ID_O, (kb | kk) != 0);
+        // [C] next chunk's KK^T / QK^T
+        if (c + 1 < nc) {
+            if (!wait(x, bar(x, B_FULL + (c + 1) % NS), ((c + 1) / NS) & 1)) goto drain;
+            if (!wait(x, bar(x, B_KQ_EMPTY), ((c + 1) & 1) ^ 1)) goto drain;
+            tc_fence_after();
+            issue_kq(x, tm, c + 1);
+            mma_commit(bar(x, B_KQ_FULL));
+        }
+        // [D] state update and intra-chunk output
+        if (!wait(x, bar(x, B_VSM_FULL), par)) goto drain;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tm + TM_S, tm + TM_V + 32 + kk * 8, sdesc(st + kk * 2048, 16384, 1024), ID_DS, 1);
+        const uint32_t pbuf = x.base + OFF_P + (c & 1) * 8192;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tm + TM_P, tm + TM_V + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, kk != 0);
+        mma_commit(bar(x, B_D_FULL));
+        mma_commit(bar(x, B_EMPTY + s));
+        // [E] next chunk's W and U
+        if (c + 1 < nc) {
+            if (!wait(x, bar(x, B_T_FULL), (c + 1) & 1)) goto drain;
+            if (!wait(x, bar(x, B_W_EMPTY), ((c + 1) & 1) ^ 1)) goto drain;
+            tc_fence_after();
+            issue_w(x, tm, c + 1);
+            mma_commit(bar(x, B_W_FULL));
+            // U overwrites the v_new operands DS/PV read: wait for them
+            if (!wait(x, bar(x, B_D_FULL), par)) goto drain;
+            tc_fence_after();
+            issue_u(x, tm, c + 1);
+        }
+    }
+drain:
+    // every MMA issued so far completes before tensor memory is released
+    mma_commit(bar(x, B_DRAIN));
+    wait_drain(bar(x, B_DRAIN), 0);
+}
+
+// ---------------------------------------------------------------------------
+// Prep warpgroup: A, P, T = (I - A)^-1, T', T'', W^T operand.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
+// LDA).  128 threads (4 warps).  Diagonal 16 x 16 blocks by forward
+// substitution in fp32; block row r then gets
+//     T[r, <r] = T_rr (A[r, <r] T[<r, <r])
+// with TF32 tensor-core products (m16n8k8) accumulated in fp32.
+__device__ void solve_T(float *sA, float *sX, int pw, int lane) {
+    // ---- diagonal blocks: warp pw inverts block pw ----
+    {
+        const int c = lane & 15, h = lane >> 4, o = 16 * pw;
+        float xv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) xv[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            float part = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m)
+                if ((m & 1) == h) part = fmaf(sA[(o + r) * LDA + o + m], xv[m], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 16);
+            if (r > c) xv[r] = part;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if ((r & 1) == h) sA[(o + r) * LDA + o + c] = xv[r];
+    }
+    named_bar_sync(1, 128);
+    const int g = lane >> 2, t = lane & 3;
+    for (int r = 1; r < 4; ++r) {
+        const int R = 16 * r;
+        // X = A[R:R+16, 0:R] T[0:R, 0:R]  -> sX (16 x R)
+        for (int nt = pw; nt < 2 * r; nt += 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int kt = nt; kt < 2 * r; ++kt) {
+                uint32_t a[4], b[2];
+                a[0] = to_tf32(sA[(R + g) * LDA + 8 * kt + t]);
+                a[1] = to_tf32(sA[(R + g + 8) * LDA + 8 * kt + t]);
+                a[2] = to_tf32(sA[(R + g) * LDA + 8 * kt + t + 4]);
+                a[3] = to_tf32(sA[(R + g + 8) * LDA + 8 * kt + t + 4]);
+                b[0] = to_tf32(sA[(8 * kt + t) * LDA + 8 * nt + g]);
+                b[1] = to_tf32(sA[(8 * kt + t + 4) * LDA + 8 * nt + g]);
+                mma_tf32(acc, a, b);
+            }
+            sX[g * LDX + 8 * nt + 2 * t] = acc[0];
+            sX[g * LDX + 8 * nt + 2 * t + 1] = acc[1];
+            sX[(g + 8) * LDX + 8 * nt + 2 * t] = acc[2];
+            sX[(g + 8) * LDX + 8 * nt + 2 * t + 1] = acc[3];
+        }
+        named_bar_sync(1, 128);
+        // T[R:R+16, 0:R] = T_rr X
+        for (int nt = pw; nt < 2 * r; nt += 4) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                uint32_t a[4], b[2];
+                a[0] = to_tf32(sA[(R + g) * LDA + R + 8 * kt + t]);
+                a[1] = to_tf32(sA[(R + g + 8) * LDA + R + 8 * kt + t]);
+                a[2] = to_tf32(sA[(R + g) * LDA + R + 8 * kt + t + 4]);
+                a[3] = to_tf32(sA[(R + g + 8) * LDA + R + 8 * kt + t + 4]);
+                b[0] = to_tf32(sX[(8 * kt + t) * LDX + 8 * nt + g]);
+                b[1] = to_tf32(sX[(8 * kt + t + 4) * LDX + 8 * nt + g]);
+                mma_tf32(acc, a, b);
+            }
+            sA[(R + g) * LDA + 8 * nt + 2 * t] = acc[0];
+            sA[(R + g) * LDA + 8 * nt + 2 * t + 1] = acc[1];
+            sA[(R + g + 8) * LDA + 8 * nt + 2 * t] = acc[2];
+            sA[(R + g + 8) * LDA + 8 * nt + 2 * t + 1] = acc[3];
+        }
+        named_bar_sync(1, 128);
+    }
+}
+
+__device__ void prep_role(const Ctx &x, const Unit &u, uint32_t tm, float scale) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pw = warp - 2;                  // 0..3: diagonal block of the solve
+    const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
+    float *sA = reinterpret_cast<float *>(x.gbase + OFF_A);
+    float *sX = reinterpret_cast<float *>(x.gbase + OFF_X);
+    const uint32_t lb = lane_base(tm, warp);
+    for (int c = 0; c < u.nc; ++c) {
+        const int s = c % NS;
+        const uint32_t par = c & 1;
+        // A failed wait leaves `ok` false but the chunk body still runs to its
+        // end (on garbage), so all four warps meet every named barrier; the
+        // group then leaves together.
+        bool ok = wwait(x, bar(x, B_KQ_FULL), par);
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lb + TM_KQ, r0);
+        tmem_ld32(lb + TM_KQ + 32, r1);
+        tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive(bar(x, B_KQ_EMPTY));
+        ok = ok && wwait(x, bar(x, B_FULL + s), (c / NS) & 1);
+        const float *sc = scal(x, s);
+        const int i = row & 63;  // row of KK^T (TMEM lanes 0-63) or QK^T (64-127)
+        const int ib = i >> 4;
+        const float Gi = sc[SC_G + i], Fi = sc[SC_F + i];
+        // D_ij = e^{G_i - G_j} (j <= i), per 16-column block jb of the row:
+        // below the row's block through its start b (both factors <= 1),
+        //   D = e^{G_i - G_b} e^{G_b - G_j};
+        // inside the row's block directly; above it zero.
+        const bool rowA = row < 64;  // KK^T rows -> A, QK^T rows -> P
+        const float rs = rowA ? -sc[SC_BETA + i] : scale;
+        const uint32_t pb = x.base + OFF_P + (c & 1) * 8192;
+        float *arow = sA + i * LDA;
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+            float dcy[16];
+            if (jb < ib) {
+                const float *Hrow = sc + SC_H + (ib - 1) * 64 + 16 * jb;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dcy[jj] = Fi * Hrow[jj];
+            } else if (jb == ib) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = 16 * jb + jj;
+                    dcy[jj] = j <= i ? __expf(Gi - sc[SC_G + j]) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dcy[jj] = 0.f;
+            }
+            float val[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+                const int j = 16 * jb + jj;
+                const float kq = __uint_as_float(j < 32 ? r0[j & 31] : r1[j & 31]);
+                // A keeps j < i; P keeps j <= i (dcy is 0 above the diagonal)
+                val[jj] = (rowA && j == i) ? 0.f : rs * dcy[jj] * kq;
+            }
+            if (rowA) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4 *>(arow + 16 * jb + 4 * q4) =
+                        make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3]);
+            } else {
+#pragma unroll
+                for (int h8 = 0; h8 < 2; ++h8)
+                    st_shared_v4(pb + sw128(i, 2 * jb + h8), pack_bf16(val[8 * h8], val[8 * h8 + 1]),
+                                 pack_bf16(val[8 * h8 + 2], val[8 * h8 + 3]),
+                                 pack_bf16(val[8 * h8 + 4], val[8 * h8 + 5]),
+                                 pack_bf16(val[8 * h8 + 6], val[8 * h8 + 7]));
+            }
+        }
+        named_bar_sync(1, 128);
+        solve_T(sA, sX, pw, lane);
+        // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
+        {
+            const float *row = sA + i * LDA;
+            const float *cs = sc + (rowA ? SC_BEG : SC_BETA);
+            const uint32_t dst = x.base + (rowA ? OFF_TP : OFF_TPP);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const float4 a = *reinterpret_cast<const float4 *>(row + 8 * ch);
+                const float4 b = *reinterpret_cast<const float4 *>(row + 8 * ch + 4);
+                const float4 ca = *reinterpret_cast<const float4 *>(cs + 8 * ch);
+                const float4 cb = *reinterpret_cast<const float4 *>(cs + 8 * ch + 4);
+                st_shared_v4(dst + sw128(i, ch), pack_bf16(a.x * ca.x, a.y * ca.y),
+                             pack_bf16(a.z * ca.z, a.w * ca.w), pack_bf16(b.x * cb.x, b.y * cb.y),
+                             pack_bf16(b.z * cb.z, b.w * cb.w));
+            }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(bar(x, B_T_FULL));
+        warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
+        // W^T (lane d) -> -W^T bf16 operand, rows d
+        ok = ok && wwait(x, bar(x, B_W_FULL), par);
+        tc_fence_after();
+        tmem_ld32(lb + TM_W, r0);
+        tmem_ld32(lb + TM_W + 32, r1);
+        tmem_wait_ld();
+        tc_fence_before();
+        warp_arrive(bar(x, B_W_EMPTY));
+        {
+            const int d = row;
+            const uint32_t dst = x.base + OFF_WT;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j0 = 8 * ch + 2 * e;
+                    const float a0 = __uint_as_float(j0 < 32 ? r0[j0 & 31] : r1[j0 & 31]);
+                    const float a1 = __uint_as_float(j0 + 1 < 32 ? r0[(j0 + 1) & 31] : r1[(j0 + 1) & 31]);
+                    w[e] = pack_bf16(-a0, -a1);
+                }
+                st_shared_v4(dst + sw128(d, ch), w[0], w[1], w[2], w[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(bar(x, B_WSM_FULL));
+        if (bar_red_or(1, 128, !ok || *x.abort_flag)) return;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// State warpgroup: v_new operands, fp32 state, ht.
+// ---------------------------------------------------------------------------
+__device__ void state_role(const Ctx &x, const Params &p, const Unit &u, uint32_t tm) {
+    const int warp = threadIdx.x >> 5;
+    const int v = 32 * (warp & 3) + (threadIdx.x & 31);  // value column = TMEM lane
+    const uint32_t lb = lane_base(tm, warp);
+    const size_t sbase = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;
+    uint32_t r[32], pk[16];
+
+    const int dv = p.dv;
+    if (u.nc == 0) {  // empty sequence: ht = h0
+        if (p.ht)
+            for (int d = 0; d < DK; ++d) p.ht[sbase + (size_t)d * dv] = p.h0 ? p.h0[sbase + (size_t)d * dv] : 0.f;
+        return;
+    }
+    // initial state: acc_s = alpha_0 h0^T, SB = bf16(h0^T)
+    if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
+    {
+        const float alpha = scal(x, 0)[SC_ALPHA];
+        for (int blk = 0; blk < 4; ++blk) {
+            float f[32];
+            const float *hp = p.h0 ? p.h0 + sbase + (size_t)(32 * blk) * dv : nullptr;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                f[k] = hp ? *hp : 0.f;
+                if (hp) hp += dv;
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
+            tmem_st16(lb + TM_SB + 16 * blk, pk);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * f[k]);
+            tmem_st32(lb + TM_S + 32 * blk, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(bar(x, B_S_FULL));
+    }
+    for (int c = 0; c < u.nc; ++c) {
+        const int s = c % NS;
+        const uint32_t par = c & 1;
+        // ---- v_new^T and v~^T operands --------------------------------
+        if (!wwait(x, bar(x, B_V_FULL), par)) return;
+        tc_fence_after();
+        {
+            // acc_v columns j = 0..63 (fp32) become v_new^T packed in columns
+            // 0..31 and v~^T packed in columns 32..63; a column is rewritten
+            // only after it has been read.
+            const float *dec = scal(x, s) + SC_DEC;
+            uint32_t ta[16];
+            tmem_ld32(lb + TM_V, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float a0 = __uint_as_float(r[2 * k]), a1 = __uint_as_float(r[2 * k + 1]);
+                pk[k] = pack_bf16(a0, a1);
+                ta[k] = pack_bf16(a0 * dec[2 * k], a1 * dec[2 * k + 1]);
+            }
+            tmem_st16(lb + TM_V, pk);  // columns 0..31 are read already
+            tmem_ld32(lb + TM_V + 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+            tmem_st16(lb + TM_V + 16, pk);
+            tmem_st16(lb + TM_V + 32, ta);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = pack_bf16(__uint_as_float(r[2 * k]) * dec[32 + 2 * k],
+                                  __uint_as_float(r[2 * k + 1]) * dec[32 + 2 * k + 1]);
+            tmem_st16(lb + TM_V + 48, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(bar(x, B_VSM_FULL));
+            warp_arrive(bar(x, B_EMPTY + s));
+        }
+        // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
+        if (!wwait(x, bar(x, B_D_FULL), par)) return;
+        tc_fence_after();
+        const bool last = (c + 1 == u.nc);
+        for (int blk = 0; blk < 4; ++blk) {
+            tmem_ld32(lb + TM_S + 32 * blk, r);
+            tmem_wait_ld();
+            if (!last) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+                tmem_st16(lb + TM_SB + 16 * blk, pk);
+            } else if (p.ht) {
+                float *hp = p.ht + sbase + (size_t)(32 * blk) * dv;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    *hp = __uint_as_float(r[k]);
+                    hp += dv;
+                }
+            }
+        }
+        if (last) break;
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(bar(x, B_S_FULL));
+        const int s1 = (c + 1) % NS;
+        if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
+        const float alpha = scal(x, s1)[SC_ALPHA];
+        for (int blk = 0; blk < 4; ++blk) {
+            tmem_ld32(lb + TM_S + 32 * blk, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * __uint_as_float(r[k]));
+            tmem_st32(lb + TM_S + 32 * blk, r);
+        }
+        tmem_wait_st();  // ordered before the next v~ arrive (fence there)
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Output warpgroup: o = scale e^{G_i} (S^T Q^T)[v][i] + (v_new^T P^T)[v][i].
+// ---------------------------------------------------------------------------
+__device__ void output_role(const Ctx &x, const Params &p, const Unit &u, uint32_t tm) {
+    const int warp = threadIdx.x >> 5;
+    const int v = 32 * (warp & 3) + (threadIdx.x & 31);  // value column = TMEM lane
+    const uint32_t lb = lane_base(tm, warp);
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    for (int c = 0; c < u.nc; ++c) {
+        const int s = c % NS;
+        const uint32_t par = c & 1;
+        if (!wwait(x, bar(x, B_D_FULL), par)) return;
+        if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return;
+        tc_fence_after();
+        const float *sc = scal(x, s);
+        const int L = __float_as_int(sc[SC_L]);
+        const long long t0 = u.bos + (long long)c * C;
+        __nv_bfloat16 *op = o + (t0 * p.Nv + u.h) * (long long)p.dv + u.v0 + v;
+        const long long rs = (long long)p.Nv * p.dv;
+        uint32_t ra[32], qa[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tmem_ld32(lb + TM_O + 32 * half, ra);
+            tmem_ld32(lb + TM_P + 32 * half, qa);
+            tmem_wait_ld();
+            if (half == 1) {
+                tc_fence_before();
+                warp_arrive(bar(x, B_O_EMPTY));
+            }
+            __nv_bfloat16 *po = op + 32 * half * rs;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int i = 32 * half + k;
+                if (i < L)
+                    *po = __float2bfloat16_rn(fmaf(sc[SC_OSC + i], __uint_as_float(ra[k]), __uint_as_float(qa[k])));
+                po += rs;
+            }
+        }
+        warp_arrive(bar(x, B_EMPTY + s));
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
+       const __grid_constant__ CUtensorMap mV, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    Ctx x;
+    x.base = (raw + 1023u) & ~1023u;
+    x.gbase = smem_raw + (x.base - raw);
+    x.abort_flag = reinterpret_cast<volatile int *>(x.gbase + OFF_MISC + 4);
+    x.status = p.status;
+    const int warp = threadIdx.x >> 5;
+    const Unit u = unit_of(p);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar(x, B_FULL + s), 2);
+            mbar_init(bar(x, B_EMPTY + s), 13);
+        }
+        mbar_init(bar(x, B_KQ_FULL), 1);
+        mbar_init(bar(x, B_KQ_EMPTY), 4);
+        mbar_init(bar(x, B_T_FULL), 4);
+        mbar_init(bar(x, B_W_FULL), 1);
+        mbar_init(bar(x, B_W_EMPTY), 4);
+        mbar_init(bar(x, B_WSM_FULL), 4);
+        mbar_init(bar(x, B_S_FULL), 4);
+        mbar_init(bar(x, B_V_FULL), 1);
+        mbar_init(bar(x, B_VSM_FULL), 4);
+        mbar_init(bar(x, B_D_FULL), 1);
+        mbar_init(bar(x, B_O_EMPTY), 4);
+        mbar_init(bar(x, B_DRAIN), 1);
+        *x.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(x.base + OFF_MISC, TM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && (threadIdx.x & 31) == 0) {
+        prefetch_tmap(&mK);
+        prefetch_tmap(&mQ);
+        prefetch_tmap(&mV);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *reinterpret_cast<volatile uint32_t *>(x.gbase + OFF_MISC);
+
+    if (warp == 0) {
+        int armed_last = -1;
+        loader_role(x, p, u, &mK, &mQ, &mV, armed_last);
+        // drain: the last NS armed stages must have landed before exit
+        if ((threadIdx.x & 31) == 0)
+            for (int c = armed_last - NS + 1; c <= armed_last; ++c)
+                if (c >= 0) wait_drain(bar(x, B_FULL + c % NS), (c / NS) & 1);
+        __syncwarp();
+    } else if (warp == 1) {
+        if ((threadIdx.x & 31) == 0) mma_role(x, u, tm);
+        __syncwarp();
+    } else if (warp < 6) {
+        prep_role(x, u, tm, p.scale);
+    } else if (warp < 10) {
+        state_role(x, p, u, tm);
+    } else {
+        output_role(x, p, u, tm);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tm, TM_COLS);
+}
+
+}  // namespace
+
+bool tc_supported(int dk, int dv, bool bf16) { return bf16 && dk == DK && dv % BVT == 0; }
+
+cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
+    CUtensorMap mK, mQ, mV;
+    const uint64_t tokens = (uint64_t)p.tokens;
+    if (!make_tmap_rows_heads_d(&mK, p.k, tokens, p.Nk, DK, 64, C) ||
+        !make_tmap_rows_heads_d(&mQ, p.q, tokens, p.Nk, DK, 64, C) ||
+        !make_tmap_rows_heads_d(&mV, p.v, tokens, p.Nv, p.dv, 64, C))
+        return cudaErrorInvalidValue;
+    const long long grid = (long long)p.N * p.Nv * (p.dv / BVT);
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    if (err != cudaSuccess) return err;
+    tc_fwd<<<(unsigned)grid, NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);
+    *name = "tc_fwd";
+    return cudaGetLastError();
+}
+
+}  // namespace dn
