@@ -21,11 +21,13 @@
 // group of four consecutive warps covers all 128 lanes):
 //   0      loader: TMA for the K, Q, V tiles of a chunk and the gate scalars
 //          (prefix sum G, e^G, decays) computed with warp shuffles;
-//   1      MMA issuer (one thread) and TMEM owner;
+//   1      chain MMA issuer (one thread: VN, O, DS, PV) and TMEM owner;
 //   2-5    prep: A and P from KK^T / QK^T, T = (I - A)^-1 (16x16 diagonal
 //          blocks by forward substitution, then block rows with TF32 mma.sync),
-//          T' and T'', then W^T from TMEM to a bf16 operand.  Runs up to one
-//          chunk ahead of the state scan;
+//          T' and T'', then W^T from TMEM to a bf16 operand.  One of its
+//          threads issues the prep MMAs (KQ of the next chunk as soon as this
+//          chunk's is read, W and U once T is ready), so the prep runs ahead
+//          of the state scan;
 //   6-9    state: v_new and v~ operands, the fp32 state update, ht;
 //   10-13  output: o = scale e^{G} (S^T Q^T) + P v_new, stored as bf16.
 //
@@ -40,6 +42,24 @@
 #include "dn_tc.h"
 #include "dn_tmap.h"
 #include "tc_ptx.cuh"
+
+// Optional per-chunk event trace of CTA 0 (SM clock), compiled in only with
+// -DDN_TRACE for profiling builds; the default build contains no trace code.
+#ifdef DN_TRACE
+__device__ unsigned long long g_dn_trace[14][1024][16];
+#define DN_TRACE_EV(ev, c)                                                    \
+    do {                                                                      \
+        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (c) < 1024)         \
+            g_dn_trace[threadIdx.x >> 5][(c)][(ev)] = clock64();              \
+    } while (0)
+extern "C" __attribute__((visibility("default"))) int dn_trace_dump(void *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_dn_trace, sizeof(g_dn_trace));
+}
+#else
+#define DN_TRACE_EV(ev, c) \
+    do {                   \
+    } while (0)
+#endif
 
 namespace dn {
 namespace {
@@ -84,18 +104,16 @@ constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, 
 enum {
     B_FULL = 0,                 // NS: TMA bytes + loader scalars
     B_EMPTY = B_FULL + NS,      // NS: every reader of the stage is done
-    B_KQ_FULL = B_EMPTY + NS,
-    B_KQ_EMPTY,
-    B_T_FULL,
-    B_W_FULL,
-    B_W_EMPTY,
-    B_WSM_FULL,
+    B_KQ_FULL = B_EMPTY + NS,   // KK^T / QK^T of a chunk in acc_kq
+    B_WU_FULL,                  // W^T in acc_w and U^T in acc_v
+    B_WSM_FULL,                 // -W^T bf16 operand in shared memory
     B_S_FULL,
     B_V_FULL,
     B_VSM_FULL,
     B_D_FULL,
     B_O_EMPTY,
     B_DRAIN,
+    B_DRAIN2,
     B_COUNT
 };
 static_assert(B_COUNT <= NBARS, "barrier space");
@@ -129,7 +147,11 @@ __device__ __forceinline__ float *scal(const Ctx &x, int s) {
 __device__ __noinline__ bool wait_slow(const Ctx &x, uint32_t b, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
+#ifdef DN_WAIT_HINT
+        if (mbar_try_wait_sleep(b, parity, DN_WAIT_HINT)) return true;
+#else
         if (mbar_try_wait(b, parity)) return true;
+#endif
         if ((it & 31u) == 0) {
             if (*x.abort_flag) return false;
             if (globaltimer() - t0 > kTimeoutNs) {
@@ -215,13 +237,14 @@ __device__ __forceinline__ Unit unit_of(const Params &p) {
 // ---------------------------------------------------------------------------
 // Loader warp: TMA tiles + gate scalars of each chunk.
 // ---------------------------------------------------------------------------
-__device__ void loader_role(const Ctx &x, const Params &p, const Unit &u, const CUtensorMap *mK,
+__device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
                             const CUtensorMap *mQ, const CUtensorMap *mV, int &armed_last) {
     const int lane = threadIdx.x & 31;
     armed_last = -1;
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
+        DN_TRACE_EV(0, c);
         const long long t0 = u.bos + (long long)c * C;
         const int L = (int)min((long long)C, u.eos - t0);
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
@@ -289,11 +312,12 @@ __device__ void loader_role(const Ctx &x, const Params &p, const Unit &u, const 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
+        DN_TRACE_EV(1, c);
     }
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread).
+// MMA issue helpers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void issue_kq(const Ctx &x, uint32_t tm, int c) {
     const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
@@ -322,33 +346,25 @@ __device__ __forceinline__ void issue_u(const Ctx &x, uint32_t tm, int c) {
                ID_U, kk != 0);
 }
 
-__device__ void mma_role(const Ctx &x, const Unit &u, uint32_t tm) {
-    const int nc = u.nc;
-    if (nc == 0) return;
-    // prologue: KQ(0), W(0), U(0)
-    if (!wait(x, bar(x, B_FULL + 0), 0)) goto drain;
-    tc_fence_after();
-    issue_kq(x, tm, 0);
-    mma_commit(bar(x, B_KQ_FULL));
-    if (!wait(x, bar(x, B_T_FULL), 0)) goto drain;
-    tc_fence_after();
-    issue_w(x, tm, 0);
-    mma_commit(bar(x, B_W_FULL));
-    issue_u(x, tm, 0);
-    for (int c = 0; c < nc; ++c) {
+// ---------------------------------------------------------------------------
+// Chain MMA issuer (one thread): the state-dependent contractions only.
+// ---------------------------------------------------------------------------
+__device__ void mma_role(const Ctx x, const Unit u, uint32_t tm) {
+    for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         const uint32_t par = c & 1;
-        // [A] v_new^T = U^T + S^T (-W^T)
-        if (!wait(x, bar(x, B_WSM_FULL), par)) goto drain;
-        if (!wait(x, bar(x, B_S_FULL), par)) goto drain;
+        // v_new^T = U^T + S^T (-W^T)   (U^T was written into acc_v by the prep)
+        if (!wait(x, bar(x, B_WSM_FULL), par)) break;
+        if (!wait(x, bar(x, B_S_FULL), par)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_ts(tm + TM_V, tm + TM_SB + kk * 8, sdesc(x.base + OFF_WT + kk * 2048, 8192, 1024), ID_VN, 1);
         mma_commit(bar(x, B_V_FULL));
-        // [B] inter-chunk output S^T Q^T
-        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) goto drain;
+        DN_TRACE_EV(0, c);
+        // inter-chunk output S^T Q^T
+        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) break;
         tc_fence_after();
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
@@ -356,16 +372,8 @@ __device__ void mma_role(const Ctx &x, const Unit &u, uint32_t tm) {
             for (int kk = 0; kk < 4; ++kk)
                 mma_ts(tm + TM_O, tm + TM_SB + kb * 32 + kk * 8,
                        sdesc(st + 8192 + kb * 16384 + kk * 32, 16, 1024), ID_O, (kb | kk) != 0);
-        // [C] next chunk's KK^T / QK^T
-        if (c + 1 < nc) {
-            if (!wait(x, bar(x, B_FULL + (c + 1) % NS), ((c + 1) / NS) & 1)) goto drain;
-            if (!wait(x, bar(x, B_KQ_EMPTY), ((c + 1) & 1) ^ 1)) goto drain;
-            tc_fence_after();
-            issue_kq(x, tm, c + 1);
-            mma_commit(bar(x, B_KQ_FULL));
-        }
-        // [D] state update and intra-chunk output
-        if (!wait(x, bar(x, B_VSM_FULL), par)) goto drain;
+        // state update and intra-chunk output
+        if (!wait(x, bar(x, B_VSM_FULL), par)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -376,27 +384,16 @@ __device__ void mma_role(const Ctx &x, const Unit &u, uint32_t tm) {
             mma_ts(tm + TM_P, tm + TM_V + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, kk != 0);
         mma_commit(bar(x, B_D_FULL));
         mma_commit(bar(x, B_EMPTY + s));
-        // [E] next chunk's W and U
-        if (c + 1 < nc) {
-            if (!wait(x, bar(x, B_T_FULL), (c + 1) & 1)) goto drain;
-            if (!wait(x, bar(x, B_W_EMPTY), ((c + 1) & 1) ^ 1)) goto drain;
-            tc_fence_after();
-            issue_w(x, tm, c + 1);
-            mma_commit(bar(x, B_W_FULL));
-            // U overwrites the v_new operands DS/PV read: wait for them
-            if (!wait(x, bar(x, B_D_FULL), par)) goto drain;
-            tc_fence_after();
-            issue_u(x, tm, c + 1);
-        }
+        DN_TRACE_EV(3, c);
     }
-drain:
-    // every MMA issued so far completes before tensor memory is released
+    // every MMA issued by this thread completes before tensor memory is freed
     mma_commit(bar(x, B_DRAIN));
     wait_drain(bar(x, B_DRAIN), 0);
 }
 
 // ---------------------------------------------------------------------------
-// Prep warpgroup: A, P, T = (I - A)^-1, T', T'', W^T operand.
+// Prep warpgroup: A, P, T = (I - A)^-1, T', T'', and the prep MMAs (KQ of the
+// next chunk, W and U of this one), so the prep runs ahead of the state scan.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t to_tf32(float f) {
     uint32_t r;
@@ -412,124 +409,178 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
-// LDA).  128 threads (4 warps).  Diagonal 16 x 16 blocks by forward
-// substitution in fp32; block row r then gets
-//     T[r, <r] = T_rr (A[r, <r] T[<r, <r])
-// with TF32 tensor-core products (m16n8k8) accumulated in fp32.
-__device__ void solve_T(float *sA, float *sX, int pw, int lane) {
-    // ---- diagonal blocks: warp pw inverts block pw ----
-    {
-        const int c = lane & 15, h = lane >> 4, o = 16 * pw;
-        float xv[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) xv[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            float part = 0.f;
-#pragma unroll
-            for (int m = 0; m < r; ++m)
-                if ((m & 1) == h) part = fmaf(sA[(o + r) * LDA + o + m], xv[m], part);
-            part += __shfl_xor_sync(0xffffffffu, part, 16);
-            if (r > c) xv[r] = part;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if ((r & 1) == h) sA[(o + r) * LDA + o + c] = xv[r];
-    }
-    named_bar_sync(1, 128);
-    const int g = lane >> 2, t = lane & 3;
-    for (int r = 1; r < 4; ++r) {
-        const int R = 16 * r;
-        // X = A[R:R+16, 0:R] T[0:R, 0:R]  -> sX (16 x R)
-        for (int nt = pw; nt < 2 * r; nt += 4) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int kt = nt; kt < 2 * r; ++kt) {
-                uint32_t a[4], b[2];
-                a[0] = to_tf32(sA[(R + g) * LDA + 8 * kt + t]);
-                a[1] = to_tf32(sA[(R + g + 8) * LDA + 8 * kt + t]);
-                a[2] = to_tf32(sA[(R + g) * LDA + 8 * kt + t + 4]);
-                a[3] = to_tf32(sA[(R + g + 8) * LDA + 8 * kt + t + 4]);
-                b[0] = to_tf32(sA[(8 * kt + t) * LDA + 8 * nt + g]);
-                b[1] = to_tf32(sA[(8 * kt + t + 4) * LDA + 8 * nt + g]);
-                mma_tf32(acc, a, b);
-            }
-            sX[g * LDX + 8 * nt + 2 * t] = acc[0];
-            sX[g * LDX + 8 * nt + 2 * t + 1] = acc[1];
-            sX[(g + 8) * LDX + 8 * nt + 2 * t] = acc[2];
-            sX[(g + 8) * LDX + 8 * nt + 2 * t + 1] = acc[3];
-        }
-        named_bar_sync(1, 128);
-        // T[R:R+16, 0:R] = T_rr X
-        for (int nt = pw; nt < 2 * r; nt += 4) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                uint32_t a[4], b[2];
-                a[0] = to_tf32(sA[(R + g) * LDA + R + 8 * kt + t]);
-                a[1] = to_tf32(sA[(R + g + 8) * LDA + R + 8 * kt + t]);
-                a[2] = to_tf32(sA[(R + g) * LDA + R + 8 * kt + t + 4]);
-                a[3] = to_tf32(sA[(R + g + 8) * LDA + R + 8 * kt + t + 4]);
-                b[0] = to_tf32(sX[(8 * kt + t) * LDX + 8 * nt + g]);
-                b[1] = to_tf32(sX[(8 * kt + t + 4) * LDX + 8 * nt + g]);
-                mma_tf32(acc, a, b);
-            }
-            sA[(R + g) * LDA + 8 * nt + 2 * t] = acc[0];
-            sA[(R + g) * LDA + 8 * nt + 2 * t + 1] = acc[1];
-            sA[(R + g + 8) * LDA + 8 * nt + 2 * t] = acc[2];
-            sA[(R + g + 8) * LDA + 8 * nt + 2 * t + 1] = acc[3];
-        }
-        named_bar_sync(1, 128);
-    }
+// 16 x 8 A fragment (rows R.., cols K..) of a row-major fp32 matrix, as TF32.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *m, int ld, int R, int K, int g, int t) {
+    a[0] = to_tf32(m[(R + g) * ld + K + t]);
+    a[1] = to_tf32(m[(R + g + 8) * ld + K + t]);
+    a[2] = to_tf32(m[(R + g) * ld + K + t + 4]);
+    a[3] = to_tf32(m[(R + g + 8) * ld + K + t + 4]);
 }
 
-__device__ void prep_role(const Ctx &x, const Unit &u, uint32_t tm, float scale) {
+// 8 x 8 B fragment (rows K.., cols N..) of a row-major fp32 matrix, as TF32.
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *m, int ld, int K, int N, int g, int t) {
+    b[0] = to_tf32(m[(K + t) * ld + N + g]);
+    b[1] = to_tf32(m[(K + t + 4) * ld + N + g]);
+}
+
+// Block row r of T (rows 16r..16r+15, columns 0..16r-1), with the diagonal
+// blocks and block rows above already in place:
+//     X = A[16r:, :16r] T[:16r, :16r],   T[16r:, :16r] = T_rr X.
+// Warp pw owns the 8-column tiles nt = pw, pw + 4 (< 2r).  Two accumulators
+// split the k chain in half.
+template <int r>
+__device__ __forceinline__ void solve_block_row(float *sA, float *sX, int pw, int g, int t) {
+    constexpr int R = 16 * r;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int nt = pw + 4 * q;
+        if (nt < 2 * r) {
+            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kt = 0; kt < 2 * r; ++kt) {
+                if (kt >= nt) {  // T is lower triangular: rows < 8 nt of column tile nt vanish
+                    uint32_t a[4], b[2];
+                    frag_a(a, sA, LDA, R, 8 * kt, g, t);
+                    frag_b(b, sA, LDA, 8 * kt, 8 * nt, g, t);
+                    if (kt & 1) mma_tf32(acc1, a, b);
+                    else mma_tf32(acc0, a, b);
+                }
+            }
+            sX[g * LDX + 8 * nt + 2 * t] = acc0[0] + acc1[0];
+            sX[g * LDX + 8 * nt + 2 * t + 1] = acc0[1] + acc1[1];
+            sX[(g + 8) * LDX + 8 * nt + 2 * t] = acc0[2] + acc1[2];
+            sX[(g + 8) * LDX + 8 * nt + 2 * t + 1] = acc0[3] + acc1[3];
+        }
+    }
+    named_bar_sync(1, 128);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int nt = pw + 4 * q;
+        if (nt < 2 * r) {
+            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t a[4], b[2];
+            frag_a(a, sA, LDA, R, R, g, t);
+            frag_b(b, sX, LDX, 0, 8 * nt, g, t);
+            mma_tf32(acc0, a, b);
+            frag_a(a, sA, LDA, R, R + 8, g, t);
+            frag_b(b, sX, LDX, 8, 8 * nt, g, t);
+            mma_tf32(acc1, a, b);
+            sA[(R + g) * LDA + 8 * nt + 2 * t] = acc0[0] + acc1[0];
+            sA[(R + g) * LDA + 8 * nt + 2 * t + 1] = acc0[1] + acc1[1];
+            sA[(R + g + 8) * LDA + 8 * nt + 2 * t] = acc0[2] + acc1[2];
+            sA[(R + g + 8) * LDA + 8 * nt + 2 * t + 1] = acc0[3] + acc1[3];
+        }
+    }
+    named_bar_sync(1, 128);
+}
+
+// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA.  128
+// threads.  The 16 x 16 diagonal blocks are inverted by forward substitution
+// in fp32 (warp pw owns block pw, lane l the column l % 16); the block rows
+// below follow with TF32 tensor-core products accumulated in fp32.
+__device__ void solve_T(float *sA, float *sX, int pw, int lane, int c) {
+    {
+        const int col = lane & 15, o = 16 * pw;
+        float xv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) xv[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
+            // x_r = sum_{m < r} A[r][m] x_m  (x_m = 0 for m < col)
+            const float *ar = sA + (o + r) * LDA + o;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) {
+                if (m & 1) s1 = fmaf(ar[m], xv[m], s1);
+                else s0 = fmaf(ar[m], xv[m], s0);
+            }
+            xv[r] = (r > col) ? s0 + s1 : xv[r];
+        }
+        __syncwarp();
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sA[(o + r) * LDA + o + col] = xv[r];
+        }
+    }
+    named_bar_sync(1, 128);
+    DN_TRACE_EV(3, c);
+    const int g = lane >> 2, t = lane & 3;
+    solve_block_row<1>(sA, sX, pw, g, t);
+    DN_TRACE_EV(14, c);
+    solve_block_row<2>(sA, sX, pw, g, t);
+    DN_TRACE_EV(15, c);
+    solve_block_row<3>(sA, sX, pw, g, t);
+}
+
+__device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pw = warp - 2;                  // 0..3: diagonal block of the solve
     const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
+    const bool leader = (pw == 0 && lane == 0);
     float *sA = reinterpret_cast<float *>(x.gbase + OFF_A);
     float *sX = reinterpret_cast<float *>(x.gbase + OFF_X);
     const uint32_t lb = lane_base(tm, warp);
+    const int i = row & 63;       // row of KK^T (TMEM lanes 0-63) or QK^T (64-127)
+    const bool rowA = row < 64;   // KK^T rows -> A (j < i), QK^T rows -> P (j <= i)
+    const int ib = i >> 4;
+    const int jmax = rowA ? i - 1 : i;
+    bool ok = true;
+    if (u.nc > 0 && leader) {
+        ok = wait(x, bar(x, B_FULL + 0), 0);
+        tc_fence_after();
+        issue_kq(x, tm, 0);
+        mma_commit(bar(x, B_KQ_FULL));
+    }
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const uint32_t par = c & 1;
         // A failed wait leaves `ok` false but the chunk body still runs to its
         // end (on garbage), so all four warps meet every named barrier; the
         // group then leaves together.
-        bool ok = wwait(x, bar(x, B_KQ_FULL), par);
+        ok = ok && wwait(x, bar(x, B_KQ_FULL), par);
+        DN_TRACE_EV(0, c);
         tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(lb + TM_KQ, r0);
-        tmem_ld32(lb + TM_KQ + 32, r1);
-        tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(bar(x, B_KQ_EMPTY));
+        uint32_t r0[32];
+        DN_TRACE_EV(8, c);
         ok = ok && wwait(x, bar(x, B_FULL + s), (c / NS) & 1);
+        DN_TRACE_EV(9, c);
         const float *sc = scal(x, s);
-        const int i = row & 63;  // row of KK^T (TMEM lanes 0-63) or QK^T (64-127)
-        const int ib = i >> 4;
         const float Gi = sc[SC_G + i], Fi = sc[SC_F + i];
-        // D_ij = e^{G_i - G_j} (j <= i), per 16-column block jb of the row:
-        // below the row's block through its start b (both factors <= 1),
-        //   D = e^{G_i - G_b} e^{G_b - G_j};
-        // inside the row's block directly; above it zero.
-        const bool rowA = row < 64;  // KK^T rows -> A, QK^T rows -> P
         const float rs = rowA ? -sc[SC_BETA + i] : scale;
         const uint32_t pb = x.base + OFF_P + (c & 1) * 8192;
         float *arow = sA + i * LDA;
+        // D_ij = e^{G_i - G_j} per 16-column block jb of the row: below the
+        // row's block through its start b (D = e^{G_i - G_b} e^{G_b - G_j},
+        // both factors <= 1); inside it directly (masked to j <= jmax);
+        // above it zero.
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
+            if ((jb & 1) == 0) {  // columns 32 (jb/2) .. +31 of this row
+                tmem_ld32(lb + TM_KQ + 16 * jb, r0);
+                tmem_wait_ld_dep(r0);
+            }
             float dcy[16];
             if (jb < ib) {
-                const float *Hrow = sc + SC_H + (ib - 1) * 64 + 16 * jb;
+                const float4 *h4 = reinterpret_cast<const float4 *>(sc + SC_H + (ib - 1) * 64 + 16 * jb);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) dcy[jj] = Fi * Hrow[jj];
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 h = h4[q4];
+                    dcy[4 * q4] = Fi * h.x;
+                    dcy[4 * q4 + 1] = Fi * h.y;
+                    dcy[4 * q4 + 2] = Fi * h.z;
+                    dcy[4 * q4 + 3] = Fi * h.w;
+                }
             } else if (jb == ib) {
+                const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 16 * jb);
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = 16 * jb + jj;
-                    dcy[jj] = j <= i ? __expf(Gi - sc[SC_G + j]) : 0.f;
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 gg = g4[q4];
+                    const float gv[4] = {gg.x, gg.y, gg.z, gg.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 16 * jb + 4 * q4 + e;
+                        dcy[4 * q4 + e] = __expf(j <= jmax ? Gi - gv[e] : -INFINITY);
+                    }
                 }
             } else {
 #pragma unroll
@@ -539,9 +590,7 @@ __device__ void prep_role(const Ctx &x, const Unit &u, uint32_t tm, float scale)
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const int j = 16 * jb + jj;
-                const float kq = __uint_as_float(j < 32 ? r0[j & 31] : r1[j & 31]);
-                // A keeps j < i; P keeps j <= i (dcy is 0 above the diagonal)
-                val[jj] = (rowA && j == i) ? 0.f : rs * dcy[jj] * kq;
+                val[jj] = rs * dcy[jj] * __uint_as_float(r0[j & 31]);
             }
             if (rowA) {
 #pragma unroll
@@ -556,69 +605,103 @@ __device__ void prep_role(const Ctx &x, const Unit &u, uint32_t tm, float scale)
                                  pack_bf16(val[8 * h8 + 4], val[8 * h8 + 5]),
                                  pack_bf16(val[8 * h8 + 6], val[8 * h8 + 7]));
             }
+            DN_TRACE_EV(10 + jb, c);
         }
+        DN_TRACE_EV(1, c);
+        // acc_kq is read by all four warps: the next chunk's KK^T/QK^T may go
+        tc_fence_before();
         named_bar_sync(1, 128);
-        solve_T(sA, sX, pw, lane);
-        // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
+        tc_fence_after();
+        DN_TRACE_EV(2, c);
+        if (leader && c + 1 < u.nc) {
+            ok = ok && wait(x, bar(x, B_FULL + (c + 1) % NS), ((c + 1) / NS) & 1);
+            tc_fence_after();
+            issue_kq(x, tm, c + 1);
+            mma_commit(bar(x, B_KQ_FULL));
+        }
+        solve_T(sA, sX, pw, lane, c);
+        DN_TRACE_EV(4, c);
+        // T' = T diag(beta e^G) (KK^T-row threads), T'' = T diag(beta) (others)
         {
-            const float *row = sA + i * LDA;
+            const float *trow = sA + i * LDA;
             const float *cs = sc + (rowA ? SC_BEG : SC_BETA);
             const uint32_t dst = x.base + (rowA ? OFF_TP : OFF_TPP);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const float4 a = *reinterpret_cast<const float4 *>(row + 8 * ch);
-                const float4 b = *reinterpret_cast<const float4 *>(row + 8 * ch + 4);
-                const float4 ca = *reinterpret_cast<const float4 *>(cs + 8 * ch);
-                const float4 cb = *reinterpret_cast<const float4 *>(cs + 8 * ch + 4);
-                st_shared_v4(dst + sw128(i, ch), pack_bf16(a.x * ca.x, a.y * ca.y),
-                             pack_bf16(a.z * ca.z, a.w * ca.w), pack_bf16(b.x * cb.x, b.y * cb.y),
-                             pack_bf16(b.z * cb.z, b.w * cb.w));
+            for (int hf = 0; hf < 2; ++hf) {
+                float tv[32];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(trow + 32 * hf + 4 * q4);
+                    const float4 cc = *reinterpret_cast<const float4 *>(cs + 32 * hf + 4 * q4);
+                    tv[4 * q4] = a.x * cc.x;
+                    tv[4 * q4 + 1] = a.y * cc.y;
+                    tv[4 * q4 + 2] = a.z * cc.z;
+                    tv[4 * q4 + 3] = a.w * cc.w;
+                }
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    st_shared_v4(dst + sw128(i, 4 * hf + ch), pack_bf16(tv[8 * ch], tv[8 * ch + 1]),
+                                 pack_bf16(tv[8 * ch + 2], tv[8 * ch + 3]),
+                                 pack_bf16(tv[8 * ch + 4], tv[8 * ch + 5]),
+                                 pack_bf16(tv[8 * ch + 6], tv[8 * ch + 7]));
             }
         }
         fence_proxy_async_smem();
-        warp_arrive(bar(x, B_T_FULL));
+        named_bar_sync(1, 128);
+        DN_TRACE_EV(5, c);
+        // W^T and U^T of this chunk.  U^T overwrites acc_v, whose previous
+        // contents (the chunk before's v_new operands) the chain MMAs read:
+        // wait for them.
+        if (leader) {
+            if (c > 0) ok = ok && wait(x, bar(x, B_D_FULL), (c - 1) & 1);
+            tc_fence_after();
+            issue_w(x, tm, c);
+            issue_u(x, tm, c);
+            mma_commit(bar(x, B_WU_FULL));
+        }
         warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
-        // W^T (lane d) -> -W^T bf16 operand, rows d
-        ok = ok && wwait(x, bar(x, B_W_FULL), par);
+        ok = ok && wwait(x, bar(x, B_WU_FULL), par);
+        DN_TRACE_EV(6, c);
         tc_fence_after();
-        tmem_ld32(lb + TM_W, r0);
-        tmem_ld32(lb + TM_W + 32, r1);
-        tmem_wait_ld();
-        tc_fence_before();
-        warp_arrive(bar(x, B_W_EMPTY));
         {
-            const int d = row;
+            // -W^T bf16 operand, row d = this thread's TMEM lane
             const uint32_t dst = x.base + OFF_WT;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t w[4];
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32(lb + TM_W + 32 * hf, r0);
+                tmem_wait_ld_dep(r0);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j0 = 8 * ch + 2 * e;
-                    const float a0 = __uint_as_float(j0 < 32 ? r0[j0 & 31] : r1[j0 & 31]);
-                    const float a1 = __uint_as_float(j0 + 1 < 32 ? r0[(j0 + 1) & 31] : r1[(j0 + 1) & 31]);
-                    w[e] = pack_bf16(-a0, -a1);
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack_bf16(-__uint_as_float(r0[8 * ch + 2 * e]), -__uint_as_float(r0[8 * ch + 2 * e + 1]));
+                    st_shared_v4(dst + sw128(row, 4 * hf + ch), w[0], w[1], w[2], w[3]);
                 }
-                st_shared_v4(dst + sw128(d, ch), w[0], w[1], w[2], w[3]);
             }
         }
         fence_proxy_async_smem();
         warp_arrive(bar(x, B_WSM_FULL));
-        if (bar_red_or(1, 128, !ok || *x.abort_flag)) return;
+        DN_TRACE_EV(7, c);
+        if (bar_red_or(1, 128, !ok || *x.abort_flag)) break;
+    }
+    if (leader) {  // prep MMAs complete before tensor memory is freed
+        mma_commit(bar(x, B_DRAIN2));
+        wait_drain(bar(x, B_DRAIN2), 0);
     }
 }
 
 // ---------------------------------------------------------------------------
 // State warpgroup: v_new operands, fp32 state, ht.
 // ---------------------------------------------------------------------------
-__device__ void state_role(const Ctx &x, const Params &p, const Unit &u, uint32_t tm) {
+__device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
     const int v = 32 * (warp & 3) + (threadIdx.x & 31);  // value column = TMEM lane
     const uint32_t lb = lane_base(tm, warp);
     const size_t sbase = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;
+    const int dv = p.dv;
     uint32_t r[32], pk[16];
 
-    const int dv = p.dv;
     if (u.nc == 0) {  // empty sequence: ht = h0
         if (p.ht)
             for (int d = 0; d < DK; ++d) p.ht[sbase + (size_t)d * dv] = p.h0 ? p.h0[sbase + (size_t)d * dv] : 0.f;
@@ -651,47 +734,61 @@ __device__ void state_role(const Ctx &x, const Params &p, const Unit &u, uint32_
         const int s = c % NS;
         const uint32_t par = c & 1;
         // ---- v_new^T and v~^T operands --------------------------------
+        // acc_v columns j = 0..63 (fp32) become v_new^T packed in columns
+        // 0..31 and v~^T packed in columns 32..63; a column is rewritten only
+        // after it has been read.
         if (!wwait(x, bar(x, B_V_FULL), par)) return;
+        DN_TRACE_EV(0, c);
         tc_fence_after();
         {
-            // acc_v columns j = 0..63 (fp32) become v_new^T packed in columns
-            // 0..31 and v~^T packed in columns 32..63; a column is rewritten
-            // only after it has been read.
-            const float *dec = scal(x, s) + SC_DEC;
-            uint32_t ta[16];
-            tmem_ld32(lb + TM_V, r);
-            tmem_wait_ld();
+            // quarter qq holds j = 16 qq .. 16 qq + 15 in columns 16 qq ..;
+            // v_new^T pairs go to columns 8 qq .., v~^T pairs to 32 + 8 qq ..
+            // (each destination column has been read before it is written).
+            const float4 *dec4 = reinterpret_cast<const float4 *>(scal(x, s) + SC_DEC);
+            uint32_t q16[16], pv8[8], t8[3][8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float a0 = __uint_as_float(r[2 * k]), a1 = __uint_as_float(r[2 * k + 1]);
-                pk[k] = pack_bf16(a0, a1);
-                ta[k] = pack_bf16(a0 * dec[2 * k], a1 * dec[2 * k + 1]);
+            for (int qq = 0; qq < 4; ++qq) {
+                tmem_ld16(lb + TM_V + 16 * qq, q16);
+                tmem_wait_ld_dep16(q16);
+                uint32_t tq[8];
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 dd = dec4[4 * qq + k4];
+                    const float a0 = __uint_as_float(q16[4 * k4]), a1 = __uint_as_float(q16[4 * k4 + 1]);
+                    const float a2 = __uint_as_float(q16[4 * k4 + 2]), a3 = __uint_as_float(q16[4 * k4 + 3]);
+                    pv8[2 * k4] = pack_bf16(a0, a1);
+                    pv8[2 * k4 + 1] = pack_bf16(a2, a3);
+                    tq[2 * k4] = pack_bf16(a0 * dd.x, a1 * dd.y);
+                    tq[2 * k4 + 1] = pack_bf16(a2 * dd.z, a3 * dd.w);
+                }
+                tmem_st8(lb + TM_V + 8 * qq, pv8);
+                if (qq < 2) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) t8[qq][k] = tq[k];
+                } else if (qq == 2) {
+                    tmem_st8(lb + TM_V + 32, t8[0]);
+                    tmem_st8(lb + TM_V + 40, t8[1]);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) t8[2][k] = tq[k];
+                } else {
+                    tmem_st8(lb + TM_V + 48, t8[2]);
+                    tmem_st8(lb + TM_V + 56, tq);
+                }
             }
-            tmem_st16(lb + TM_V, pk);  // columns 0..31 are read already
-            tmem_ld32(lb + TM_V + 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-            tmem_st16(lb + TM_V + 16, pk);
-            tmem_st16(lb + TM_V + 32, ta);
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                pk[k] = pack_bf16(__uint_as_float(r[2 * k]) * dec[32 + 2 * k],
-                                  __uint_as_float(r[2 * k + 1]) * dec[32 + 2 * k + 1]);
-            tmem_st16(lb + TM_V + 48, pk);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_VSM_FULL));
+            DN_TRACE_EV(1, c);
             warp_arrive(bar(x, B_EMPTY + s));
         }
         // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
         if (!wwait(x, bar(x, B_D_FULL), par)) return;
+        DN_TRACE_EV(2, c);
         tc_fence_after();
         const bool last = (c + 1 == u.nc);
         for (int blk = 0; blk < 4; ++blk) {
             tmem_ld32(lb + TM_S + 32 * blk, r);
-            tmem_wait_ld();
+            tmem_wait_ld_dep(r);
             if (!last) {
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
@@ -710,65 +807,76 @@ __device__ void state_role(const Ctx &x, const Params &p, const Unit &u, uint32_
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(bar(x, B_S_FULL));
+        DN_TRACE_EV(3, c);
         const int s1 = (c + 1) % NS;
         if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
         const float alpha = scal(x, s1)[SC_ALPHA];
         for (int blk = 0; blk < 4; ++blk) {
             tmem_ld32(lb + TM_S + 32 * blk, r);
-            tmem_wait_ld();
+            tmem_wait_ld_dep(r);
 #pragma unroll
             for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * __uint_as_float(r[k]));
             tmem_st32(lb + TM_S + 32 * blk, r);
         }
         tmem_wait_st();  // ordered before the next v~ arrive (fence there)
+        DN_TRACE_EV(4, c);
     }
 }
 
 // ---------------------------------------------------------------------------
 // Output warpgroup: o = scale e^{G_i} (S^T Q^T)[v][i] + (v_new^T P^T)[v][i].
 // ---------------------------------------------------------------------------
-__device__ void output_role(const Ctx &x, const Params &p, const Unit &u, uint32_t tm) {
+__device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
     const int v = 32 * (warp & 3) + (threadIdx.x & 31);  // value column = TMEM lane
     const uint32_t lb = lane_base(tm, warp);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    const long long rs = (long long)p.Nv * p.dv;
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const uint32_t par = c & 1;
         if (!wwait(x, bar(x, B_D_FULL), par)) return;
         if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return;
+        DN_TRACE_EV(0, c);
         tc_fence_after();
         const float *sc = scal(x, s);
         const int L = __float_as_int(sc[SC_L]);
         const long long t0 = u.bos + (long long)c * C;
         __nv_bfloat16 *op = o + (t0 * p.Nv + u.h) * (long long)p.dv + u.v0 + v;
-        const long long rs = (long long)p.Nv * p.dv;
         uint32_t ra[32], qa[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             tmem_ld32(lb + TM_O + 32 * half, ra);
+            tmem_wait_ld_dep(ra);
             tmem_ld32(lb + TM_P + 32 * half, qa);
-            tmem_wait_ld();
+            tmem_wait_ld_dep(qa);
             if (half == 1) {
                 tc_fence_before();
                 warp_arrive(bar(x, B_O_EMPTY));
             }
+            const float4 *osc4 = reinterpret_cast<const float4 *>(sc + SC_OSC + 32 * half);
             __nv_bfloat16 *po = op + 32 * half * rs;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const int i = 32 * half + k;
-                if (i < L)
-                    *po = __float2bfloat16_rn(fmaf(sc[SC_OSC + i], __uint_as_float(ra[k]), __uint_as_float(qa[k])));
-                po += rs;
+            for (int k4 = 0; k4 < 8; ++k4) {
+                const float4 os = osc4[k4];
+                const float osv[4] = {os.x, os.y, os.z, os.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 4 * k4 + e;
+                    if (32 * half + k < L)
+                        *po = __float2bfloat16_rn(fmaf(osv[e], __uint_as_float(ra[k]), __uint_as_float(qa[k])));
+                    po += rs;
+                }
             }
         }
         warp_arrive(bar(x, B_EMPTY + s));
+        DN_TRACE_EV(1, c);
     }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
-       const __grid_constant__ CUtensorMap mV, Params p) {
+       const __grid_constant__ CUtensorMap mV, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Ctx x;
@@ -785,10 +893,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
             mbar_init(bar(x, B_EMPTY + s), 13);
         }
         mbar_init(bar(x, B_KQ_FULL), 1);
-        mbar_init(bar(x, B_KQ_EMPTY), 4);
-        mbar_init(bar(x, B_T_FULL), 4);
-        mbar_init(bar(x, B_W_FULL), 1);
-        mbar_init(bar(x, B_W_EMPTY), 4);
+        mbar_init(bar(x, B_WU_FULL), 1);
         mbar_init(bar(x, B_WSM_FULL), 4);
         mbar_init(bar(x, B_S_FULL), 4);
         mbar_init(bar(x, B_V_FULL), 1);
@@ -796,6 +901,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         mbar_init(bar(x, B_D_FULL), 1);
         mbar_init(bar(x, B_O_EMPTY), 4);
         mbar_init(bar(x, B_DRAIN), 1);
+        mbar_init(bar(x, B_DRAIN2), 1);
         *x.abort_flag = 0;
         fence_barrier_init();
     }
@@ -823,7 +929,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
                 if (c >= 0) wait_drain(bar(x, B_FULL + c % NS), (c / NS) & 1);
         __syncwarp();
     } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0) mma_role(x, u, tm);
+        if ((threadIdx.x & 31) == 0 && u.nc > 0) mma_role(x, u, tm);
         __syncwarp();
     } else if (warp < 6) {
         prep_role(x, u, tm, p.scale);
