@@ -82,10 +82,8 @@ constexpr uint32_t OFF_TPP = OFF_TP + 8192;                // T'' 8 KB
 constexpr uint32_t OFF_WT = OFF_TPP + 8192;                // -W^T 16 KB
 constexpr int LDA = 68;                                    // fp32 row stride of A / T
 constexpr uint32_t OFF_A = OFF_WT + 16384;                 // 64 x 68 fp32
-constexpr int LDX = 56;
-constexpr uint32_t OFF_X = OFF_A + 64 * LDA * 4;           // 16 x 56 fp32
-constexpr int SCAL_FLOATS = 640;
-constexpr uint32_t OFF_SCAL = OFF_X + 16 * LDX * 4;        // NS x 2560 B
+constexpr int SCAL_FLOATS = 512;
+constexpr uint32_t OFF_SCAL = OFF_A + 64 * LDA * 4;        // NS x 2048 B
 constexpr uint32_t OFF_BAR = OFF_SCAL + NS * SCAL_FLOATS * 4;
 constexpr int NBARS = 32;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;         // TMEM base, abort flag
@@ -96,9 +94,13 @@ static_assert(OFF_P % 1024 == 0 && OFF_TP % 1024 == 0 && OFF_TPP % 1024 == 0 && 
               "MMA operands need 1024-byte aligned swizzle atoms");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB of shared memory per CTA");
 
-// Scalars of one chunk (floats within a stage's scalar block).
-constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, SC_F = 320,
-              SC_H = 384 /* 3 x 64 */, SC_ALPHA = 576, SC_L = 577;
+// Scalars of one chunk (floats within a stage's scalar block): G, beta,
+// beta e^G, e^{G_L - G}, scale e^G, the decay factors e^{G_i - G_0} and
+// e^{G_0 - G_j}, alpha = e^{G_L}, L, and whether the factors may be used
+// (the chunk's log-gate span is at most kSpanMax).
+constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, SC_AF = 320,
+              SC_BF = 384, SC_ALPHA = 448, SC_L = 449, SC_FACT = 450;
+constexpr float kSpanMax = 80.f;
 
 // Barrier indices.
 enum {
@@ -280,11 +282,15 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         const float GLa = __shfl_sync(0xffffffffu, ga, (L - 1) & 31);
         const float GLb = __shfl_sync(0xffffffffu, gb, (L - 1) & 31);
         const float GL = (L - 1) < 32 ? GLa : GLb;
-        // block-start prefix values G_0, G_16, G_32, G_48
-        const float Gb0 = __shfl_sync(0xffffffffu, ga, 0);
-        const float Gb1 = __shfl_sync(0xffffffffu, ga, 16);
-        const float Gb2 = __shfl_sync(0xffffffffu, gb, 0);
-        const float Gb3 = __shfl_sync(0xffffffffu, gb, 16);
+        // e^{G_i - G_j} = e^{G_i - G_0} e^{G_0 - G_j} is safe when the chunk's
+        // log-gate span is small enough that neither factor leaves fp32 range
+        const float G0 = __shfl_sync(0xffffffffu, ga, 0);
+        float gmax = fmaxf(ga, gb), gmin = fminf(ga, gb);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+            gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
+        }
         float *sc = scal(x, s);
         const int ia = lane, ib = lane + 32;
         sc[SC_G + ia] = ga;
@@ -297,18 +303,14 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         sc[SC_DEC + ib] = ib < L ? __expf(GL - gb) : 0.f;
         sc[SC_OSC + ia] = p.scale * __expf(ga);
         sc[SC_OSC + ib] = p.scale * __expf(gb);
-        sc[SC_F + ia] = __expf(ga - (lane < 16 ? Gb0 : Gb1));
-        sc[SC_F + ib] = __expf(gb - (lane < 16 ? Gb2 : Gb3));
-        // H[blk][j] = e^{G_{16 blk} - G_j} for j <= 16 blk (blk = 1..3)
-        sc[SC_H + 0 * 64 + ia] = ia <= 16 ? __expf(Gb1 - ga) : 0.f;
-        sc[SC_H + 0 * 64 + ib] = 0.f;
-        sc[SC_H + 1 * 64 + ia] = __expf(Gb2 - ga);
-        sc[SC_H + 1 * 64 + ib] = ib <= 32 ? __expf(Gb2 - gb) : 0.f;
-        sc[SC_H + 2 * 64 + ia] = __expf(Gb3 - ga);
-        sc[SC_H + 2 * 64 + ib] = ib <= 48 ? __expf(Gb3 - gb) : 0.f;
+        sc[SC_AF + ia] = __expf(ga - G0);
+        sc[SC_AF + ib] = __expf(gb - G0);
+        sc[SC_BF + ia] = __expf(G0 - ga);
+        sc[SC_BF + ib] = __expf(G0 - gb);
         if (lane == 0) {
             sc[SC_ALPHA] = __expf(GL);
             sc[SC_L] = __int_as_float(L);
+            sc[SC_FACT] = (gmax - gmin <= kSpanMax) ? 1.f : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
@@ -409,92 +411,86 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// 16 x 8 A fragment (rows R.., cols K..) of a row-major fp32 matrix, as TF32.
-__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *m, int ld, int R, int K, int g, int t) {
-    a[0] = to_tf32(m[(R + g) * ld + K + t]);
-    a[1] = to_tf32(m[(R + g + 8) * ld + K + t]);
-    a[2] = to_tf32(m[(R + g) * ld + K + t + 4]);
-    a[3] = to_tf32(m[(R + g + 8) * ld + K + t + 4]);
-}
-
-// 8 x 8 B fragment (rows K.., cols N..) of a row-major fp32 matrix, as TF32.
-__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *m, int ld, int K, int N, int g, int t) {
-    b[0] = to_tf32(m[(K + t) * ld + N + g]);
-    b[1] = to_tf32(m[(K + t + 4) * ld + N + g]);
-}
-
-// Block row r of T (rows 16r..16r+15, columns 0..16r-1), with the diagonal
-// blocks and block rows above already in place:
-//     X = A[16r:, :16r] T[:16r, :16r],   T[16r:, :16r] = T_rr X.
-// Warp pw owns the 8-column tiles nt = pw, pw + 4 (< 2r).  Two accumulators
-// split the k chain in half.
-template <int r>
-__device__ __forceinline__ void solve_block_row(float *sA, float *sX, int pw, int g, int t) {
-    constexpr int R = 16 * r;
+// ---- 16 x 16 block helpers for the solve (fp32 blocks, TF32 mma.sync) -------
+// acc (16 x 8 tile, columns n0..n0+7 of the product) += Ab (16 x 16) Bb (16 x 16).
+__device__ __forceinline__ void tile_mma(float (&acc)[4], const float *Ab, int lda, const float *Bb,
+                                         int ldb, int n0, int g, int t) {
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int nt = pw + 4 * q;
-        if (nt < 2 * r) {
-            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kt = 0; kt < 2 * r; ++kt) {
-                if (kt >= nt) {  // T is lower triangular: rows < 8 nt of column tile nt vanish
-                    uint32_t a[4], b[2];
-                    frag_a(a, sA, LDA, R, 8 * kt, g, t);
-                    frag_b(b, sA, LDA, 8 * kt, 8 * nt, g, t);
-                    if (kt & 1) mma_tf32(acc1, a, b);
-                    else mma_tf32(acc0, a, b);
-                }
-            }
-            sX[g * LDX + 8 * nt + 2 * t] = acc0[0] + acc1[0];
-            sX[g * LDX + 8 * nt + 2 * t + 1] = acc0[1] + acc1[1];
-            sX[(g + 8) * LDX + 8 * nt + 2 * t] = acc0[2] + acc1[2];
-            sX[(g + 8) * LDX + 8 * nt + 2 * t + 1] = acc0[3] + acc1[3];
-        }
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4], b[2];
+        a[0] = to_tf32(Ab[g * lda + 8 * kk + t]);
+        a[1] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t]);
+        a[2] = to_tf32(Ab[g * lda + 8 * kk + t + 4]);
+        a[3] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t + 4]);
+        b[0] = to_tf32(Bb[(8 * kk + t) * ldb + n0 + g]);
+        b[1] = to_tf32(Bb[(8 * kk + t + 4) * ldb + n0 + g]);
+        mma_tf32(acc, a, b);
     }
-    named_bar_sync(1, 128);
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const int nt = pw + 4 * q;
-        if (nt < 2 * r) {
-            float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t a[4], b[2];
-            frag_a(a, sA, LDA, R, R, g, t);
-            frag_b(b, sX, LDX, 0, 8 * nt, g, t);
-            mma_tf32(acc0, a, b);
-            frag_a(a, sA, LDA, R, R + 8, g, t);
-            frag_b(b, sX, LDX, 8, 8 * nt, g, t);
-            mma_tf32(acc1, a, b);
-            sA[(R + g) * LDA + 8 * nt + 2 * t] = acc0[0] + acc1[0];
-            sA[(R + g) * LDA + 8 * nt + 2 * t + 1] = acc0[1] + acc1[1];
-            sA[(R + g + 8) * LDA + 8 * nt + 2 * t] = acc0[2] + acc1[2];
-            sA[(R + g + 8) * LDA + 8 * nt + 2 * t + 1] = acc0[3] + acc1[3];
-        }
-    }
-    named_bar_sync(1, 128);
 }
 
-// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA.  128
-// threads.  The 16 x 16 diagonal blocks are inverted by forward substitution
-// in fp32 (warp pw owns block pw, lane l the column l % 16); the block rows
-// below follow with TF32 tensor-core products accumulated in fp32.
-__device__ void solve_T(float *sA, float *sX, int pw, int lane, int c) {
+// Same with A = Ab + Ab2 (two blocks of the same layout).
+__device__ __forceinline__ void tile_mma_sum(float (&acc)[4], const float *Ab, const float *Ab2, int lda,
+                                             const float *Bb, int ldb, int n0, int g, int t) {
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4], b[2];
+        a[0] = to_tf32(Ab[g * lda + 8 * kk + t] + Ab2[g * lda + 8 * kk + t]);
+        a[1] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t] + Ab2[(g + 8) * lda + 8 * kk + t]);
+        a[2] = to_tf32(Ab[g * lda + 8 * kk + t + 4] + Ab2[g * lda + 8 * kk + t + 4]);
+        a[3] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t + 4] + Ab2[(g + 8) * lda + 8 * kk + t + 4]);
+        b[0] = to_tf32(Bb[(8 * kk + t) * ldb + n0 + g]);
+        b[1] = to_tf32(Bb[(8 * kk + t + 4) * ldb + n0 + g]);
+        mma_tf32(acc, a, b);
+    }
+}
+
+__device__ __forceinline__ void tile_load(float (&acc)[4], const float *Cb, int ldc, int n0, int g, int t) {
+    acc[0] = Cb[g * ldc + n0 + 2 * t];
+    acc[1] = Cb[g * ldc + n0 + 2 * t + 1];
+    acc[2] = Cb[(g + 8) * ldc + n0 + 2 * t];
+    acc[3] = Cb[(g + 8) * ldc + n0 + 2 * t + 1];
+}
+
+__device__ __forceinline__ void tile_store(float *Cb, int ldc, int n0, const float (&acc)[4], int g, int t) {
+    Cb[g * ldc + n0 + 2 * t] = acc[0];
+    Cb[g * ldc + n0 + 2 * t + 1] = acc[1];
+    Cb[(g + 8) * ldc + n0 + 2 * t] = acc[2];
+    Cb[(g + 8) * ldc + n0 + 2 * t + 1] = acc[3];
+}
+
+// Scratch blocks of the solve (fp32, row stride SLD) in the T'/T'' buffer,
+// which is free while T is being computed.
+constexpr int SLD = 20, SBLK = 16 * SLD;
+enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30 };
+
+// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
+// LDA); 128 threads.  With A_D the four 16 x 16 diagonal blocks and A_O the
+// rest, I - A = (I - A_D)(I - N) with N = (I - A_D)^-1 A_O strictly block
+// lower, so N^4 = 0 and
+//     T = (I + N + N^2 + N^3) T_D,   T_D = (I - A_D)^-1,   N_ij = T_ii A_ij.
+// The diagonal blocks are inverted by forward substitution in fp32 (warp pw
+// owns block pw, lane l the column l % 16); the products are TF32 tensor-core
+// tiles accumulated in fp32, in four barrier-separated phases.
+__device__ void solve_T(float *sA, float *scr, int pw, int lane, int c) {
     {
+        // x = column `col` of (I - A_bb)^-1:  x_r = [r == col] + sum_{m < r} A[r][m] x_m.
+        // Rows of the block are read as float4 (one broadcast wavefront per
+        // four elements); four partial sums shorten the dependency chain.
         const int col = lane & 15, o = 16 * pw;
         float xv[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) xv[r] = (r == col) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) {
+            const float4 *ar = reinterpret_cast<const float4 *>(sA + (o + r) * LDA + o);
+            float p4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int r = 1; r < 16; ++r) {
-            // x_r = sum_{m < r} A[r][m] x_m  (x_m = 0 for m < col)
-            const float *ar = sA + (o + r) * LDA + o;
-            float s0 = 0.f, s1 = 0.f;
+            for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
+                const float4 a = ar[q4];
+                const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-            for (int m = 0; m < r; ++m) {
-                if (m & 1) s1 = fmaf(ar[m], xv[m], s1);
-                else s0 = fmaf(ar[m], xv[m], s0);
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q4 + e < r) p4[e] = fmaf(av[e], xv[4 * q4 + e], p4[e]);
             }
-            xv[r] = (r > col) ? s0 + s1 : xv[r];
+            xv[r] = (p4[0] + p4[1]) + (p4[2] + p4[3]) + ((r == col) ? 1.f : 0.f);
         }
         __syncwarp();
         if (lane < 16) {
@@ -505,11 +501,85 @@ __device__ void solve_T(float *sA, float *sX, int pw, int lane, int c) {
     named_bar_sync(1, 128);
     DN_TRACE_EV(3, c);
     const int g = lane >> 2, t = lane & 3;
-    solve_block_row<1>(sA, sX, pw, g, t);
+    auto blkA = [&](int i, int j) { return sA + 16 * i * LDA + 16 * j; };
+    auto blkX = [&](int k) { return scr + k * SBLK; };
+    // phase 1: N_ij = T_ii A_ij, six blocks x two column halves
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const int task = pw + 4 * q, b = task >> 1, n0 = 8 * (task & 1);
+        const int bi = (b == 0) ? 1 : (b < 3 ? 2 : 3);
+        const int bj = (b == 0) ? 0 : (b < 3 ? b - 1 : b - 3);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(acc, blkA(bi, bi), LDA, blkA(bi, bj), LDA, n0, g, t);
+        tile_store(blkX(b), SLD, n0, acc, g, t);
+    }
+    named_bar_sync(1, 128);
+    // phase 2: P20 = N21 N10, S31 = N31 + N32 N21, S30 = N30 + N31 N10 + N32 N20
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int task = pw + 4 * q;
+        if (task < 6) {
+            const int n0 = 8 * (task & 1);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (task < 2) {
+                tile_mma(acc, blkX(XN21), SLD, blkX(XN10), SLD, n0, g, t);
+                tile_store(blkX(XP20), SLD, n0, acc, g, t);
+            } else if (task < 4) {
+                tile_load(acc, blkX(XN31), SLD, n0, g, t);
+                tile_mma(acc, blkX(XN32), SLD, blkX(XN21), SLD, n0, g, t);
+                tile_store(blkX(XS31), SLD, n0, acc, g, t);
+            } else {
+                tile_load(acc, blkX(XN30), SLD, n0, g, t);
+                tile_mma(acc, blkX(XN31), SLD, blkX(XN10), SLD, n0, g, t);
+                tile_mma(acc, blkX(XN32), SLD, blkX(XN20), SLD, n0, g, t);
+                tile_store(blkX(XS30), SLD, n0, acc, g, t);
+            }
+        }
+    }
+    named_bar_sync(1, 128);
+    // phase 3: S30 += N32 P20, and T_ij = S_ij T_jj for every block but (3,0)
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const int task = pw + 4 * q, n0 = 8 * (task & 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        switch (task >> 1) {
+            case 0:
+                tile_load(acc, blkX(XS30), SLD, n0, g, t);
+                tile_mma(acc, blkX(XN32), SLD, blkX(XP20), SLD, n0, g, t);
+                tile_store(blkX(XS30), SLD, n0, acc, g, t);
+                break;
+            case 1:
+                tile_mma(acc, blkX(XN10), SLD, blkA(0, 0), LDA, n0, g, t);
+                tile_store(blkA(1, 0), LDA, n0, acc, g, t);
+                break;
+            case 2:
+                tile_mma(acc, blkX(XN21), SLD, blkA(1, 1), LDA, n0, g, t);
+                tile_store(blkA(2, 1), LDA, n0, acc, g, t);
+                break;
+            case 3:
+                tile_mma(acc, blkX(XN32), SLD, blkA(2, 2), LDA, n0, g, t);
+                tile_store(blkA(3, 2), LDA, n0, acc, g, t);
+                break;
+            case 4:
+                tile_mma(acc, blkX(XS31), SLD, blkA(1, 1), LDA, n0, g, t);
+                tile_store(blkA(3, 1), LDA, n0, acc, g, t);
+                break;
+            default:
+                tile_mma_sum(acc, blkX(XN20), blkX(XP20), SLD, blkA(0, 0), LDA, n0, g, t);
+                tile_store(blkA(2, 0), LDA, n0, acc, g, t);
+                break;
+        }
+    }
+    named_bar_sync(1, 128);
     DN_TRACE_EV(14, c);
-    solve_block_row<2>(sA, sX, pw, g, t);
-    DN_TRACE_EV(15, c);
-    solve_block_row<3>(sA, sX, pw, g, t);
+    // phase 4: T30 = S30 T00
+    if (pw < 2) {
+        const int n0 = 8 * pw;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(acc, blkX(XS30), SLD, blkA(0, 0), LDA, n0, g, t);
+        tile_store(blkA(3, 0), LDA, n0, acc, g, t);
+    }
+    named_bar_sync(1, 128);
 }
 
 __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
@@ -518,7 +588,7 @@ __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
     const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
     const bool leader = (pw == 0 && lane == 0);
     float *sA = reinterpret_cast<float *>(x.gbase + OFF_A);
-    float *sX = reinterpret_cast<float *>(x.gbase + OFF_X);
+    float *scr = reinterpret_cast<float *>(x.gbase + OFF_TP);  // solve scratch
     const uint32_t lb = lane_base(tm, warp);
     const int i = row & 63;       // row of KK^T (TMEM lanes 0-63) or QK^T (64-127)
     const bool rowA = row < 64;   // KK^T rows -> A (j < i), QK^T rows -> P (j <= i)
@@ -545,14 +615,14 @@ __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
         ok = ok && wwait(x, bar(x, B_FULL + s), (c / NS) & 1);
         DN_TRACE_EV(9, c);
         const float *sc = scal(x, s);
-        const float Gi = sc[SC_G + i], Fi = sc[SC_F + i];
+        const float Gi = sc[SC_G + i], ai = sc[SC_AF + i];
+        const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
         const float rs = rowA ? -sc[SC_BETA + i] : scale;
         const uint32_t pb = x.base + OFF_P + (c & 1) * 8192;
         float *arow = sA + i * LDA;
-        // D_ij = e^{G_i - G_j} per 16-column block jb of the row: below the
-        // row's block through its start b (D = e^{G_i - G_b} e^{G_b - G_j},
-        // both factors <= 1); inside it directly (masked to j <= jmax);
-        // above it zero.
+        // D_ij = e^{G_i - G_j} for j <= jmax, else 0: the product of the two
+        // per-chunk factors when the chunk's log-gate span allows it, else
+        // one exponential per element.
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
             if ((jb & 1) == 0) {  // columns 32 (jb/2) .. +31 of this row
@@ -560,17 +630,22 @@ __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
                 tmem_wait_ld_dep(r0);
             }
             float dcy[16];
-            if (jb < ib) {
-                const float4 *h4 = reinterpret_cast<const float4 *>(sc + SC_H + (ib - 1) * 64 + 16 * jb);
+            if (jb > ib) {
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dcy[jj] = 0.f;
+            } else if (fact) {
+                const float4 *b4 = reinterpret_cast<const float4 *>(sc + SC_BF + 16 * jb);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 h = h4[q4];
-                    dcy[4 * q4] = Fi * h.x;
-                    dcy[4 * q4 + 1] = Fi * h.y;
-                    dcy[4 * q4 + 2] = Fi * h.z;
-                    dcy[4 * q4 + 3] = Fi * h.w;
+                    const float4 bb = b4[q4];
+                    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = 16 * jb + 4 * q4 + e;
+                        dcy[4 * q4 + e] = j <= jmax ? ai * bv[e] : 0.f;
+                    }
                 }
-            } else if (jb == ib) {
+            } else {
                 const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 16 * jb);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -582,9 +657,6 @@ __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
                         dcy[4 * q4 + e] = __expf(j <= jmax ? Gi - gv[e] : -INFINITY);
                     }
                 }
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj) dcy[jj] = 0.f;
             }
             float val[16];
 #pragma unroll
@@ -619,7 +691,7 @@ __device__ void prep_role(const Ctx x, const Unit u, uint32_t tm, float scale) {
             issue_kq(x, tm, c + 1);
             mma_commit(bar(x, B_KQ_FULL));
         }
-        solve_T(sA, sX, pw, lane, c);
+        solve_T(sA, scr, pw, lane, c);
         DN_TRACE_EV(4, c);
         // T' = T diag(beta e^G) (KK^T-row threads), T'' = T diag(beta) (others)
         {
@@ -843,31 +915,35 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         const int L = __float_as_int(sc[SC_L]);
         const long long t0 = u.bos + (long long)c * C;
         __nv_bfloat16 *op = o + (t0 * p.Nv + u.h) * (long long)p.dv + u.v0 + v;
-        uint32_t ra[32], qa[32];
+        // combine both halves into packed bf16 pairs first, release the
+        // accumulators, then store
+        uint32_t ra[16], qa[16], ob[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            tmem_ld32(lb + TM_O + 32 * half, ra);
-            tmem_wait_ld_dep(ra);
-            tmem_ld32(lb + TM_P + 32 * half, qa);
-            tmem_wait_ld_dep(qa);
-            if (half == 1) {
-                tc_fence_before();
-                warp_arrive(bar(x, B_O_EMPTY));
-            }
-            const float4 *osc4 = reinterpret_cast<const float4 *>(sc + SC_OSC + 32 * half);
-            __nv_bfloat16 *po = op + 32 * half * rs;
+        for (int qq = 0; qq < 4; ++qq) {
+            tmem_ld16(lb + TM_O + 16 * qq, ra);
+            tmem_wait_ld_dep16(ra);
+            tmem_ld16(lb + TM_P + 16 * qq, qa);
+            tmem_wait_ld_dep16(qa);
+            const float4 *osc4 = reinterpret_cast<const float4 *>(sc + SC_OSC + 16 * qq);
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
+            for (int k4 = 0; k4 < 4; ++k4) {
                 const float4 os = osc4[k4];
-                const float osv[4] = {os.x, os.y, os.z, os.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int k = 4 * k4 + e;
-                    if (32 * half + k < L)
-                        *po = __float2bfloat16_rn(fmaf(osv[e], __uint_as_float(ra[k]), __uint_as_float(qa[k])));
-                    po += rs;
-                }
+                ob[8 * qq + 2 * k4] =
+                    pack_bf16(fmaf(os.x, __uint_as_float(ra[4 * k4]), __uint_as_float(qa[4 * k4])),
+                              fmaf(os.y, __uint_as_float(ra[4 * k4 + 1]), __uint_as_float(qa[4 * k4 + 1])));
+                ob[8 * qq + 2 * k4 + 1] =
+                    pack_bf16(fmaf(os.z, __uint_as_float(ra[4 * k4 + 2]), __uint_as_float(qa[4 * k4 + 2])),
+                              fmaf(os.w, __uint_as_float(ra[4 * k4 + 3]), __uint_as_float(qa[4 * k4 + 3])));
             }
+        }
+        tc_fence_before();
+        warp_arrive(bar(x, B_O_EMPTY));
+        // rows i < L of column v; bf16 pair k holds rows 2k (low) and 2k + 1
+        uint16_t *po = reinterpret_cast<uint16_t *>(op);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (2 * k < L) po[(2 * k) * rs] = (uint16_t)(ob[k] & 0xffffu);
+            if (2 * k + 1 < L) po[(2 * k + 1) * rs] = (uint16_t)(ob[k] >> 16);
         }
         warp_arrive(bar(x, B_EMPTY + s));
         DN_TRACE_EV(1, c);
