@@ -230,6 +230,20 @@ def reference_arm(args, inp, wl_name, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest value of `x` over all ranks (the slowest rank's time)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Tokens all ranks processed per second of the slowest rank."""
+    return tokens_per_rank * world / (ms_max / 1e3)
+
+
 def config_of(wl_name, inp, l2):
     B, T, Nk, dk = inp["q"].shape
     Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
@@ -325,11 +339,7 @@ def main():
     st = dn.dn_check(stream)
     if st != dn.DN_OK:
         raise dn.DnError(st, "timed region")
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dist, dev)
 
     # ---------------- end to end through the public API -------------------
     # per step: pinned host -> device copies of the inputs, the call, and the
@@ -363,11 +373,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / E
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dist, dev)
 
     if rank != 0:
         dist.destroy_process_group()
@@ -396,7 +402,7 @@ def main():
     roof["tflops"] = tflops
     roof["kernel"] = kernel
 
-    line = dict(metric=METRIC, value=alg["tokens"] * world / (ms_max / 1e3), unit=UNIT,
+    line = dict(metric=METRIC, value=weak_scaling_value(alg["tokens"], world, ms_max), unit=UNIT,
                 n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16"
                 if d["q"].dtype == torch.bfloat16 else "f32", data="synthetic",
@@ -404,7 +410,7 @@ def main():
                                  "(256 MiB write, outside the step's events)"),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
                 gpu_launches=K, roofline=roof,
-                e2e=dict(value=alg["tokens"] * world / (e2e_ms / 1e3), unit=UNIT,
+                e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                          ms_per_step=e2e_ms),
                 wall_ms_timed_loop=1e3 * wall)
