@@ -298,10 +298,12 @@ def main():
     dt = dn.dtype_code(d["q"].dtype)
     stream = torch.cuda.current_stream(dev)
 
+    ws = dn.workspace_for(d["q"], d["v"], N)
+
     def launch(q=d["q"], k=d["k"], v=d["v"], beta=d["beta"], g=d["g"], h0=d["h0"],
                cu=d["cu_seqlens"], o=o, ht=ht):
         st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
-                             inp["scale"], 64, o, ht, stream)
+                             inp["scale"], 64, o, ht, ws, stream=stream)
         if st != dn.DN_OK:
             raise dn.DnError(st)
 

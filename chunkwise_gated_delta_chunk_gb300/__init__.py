@@ -5,10 +5,10 @@ CUDA kernels of ``libdnchunk.so`` (declared in ``include/dn_chunk_fwd.h``).
 There is no CPU path: if the library is missing, :func:`load` raises.
 PyTorch supplies device memory and streams.
 
-Names follow the C ABI: :func:`dn_chunk_fwd`, :func:`dn_check`,
-:func:`dn_status_str`, :func:`dn_last_kernel`.  :func:`chunk_fwd` is a
-convenience that allocates ``o`` and ``ht`` with torch and calls
-:func:`dn_chunk_fwd`.
+Names follow the C ABI: :func:`dn_chunk_fwd`,
+:func:`dn_chunk_fwd_workspace_bytes`, :func:`dn_check`, :func:`dn_status_str`,
+:func:`dn_last_kernel`.  :func:`chunk_fwd` is a convenience that allocates
+``o``, ``ht`` and the workspace with torch and calls :func:`dn_chunk_fwd`.
 """
 from __future__ import annotations
 
@@ -29,7 +29,8 @@ DN_BF16 = 0
 DN_F32 = 1
 
 # Every symbol the public header declares.
-ABI_SYMBOLS = ("dn_chunk_fwd", "dn_check", "dn_status_str", "dn_last_kernel")
+ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_check", "dn_status_str",
+               "dn_last_kernel")
 
 _lib = None
 _lock = threading.Lock()
@@ -54,8 +55,11 @@ def load(path: str | None = None):
                 "g.build()\"` -- there is no fallback path" % p)
         lib = ctypes.CDLL(p)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        lib.dn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P]
+        Z = ctypes.c_size_t
+        lib.dn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, Z, P]
         lib.dn_chunk_fwd.restype = I
+        lib.dn_chunk_fwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
+        lib.dn_chunk_fwd_workspace_bytes.restype = Z
         lib.dn_check.argtypes = [P]
         lib.dn_check.restype = I
         lib.dn_status_str.argtypes = [I]
@@ -88,13 +92,37 @@ def _stream(stream):
 
 
 def dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
-                 scale, chunk, o, ht, stream=None) -> int:
-    """Call the C entry point as is; returns its status code."""
+                 scale, chunk, o, ht, workspace=None, workspace_bytes=None, stream=None) -> int:
+    """Call the C entry point as is; returns its status code.
+
+    ``workspace`` is a device tensor (its byte size is passed unless
+    ``workspace_bytes`` is given), an int address, or None.
+    """
     lib = load()
+    if workspace_bytes is None:
+        workspace_bytes = 0
+        if workspace is not None and not isinstance(workspace, int):
+            workspace_bytes = workspace.numel() * workspace.element_size()
     return lib.dn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                             _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
                             int(dk), int(dv), int(dtype), float(scale), int(chunk), _ptr(o),
-                            _ptr(ht), _stream(stream))
+                            _ptr(ht), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype, chunk=64) -> int:
+    return int(load().dn_chunk_fwd_workspace_bytes(int(n_seqs), int(B), int(T), int(Nk), int(Nv),
+                                                   int(dk), int(dv), int(dtype), int(chunk)))
+
+
+def workspace_for(q, v, n_seqs, chunk=64):
+    """A uint8 device tensor of the workspace size for these inputs (or None)."""
+    import torch
+    B, T, Nk, dk = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    nbytes = dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype_code(q.dtype), chunk)
+    if nbytes == 0:
+        return None
+    return torch.empty(nbytes, dtype=torch.uint8, device=q.device)
 
 
 def dn_check(stream=None) -> int:
@@ -122,8 +150,8 @@ def dtype_code(dtype) -> int:
 
 
 def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
-              output_final_state=True, chunk=64, stream=None, o=None, ht=None):
-    """Allocate ``o`` (and ``ht``) and run :func:`dn_chunk_fwd`.
+              output_final_state=True, chunk=64, stream=None, o=None, ht=None, workspace=None):
+    """Allocate ``o`` (and ``ht``, and the workspace) and run :func:`dn_chunk_fwd`.
 
     q, k ``[B, T, Nk, dk]``; v ``[B, T, Nv, dv]``; beta, g ``[B, T, Nv]`` fp32;
     h0 ``[N, Nv, dk, dv]`` fp32; cu_seqlens int64 ``[N+1]`` on the device.
@@ -137,9 +165,11 @@ def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
         o = torch.empty(B, T, Nv, dv, dtype=q.dtype, device=q.device)
     if ht is None and output_final_state:
         ht = torch.empty(N, Nv, dk, dv, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(q, v, N, chunk)
     st = dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
                       dtype_code(q.dtype), 0.0 if scale is None else scale, chunk, o,
-                      ht if output_final_state else None, stream)
+                      ht if output_final_state else None, workspace, stream=stream)
     if st != DN_OK:
         raise DnError(st)
     return o, (ht if output_final_state else None)

@@ -47,14 +47,28 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
 
+// Bytes of workspace the call with these sizes needs (0: none).  The
+// tensor-core path keeps T' | T'' of every chunk there between its two kernels.
+size_t workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype) {
+    if (tokens <= 0 || !dn::tc_supported(dk, dv, dtype == DN_BF16)) return 0;
+    return dn::tc_workspace_bytes(tokens, n_seqs, Nv);
+}
+
 }  // namespace
+
+DN_EXPORT size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
+                                              dn_dtype dtype, int chunk) {
+    if (n_seqs <= 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || chunk != dn::kChunk) return 0;
+    return workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv, dtype);
+}
 
 DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                                  const float *beta, const float *g, const float *h0,
                                  const int64_t *cu_seqlens, int n_seqs,
                                  int B, int T, int Nk, int Nv, int dk, int dv,
                                  dn_dtype dtype, float scale, int chunk,
-                                 void *o, float *ht, dn_stream_t stream) {
+                                 void *o, float *ht, void *workspace, size_t workspace_bytes_,
+                                 dn_stream_t stream) {
     // ---- arguments that are wrong whatever is built ----------------------
     if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
     if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
@@ -73,6 +87,9 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     if (!dim_ok(dk) || !dim_ok(dv)) return DN_ERR_UNSUPPORTED;
     if (dtype == DN_F32 && dk > 128) return DN_ERR_UNSUPPORTED;
     if (n_seqs == 0) return DN_OK;
+    const size_t ws_need = workspace_bytes(tokens, n_seqs, Nv, dk, dv, dtype);
+    if (ws_need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes_ < ws_need))
+        return DN_ERR_INVALID_ARG;
 
     dn::Params p{};
     p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.cu = cu_seqlens;
@@ -80,6 +97,8 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     p.N = n_seqs; p.B = B; p.T = T; p.Nk = Nk; p.Nv = Nv; p.dk = dk; p.dv = dv;
     p.tokens = tokens;
     p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
+    p.ws = workspace;
+    p.nslots = tokens / dn::kChunk + n_seqs;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
 
     const char *name = "";

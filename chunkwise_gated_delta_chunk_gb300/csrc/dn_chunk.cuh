@@ -1,0 +1,99 @@
+// Per-chunk pieces shared by the WY kernel (T of every chunk) and the scan
+// kernel: sequence bounds, the workspace slot of a chunk and the gate scalars.
+//
+// Sources: [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1 (gate
+//          prefix sum G and the decay matrix D_ij = e^{G_i - G_j});
+//          [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §2.4.
+#pragma once
+
+#include "dn_internal.h"
+
+namespace dn {
+
+// Scalars of one chunk (floats within a scalar block): G, beta, beta e^G,
+// e^{G_L - G} (zero past the chunk's length), scale e^G, the decay factors
+// e^{G_i - G_0} and e^{G_0 - G_j}, alpha = e^{G_L}, L, and whether the factors
+// may be used (the chunk's log-gate span is at most kSpanMax).
+constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, SC_AF = 320,
+              SC_BF = 384, SC_ALPHA = 448, SC_L = 449, SC_FACT = 450;
+constexpr int SCAL_FLOATS = 512;
+constexpr float kSpanMax = 80.f;
+
+// Bytes of one workspace slot: T' = T diag(beta e^G) and T'' = T diag(beta),
+// each a 64 x 64 bf16 matrix stored as the 128-byte-swizzled K-major image
+// the MMAs read (row i at 128 i, 16-byte chunk c at (c ^ (i & 7)) * 16).
+constexpr uint32_t kSlotBytes = 16384;
+
+__device__ __forceinline__ long long seq_bos(const Params &p, int n) {
+    return p.cu ? p.cu[n] : (long long)n * p.T;
+}
+
+__device__ __forceinline__ long long seq_eos(const Params &p, int n) {
+    return p.cu ? p.cu[n + 1] : (long long)(n + 1) * p.T;
+}
+
+// Workspace slot of the chunk that starts at token t0 of sequence n.  With
+// non-decreasing offsets, floor(t0 / C) + n is one-to-one over every chunk of
+// every sequence and stays below floor(tokens / C) + N.
+__device__ __forceinline__ long long wy_slot(long long t0, int n) { return t0 / kChunk + n; }
+
+// Gate scalars of the chunk [t0, t0 + L) of value head h, computed by one
+// warp (lane owns tokens lane and lane + 32) into `sc`.  Tokens past L get
+// beta = 0 and g = 0, so they write nothing and decay nothing.
+__device__ __forceinline__ void chunk_scalars(const Params &p, int h, long long t0, int L, float *sc,
+                                              int lane) {
+    float ga = 0.f, gb = 0.f, ba = 0.f, bb = 0.f;
+    if (lane < L) {
+        ba = p.beta[(t0 + lane) * p.Nv + h];
+        if (p.g) ga = p.g[(t0 + lane) * p.Nv + h];
+    }
+    if (lane + 32 < L) {
+        bb = p.beta[(t0 + lane + 32) * p.Nv + h];
+        if (p.g) gb = p.g[(t0 + lane + 32) * p.Nv + h];
+    }
+    // inclusive prefix sums G_i = g_0 + ... + g_i
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float ta = __shfl_up_sync(0xffffffffu, ga, off);
+        const float tb = __shfl_up_sync(0xffffffffu, gb, off);
+        if (lane >= off) {
+            ga += ta;
+            gb += tb;
+        }
+    }
+    gb += __shfl_sync(0xffffffffu, ga, 31);
+    const float GLa = __shfl_sync(0xffffffffu, ga, (L - 1) & 31);
+    const float GLb = __shfl_sync(0xffffffffu, gb, (L - 1) & 31);
+    const float GL = (L - 1) < 32 ? GLa : GLb;
+    // e^{G_i - G_j} = e^{G_i - G_0} e^{G_0 - G_j} is safe when the chunk's
+    // log-gate span is small enough that neither factor leaves fp32 range
+    const float G0 = __shfl_sync(0xffffffffu, ga, 0);
+    float gmax = fmaxf(ga, gb), gmin = fminf(ga, gb);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+        gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
+    }
+    const int ia = lane, ib = lane + 32;
+    sc[SC_G + ia] = ga;
+    sc[SC_G + ib] = gb;
+    sc[SC_BETA + ia] = ba;
+    sc[SC_BETA + ib] = bb;
+    sc[SC_BEG + ia] = ba * __expf(ga);
+    sc[SC_BEG + ib] = bb * __expf(gb);
+    sc[SC_DEC + ia] = ia < L ? __expf(GL - ga) : 0.f;
+    sc[SC_DEC + ib] = ib < L ? __expf(GL - gb) : 0.f;
+    sc[SC_OSC + ia] = p.scale * __expf(ga);
+    sc[SC_OSC + ib] = p.scale * __expf(gb);
+    sc[SC_AF + ia] = __expf(ga - G0);
+    sc[SC_AF + ib] = __expf(gb - G0);
+    sc[SC_BF + ia] = __expf(G0 - ga);
+    sc[SC_BF + ib] = __expf(G0 - gb);
+    if (lane == 0) {
+        sc[SC_ALPHA] = __expf(GL);
+        sc[SC_L] = __int_as_float(L);
+        sc[SC_FACT] = (gmax - gmin <= kSpanMax) ? 1.f : 0.f;
+    }
+}
+
+}  // namespace dn

@@ -23,6 +23,8 @@ struct Params {
     long long tokens;          // B*T
     float scale;
     unsigned *status;          // per-device status word
+    void *ws;                  // workspace: nslots x Nv slots of T' | T'' (tensor-core path)
+    long long nslots;          // floor(tokens / C) + N
 };
 
 // CUDA-core kernel: fp32 arithmetic for every product; any supported shape.

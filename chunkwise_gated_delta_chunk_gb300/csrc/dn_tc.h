@@ -1,11 +1,17 @@
-// Tensor-core kernel entry (bf16, dk = 128, dv a multiple of 128).
+// Tensor-core path (bf16, dk = 128, dv a multiple of 128): the WY kernel
+// (T of every chunk, into the workspace) and the scan kernel that reads it.
 #pragma once
+
+#include <cuda.h>
 
 #include "dn_internal.h"
 
 namespace dn {
 
 bool tc_supported(int dk, int dv, bool bf16);
+// Workspace bytes the tensor-core path needs (0 for no tokens).
+size_t tc_workspace_bytes(long long tokens, int N, int Nv);
 cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name);
+cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, cudaStream_t stream);
 
 }  // namespace dn

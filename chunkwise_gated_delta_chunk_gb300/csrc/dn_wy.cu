@@ -1,0 +1,468 @@
+// WY kernel of the chunkwise gated delta rule forward (bf16 k, dk = 128):
+// for every chunk of every (sequence, value head), the lower-triangular
+// inverse T = (I - A)^-1 of the chunk's WY representation, written to the
+// workspace as the two bf16 MMA operands T' = T diag(beta e^G) and
+// T'' = T diag(beta) that give W = T' K and U = T'' V.
+//
+// Sources: [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现"
+//                 §2.3 (A = -tril(diag(beta) K K^T, -1), T = (I - A)^-1 by
+//                 forward substitution), §2.4 (W = T diag(beta) K, U = T diag(beta) V);
+//          [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1 (gated form:
+//                 A_ij carries e^{G_i - G_j}, W carries e^{G}).
+//
+// Every chunk is independent, so this kernel runs all of them in parallel
+// (one 128-thread CTA per chunk and value head, several CTAs per SM) ahead of
+// the sequential scan kernel, which then only reads T' and T''.  Per CTA:
+//   1. TMA brings the chunk's K (64 x 128 bf16, two 128-byte-swizzled column
+//      halves); warp 0 computes the gate scalars meanwhile;
+//   2. one tcgen05 MMA chain computes K K^T into tensor memory (M = 128: the
+//      operand rows 64-127 run past the tile and land in TMEM lanes 64-127,
+//      which nothing reads);
+//   3. warps 0-1 turn lanes 0-63 into A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij
+//      (j < i) in shared memory, fp32;
+//   4. the four warps invert I - A in fp32 (blocked, below);
+//   5. T' and T'' are scaled, rounded to bf16 in the swizzled image and
+//      copied to the chunk's workspace slot with coalesced 16-byte stores.
+// Waits are bounded: a wait that runs out records kStatusTimeout in the status
+// word, the CTA skips the rest and drains its own TMA / MMA work before it
+// frees its tensor memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "dn_chunk.cuh"
+#include "dn_internal.h"
+#include "dn_tc.h"
+#include "tc_ptx.cuh"
+
+// Optional per-CTA phase trace (SM clock) of the first 4096 CTAs, compiled
+// in only with -DDN_TRACE for profiling builds.
+#ifdef DN_TRACE
+__device__ unsigned long long g_wy_trace[4096][8];
+#define WY_TRACE_EV(ev)                                                             \
+    do {                                                                            \
+        if (threadIdx.x == 0 && blockIdx.x < 4096) {                                \
+            unsigned long long t_;                                                  \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                  \
+            g_wy_trace[blockIdx.x][(ev)] = t_;                                      \
+        }                                                                           \
+    } while (0)
+extern "C" __attribute__((visibility("default"))) int dn_wy_trace_dump(void *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_wy_trace, sizeof(g_wy_trace));
+}
+#else
+#define WY_TRACE_EV(ev) \
+    do {                \
+    } while (0)
+#endif
+
+namespace dn {
+namespace {
+
+using namespace ptx;
+
+constexpr int C = kChunk;  // 64
+constexpr int NT = 128;
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr uint32_t OFF_K = 0;                    // K[:, 0:64] | K[:, 64:128] | 8 KB the MMA reads past
+constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases OFF_K)
+constexpr uint32_t OFF_T = 24576;                // T' | T'' images; solve scratch before that
+constexpr uint32_t OFF_SC = OFF_T + 2 * 8192;    // gate scalars
+constexpr uint32_t OFF_BAR = OFF_SC + SCAL_FLOATS * 4;
+constexpr uint32_t SMEM_USED = OFF_BAR + 32;     // 2 mbarriers, TMEM base, flag
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(64 * LDA * 4 <= OFF_T, "A overlaps the T images");
+static_assert(OFF_T % 1024 == 0, "swizzled images need 1024-byte alignment");
+
+constexpr uint32_t TM_COLS = 64;
+constexpr uint32_t ID_KK = idesc_bf16(128, 64, 0, 0);  // A, B K-major
+
+__device__ bool wait_bounded(uint32_t b, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(b, parity))
+        if (globaltimer() - t0 > kTimeoutNs) return false;
+    return true;
+}
+
+// ---- 16 x 16 block helpers for the solve (fp32 blocks, fp32 FMA) -----------
+// A 16 x 8 output tile (columns n0..n0+7) per warp: lane l owns row l >> 1 and
+// the four columns n0 + 4 (l & 1) .. +3.  B rows are read as float4 (one
+// broadcast wavefront for the two column halves), A rows as float4 along k.
+__device__ __forceinline__ void tile_mma(float (&acc)[4], const float *Ab, int lda, const float *Bb,
+                                         int ldb, int n0, int lane) {
+    const int r = lane >> 1, cb = n0 + 4 * (lane & 1);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 a = *reinterpret_cast<const float4 *>(Ab + r * lda + 4 * k4);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 bb = *reinterpret_cast<const float4 *>(Bb + (4 * k4 + e) * ldb + cb);
+            acc[0] = fmaf(av[e], bb.x, acc[0]);
+            acc[1] = fmaf(av[e], bb.y, acc[1]);
+            acc[2] = fmaf(av[e], bb.z, acc[2]);
+            acc[3] = fmaf(av[e], bb.w, acc[3]);
+        }
+    }
+}
+
+// Same with A = Ab + Ab2 (two blocks of the same layout).
+__device__ __forceinline__ void tile_mma_sum(float (&acc)[4], const float *Ab, const float *Ab2, int lda,
+                                             const float *Bb, int ldb, int n0, int lane) {
+    const int r = lane >> 1, cb = n0 + 4 * (lane & 1);
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 a = *reinterpret_cast<const float4 *>(Ab + r * lda + 4 * k4);
+        const float4 a2 = *reinterpret_cast<const float4 *>(Ab2 + r * lda + 4 * k4);
+        const float av[4] = {a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 bb = *reinterpret_cast<const float4 *>(Bb + (4 * k4 + e) * ldb + cb);
+            acc[0] = fmaf(av[e], bb.x, acc[0]);
+            acc[1] = fmaf(av[e], bb.y, acc[1]);
+            acc[2] = fmaf(av[e], bb.z, acc[2]);
+            acc[3] = fmaf(av[e], bb.w, acc[3]);
+        }
+    }
+}
+
+__device__ __forceinline__ void tile_load(float (&acc)[4], const float *Cb, int ldc, int n0, int lane) {
+    const float4 v = *reinterpret_cast<const float4 *>(Cb + (lane >> 1) * ldc + n0 + 4 * (lane & 1));
+    acc[0] = v.x;
+    acc[1] = v.y;
+    acc[2] = v.z;
+    acc[3] = v.w;
+}
+
+__device__ __forceinline__ void tile_store(float *Cb, int ldc, int n0, const float (&acc)[4], int lane) {
+    *reinterpret_cast<float4 *>(Cb + (lane >> 1) * ldc + n0 + 4 * (lane & 1)) =
+        make_float4(acc[0], acc[1], acc[2], acc[3]);
+}
+
+// Scratch blocks of the solve (fp32, row stride SLD) in the T'/T'' buffer,
+// which is free while T is being computed.
+constexpr int SLD = 20, SBLK = 16 * SLD;
+enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30 };
+
+// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
+// LDA); 128 threads.  With A_D the four 16 x 16 diagonal blocks and A_O the
+// rest, I - A = (I - A_D)(I - N) with N = (I - A_D)^-1 A_O strictly block
+// lower, so N^4 = 0 and
+//     T = (I + N + N^2 + N^3) T_D,   T_D = (I - A_D)^-1,   N_ij = T_ii A_ij.
+// The diagonal blocks are inverted by forward substitution in fp32 (warp pw
+// owns block pw, lane l the column l % 16); the block products are fp32 FMA
+// tiles, in four barrier-separated phases.
+__device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane, uint32_t bid) {
+    {
+        // x = column `col` of (I - A_bb)^-1:  x_r = [r == col] + sum_{m < r} A[r][m] x_m.
+        // Rows of the block are read as float4 (one broadcast wavefront per
+        // four elements); four partial sums shorten the dependency chain.
+        const int col = lane & 15, o = 16 * pw;
+        float xv[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float4 *ar = reinterpret_cast<const float4 *>(sA + (o + r) * LDA + o);
+            float p4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
+                const float4 a = ar[q4];
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * q4 + e < r) p4[e] = fmaf(av[e], xv[4 * q4 + e], p4[e]);
+            }
+            xv[r] = (p4[0] + p4[1]) + (p4[2] + p4[3]) + ((r == col) ? 1.f : 0.f);
+        }
+        __syncwarp();
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sA[(o + r) * LDA + o + col] = xv[r];
+        }
+    }
+    named_bar_sync(bid, 128);
+    auto blkA = [&](int i, int j) { return sA + 16 * i * LDA + 16 * j; };
+    auto blkX = [&](int k) { return scr + k * SBLK; };
+    // phase 1: N_ij = T_ii A_ij, six blocks x two column halves (3 per warp)
+    {
+        float acc[3][4];
+        float *dst[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int task = pw + 4 * q, b = task >> 1, n0 = 8 * (task & 1);
+            const int bi = (b == 0) ? 1 : (b < 3 ? 2 : 3);
+            const int bj = (b == 0) ? 0 : (b < 3 ? b - 1 : b - 3);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+            tile_mma(acc[q], blkA(bi, bi), LDA, blkA(bi, bj), LDA, n0, lane);
+            dst[q] = blkX(b) + n0;
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) tile_store(dst[q], SLD, 0, acc[q], lane);
+    }
+    named_bar_sync(bid, 128);
+    // phase 2: P20 = N21 N10, S31 = N31 + N32 N21, S30 = N30 + N31 N10 + N32 N20
+    {
+        float acc[2][4];
+        float *dst[2];
+        bool live[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int task = pw + 4 * q, n0 = 8 * (task & 1);
+            live[q] = task < 6;
+            const int kind = task >> 1;  // 0: P20, 1: S31, 2: S30
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+            if (live[q]) {
+                if (kind == 1) tile_load(acc[q], blkX(XN31), SLD, n0, lane);
+                if (kind == 2) tile_load(acc[q], blkX(XN30), SLD, n0, lane);
+                const float *A0 = blkX(kind == 0 ? XN21 : (kind == 1 ? XN32 : XN31));
+                const float *B0 = blkX(kind == 0 ? XN10 : (kind == 1 ? XN21 : XN10));
+                tile_mma(acc[q], A0, SLD, B0, SLD, n0, lane);
+                if (kind == 2) tile_mma(acc[q], blkX(XN32), SLD, blkX(XN20), SLD, n0, lane);
+            }
+            dst[q] = blkX(kind == 0 ? XP20 : (kind == 1 ? XS31 : XS30)) + n0;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (live[q]) tile_store(dst[q], SLD, 0, acc[q], lane);
+    }
+    named_bar_sync(bid, 128);
+    // phase 3: S30 += N32 P20, and T_ij = S_ij T_jj for every block but (3,0)
+    {
+        float acc[3][4];
+        float *dst[3];
+        int ldd[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int task = pw + 4 * q, n0 = 8 * (task & 1), kind = task >> 1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][e] = 0.f;
+            if (kind == 0) {
+                tile_load(acc[q], blkX(XS30), SLD, n0, lane);
+                tile_mma(acc[q], blkX(XN32), SLD, blkX(XP20), SLD, n0, lane);
+                dst[q] = blkX(XS30) + n0;
+                ldd[q] = SLD;
+            } else if (kind == 5) {
+                tile_mma_sum(acc[q], blkX(XN20), blkX(XP20), SLD, blkA(0, 0), LDA, n0, lane);
+                dst[q] = blkA(2, 0) + n0;
+                ldd[q] = LDA;
+            } else {
+                // kind 1: T10 = N10 T00, 2: T21 = N21 T11, 3: T32 = N32 T22, 4: T31 = S31 T11
+                const int xa = kind == 1 ? XN10 : (kind == 2 ? XN21 : (kind == 3 ? XN32 : XS31));
+                const int dj = kind == 1 ? 0 : (kind == 3 ? 2 : 1);
+                const int di = kind == 1 ? 1 : (kind == 2 ? 2 : 3);
+                tile_mma(acc[q], blkX(xa), SLD, blkA(dj, dj), LDA, n0, lane);
+                dst[q] = blkA(di, dj) + n0;
+                ldd[q] = LDA;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) tile_store(dst[q], ldd[q], 0, acc[q], lane);
+    }
+    named_bar_sync(bid, 128);
+    // phase 4: T30 = S30 T00
+    if (pw < 2) {
+        const int n0 = 8 * pw;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma(acc, blkX(XS30), SLD, blkA(0, 0), LDA, n0, lane);
+        tile_store(blkA(3, 0), LDA, n0, acc, lane);
+    }
+    named_bar_sync(bid, 128);
+}
+
+
+__global__ void __launch_bounds__(NT, 5)
+wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gb = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- which chunk: slot -> (sequence n, chunk c) ----------------------
+    const int h = (int)(blockIdx.x % (unsigned)p.Nv);
+    const long long slot = blockIdx.x / (unsigned)p.Nv;
+    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wy_slot(seq_bos(p, mid), mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int n = lo;
+    const long long bos = seq_bos(p, n), eos = seq_eos(p, n);
+    if (bos < 0 || eos < bos || eos > p.tokens) return;  // the scan kernel reports it
+    const long long c = slot - wy_slot(bos, n);
+    const long long t0 = bos + c * C;
+    if (c < 0 || t0 >= eos) return;  // a slot no chunk maps to
+    const int L = (int)min((long long)C, eos - t0);
+    const int hk = h / (p.Nv / p.Nk);
+    WY_TRACE_EV(0);
+
+    const uint32_t b_tma = base + OFF_BAR, b_mma = base + OFF_BAR + 8;
+    volatile int *okf = reinterpret_cast<volatile int *>(gb + OFF_BAR + 20);
+    float *sc = reinterpret_cast<float *>(gb + OFF_SC);
+    if (threadIdx.x == 0) {
+        mbar_init(b_tma, 1);
+        mbar_init(b_mma, 1);
+        *okf = 1;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(base + OFF_BAR + 16, TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *reinterpret_cast<volatile uint32_t *>(gb + OFF_BAR + 16);
+    WY_TRACE_EV(1);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_tma, 16384);
+            tma_load_3d(base + OFF_K, &mK, b_tma, 0, hk, (int)t0);
+            tma_load_3d(base + OFF_K + 8192, &mK, b_tma, 64, hk, (int)t0);
+        }
+        chunk_scalars(p, h, t0, L, sc, lane);
+        __syncwarp();
+        if (lane == 0) {
+            bool ok = wait_bounded(b_tma, 0);
+            WY_TRACE_EV(2);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t a = base + OFF_K + kb * 8192 + kk * 32;
+                        mma_ss(tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KK, (kb | kk) != 0);
+                    }
+                mma_commit(b_mma);
+                ok = wait_bounded(b_mma, 0);
+                WY_TRACE_EV(3);
+                if (!ok) wait_bounded(b_mma, 0);  // drain: the MMA still reads shared memory
+            } else {
+                wait_bounded(b_tma, 0);  // drain: the copy may still land
+            }
+            if (!ok) {
+                *okf = 0;
+                atomicOr(p.status, kStatusTimeout);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const bool ok = *okf != 0;
+
+    float *sA = reinterpret_cast<float *>(gb + OFF_K);  // K is no longer read
+    if (ok && warp < 2) {
+        // A row i (TMEM lane i): A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij, j < i
+        const int i = threadIdx.x;
+        const float Gi = sc[SC_G + i], ai = -sc[SC_BETA + i] * sc[SC_AF + i];
+        const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
+        uint32_t r[32];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            tmem_ld32(tm + ((uint32_t)(32 * warp) << 16) + 32 * hf, r);
+            // D_ij = e^{G_i - G_j}: the product of the two per-chunk factors
+            // when the chunk's log-gate span allows it, else one exponential
+            float dcy[32];
+            if (fact) {
+                const float4 *b4 = reinterpret_cast<const float4 *>(sc + SC_BF + 32 * hf);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 bb = b4[q4];
+                    dcy[4 * q4] = ai * bb.x;
+                    dcy[4 * q4 + 1] = ai * bb.y;
+                    dcy[4 * q4 + 2] = ai * bb.z;
+                    dcy[4 * q4 + 3] = ai * bb.w;
+                }
+            } else {
+                const float nb = -sc[SC_BETA + i];
+                const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 32 * hf);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 gg = g4[q4];
+                    const int j = 32 * hf + 4 * q4;
+                    dcy[4 * q4] = nb * __expf(j < i ? Gi - gg.x : -INFINITY);
+                    dcy[4 * q4 + 1] = nb * __expf(j + 1 < i ? Gi - gg.y : -INFINITY);
+                    dcy[4 * q4 + 2] = nb * __expf(j + 2 < i ? Gi - gg.z : -INFINITY);
+                    dcy[4 * q4 + 3] = nb * __expf(j + 3 < i ? Gi - gg.w : -INFINITY);
+                }
+            }
+            tmem_wait_ld_dep(r);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                float val[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 32 * hf + 4 * q4 + e;
+                    val[e] = j < i ? dcy[4 * q4 + e] * __uint_as_float(r[4 * q4 + e]) : 0.f;
+                }
+                *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
+                    make_float4(val[0], val[1], val[2], val[3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    WY_TRACE_EV(4);
+    if (ok) {
+        float *scr = reinterpret_cast<float *>(gb + OFF_T);
+        solve_T(sA, scr, warp, lane, 1);
+        WY_TRACE_EV(5);
+        // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
+        const int i = threadIdx.x & 63;
+        const bool tp = threadIdx.x < 64;
+        const float *trow = sA + i * LDA;
+        const float *cs = sc + (tp ? SC_BEG : SC_BETA);
+        const uint32_t dst = base + OFF_T + (tp ? 0u : 8192u);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float tv[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 a = *reinterpret_cast<const float4 *>(trow + 32 * hf + 4 * q4);
+                const float4 cc = *reinterpret_cast<const float4 *>(cs + 32 * hf + 4 * q4);
+                tv[4 * q4] = a.x * cc.x;
+                tv[4 * q4 + 1] = a.y * cc.y;
+                tv[4 * q4 + 2] = a.z * cc.z;
+                tv[4 * q4 + 3] = a.w * cc.w;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                st_shared_v4(dst + sw128(i, 4 * hf + ch), pack_bf16(tv[8 * ch], tv[8 * ch + 1]),
+                             pack_bf16(tv[8 * ch + 2], tv[8 * ch + 3]), pack_bf16(tv[8 * ch + 4], tv[8 * ch + 5]),
+                             pack_bf16(tv[8 * ch + 6], tv[8 * ch + 7]));
+        }
+        __syncthreads();
+        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.ws) +
+                                               ((size_t)h * p.nslots + slot) * kSlotBytes);
+        const uint4 *src = reinterpret_cast<const uint4 *>(gb + OFF_T);
+#pragma unroll
+        for (int k = 0; k < (int)(kSlotBytes / 16 / NT); ++k) out[threadIdx.x + NT * k] = src[threadIdx.x + NT * k];
+        WY_TRACE_EV(6);
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tm, TM_COLS);
+    }
+}
+
+}  // namespace
+
+size_t wy_smem_bytes() { return SMEM_ALLOC; }
+
+cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, cudaStream_t stream) {
+    const long long grid = p.nslots * p.Nv;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(wy_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    if (err != cudaSuccess) return err;
+    wy_fwd<<<(unsigned)grid, NT, SMEM_ALLOC, stream>>>(mK, p);
+    return cudaGetLastError();
+}
+
+}  // namespace dn

@@ -21,7 +21,9 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major
  *     and contiguous, 16-byte aligned.  The library keeps no reference to
- *     them after the call and allocates no device memory per call.
+ *     them after the call and allocates no device memory: scratch space the
+ *     computation needs is a caller-owned workspace (see
+ *     dn_chunk_fwd_workspace_bytes).
  *   - Calls are asynchronous and ordered on `stream` (NULL = legacy default
  *     stream).  Outputs are valid once the stream reaches the call.
  *   - Errors are returned as a dn_status, never thrown or aborted.  Argument
@@ -33,6 +35,7 @@
 #ifndef DN_CHUNK_FWD_H
 #define DN_CHUNK_FWD_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -88,16 +91,39 @@ typedef enum {
  *                                           every sequence (rounded to nearest
  *                                           even from fp32 for DN_BF16).
  *   ht          [N, Nv, dk, dv] float32     final state; NULL: not written.
+ *   workspace   device scratch of at least dn_chunk_fwd_workspace_bytes()
+ *               bytes for these sizes, 16-byte aligned, owned by the caller
+ *               and not touched by anyone else until the stream has passed
+ *               the call.  May be NULL when that size is 0.  Its contents on
+ *               entry do not matter; on exit they are unspecified.
+ *   workspace_bytes  its size in bytes.
  *   stream      CUDA stream for the launch.
  *
- * Returns DN_OK once the work is enqueued.  One kernel launch per call.
+ * Returns DN_OK once the work is enqueued; DN_ERR_INVALID_ARG also when the
+ * workspace is missing, misaligned or too small.  The tensor-core path
+ * (bf16, dk = 128, dv a multiple of 128) launches two kernels per call: the
+ * per-chunk WY inverse T of every chunk in parallel ([WY] §2.3-§2.4), then
+ * the sequential state scan and output ([CGDR] §3.2-§3.3).  Other shapes
+ * launch one CUDA-core kernel.
  */
 dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,
                        const int64_t *cu_seqlens, int n_seqs,
                        int B, int T, int Nk, int Nv, int dk, int dv,
                        dn_dtype dtype, float scale, int chunk,
-                       void *o, float *ht, dn_stream_t stream);
+                       void *o, float *ht, void *workspace, size_t workspace_bytes,
+                       dn_stream_t stream);
+
+/*
+ * dn_chunk_fwd_workspace_bytes -- bytes of workspace dn_chunk_fwd needs for
+ * these sizes (same meaning as there).  For the tensor-core path it is
+ * (floor(B*T / 64) + n_seqs) * Nv * 16384: one 16 KB slot per chunk and value
+ * head holding the bf16 matrices T diag(beta e^G) and T diag(beta) of the
+ * chunk's WY representation ([WY] §2.4).  Returns 0 when no workspace is
+ * needed, and for sizes dn_chunk_fwd would reject.  Host-only; no CUDA call.
+ */
+size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
+                                    dn_dtype dtype, int chunk);
 
 /*
  * dn_check -- wait for `stream`, then read and clear the device status word

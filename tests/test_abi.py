@@ -63,12 +63,13 @@ A = 1 << 20
 
 def call(clib, **over):
     args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
-                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, chunk=64, o=A, ht=None)
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, chunk=64, o=A, ht=None, ws=None,
+                wsb=0)
     args.update(over)
     return clib.dn_chunk_fwd(args["q"], args["k"], args["v"], args["beta"], args["g"], args["h0"],
                              args["cu"], args["n"], args["B"], args["T"], args["Nk"], args["Nv"],
                              args["dk"], args["dv"], args["dtype"], args["scale"], args["chunk"],
-                             args["o"], args["ht"], None)
+                             args["o"], args["ht"], args["ws"], args["wsb"], None)
 
 
 @pytest.mark.parametrize("over,code", [
@@ -92,6 +93,24 @@ def call(clib, **over):
 ])
 def test_invalid_arguments_rejected_on_host(clib, over, code):
     assert call(clib, **over) == code
+
+
+def test_workspace_size(clib):
+    """One 16 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
+    ws = clib.dn_chunk_fwd_workspace_bytes
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 16384
+    assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 16384
+    assert ws(2, 2, 64, 2, 4, 64, 64, dn.DN_BF16, 64) == 0       # CUDA-core path
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
+    assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
+    assert ws(0, 0, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 32) == 0     # rejected chunk size
+
+
+@pytest.mark.parametrize("ws,wsb", [(None, 0), (A, 1024), (A + 8, 1 << 30), (None, 1 << 30)])
+def test_workspace_checked_on_host(clib, ws, wsb):
+    """The tensor-core path rejects a missing, small or misaligned workspace before any launch."""
+    assert call(clib, dk=128, dv=128, Nk=2, Nv=4, ws=ws, wsb=wsb) == dn.DN_ERR_INVALID_ARG
 
 
 def test_zero_sequences_is_a_noop(clib):

@@ -131,6 +131,35 @@ def test_guard_regions_untouched(lib):
     check(inp, o, ht, label="guards")
 
 
+def test_workspace_bounds_and_contents(lib):
+    """The WY kernel writes inside the queried workspace size only, and the
+    result does not depend on what the workspace held before the call."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = inputs(B=1, Nk=2, Nv=4, dk=128, dv=128, lengths=[64, 1, 130, 0, 65], seed=311)
+    d = workloads.to_device(inp, "cuda")
+    nbytes = dn.workspace_for(d["q"], d["v"], inp["N"]).numel()
+    buf = torch.full((nbytes + 65536,), 0xA5, dtype=torch.uint8, device="cuda")
+    o1, h1 = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
+                          scale=inp["scale"], workspace=buf[:nbytes])
+    assert dn.dn_check() == dn.DN_OK
+    assert bool((buf[nbytes:] == 0xA5).all())
+    buf[:nbytes].fill_(0xFF)  # NaN bit patterns everywhere
+    o2, h2 = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
+                          scale=inp["scale"], workspace=buf[:nbytes])
+    assert dn.dn_check() == dn.DN_OK
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    check(inp, o1, h1, label="workspace")
+
+
+def test_varlen_many_short(lib):
+    """Many sequences, aligned and ragged, packed: every chunk keeps its own
+    workspace slot."""
+    lengths = [64, 64, 64, 1, 1, 1, 1, 1, 130, 0, 0, 65, 127, 63, 2, 256]
+    inp = inputs(B=1, Nk=2, Nv=4, dk=128, dv=128, lengths=lengths, seed=312)
+    o, ht = run_gpu(inp)
+    check(inp, o, ht, label="many short")
+
+
 def test_empty_sequences_keep_h0(lib):
     inp = inputs(B=1, dk=128, dv=128, lengths=[0, 5, 0], seed=308)
     o, ht = run_gpu(inp)
@@ -144,11 +173,12 @@ def test_zero_tokens(lib):
     assert o.numel() == 0 and torch.equal(ht.cpu(), inp["h0"])
 
 
-def test_malformed_cu_seqlens_reported(lib):
-    """A decreasing cu_seqlens is caught by the kernel's own bounds check and
+@pytest.mark.parametrize("dk", [64, 128])
+def test_malformed_cu_seqlens_reported(lib, dk):
+    """A decreasing cu_seqlens is caught by the kernels' own bounds checks and
     reported by dn_check; the bad sequence is skipped, the others computed."""
     import chunkwise_gated_delta_chunk_gb300 as dn
-    inp = inputs(B=1, dk=64, dv=64, lengths=[10, 20, 30], seed=310)
+    inp = inputs(B=1, dk=dk, dv=dk, lengths=[10, 20, 30], seed=310)
     d = workloads.to_device(inp, "cuda")
     cu = torch.tensor([0, 10, 5, 60], dtype=torch.int64, device="cuda")
     o, ht = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], cu,
