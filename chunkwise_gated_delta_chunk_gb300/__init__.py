@@ -6,8 +6,8 @@ There is no CPU path: if the library is missing, :func:`load` raises.
 PyTorch supplies device memory and streams.
 
 Names follow the C ABI: :func:`dn_chunk_fwd`,
-:func:`dn_chunk_fwd_workspace_bytes`, :func:`dn_check`, :func:`dn_status_str`,
-:func:`dn_last_kernel`.  :func:`chunk_fwd` is a convenience that allocates
+:func:`dn_chunk_fwd_workspace_bytes`, :func:`dn_chunk_fwd_noalloc`,
+:func:`dn_check`, :func:`dn_status_str`, :func:`dn_last_kernel`.  :func:`chunk_fwd` is a convenience that allocates
 ``o``, ``ht`` and the workspace with torch and calls :func:`dn_chunk_fwd`.
 """
 from __future__ import annotations
@@ -29,8 +29,11 @@ DN_BF16 = 0
 DN_F32 = 1
 
 # Every symbol the public header declares.
-ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_check", "dn_status_str",
-               "dn_last_kernel")
+ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_chunk_fwd_noalloc", "dn_check",
+               "dn_status_str", "dn_last_kernel")
+
+# Size of the library's fixed scratch array used by dn_chunk_fwd_noalloc.
+DN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 _lib = None
 _lock = threading.Lock()
@@ -60,6 +63,8 @@ def load(path: str | None = None):
         lib.dn_chunk_fwd.restype = I
         lib.dn_chunk_fwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
         lib.dn_chunk_fwd_workspace_bytes.restype = Z
+        lib.dn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P]
+        lib.dn_chunk_fwd_noalloc.restype = I
         lib.dn_check.argtypes = [P]
         lib.dn_check.restype = I
         lib.dn_status_str.argtypes = [I]
@@ -107,6 +112,17 @@ def dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv,
                             _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
                             int(dk), int(dv), int(dtype), float(scale), int(chunk), _ptr(o),
                             _ptr(ht), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def dn_chunk_fwd_noalloc(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
+                         scale, chunk, o, ht, stream=None) -> int:
+    """Call the C entry point that takes no workspace (it uses the library's
+    fixed scratch array and allocates nothing); returns its status code."""
+    lib = load()
+    return lib.dn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                                    _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk),
+                                    int(Nv), int(dk), int(dv), int(dtype), float(scale), int(chunk),
+                                    _ptr(o), _ptr(ht), _stream(stream))
 
 
 def dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype, chunk=64) -> int:

@@ -126,6 +126,39 @@ size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, in
                                     dn_dtype dtype, int chunk);
 
 /*
+ * dn_chunk_fwd_noalloc -- dn_chunk_fwd for callers that cannot allocate
+ * device memory where they call it (for example a plugin host whose execute
+ * path may not allocate because the host owns every device buffer, or a
+ * runtime that committed all device memory to its own pool, where cudaMalloc
+ * would fail or stall the device).  The paper has no counterpart: this is a
+ * packaging variant of the same computation, not a step of the method.
+ *
+ * Same arguments and results as dn_chunk_fwd, without a workspace: the
+ * scratch space lives in one fixed device array of this library,
+ * DN_NOALLOC_SCRATCH_BYTES long, that each GPU holds from the time the
+ * library's code is loaded on it until the process exits.  The call
+ * allocates nothing.
+ *   - Sizes whose dn_chunk_fwd_workspace_bytes() exceeds
+ *     DN_NOALLOC_SCRATCH_BYTES are rejected with DN_ERR_UNSUPPORTED before
+ *     anything is launched (64 MiB covers (floor(B*T/64) + n_seqs) * Nv <=
+ *     4096, e.g. B = 4, T = 2048, Nv = 16).
+ *   - The first call with a given device current looks up the array's device
+ *     address there (a host query that allocates nothing); make that first
+ *     call before any stream capture on that device.
+ *   - Every call uses the same array; its contents on entry do not matter.
+ *     Calls whose kernels can overlap on one GPU (other streams, other host
+ *     threads) race on it; calls ordered in one stream do not.
+ */
+#define DN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                               const float *beta, const float *g, const float *h0,
+                               const int64_t *cu_seqlens, int n_seqs,
+                               int B, int T, int Nk, int Nv, int dk, int dv,
+                               dn_dtype dtype, float scale, int chunk,
+                               void *o, float *ht, dn_stream_t stream);
+
+/*
  * dn_check -- wait for `stream`, then read and clear the device status word
  * of the current device.  Returns DN_ERR_TIMEOUT or DN_ERR_DEVICE_ARG if a
  * kernel of this library recorded one since the last check, DN_ERR_CUDA if
