@@ -19,10 +19,11 @@ constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, 
 constexpr int SCAL_FLOATS = 512;
 constexpr float kSpanMax = 80.f;
 
-// Bytes of one workspace slot: T' = T diag(beta e^G) and T'' = T diag(beta),
-// each a 64 x 64 bf16 matrix stored as the 128-byte-swizzled K-major image
-// the MMAs read (row i at 128 i, 16-byte chunk c at (c ^ (i & 7)) * 16).
-constexpr uint32_t kSlotBytes = 16384;
+// Bytes of one workspace slot: T' = T diag(beta e^G), T'' = T diag(beta) and
+// P = tril(scale QK^T . D), each a 64 x 64 bf16 matrix stored as the
+// 128-byte-swizzled K-major image the MMAs read (row i at 128 i, 16-byte
+// chunk c at (c ^ (i & 7)) * 16), in that order.
+constexpr uint32_t kSlotBytes = 24576;
 
 __device__ __forceinline__ long long seq_bos(const Params &p, int n) {
     return p.cu ? p.cu[n] : (long long)n * p.T;
@@ -37,11 +38,18 @@ __device__ __forceinline__ long long seq_eos(const Params &p, int n) {
 // every sequence and stays below floor(tokens / C) + N.
 __device__ __forceinline__ long long wy_slot(long long t0, int n) { return t0 / kChunk + n; }
 
-// Gate scalars of the chunk [t0, t0 + L) of value head h, computed by one
-// warp (lane owns tokens lane and lane + 32) into `sc`.  Tokens past L get
-// beta = 0 and g = 0, so they write nothing and decay nothing.
-__device__ __forceinline__ void chunk_scalars(const Params &p, int h, long long t0, int L, float *sc,
-                                              int lane) {
+// Gate scalars of one chunk, per lane (tokens lane and lane + 32).
+struct ChunkScalars {
+    float ga, gb, ba, bb;      // G and beta of the lane's two tokens
+    float GL, G0, span;        // G at the last token and at the first, max - min of G
+    int L;
+};
+
+// Loads and prefix-sums the gates of the chunk [t0, t0 + L) of value head h
+// (one warp).  Tokens past L get beta = 0 and g = 0, so they write nothing
+// and decay nothing.
+__device__ __forceinline__ ChunkScalars chunk_scalars_load(const Params &p, int h, long long t0, int L, int lane) {
+    ChunkScalars r;
     float ga = 0.f, gb = 0.f, ba = 0.f, bb = 0.f;
     if (lane < L) {
         ba = p.beta[(t0 + lane) * p.Nv + h];
@@ -64,36 +72,54 @@ __device__ __forceinline__ void chunk_scalars(const Params &p, int h, long long 
     gb += __shfl_sync(0xffffffffu, ga, 31);
     const float GLa = __shfl_sync(0xffffffffu, ga, (L - 1) & 31);
     const float GLb = __shfl_sync(0xffffffffu, gb, (L - 1) & 31);
-    const float GL = (L - 1) < 32 ? GLa : GLb;
-    // e^{G_i - G_j} = e^{G_i - G_0} e^{G_0 - G_j} is safe when the chunk's
-    // log-gate span is small enough that neither factor leaves fp32 range
-    const float G0 = __shfl_sync(0xffffffffu, ga, 0);
+    r.GL = (L - 1) < 32 ? GLa : GLb;
+    r.G0 = __shfl_sync(0xffffffffu, ga, 0);
     float gmax = fmaxf(ga, gb), gmin = fminf(ga, gb);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
         gmin = fminf(gmin, __shfl_xor_sync(0xffffffffu, gmin, off));
     }
+    r.span = gmax - gmin;
+    r.ga = ga;
+    r.gb = gb;
+    r.ba = ba;
+    r.bb = bb;
+    r.L = L;
+    return r;
+}
+
+// Writes the scalar block of a chunk (see the SC_ offsets) into `sc`.
+__device__ __forceinline__ void chunk_scalars_store(const Params &p, const ChunkScalars &r, float *sc, int lane) {
     const int ia = lane, ib = lane + 32;
-    sc[SC_G + ia] = ga;
-    sc[SC_G + ib] = gb;
-    sc[SC_BETA + ia] = ba;
-    sc[SC_BETA + ib] = bb;
-    sc[SC_BEG + ia] = ba * __expf(ga);
-    sc[SC_BEG + ib] = bb * __expf(gb);
-    sc[SC_DEC + ia] = ia < L ? __expf(GL - ga) : 0.f;
-    sc[SC_DEC + ib] = ib < L ? __expf(GL - gb) : 0.f;
-    sc[SC_OSC + ia] = p.scale * __expf(ga);
-    sc[SC_OSC + ib] = p.scale * __expf(gb);
-    sc[SC_AF + ia] = __expf(ga - G0);
-    sc[SC_AF + ib] = __expf(gb - G0);
-    sc[SC_BF + ia] = __expf(G0 - ga);
-    sc[SC_BF + ib] = __expf(G0 - gb);
+    sc[SC_G + ia] = r.ga;
+    sc[SC_G + ib] = r.gb;
+    sc[SC_BETA + ia] = r.ba;
+    sc[SC_BETA + ib] = r.bb;
+    sc[SC_BEG + ia] = r.ba * __expf(r.ga);
+    sc[SC_BEG + ib] = r.bb * __expf(r.gb);
+    sc[SC_DEC + ia] = ia < r.L ? __expf(r.GL - r.ga) : 0.f;
+    sc[SC_DEC + ib] = ib < r.L ? __expf(r.GL - r.gb) : 0.f;
+    sc[SC_OSC + ia] = p.scale * __expf(r.ga);
+    sc[SC_OSC + ib] = p.scale * __expf(r.gb);
+    // e^{G_i - G_j} = e^{G_i - G_0} e^{G_0 - G_j} is safe when the chunk's
+    // log-gate span is small enough that neither factor leaves fp32 range
+    sc[SC_AF + ia] = __expf(r.ga - r.G0);
+    sc[SC_AF + ib] = __expf(r.gb - r.G0);
+    sc[SC_BF + ia] = __expf(r.G0 - r.ga);
+    sc[SC_BF + ib] = __expf(r.G0 - r.gb);
     if (lane == 0) {
-        sc[SC_ALPHA] = __expf(GL);
-        sc[SC_L] = __int_as_float(L);
-        sc[SC_FACT] = (gmax - gmin <= kSpanMax) ? 1.f : 0.f;
+        sc[SC_ALPHA] = __expf(r.GL);
+        sc[SC_L] = __int_as_float(r.L);
+        sc[SC_FACT] = (r.span <= kSpanMax) ? 1.f : 0.f;
     }
+}
+
+// Gate scalars of the chunk [t0, t0 + L) of value head h, computed by one
+// warp into `sc`.
+__device__ __forceinline__ void chunk_scalars(const Params &p, int h, long long t0, int L, float *sc,
+                                              int lane) {
+    chunk_scalars_store(p, chunk_scalars_load(p, h, t0, L, lane), sc, lane);
 }
 
 }  // namespace dn

@@ -4,33 +4,33 @@
 // Sources: [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1-§3.3;
 //          [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §2.3-§3.4.
 //
-// The WY kernel (dn_wy.cu) has already written T' = T diag(beta e^G) and
-// T'' = T diag(beta) of every chunk to the workspace.  One persistent CTA per
-// (sequence, value head, 128-column value tile) then walks the sequence's
-// 64-token chunks in order.  The fp32 state lives in tensor memory,
-// transposed (lane = value column v, column = key index d), for the whole
-// sequence.  Every contraction is a tcgen05 MMA with M = 128:
+// The WY kernel (dn_wy.cu) has already written T' = T diag(beta e^G),
+// T'' = T diag(beta) and P = tril(scale QK^T . D) of every chunk to the
+// workspace.  One persistent CTA per (sequence, value head, 128-column value
+// tile) then walks the sequence's 64-token chunks in order.  The fp32 state
+// lives in tensor memory, transposed (lane = value column v, column = key
+// index d), for the whole sequence.  Every contraction is a tcgen05 MMA with
+// M = 128:
 //
-//   KQ  [K;Q] K^T        -> QK^T (rows 64-127; rows 0-63 unused)  (a6)
-//   W   K^T T'^T         -> W^T                                   (a4)
+//   W   K^T T'^T         -> W^T (double buffered)                 (a4)
 //   U   V^T T''^T        -> U^T                                   (a4)
 //   VN  U^T - S^T W^T    -> v_new^T (S^T as a bf16 TMEM operand)  (a5)
-//   O   S^T Q^T          -> inter-chunk output                    (a6)
 //   DS  S^T += v~^T K    -> state update, v~ = e^{G_L-G} v_new    (a5)
-//   PV  v_new^T P^T      -> intra-chunk output, P = tril(QK^T.D)  (a6)
+//   O   S^T Q~^T         -> inter-chunk output, Q~ = diag(scale e^G) Q  (a6)
+//   PV  += v_new^T P^T   -> intra-chunk output, same accumulator   (a6)
 //
-// Warp roles (10 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
+// Warp roles (14 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
 // group of four consecutive warps covers all 128 lanes):
-//   0      loader: TMA for the K, Q, V tiles of a chunk, one bulk copy of the
-//          chunk's T' | T'' slot, and the gate scalars (prefix sum G, e^G,
-//          decays) computed with warp shuffles;
+//   0      loader: TMA for the K, Q, V tiles of a chunk, bulk copies of the
+//          chunk's T', T'' and P into three two-deep rings, and the gate
+//          scalars (prefix sum G, e^G, decays) computed with warp shuffles;
 //   1      chain MMA issuer (one thread: U, VN, O, DS, PV) and TMEM owner;
-//   2-5    prep: one thread issues KQ and W as soon as a chunk has landed;
-//          the warpgroup turns QK^T into the masked, decayed P and W^T into
-//          the bf16 -W^T operand, running ahead of the state scan;
-//   6-9    state: v_new and v~ operands, the fp32 state update, ht, and
-//          the output o = scale e^{G} (S^T Q^T) + P v_new, stored as bf16,
-//          after the next state operand has been released.
+//   2-5    prep: one thread issues W of the next chunk as soon as its tiles
+//          and T' have landed; the warpgroup turns W^T into the bf16 -W^T
+//          operand, running ahead of the state scan;
+//   6-9    state: v_new and v~ operands, the fp32 state update, ht;
+//   10-13  output: o = scale e^{G} (S^T Q^T) + P v_new, transposed through
+//          shared memory and stored as bf16 rows.
 //
 // Every wait is bounded: after kTimeoutNs a CTA records kStatusTimeout in the
 // status word, raises a shared abort flag so the other roles stop too, drains
@@ -78,9 +78,10 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
 constexpr uint32_t STAGE_BYTES = 49152;  // K0 Q0 K1 Q1 V0 V1, 8 KB each
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_TB = OFF_STAGE + NS * STAGE_BYTES;  // 2 x (T' | T''), 16 KB each
-constexpr uint32_t OFF_P = OFF_TB + 2 * kSlotBytes;         // 2 x 8 KB (double buffered)
-constexpr uint32_t OFF_WT = OFF_P + 2 * 8192;               // -W^T 16 KB
+constexpr uint32_t OFF_TP = OFF_STAGE + NS * STAGE_BYTES;  // T'  ring, 2 x 8 KB
+constexpr uint32_t OFF_TU = OFF_TP + 2 * 8192;              // T'' ring, 2 x 8 KB
+constexpr uint32_t OFF_PR = OFF_TU + 2 * 8192;              // P   ring, 2 x 8 KB
+constexpr uint32_t OFF_WT = OFF_PR + 2 * 8192;              // -W^T 16 KB
 constexpr uint32_t OFF_SCAL = OFF_WT + 16384;               // NS x 2048 B
 constexpr uint32_t OFF_OST = OFF_SCAL + NS * SCAL_FLOATS * 4;  // output staging, 32 x 256 B
 constexpr uint32_t OFF_BAR = OFF_OST + 8192;
@@ -89,7 +90,7 @@ constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;          // TMEM base, abort 
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;           // alignment slack
 
-static_assert(OFF_TB % 1024 == 0 && OFF_P % 1024 == 0 && OFF_WT % 1024 == 0,
+static_assert(OFF_TP % 1024 == 0 && OFF_TU % 1024 == 0 && OFF_PR % 1024 == 0 && OFF_WT % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB of shared memory per CTA");
 
@@ -97,15 +98,17 @@ static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB of shared memory per CTA
 enum {
     B_FULL = 0,                 // NS: TMA bytes + loader scalars
     B_EMPTY = B_FULL + NS,      // NS: every reader of the stage is done
-    B_TF = B_EMPTY + NS,        // 2: T' | T'' slot landed
-    B_TE = B_TF + 2,            // 2: W (prep) and U (chain) MMAs done with it
-    B_KQW_FULL = B_TE + 2,      // QK^T in acc_kq and W^T in acc_w
-    B_WSM_FULL,                 // -W^T and P bf16 operands in shared memory
+    B_QS = B_EMPTY + NS,        // NS: the stage's Q rows scaled by scale e^G (prep)
+    B_TPF = B_QS + NS,          // 2: T' landed    (ring r's full barriers at B_TPF + 4 r)
+    B_TUF = B_TPF + 4,          // 2: T'' landed
+    B_PF = B_TUF + 4,           // 2: P landed
+    B_WF = B_PF + 2,            // W^T in acc_w
+    B_WSM_FULL,                 // -W^T bf16 operand in shared memory
     B_S_FULL,
     B_V_FULL,
     B_VSM_FULL,
-    B_S_UPD,                    // O and DS (state update) done
-    B_D_FULL,                   // O, DS and PV done
+    B_S_UPD,                    // DS of the chunk (and every earlier MMA) done
+    B_D_FULL,                   // every MMA of the chunk done
     B_O_EMPTY,
     B_DRAIN,
     B_DRAIN2,
@@ -114,11 +117,11 @@ enum {
 static_assert(B_COUNT <= NBARS, "barrier space");
 
 // Tensor memory columns (fp32 accumulators; SB holds bf16 pairs).
-constexpr uint32_t TM_KQ = 0, TM_W = 64, TM_V = 128, TM_S = 192, TM_SB = 320, TM_O = 384,
-                   TM_P = 448, TM_COLS = 512;
+// TM_V: two 64-column buffers (chunk parity); TM_SB: two 64-column buffers
+// (bf16 S^T at the start of chunk c in buffer c & 1); TM_O: O and PV of a chunk.
+constexpr uint32_t TM_W = 0, TM_V = 64, TM_S = 192, TM_SB = 320, TM_O = 448, TM_COLS = 512;
 
 // Instruction descriptors.
-constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);   // A, B K-major
 constexpr uint32_t ID_W = idesc_bf16(128, 64, 1, 0);    // A MN-major (K^T), B K-major
 constexpr uint32_t ID_U = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_VN = idesc_bf16(128, 64, 0, 1);   // A TMEM, B MN-major (-W^T rows d)
@@ -229,20 +232,38 @@ __device__ __forceinline__ Unit unit_of(const Params &p) {
     return u;
 }
 
+// Bulk copy of ring r (0: T', 1: T'', 2: P) of chunk c into buffer c & 1
+// (one thread; the buffer must be free).
+__device__ __forceinline__ void load_ring(const Ctx &x, const Params &p, const Unit &u, int r, int c) {
+    const long long t0 = u.bos + (long long)c * C;
+    const uint8_t *slot = static_cast<const uint8_t *>(p.ws) +
+                          ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n)) * kSlotBytes + 8192 * r;
+    const uint32_t fb = bar(x, B_TPF + 4 * r + (c & 1));
+    mbar_arrive_expect_tx(fb, 8192);
+    bulk_load(x.base + OFF_TP + r * 16384 + (c & 1) * 8192, slot, 8192, fb);
+}
+
 // ---------------------------------------------------------------------------
-// Loader warp: TMA tiles, the T' | T'' slot and the gate scalars of each chunk.
+// Loader warp: TMA tiles and gate scalars of each chunk, and the first two
+// chunks' T', T'' and P images (later ones are fetched by their readers as
+// soon as a ring buffer frees up).  armed is the last chunk whose stage was
+// armed.
 // ---------------------------------------------------------------------------
 __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
-                            const CUtensorMap *mQ, const CUtensorMap *mV, int &armed_last, int &armed_t) {
+                            const CUtensorMap *mQ, const CUtensorMap *mV, int &armed) {
     const int lane = threadIdx.x & 31;
-    armed_last = armed_t = -1;
-    const uint8_t *wsu = static_cast<const uint8_t *>(p.ws) + (size_t)u.h * p.nslots * kSlotBytes;
+    armed = -1;
+    if (lane == 0)
+        for (int c = 0; c < min(u.nc, 2); ++c)
+            for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c);
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
-        if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
-        DN_TRACE_EV(0, c);
         const long long t0 = u.bos + (long long)c * C;
         const int L = (int)min((long long)C, u.eos - t0);
+        // the gates come from global memory while the stage is still in use
+        const ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
+        if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
+        DN_TRACE_EV(0, c);
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         if (lane == 0) {
             const uint32_t fb = bar(x, B_FULL + s);
@@ -255,21 +276,11 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
             tma_load_3d(st + 32768, mV, fb, u.v0, u.h, tt);
             tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
         }
-        armed_last = c;
-        chunk_scalars(p, u.h, t0, L, scal(x, s), lane);
+        armed = c;
+        DN_TRACE_EV(2, c);
+        chunk_scalars_store(p, cs, scal(x, s), lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
-        // T' | T'' of the chunk into buffer c & 1, once both of its readers
-        // are done with chunk c - 2's
-        const int t = c & 1;
-        if (!wwait(x, bar(x, B_TE + t), ((c >> 1) & 1) ^ 1)) return;
-        if (lane == 0) {
-            const uint32_t tf = bar(x, B_TF + t);
-            mbar_arrive_expect_tx(tf, kSlotBytes);
-            bulk_load(x.base + OFF_TB + t * kSlotBytes, wsu + (size_t)wy_slot(t0, u.n) * kSlotBytes, kSlotBytes,
-                      tf);
-        }
-        armed_t = c;
         DN_TRACE_EV(1, c);
     }
 }
@@ -277,100 +288,142 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
 // ---------------------------------------------------------------------------
 // MMA issue helpers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void issue_kq(const Ctx &x, uint32_t tm, int c) {
-    const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t a = st + kb * 16384 + kk * 32;
-            mma_ss(tm + TM_KQ, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
-        }
-}
-
+// W^T = K^T T'^T of chunk c into acc_w.
 __device__ __forceinline__ void issue_w(const Ctx &x, uint32_t tm, int c) {
     const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
-    const uint32_t tp = x.base + OFF_TB + (c & 1) * kSlotBytes;  // T'
+    const uint32_t tp = x.base + OFF_TP + (c & 1) * 8192;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
         mma_ss(tm + TM_W, sdesc(st + kk * 2048, 16384, 1024), sdesc(tp + kk * 32, 16, 1024), ID_W, kk != 0);
 }
 
+// U^T = V^T T''^T of chunk c into acc_v[c & 1].
 __device__ __forceinline__ void issue_u(const Ctx &x, uint32_t tm, int c) {
     const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES + 32768;
-    const uint32_t tpp = x.base + OFF_TB + (c & 1) * kSlotBytes + 8192;  // T''
+    const uint32_t tpp = x.base + OFF_TU + (c & 1) * 8192;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
-        mma_ss(tm + TM_V, sdesc(st + kk * 2048, 8192, 1024), sdesc(tpp + kk * 32, 16, 1024), ID_U, kk != 0);
+        mma_ss(tm + TM_V + 64 * (c & 1), sdesc(st + kk * 2048, 8192, 1024), sdesc(tpp + kk * 32, 16, 1024), ID_U,
+               kk != 0);
 }
 
-// O^T = S^T Q^T (inter-chunk output) of chunk c into acc_o.
+// O^T = S^T Q~^T (inter-chunk output, Q~ = diag(scale e^G) Q) of chunk c into acc_o.
 __device__ __forceinline__ void issue_o(const Ctx &x, uint32_t tm, int c) {
     const uint32_t st = x.base + OFF_STAGE + (c % NS) * STAGE_BYTES;
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tm + TM_O, tm + TM_SB + kb * 32 + kk * 8, sdesc(st + 8192 + kb * 16384 + kk * 32, 16, 1024),
-                   ID_O, (kb | kk) != 0);
+            mma_ts(tm + TM_O, tm + TM_SB + 64 * (c & 1) + kb * 32 + kk * 8,
+                   sdesc(st + 8192 + kb * 16384 + kk * 32, 16, 1024), ID_O, (kb | kk) != 0);
 }
 
 // ---------------------------------------------------------------------------
-// Chain MMA issuer (one thread): U, VN, O, DS and PV.
+// Chain MMA issuer (one thread).  The tensor pipe runs MMAs in issue order,
+// so the state-dependent VN and DS go first and the others fill the gaps
+// while the state warpgroup converts operands:
+//   VN(c); U(c+1) while v_new^T is converted; DS(c);
+//   O(c) and PV(c) while S^T is converted (into the other S^T buffer).
+// It also refills the T'' and P rings as their buffers free up (W and the
+// T' ring belong to the prep warpgroup).
 // ---------------------------------------------------------------------------
-__device__ void mma_role(const Ctx x, const Unit u, uint32_t tm) {
-    for (int c = 0; c < u.nc; ++c) {
+__device__ __forceinline__ bool wait_tiles(const Ctx &x, int c, int ring) {
+    return wait(x, bar(x, B_FULL + c % NS), (c / NS) & 1) &&
+           wait(x, bar(x, B_TPF + 4 * ring + (c & 1)), (c >> 1) & 1);
+}
+
+__device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
+    int loaded[3];  // last chunk whose T'' / P copy was issued (index 1, 2)
+    loaded[1] = loaded[2] = min(u.nc, 2) - 1;
+    int c = 0;
+    if (wait_tiles(x, 0, 1)) {
+        tc_fence_after();
+        issue_u(x, tm, 0);
+    } else {
+        c = u.nc;
+    }
+    for (; c < u.nc; ++c) {
         const int s = c % NS, t = c & 1;
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         const uint32_t par = c & 1;
-        // U^T into acc_v, once the previous chunk's DS / PV (which read acc_v)
-        // are done; then v_new^T = U^T + S^T (-W^T), in issue order.
-        if (c > 0 && !wait(x, bar(x, B_D_FULL), (c - 1) & 1)) break;
-        if (!wait(x, bar(x, B_FULL + s), (c / NS) & 1)) break;
-        if (!wait(x, bar(x, B_TF + t), (c >> 1) & 1)) break;
-        tc_fence_after();
-        issue_u(x, tm, c);
-        DN_TRACE_EV(1, c);
+        const uint32_t av = tm + TM_V + 64 * t;  // acc_v of this chunk
+        // v_new^T = U^T + S^T (-W^T), accumulated onto U^T (issued before by
+        // this thread, so in order)
         if (!wait(x, bar(x, B_WSM_FULL), par)) break;
         if (!wait(x, bar(x, B_S_FULL), par)) break;
         DN_TRACE_EV(2, c);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tm + TM_V, tm + TM_SB + kk * 8, sdesc(x.base + OFF_WT + kk * 2048, 8192, 1024), ID_VN, 1);
+            mma_ts(av, tm + TM_SB + 64 * t + kk * 8, sdesc(x.base + OFF_WT + kk * 2048, 8192, 1024), ID_VN, 1);
         mma_commit(bar(x, B_V_FULL));
-        mma_commit(bar(x, B_TE + t));
         DN_TRACE_EV(0, c);
-        // inter-chunk output S^T Q^T, once the output of the chunk before has
-        // read acc_o and acc_p; it runs while the state warpgroup prepares
-        // the v_new operands
-        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) break;
-        tc_fence_after();
-        issue_o(x, tm, c);
-        // state update and intra-chunk output
+        // U of the next chunk into the other acc_v buffer, whose last readers
+        // (DS / PV of chunk c - 1) are done; PV of c - 1 also freed the P
+        // buffer of chunk c + 1
+        if (c > 0) {
+            if (!wait(x, bar(x, B_D_FULL), (c - 1) & 1)) break;
+            if (c + 1 < u.nc) {
+                load_ring(x, p, u, 2, c + 1);
+                loaded[2] = c + 1;
+            }
+        }
+        // (only if its tiles are already in: a late stage must not hold up DS)
+        bool u_next = c + 1 >= u.nc;
+        if (!u_next && mbar_test_wait(bar(x, B_FULL + (c + 1) % NS), ((c + 1) / NS) & 1) &&
+            mbar_test_wait(bar(x, B_TUF + ((c + 1) & 1)), ((c + 1) >> 1) & 1)) {
+            tc_fence_after();
+            issue_u(x, tm, c + 1);
+            u_next = true;
+        }
+        // state update (VSM also means VN, hence U, of this chunk is done:
+        // its T'' buffer takes chunk c + 2's)
         if (!wait(x, bar(x, B_VSM_FULL), par)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tm + TM_S, tm + TM_V + 32 + kk * 8, sdesc(st + kk * 2048, 16384, 1024), ID_DS, 1);
+            mma_ts(tm + TM_S, av + 32 + kk * 8, sdesc(st + kk * 2048, 16384, 1024), ID_DS, 1);
         mma_commit(bar(x, B_S_UPD));
-        const uint32_t pbuf = x.base + OFF_P + (c & 1) * 8192;
+        DN_TRACE_EV(1, c);
+        if (!u_next) {
+            if (!wait_tiles(x, c + 1, 1)) break;
+            tc_fence_after();
+            issue_u(x, tm, c + 1);
+        }
+        if (c + 2 < u.nc) {
+            load_ring(x, p, u, 1, c + 2);
+            loaded[1] = c + 2;
+        }
+        // output: inter-chunk part O (reads S^T buffer c & 1, which the state
+        // warpgroup rewrites only after DS of the next chunk, a later commit
+        // of this thread) and the intra-chunk part PV on top, once the output
+        // of chunk c - 1 has read acc_o
+        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) break;
+        if (!wait(x, bar(x, B_QS + s), (c / NS) & 1)) break;
+        if (!wait(x, bar(x, B_PF + t), (c >> 1) & 1)) break;
+        tc_fence_after();
+        issue_o(x, tm, c);
+        const uint32_t pbuf = x.base + OFF_PR + t * 8192;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tm + TM_P, tm + TM_V + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, kk != 0);
+            mma_ts(tm + TM_O, av + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, 1);
         mma_commit(bar(x, B_D_FULL));
         mma_commit(bar(x, B_EMPTY + s));
         DN_TRACE_EV(3, c);
     }
-    // every MMA issued by this thread completes before tensor memory is freed
+    // every MMA issued by this thread completes before tensor memory is
+    // freed, and the last ring copies it issued land before shared memory
+    // goes
     mma_commit(bar(x, B_DRAIN));
     wait_drain(bar(x, B_DRAIN), 0);
+    for (int r = 1; r < 3; ++r)
+        for (int k = max(loaded[r] - 1, 0); k <= loaded[r]; ++k)
+            wait_drain(bar(x, B_TPF + 4 * r + (k & 1)), (k >> 1) & 1);
 }
 
 // ---------------------------------------------------------------------------
-// Output warpgroup: o = scale e^{G_i} (S^T Q^T)[v][i] + (v_new^T P^T)[v][i]
-// for value column v = this thread's TMEM lane, chunk by chunk after O, DS
-// and PV of the chunk are done.
+// Output warpgroup: o[i][v] = (S^T Q~^T + v_new^T P^T)[v][i] for value column
+// v = this thread's TMEM lane, chunk by chunk once O and PV are done.
 // ---------------------------------------------------------------------------
 __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
@@ -381,41 +434,28 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     const uint8_t *gbuf = x.gbase + OFF_OST;
     const long long rstride = (long long)p.Nv * p.dv * 2;  // bytes between tokens
     for (int c = 0; c < u.nc; ++c) {
-        const int s = c % NS;
-        if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return;
-        if (!wwait(x, bar(x, B_D_FULL), c & 1)) return;
+        // Every exit is taken by the whole warpgroup together (bar_red_or), so
+        // no warp is left waiting at one of its named barriers.
+        if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
         tc_fence_after();
-        const float *sc = scal(x, s);
-        const int L = __float_as_int(sc[SC_L]);
-        // combine both accumulators into packed bf16 pairs (tokens 2k, 2k + 1)
-        // and release them
+        const long long t0 = u.bos + (long long)c * C;
+        const int L = (int)min((long long)C, u.eos - t0);
+        // the chunk's output column v as packed bf16 pairs (tokens 2k, 2k + 1)
         uint32_t ob[32];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            uint32_t ra[32], qa[32];
+            uint32_t ra[32];
             tmem_ld32(lb + TM_O + 32 * hf, ra);
-            tmem_ld32(lb + TM_P + 32 * hf, qa);
             tmem_wait_ld_dep(ra);
-            tmem_wait_ld_dep(qa);
-            const float4 *osc4 = reinterpret_cast<const float4 *>(sc + SC_OSC + 32 * hf);
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4) {
-                const float4 os = osc4[k4];
-                ob[16 * hf + 2 * k4] =
-                    pack_bf16(fmaf(os.x, __uint_as_float(ra[4 * k4]), __uint_as_float(qa[4 * k4])),
-                              fmaf(os.y, __uint_as_float(ra[4 * k4 + 1]), __uint_as_float(qa[4 * k4 + 1])));
-                ob[16 * hf + 2 * k4 + 1] =
-                    pack_bf16(fmaf(os.z, __uint_as_float(ra[4 * k4 + 2]), __uint_as_float(qa[4 * k4 + 2])),
-                              fmaf(os.w, __uint_as_float(ra[4 * k4 + 3]), __uint_as_float(qa[4 * k4 + 3])));
-            }
+            for (int k = 0; k < 16; ++k)
+                ob[16 * hf + k] = pack_bf16(__uint_as_float(ra[2 * k]), __uint_as_float(ra[2 * k + 1]));
         }
         tc_fence_before();
         warp_arrive(bar(x, B_O_EMPTY));
-        warp_arrive(bar(x, B_EMPTY + s));  // done with the chunk's scalars
         DN_TRACE_EV(0, c);
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
-        const long long t0 = u.bos + (long long)c * C;
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -442,114 +482,76 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// Prep warpgroup: the KQ and W MMAs of each chunk as soon as its tiles and
-// T' have landed, then P = tril(scale QK^T . D) and -W^T as bf16 operands.
+// Prep warpgroup: W^T of each chunk (acc_w) into the bf16 -W^T operand of VN.
+// One thread issues W of the next chunk as soon as this chunk's operand is
+// out, and refills the T' ring.
 // ---------------------------------------------------------------------------
-// One thread of warp 2 issues KQ and W of chunk c once its tiles and T' have
-// landed; returns (to every lane of the warp) whether the waits succeeded.
-__device__ __forceinline__ bool issue_prep_mmas(const Ctx &x, uint32_t tm, int c) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) {
-        const int s = c % NS, t = c & 1;
-        ok = wait(x, bar(x, B_FULL + s), (c / NS) & 1) && wait(x, bar(x, B_TF + t), (c >> 1) & 1);
-        if (ok) {
-            tc_fence_after();
-            issue_kq(x, tm, c);
-            issue_w(x, tm, c);
-            mma_commit(bar(x, B_KQW_FULL));
-            mma_commit(bar(x, B_TE + t));
-        }
+__device__ __forceinline__ bool issue_w_mma(const Ctx &x, uint32_t tm, int c) {
+    const bool ok = wait_tiles(x, c, 0);
+    if (ok) {
+        tc_fence_after();
+        issue_w(x, tm, c);
+        mma_commit(bar(x, B_WF));
     }
-    return __shfl_sync(0xffffffffu, ok, 0);
+    return ok;
+}
+
+// Q row i *= scale e^{G_i} in place (bf16) for chunk c, so that O and PV
+// share one accumulator: o_i = S^T (scale e^{G_i} q_i) + sum_j P_ij v_new_j.
+// 128 threads; each step of a warp covers 512 contiguous bytes (4 rows x 8
+// chunks of 16 B), free of bank conflicts; the swizzle only permutes chunks
+// within a row.  Returns false if the stage did not arrive.
+__device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
+    const int s = c % NS;
+    if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return false;
+    const float *sc = scal(x, s);
+    const int tid = threadIdx.x - 64;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int k = tid + 128 * it, half = k >> 9, r = (k >> 3) & 63, ch = k & 7;
+        const float f = sc[SC_OSC + r];
+        uint4 *qp = reinterpret_cast<uint4 *>(x.gbase + OFF_STAGE + s * STAGE_BYTES + 8192 + 16384 * half + 128 * r +
+                                              16 * ch);
+        const uint4 q = *qp;
+        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+            w[e] = pack_bf16(lo * f, hi * f);
+        }
+        *qp = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    fence_proxy_async_smem();
+    warp_arrive(bar(x, B_QS + s));
+    return true;
 }
 
 __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
-    const float scale = p.scale;
     const int warp = threadIdx.x >> 5;
-    const int row = 32 * (warp & 3) + (threadIdx.x & 31);  // TMEM lane this thread reads
-    const bool rowP = row >= 64;              // QK^T rows (TMEM lanes 64-127)
-    const int i = row & 63;                   // token of the chunk for P
+    const bool leader = warp == 2 && (threadIdx.x & 31) == 0;
+    const int row = 32 * (warp & 3) + (threadIdx.x & 31);  // TMEM lane = key index d
     const uint32_t lb = lane_base(tm, warp);
-    bool ok = true;
-    if (warp == 2 && u.nc > 0) ok = issue_prep_mmas(x, tm, 0);
+    int loaded = min(u.nc, 2) - 1;  // last chunk whose T' copy was issued
+    bool lok = true;                // the leader's own waits
+    if (leader && u.nc > 0) lok = issue_w_mma(x, tm, 0);
+    if (u.nc > 0 && !scale_q(x, 0)) return;
     for (int c = 0; c < u.nc; ++c) {
-        const int s = c % NS;
-        const uint32_t par = c & 1;
-        // A failed wait leaves `ok` false but the chunk body still runs to its
-        // end (on garbage), so all four warps meet every named barrier; the
-        // group then leaves together.
-        ok = ok && wwait(x, bar(x, B_FULL + s), (c / NS) & 1);
-        ok = ok && wwait(x, bar(x, B_KQW_FULL), par);
-        // the operand buffers are free once the chain's VN of the chunk before
-        // has completed (its commit also covers PV of chunk c - 2, the last
-        // reader of P buffer c & 1)
-        if (c > 0) ok = ok && wwait(x, bar(x, B_V_FULL), (c - 1) & 1);
+        if (!wwait(x, bar(x, B_WF), c & 1) || !__all_sync(0xffffffffu, lok)) break;
+        // W of chunk c is done with its T' buffer: it takes chunk c + 2's
+        if (leader && c + 2 < u.nc) {
+            load_ring(x, p, u, 0, c + 2);
+            loaded = c + 2;
+        }
+        // the -W^T buffer is free once the chain's VN of the chunk before has
+        // completed
+        if (c > 0 && !wwait(x, bar(x, B_V_FULL), (c - 1) & 1)) break;
         DN_TRACE_EV(0, c);
         tc_fence_after();
-        const float *sc = scal(x, s);
         uint32_t r0[32], r1[32];
-        if (rowP) {
-            // P_ij = scale e^{G_i - G_j} (QK^T)_ij for j <= i, else 0: the
-            // product of the two per-chunk decay factors when the chunk's
-            // log-gate span allows it, else one exponential per element.
-            const float Gi = sc[SC_G + i], ai = scale * sc[SC_AF + i];
-            const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
-            tmem_ld32(lb + TM_KQ, r0);
-            tmem_ld32(lb + TM_KQ + 32, r1);
-            const uint32_t pb = x.base + OFF_P + (c & 1) * 8192;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float dcy[32];
-                if (fact) {
-                    const float4 *b4 = reinterpret_cast<const float4 *>(sc + SC_BF + 32 * hf);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 bb = b4[q4];
-                        dcy[4 * q4] = ai * bb.x;
-                        dcy[4 * q4 + 1] = ai * bb.y;
-                        dcy[4 * q4 + 2] = ai * bb.z;
-                        dcy[4 * q4 + 3] = ai * bb.w;
-                    }
-                } else {
-                    const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 32 * hf);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        const float4 gg = g4[q4];
-                        const int j = 32 * hf + 4 * q4;
-                        dcy[4 * q4] = scale * __expf(j <= i ? Gi - gg.x : -INFINITY);
-                        dcy[4 * q4 + 1] = scale * __expf(j + 1 <= i ? Gi - gg.y : -INFINITY);
-                        dcy[4 * q4 + 2] = scale * __expf(j + 2 <= i ? Gi - gg.z : -INFINITY);
-                        dcy[4 * q4 + 3] = scale * __expf(j + 3 <= i ? Gi - gg.w : -INFINITY);
-                    }
-                }
-                if (hf == 0) {
-                    tmem_wait_ld_dep(r0);
-                    tmem_wait_ld_dep(r1);
-                }
-                DN_TRACE_EV(4 + hf, c);
-                uint32_t pw[16];
-#pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
-                    const int j = 32 * hf + jj;
-                    const float a0 = __uint_as_float(hf ? r1[jj] : r0[jj]);
-                    const float a1 = __uint_as_float(hf ? r1[jj + 1] : r0[jj + 1]);
-                    const float v0 = j <= i ? dcy[jj] * a0 : 0.f;
-                    const float v1 = j + 1 <= i ? dcy[jj + 1] * a1 : 0.f;
-                    pw[jj / 2] = pack_bf16(v0, v1);
-                }
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    st_shared_v4(pb + sw128(i, 4 * hf + ch), pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2],
-                                 pw[4 * ch + 3]);
-            }
-        }
-        DN_TRACE_EV(6, c);
-        // -W^T row d = this thread's TMEM lane
         tmem_ld32(lb + TM_W, r0);
         tmem_ld32(lb + TM_W + 32, r1);
         tmem_wait_ld_dep(r0);
         tmem_wait_ld_dep(r1);
-        DN_TRACE_EV(7, c);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
@@ -563,27 +565,26 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
                 st_shared_v4(x.base + OFF_WT + sw128(row, 4 * hf + ch), w[0], w[1], w[2], w[3]);
             }
         }
-        DN_TRACE_EV(9, c);
         fence_proxy_async_smem();
         tc_fence_before();
-        // acc_kq and acc_w are read: the next chunk's KQ / W may go
-        named_bar_sync(1, 128);
-        DN_TRACE_EV(1, c);
-        warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars and tiles
         warp_arrive(bar(x, B_WSM_FULL));
         DN_TRACE_EV(3, c);
-        // the next chunk's prep MMAs, as soon as acc_kq and acc_w are free
-        if (warp == 2 && c + 1 < u.nc) ok = issue_prep_mmas(x, tm, c + 1) && ok;
-        if (bar_red_or(1, 128, !ok || *x.abort_flag)) break;
+        // the next chunk's W, once all four warps have read acc_w (their
+        // WSM arrivals)
+        if (leader && c + 1 < u.nc) lok = wait(x, bar(x, B_WSM_FULL), c & 1) && issue_w_mma(x, tm, c + 1);
+        if (c + 1 < u.nc && !scale_q(x, c + 1)) break;
     }
-    if (warp == 2 && (threadIdx.x & 31) == 0) {  // prep MMAs complete before tensor memory is freed
+    if (leader) {
+        // W completes before tensor memory is freed; the last T' copies it
+        // issued land before shared memory goes
         mma_commit(bar(x, B_DRAIN2));
         wait_drain(bar(x, B_DRAIN2), 0);
+        for (int k = max(loaded - 1, 0); k <= loaded; ++k) wait_drain(bar(x, B_TPF + (k & 1)), (k >> 1) & 1);
     }
 }
 
 // ---------------------------------------------------------------------------
-// State warpgroup: v_new operands, fp32 state, ht, and the chunk's output.
+// State warpgroup: v_new operands, fp32 state, ht.
 // ---------------------------------------------------------------------------
 __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
@@ -636,10 +637,11 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
             // v_new^T pairs go to columns 8 qq .., v~^T pairs to 32 + 8 qq ..
             // (each destination column has been read before it is written).
             const float4 *dec4 = reinterpret_cast<const float4 *>(scal(x, s) + SC_DEC);
+            const uint32_t lbv = lb + TM_V + 64 * (c & 1);  // acc_v of this chunk
             uint32_t q16[16], pv8[8], t8[3][8];
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-                tmem_ld16(lb + TM_V + 16 * qq, q16);
+                tmem_ld16(lbv + 16 * qq, q16);
                 tmem_wait_ld_dep16(q16);
                 uint32_t tq[8];
 #pragma unroll
@@ -652,18 +654,18 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
                     tq[2 * k4] = pack_bf16(a0 * dd.x, a1 * dd.y);
                     tq[2 * k4 + 1] = pack_bf16(a2 * dd.z, a3 * dd.w);
                 }
-                tmem_st8(lb + TM_V + 8 * qq, pv8);
+                tmem_st8(lbv + 8 * qq, pv8);
                 if (qq < 2) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) t8[qq][k] = tq[k];
                 } else if (qq == 2) {
-                    tmem_st8(lb + TM_V + 32, t8[0]);
-                    tmem_st8(lb + TM_V + 40, t8[1]);
+                    tmem_st8(lbv + 32, t8[0]);
+                    tmem_st8(lbv + 40, t8[1]);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) t8[2][k] = tq[k];
                 } else {
-                    tmem_st8(lb + TM_V + 48, t8[2]);
-                    tmem_st8(lb + TM_V + 56, tq);
+                    tmem_st8(lbv + 48, t8[2]);
+                    tmem_st8(lbv + 56, tq);
                 }
             }
             tmem_wait_st();
@@ -674,8 +676,8 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
         // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
         const bool last = (c + 1 == u.nc);
-        // (S_UPD also covers O of this chunk, which read the bf16 S^T
-        // operand this pass overwrites)
+        // (S_UPD also covers O of the chunk before, the last reader of the
+        // bf16 S^T buffer this pass overwrites)
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         DN_TRACE_EV(2, c);
         tc_fence_after();
@@ -686,7 +688,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
                     pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-                tmem_st16(lb + TM_SB + 16 * blk, pk);
+                tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
             } else if (p.ht) {
                 float *hp = p.ht + sbase + (size_t)(32 * blk) * dv;
 #pragma unroll
@@ -739,13 +741,15 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(x, B_FULL + s), 2);
-            mbar_init(bar(x, B_EMPTY + s), 13);
+            mbar_init(bar(x, B_EMPTY + s), 5);
+            mbar_init(bar(x, B_QS + s), 4);
         }
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(bar(x, B_TF + t), 1);
-            mbar_init(bar(x, B_TE + t), 2);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(x, B_TPF + b), 1);
+            mbar_init(bar(x, B_TUF + b), 1);
+            mbar_init(bar(x, B_PF + b), 1);
         }
-        mbar_init(bar(x, B_KQW_FULL), 1);
+        mbar_init(bar(x, B_WF), 1);
         mbar_init(bar(x, B_WSM_FULL), 4);
         mbar_init(bar(x, B_S_FULL), 4);
         mbar_init(bar(x, B_V_FULL), 1);
@@ -774,19 +778,16 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     const uint32_t tm = *reinterpret_cast<volatile uint32_t *>(x.gbase + OFF_MISC);
 
     if (warp == 0) {
-        int armed_last = -1, armed_t = -1;
-        loader_role(x, p, u, &mK, &mQ, &mV, armed_last, armed_t);
-        // drain: the last NS armed stages and the last two T' | T'' slots
-        // must have landed before exit
-        if ((threadIdx.x & 31) == 0) {
-            for (int c = armed_last - NS + 1; c <= armed_last; ++c)
+        int armed = -1;
+        loader_role(x, p, u, &mK, &mQ, &mV, armed);
+        // drain: the last NS armed stages must have landed before exit (the
+        // ring copies are drained by the roles that issued them)
+        if ((threadIdx.x & 31) == 0)
+            for (int c = armed - NS + 1; c <= armed; ++c)
                 if (c >= 0) wait_drain(bar(x, B_FULL + c % NS), (c / NS) & 1);
-            for (int c = armed_t - 1; c <= armed_t; ++c)
-                if (c >= 0) wait_drain(bar(x, B_TF + (c & 1)), (c >> 1) & 1);
-        }
         __syncwarp();
     } else if (warp == 1) {
-        if ((threadIdx.x & 31) == 0 && u.nc > 0) mma_role(x, u, tm);
+        if ((threadIdx.x & 31) == 0 && u.nc > 0) mma_role(x, p, u, tm);
         __syncwarp();
     } else if (warp < 6) {
         prep_role(x, p, u, tm);
@@ -820,8 +821,8 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     const long long grid = (long long)p.N * p.Nv * (p.dv / BVT);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    // T' | T'' of every chunk first (all chunks in parallel), then the scan
-    cudaError_t err = wy_launch(p, mK, stream);
+    // T', T'' and P of every chunk first (all chunks in parallel), then the scan
+    cudaError_t err = wy_launch(p, mK, mQ, stream);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;

@@ -12,6 +12,6 @@ bool tc_supported(int dk, int dv, bool bf16);
 // Workspace bytes the tensor-core path needs (0 for no tokens).
 size_t tc_workspace_bytes(long long tokens, int N, int Nv);
 cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name);
-cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, cudaStream_t stream);
+cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream);
 
 }  // namespace dn

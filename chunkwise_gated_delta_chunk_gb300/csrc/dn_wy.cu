@@ -1,28 +1,31 @@
-// WY kernel of the chunkwise gated delta rule forward (bf16 k, dk = 128):
+// WY kernel of the chunkwise gated delta rule forward (bf16 q/k, dk = 128):
 // for every chunk of every (sequence, value head), the lower-triangular
-// inverse T = (I - A)^-1 of the chunk's WY representation, written to the
-// workspace as the two bf16 MMA operands T' = T diag(beta e^G) and
-// T'' = T diag(beta) that give W = T' K and U = T'' V.
+// inverse T = (I - A)^-1 of the chunk's WY representation and the chunk's
+// causal score matrix, written to the workspace as the three bf16 MMA
+// operands T' = T diag(beta e^G) and T'' = T diag(beta) (which give
+// W = T' K and U = T'' V) and P = tril(scale QK^T . D).
 //
 // Sources: [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现"
 //                 §2.3 (A = -tril(diag(beta) K K^T, -1), T = (I - A)^-1 by
-//                 forward substitution), §2.4 (W = T diag(beta) K, U = T diag(beta) V);
-//          [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1 (gated form:
-//                 A_ij carries e^{G_i - G_j}, W carries e^{G}).
+//                 forward substitution), §2.4 (W = T diag(beta) K, U = T diag(beta) V,
+//                 intra-chunk output through tril(Q K^T));
+//          [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1-§3.2 (gated form:
+//                 A_ij and P_ij carry e^{G_i - G_j}, W carries e^{G}).
 //
 // Every chunk is independent, so this kernel runs all of them in parallel
 // (one 128-thread CTA per chunk and value head, several CTAs per SM) ahead of
-// the sequential scan kernel, which then only reads T' and T''.  Per CTA:
-//   1. TMA brings the chunk's K (64 x 128 bf16, two 128-byte-swizzled column
-//      halves); warp 0 computes the gate scalars meanwhile;
-//   2. one tcgen05 MMA chain computes K K^T into tensor memory (M = 128: the
-//      operand rows 64-127 run past the tile and land in TMEM lanes 64-127,
-//      which nothing reads);
-//   3. warps 0-1 turn lanes 0-63 into A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij
-//      (j < i) in shared memory, fp32;
-//   4. the four warps invert I - A in fp32 (blocked, below);
-//   5. T' and T'' are scaled, rounded to bf16 in the swizzled image and
-//      copied to the chunk's workspace slot with coalesced 16-byte stores.
+// the sequential scan kernel, which then only reads T', T'' and P.  Per CTA:
+//   1. TMA brings the chunk's K and Q (64 x 128 bf16 each, as two
+//      128-byte-swizzled column halves); warp 0 computes the gate scalars;
+//   2. one tcgen05 MMA chain computes [K; Q] K^T into tensor memory: lanes
+//      0-63 hold K K^T, lanes 64-127 hold Q K^T;
+//   3. warps 0-1 turn their rows into A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij
+//      (j < i) in shared memory, fp32; warps 2-3 turn theirs into
+//      P_ij = scale e^{G_i - G_j} (Q K^T)_ij (j <= i), bf16;
+//   4. the four warps invert I - A (blocked, below: fp32 forward substitution
+//      on the diagonal blocks, TF32 tensor-core products for the rest);
+//   5. T' and T'' are scaled and rounded to bf16; the three images are copied
+//      to the chunk's workspace slot with coalesced 16-byte stores.
 // Waits are bounded: a wait that runs out records kStatusTimeout in the status
 // word, the CTA skips the rest and drains its own TMA / MMA work before it
 // frees its tensor memory.
@@ -66,18 +69,20 @@ constexpr int NT = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr uint32_t OFF_K = 0;                    // K[:, 0:64] | K[:, 64:128] | 8 KB the MMA reads past
-constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases OFF_K)
-constexpr uint32_t OFF_T = 24576;                // T' | T'' images; solve scratch before that
+constexpr uint32_t OFF_K = 0;                    // K0 Q0 K1 Q1 (8 KB each): column halves of K and Q
+constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases the tiles)
+constexpr uint32_t OFF_PI = 18432;               // P image (aliases the tiles)
+constexpr uint32_t OFF_T = 32768;                // T' | T'' images; solve scratch before that
 constexpr uint32_t OFF_SC = OFF_T + 2 * 8192;    // gate scalars
 constexpr uint32_t OFF_BAR = OFF_SC + SCAL_FLOATS * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 32;     // 2 mbarriers, TMEM base, flag
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(64 * LDA * 4 <= OFF_T, "A overlaps the T images");
-static_assert(OFF_T % 1024 == 0, "swizzled images need 1024-byte alignment");
+static_assert(64 * LDA * 4 <= OFF_PI && OFF_PI + 8192 <= OFF_T, "A / P images overlap");
+static_assert(OFF_T % 1024 == 0, "1024-byte aligned images");
+static_assert(kSlotBytes == 3 * 8192, "slot = T' | T'' | P");
 
 constexpr uint32_t TM_COLS = 64;
-constexpr uint32_t ID_KK = idesc_bf16(128, 64, 0, 0);  // A, B K-major
+constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);  // A, B K-major
 
 __device__ bool wait_bounded(uint32_t b, uint32_t parity) {
     const uint64_t t0 = globaltimer();
@@ -86,59 +91,73 @@ __device__ bool wait_bounded(uint32_t b, uint32_t parity) {
     return true;
 }
 
-// ---- 16 x 16 block helpers for the solve (fp32 blocks, fp32 FMA) -----------
-// A 16 x 8 output tile (columns n0..n0+7) per warp: lane l owns row l >> 1 and
-// the four columns n0 + 4 (l & 1) .. +3.  B rows are read as float4 (one
-// broadcast wavefront for the two column halves), A rows as float4 along k.
-__device__ __forceinline__ void tile_mma(float (&acc)[4], const float *Ab, int lda, const float *Bb,
-                                         int ldb, int n0, int lane) {
-    const int r = lane >> 1, cb = n0 + 4 * (lane & 1);
+// ---- 16 x 16 block helpers for the solve (fp32 blocks, TF32 mma.sync) -------
+// A 16 x 8 output tile (columns n0..n0+7 of the product) per warp, in the
+// m16n8k8 fragment layout: lane l = 4 g + t holds rows g and g + 8, columns
+// 2 t and 2 t + 1.  Products run on the tensor cores with TF32 operands
+// (rounded to nearest) and fp32 accumulation.
+__device__ __forceinline__ uint32_t to_tf32(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// acc += Ab (16 x 16) Bb[:, n0 .. n0 + 7]
+__device__ __forceinline__ void tile_mma(float (&acc)[4], const float *Ab, int lda, const float *Bb, int ldb,
+                                         int n0, int lane) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 a = *reinterpret_cast<const float4 *>(Ab + r * lda + 4 * k4);
-        const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 bb = *reinterpret_cast<const float4 *>(Bb + (4 * k4 + e) * ldb + cb);
-            acc[0] = fmaf(av[e], bb.x, acc[0]);
-            acc[1] = fmaf(av[e], bb.y, acc[1]);
-            acc[2] = fmaf(av[e], bb.z, acc[2]);
-            acc[3] = fmaf(av[e], bb.w, acc[3]);
-        }
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4], b[2];
+        a[0] = to_tf32(Ab[g * lda + 8 * kk + t]);
+        a[1] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t]);
+        a[2] = to_tf32(Ab[g * lda + 8 * kk + t + 4]);
+        a[3] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t + 4]);
+        b[0] = to_tf32(Bb[(8 * kk + t) * ldb + n0 + g]);
+        b[1] = to_tf32(Bb[(8 * kk + t + 4) * ldb + n0 + g]);
+        mma_tf32(acc, a, b);
     }
 }
 
 // Same with A = Ab + Ab2 (two blocks of the same layout).
 __device__ __forceinline__ void tile_mma_sum(float (&acc)[4], const float *Ab, const float *Ab2, int lda,
                                              const float *Bb, int ldb, int n0, int lane) {
-    const int r = lane >> 1, cb = n0 + 4 * (lane & 1);
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 a = *reinterpret_cast<const float4 *>(Ab + r * lda + 4 * k4);
-        const float4 a2 = *reinterpret_cast<const float4 *>(Ab2 + r * lda + 4 * k4);
-        const float av[4] = {a.x + a2.x, a.y + a2.y, a.z + a2.z, a.w + a2.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 bb = *reinterpret_cast<const float4 *>(Bb + (4 * k4 + e) * ldb + cb);
-            acc[0] = fmaf(av[e], bb.x, acc[0]);
-            acc[1] = fmaf(av[e], bb.y, acc[1]);
-            acc[2] = fmaf(av[e], bb.z, acc[2]);
-            acc[3] = fmaf(av[e], bb.w, acc[3]);
-        }
+    for (int kk = 0; kk < 2; ++kk) {
+        uint32_t a[4], b[2];
+        a[0] = to_tf32(Ab[g * lda + 8 * kk + t] + Ab2[g * lda + 8 * kk + t]);
+        a[1] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t] + Ab2[(g + 8) * lda + 8 * kk + t]);
+        a[2] = to_tf32(Ab[g * lda + 8 * kk + t + 4] + Ab2[g * lda + 8 * kk + t + 4]);
+        a[3] = to_tf32(Ab[(g + 8) * lda + 8 * kk + t + 4] + Ab2[(g + 8) * lda + 8 * kk + t + 4]);
+        b[0] = to_tf32(Bb[(8 * kk + t) * ldb + n0 + g]);
+        b[1] = to_tf32(Bb[(8 * kk + t + 4) * ldb + n0 + g]);
+        mma_tf32(acc, a, b);
     }
 }
 
 __device__ __forceinline__ void tile_load(float (&acc)[4], const float *Cb, int ldc, int n0, int lane) {
-    const float4 v = *reinterpret_cast<const float4 *>(Cb + (lane >> 1) * ldc + n0 + 4 * (lane & 1));
-    acc[0] = v.x;
-    acc[1] = v.y;
-    acc[2] = v.z;
-    acc[3] = v.w;
+    const int g = lane >> 2, t = lane & 3;
+    acc[0] = Cb[g * ldc + n0 + 2 * t];
+    acc[1] = Cb[g * ldc + n0 + 2 * t + 1];
+    acc[2] = Cb[(g + 8) * ldc + n0 + 2 * t];
+    acc[3] = Cb[(g + 8) * ldc + n0 + 2 * t + 1];
 }
 
 __device__ __forceinline__ void tile_store(float *Cb, int ldc, int n0, const float (&acc)[4], int lane) {
-    *reinterpret_cast<float4 *>(Cb + (lane >> 1) * ldc + n0 + 4 * (lane & 1)) =
-        make_float4(acc[0], acc[1], acc[2], acc[3]);
+    const int g = lane >> 2, t = lane & 3;
+    Cb[g * ldc + n0 + 2 * t] = acc[0];
+    Cb[g * ldc + n0 + 2 * t + 1] = acc[1];
+    Cb[(g + 8) * ldc + n0 + 2 * t] = acc[2];
+    Cb[(g + 8) * ldc + n0 + 2 * t + 1] = acc[3];
 }
 
 // Scratch blocks of the solve (fp32, row stride SLD) in the T'/T'' buffer,
@@ -152,8 +171,8 @@ enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30 };
 // lower, so N^4 = 0 and
 //     T = (I + N + N^2 + N^3) T_D,   T_D = (I - A_D)^-1,   N_ij = T_ii A_ij.
 // The diagonal blocks are inverted by forward substitution in fp32 (warp pw
-// owns block pw, lane l the column l % 16); the block products are fp32 FMA
-// tiles, in four barrier-separated phases.
+// owns block pw, lane l the column l % 16); the block products are TF32
+// tensor-core tiles with fp32 accumulation, in four barrier-separated phases.
 __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane, uint32_t bid) {
     {
         // x = column `col` of (I - A_bb)^-1:  x_r = [r == col] + sum_{m < r} A[r][m] x_m.
@@ -274,7 +293,8 @@ __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane,
 
 
 __global__ void __launch_bounds__(NT, 5)
-wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p) {
+wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
+       const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -320,9 +340,11 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(b_tma, 16384);
+            mbar_arrive_expect_tx(b_tma, 32768);
             tma_load_3d(base + OFF_K, &mK, b_tma, 0, hk, (int)t0);
-            tma_load_3d(base + OFF_K + 8192, &mK, b_tma, 64, hk, (int)t0);
+            tma_load_3d(base + OFF_K + 8192, &mQ, b_tma, 0, hk, (int)t0);
+            tma_load_3d(base + OFF_K + 16384, &mK, b_tma, 64, hk, (int)t0);
+            tma_load_3d(base + OFF_K + 24576, &mQ, b_tma, 64, hk, (int)t0);
         }
         chunk_scalars(p, h, t0, L, sc, lane);
         __syncwarp();
@@ -335,8 +357,8 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
                 for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a = base + OFF_K + kb * 8192 + kk * 32;
-                        mma_ss(tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KK, (kb | kk) != 0);
+                        const uint32_t a = base + OFF_K + kb * 16384 + kk * 32;
+                        mma_ss(tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
                     }
                 mma_commit(b_mma);
                 ok = wait_bounded(b_mma, 0);
@@ -356,11 +378,17 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
     tc_fence_after();
     const bool ok = *okf != 0;
 
-    float *sA = reinterpret_cast<float *>(gb + OFF_K);  // K is no longer read
-    if (ok && warp < 2) {
-        // A row i (TMEM lane i): A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij, j < i
-        const int i = threadIdx.x;
-        const float Gi = sc[SC_G + i], ai = -sc[SC_BETA + i] * sc[SC_AF + i];
+    float *sA = reinterpret_cast<float *>(gb + OFF_K);  // the tiles are no longer read
+    if (ok) {
+        // row i of K K^T (warps 0-1) or of Q K^T (warps 2-3) = TMEM lane
+        const int row = threadIdx.x, i = row & 63;
+        const bool rowA = row < 64;
+        const float Gi = sc[SC_G + i];
+        // A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij for j < i;
+        // P_ij = scale e^{G_i - G_j} (Q K^T)_ij for j <= i
+        const float ri = rowA ? -sc[SC_BETA + i] : p.scale;
+        const float ai = ri * sc[SC_AF + i];
+        const int jmax = rowA ? i - 1 : i;
         const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
         uint32_t r[32];
 #pragma unroll
@@ -380,29 +408,36 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
                     dcy[4 * q4 + 3] = ai * bb.w;
                 }
             } else {
-                const float nb = -sc[SC_BETA + i];
                 const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 32 * hf);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
                     const float4 gg = g4[q4];
                     const int j = 32 * hf + 4 * q4;
-                    dcy[4 * q4] = nb * __expf(j < i ? Gi - gg.x : -INFINITY);
-                    dcy[4 * q4 + 1] = nb * __expf(j + 1 < i ? Gi - gg.y : -INFINITY);
-                    dcy[4 * q4 + 2] = nb * __expf(j + 2 < i ? Gi - gg.z : -INFINITY);
-                    dcy[4 * q4 + 3] = nb * __expf(j + 3 < i ? Gi - gg.w : -INFINITY);
+                    dcy[4 * q4] = ri * __expf(j <= jmax ? Gi - gg.x : -INFINITY);
+                    dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax ? Gi - gg.y : -INFINITY);
+                    dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax ? Gi - gg.z : -INFINITY);
+                    dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax ? Gi - gg.w : -INFINITY);
                 }
             }
             tmem_wait_ld_dep(r);
+            float val[32];
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                float val[4];
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * hf + jj;
+                val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
+            }
+            if (rowA) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 32 * hf + 4 * q4 + e;
-                    val[e] = j < i ? dcy[4 * q4 + e] * __uint_as_float(r[4 * q4 + e]) : 0.f;
-                }
-                *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
-                    make_float4(val[0], val[1], val[2], val[3]);
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
+                        make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3]);
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    st_shared_v4(base + OFF_PI + sw128(i, 4 * hf + ch), pack_bf16(val[8 * ch], val[8 * ch + 1]),
+                                 pack_bf16(val[8 * ch + 2], val[8 * ch + 3]),
+                                 pack_bf16(val[8 * ch + 4], val[8 * ch + 5]),
+                                 pack_bf16(val[8 * ch + 6], val[8 * ch + 7]));
             }
         }
     }
@@ -438,11 +473,15 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
                              pack_bf16(tv[8 * ch + 6], tv[8 * ch + 7]));
         }
         __syncthreads();
+        // slot = T' | T'' | P
         uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.ws) +
                                                ((size_t)h * p.nslots + slot) * kSlotBytes);
-        const uint4 *src = reinterpret_cast<const uint4 *>(gb + OFF_T);
+        const uint4 *srcT = reinterpret_cast<const uint4 *>(gb + OFF_T);
+        const uint4 *srcP = reinterpret_cast<const uint4 *>(gb + OFF_PI);
 #pragma unroll
-        for (int k = 0; k < (int)(kSlotBytes / 16 / NT); ++k) out[threadIdx.x + NT * k] = src[threadIdx.x + NT * k];
+        for (int k = 0; k < 8; ++k) out[threadIdx.x + NT * k] = srcT[threadIdx.x + NT * k];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out[1024 + threadIdx.x + NT * k] = srcP[threadIdx.x + NT * k];
         WY_TRACE_EV(6);
     }
     if (warp == 0) {
@@ -455,13 +494,13 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ Params p)
 
 size_t wy_smem_bytes() { return SMEM_ALLOC; }
 
-cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, cudaStream_t stream) {
+cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
     const long long grid = p.nslots * p.Nv;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(wy_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
-    wy_fwd<<<(unsigned)grid, NT, SMEM_ALLOC, stream>>>(mK, p);
+    wy_fwd<<<(unsigned)grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
     return cudaGetLastError();
 }
 

@@ -102,7 +102,8 @@ typedef enum {
  * Returns DN_OK once the work is enqueued; DN_ERR_INVALID_ARG also when the
  * workspace is missing, misaligned or too small.  The tensor-core path
  * (bf16, dk = 128, dv a multiple of 128) launches two kernels per call: the
- * per-chunk WY inverse T of every chunk in parallel ([WY] §2.3-§2.4), then
+ * per-chunk WY inverse T and causal scores of every chunk in parallel
+ * ([WY] §2.3-§2.4), then
  * the sequential state scan and output ([CGDR] §3.2-§3.3).  Other shapes
  * launch one CUDA-core kernel.
  */
@@ -117,9 +118,10 @@ dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
 /*
  * dn_chunk_fwd_workspace_bytes -- bytes of workspace dn_chunk_fwd needs for
  * these sizes (same meaning as there).  For the tensor-core path it is
- * (floor(B*T / 64) + n_seqs) * Nv * 16384: one 16 KB slot per chunk and value
- * head holding the bf16 matrices T diag(beta e^G) and T diag(beta) of the
- * chunk's WY representation ([WY] §2.4).  Returns 0 when no workspace is
+ * (floor(B*T / 64) + n_seqs) * Nv * 24576: one 24 KB slot per chunk and value
+ * head holding three bf16 64 x 64 matrices of the chunk, T diag(beta e^G) and
+ * T diag(beta) of its WY representation ([WY] §2.4) and its causal score
+ * matrix tril(scale QK^T . D) ([CGDR] §3.2).  Returns 0 when no workspace is
  * needed, and for sizes dn_chunk_fwd would reject.  Host-only; no CUDA call.
  */
 size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
@@ -141,7 +143,7 @@ size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, in
  *   - Sizes whose dn_chunk_fwd_workspace_bytes() exceeds
  *     DN_NOALLOC_SCRATCH_BYTES are rejected with DN_ERR_UNSUPPORTED before
  *     anything is launched (64 MiB covers (floor(B*T/64) + n_seqs) * Nv <=
- *     4096, e.g. B = 4, T = 2048, Nv = 16).
+ *     2730, e.g. B = 4, T = 2048, Nv = 16).
  *   - The first call with a given device current looks up the array's device
  *     address there (a host query that allocates nothing); make that first
  *     call before any stream capture on that device.

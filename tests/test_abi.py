@@ -96,10 +96,10 @@ def test_invalid_arguments_rejected_on_host(clib, over, code):
 
 
 def test_workspace_size(clib):
-    """One 16 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
+    """One 24 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
     ws = clib.dn_chunk_fwd_workspace_bytes
-    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 16384
-    assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 16384
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 24576
+    assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 24576
     assert ws(2, 2, 64, 2, 4, 64, 64, dn.DN_BF16, 64) == 0       # CUDA-core path
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
