@@ -13,8 +13,10 @@
 //                 A_ij and P_ij carry e^{G_i - G_j}, W carries e^{G}).
 //
 // Every chunk is independent, so this kernel runs all of them in parallel
-// (one 128-thread CTA per chunk and value head, several CTAs per SM) ahead of
-// the sequential scan kernel, which then only reads T', T'' and P.  Per CTA:
+// ahead of the sequential scan kernel, which then only reads T', T'' and P.
+// One 128-thread CTA per (chunk slot, value head) item, 35 KB of shared memory
+// and 64 TMEM columns each, 6 per SM.  (The loop below also serves a grid
+// smaller than the item count.)  Per item:
 //   1. TMA brings the chunk's K and Q (64 x 128 bf16 each, as two
 //      128-byte-swizzled column halves); warp 0 computes the gate scalars;
 //   2. one tcgen05 MMA chain computes [K; Q] K^T into tensor memory: lanes
@@ -24,8 +26,8 @@
 //      P_ij = scale e^{G_i - G_j} (Q K^T)_ij (j <= i), bf16;
 //   4. the four warps invert I - A (blocked, below: fp32 forward substitution
 //      on the diagonal blocks, TF32 tensor-core products for the rest);
-//   5. T' and T'' are scaled and rounded to bf16; the three images are copied
-//      to the chunk's workspace slot with coalesced 16-byte stores.
+//   5. T' and T'' are scaled and rounded to bf16; each thread stores its rows
+//      of the three images straight from registers into the chunk's slot.
 // Waits are bounded: a wait that runs out records kStatusTimeout in the status
 // word, the CTA skips the rest and drains its own TMA / MMA work before it
 // frees its tensor memory.
@@ -38,27 +40,6 @@
 #include "dn_tc.h"
 #include "tc_ptx.cuh"
 
-// Optional per-CTA phase trace (SM clock) of the first 4096 CTAs, compiled
-// in only with -DDN_TRACE for profiling builds.
-#ifdef DN_TRACE
-__device__ unsigned long long g_wy_trace[4096][8];
-#define WY_TRACE_EV(ev)                                                             \
-    do {                                                                            \
-        if (threadIdx.x == 0 && blockIdx.x < 4096) {                                \
-            unsigned long long t_;                                                  \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                  \
-            g_wy_trace[blockIdx.x][(ev)] = t_;                                      \
-        }                                                                           \
-    } while (0)
-extern "C" __attribute__((visibility("default"))) int dn_wy_trace_dump(void *dst) {
-    return (int)cudaMemcpyFromSymbol(dst, g_wy_trace, sizeof(g_wy_trace));
-}
-#else
-#define WY_TRACE_EV(ev) \
-    do {                \
-    } while (0)
-#endif
-
 namespace dn {
 namespace {
 
@@ -68,17 +49,15 @@ constexpr int C = kChunk;  // 64
 constexpr int NT = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
-// Shared memory (offsets from a 1024-byte aligned base).
+// Shared memory (offsets from a 1024-byte aligned base).  The tile region is
+// free once the MMA has read it and then holds A / T and the solve scratch.
 constexpr uint32_t OFF_K = 0;                    // K0 Q0 K1 Q1 (8 KB each): column halves of K and Q
 constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases the tiles)
-constexpr uint32_t OFF_PI = 18432;               // P image (aliases the tiles)
-constexpr uint32_t OFF_T = 32768;                // T' | T'' images; solve scratch before that
-constexpr uint32_t OFF_SC = OFF_T + 2 * 8192;    // gate scalars
+constexpr uint32_t OFF_SCR = 64 * LDA * 4;       // solve scratch (aliases the tiles)
+constexpr uint32_t OFF_SC = 32768;               // gate scalars
 constexpr uint32_t OFF_BAR = OFF_SC + SCAL_FLOATS * 4;
 constexpr uint32_t SMEM_USED = OFF_BAR + 32;     // 2 mbarriers, TMEM base, flag
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(64 * LDA * 4 <= OFF_PI && OFF_PI + 8192 <= OFF_T, "A / P images overlap");
-static_assert(OFF_T % 1024 == 0, "1024-byte aligned images");
 static_assert(kSlotBytes == 3 * 8192, "slot = T' | T'' | P");
 
 constexpr uint32_t TM_COLS = 64;
@@ -160,10 +139,11 @@ __device__ __forceinline__ void tile_store(float *Cb, int ldc, int n0, const flo
     Cb[(g + 8) * ldc + n0 + 2 * t + 1] = acc[3];
 }
 
-// Scratch blocks of the solve (fp32, row stride SLD) in the T'/T'' buffer,
-// which is free while T is being computed.
+// Scratch blocks of the solve (fp32, row stride SLD), after A in the tile
+// region.
 constexpr int SLD = 20, SBLK = 16 * SLD;
-enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30 };
+enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30, XCOUNT };
+static_assert(OFF_SCR + XCOUNT * SBLK * 4 <= OFF_SC, "the solve scratch fits in the tile region");
 
 // In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
 // LDA); 128 threads.  With A_D the four 16 x 16 diagonal blocks and A_O the
@@ -292,7 +272,18 @@ __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane,
 }
 
 
-__global__ void __launch_bounds__(NT, 5)
+// Row i of a 64 x 64 bf16 image (32 values in two halves of packed pairs)
+// straight to global memory, in the 128-byte-swizzled layout.
+__device__ __forceinline__ void store_image_row(uint8_t *img, int i, int hf, const uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        const int cc = 4 * hf + ch;
+        *reinterpret_cast<uint4 *>(img + i * 128 + ((cc ^ (i & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+    }
+}
+
+__global__ void __launch_bounds__(NT, 6)
 wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -300,32 +291,15 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gb = smem_raw + (base - raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- which chunk: slot -> (sequence n, chunk c) ----------------------
-    const int h = (int)(blockIdx.x % (unsigned)p.Nv);
-    const long long slot = blockIdx.x / (unsigned)p.Nv;
-    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (wy_slot(seq_bos(p, mid), mid) <= slot) lo = mid; else hi = mid - 1;
-    }
-    const int n = lo;
-    const long long bos = seq_bos(p, n), eos = seq_eos(p, n);
-    if (bos < 0 || eos < bos || eos > p.tokens) return;  // the scan kernel reports it
-    const long long c = slot - wy_slot(bos, n);
-    const long long t0 = bos + c * C;
-    if (c < 0 || t0 >= eos) return;  // a slot no chunk maps to
-    const int L = (int)min((long long)C, eos - t0);
-    const int hk = h / (p.Nv / p.Nk);
-    WY_TRACE_EV(0);
-
     const uint32_t b_tma = base + OFF_BAR, b_mma = base + OFF_BAR + 8;
     volatile int *okf = reinterpret_cast<volatile int *>(gb + OFF_BAR + 20);
     float *sc = reinterpret_cast<float *>(gb + OFF_SC);
+    float *sA = reinterpret_cast<float *>(gb + OFF_K);
+    float *scr = reinterpret_cast<float *>(gb + OFF_SCR);
+
     if (threadIdx.x == 0) {
         mbar_init(b_tma, 1);
         mbar_init(b_mma, 1);
-        *okf = 1;
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -336,153 +310,157 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *reinterpret_cast<volatile uint32_t *>(gb + OFF_BAR + 16);
-    WY_TRACE_EV(1);
 
-    if (warp == 0) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(b_tma, 32768);
-            tma_load_3d(base + OFF_K, &mK, b_tma, 0, hk, (int)t0);
-            tma_load_3d(base + OFF_K + 8192, &mQ, b_tma, 0, hk, (int)t0);
-            tma_load_3d(base + OFF_K + 16384, &mK, b_tma, 64, hk, (int)t0);
-            tma_load_3d(base + OFF_K + 24576, &mQ, b_tma, 64, hk, (int)t0);
+    const long long items = p.nslots * p.Nv;
+    uint32_t it = 0;  // items this CTA has run (mbarrier phases)
+    for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+        // ---- which chunk: slot -> (sequence n, chunk c) ------------------
+        const int h = (int)(item % p.Nv);
+        const long long slot = item / p.Nv;
+        int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (wy_slot(seq_bos(p, mid), mid) <= slot) lo = mid; else hi = mid - 1;
         }
-        chunk_scalars(p, h, t0, L, sc, lane);
-        __syncwarp();
-        if (lane == 0) {
-            bool ok = wait_bounded(b_tma, 0);
-            WY_TRACE_EV(2);
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a = base + OFF_K + kb * 16384 + kk * 32;
-                        mma_ss(tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
-                    }
-                mma_commit(b_mma);
-                ok = wait_bounded(b_mma, 0);
-                WY_TRACE_EV(3);
-                if (!ok) wait_bounded(b_mma, 0);  // drain: the MMA still reads shared memory
-            } else {
-                wait_bounded(b_tma, 0);  // drain: the copy may still land
-            }
-            if (!ok) {
-                *okf = 0;
-                atomicOr(p.status, kStatusTimeout);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const bool ok = *okf != 0;
+        const int n = lo;
+        const long long bos = seq_bos(p, n), eos = seq_eos(p, n);
+        if (bos < 0 || eos < bos || eos > p.tokens) continue;  // the scan kernel reports it
+        const long long c = slot - wy_slot(bos, n);
+        const long long t0 = bos + c * C;
+        if (c < 0 || t0 >= eos) continue;  // a slot no chunk maps to
+        const int L = (int)min((long long)C, eos - t0);
+        const int hk = h / (p.Nv / p.Nk);
+        const uint32_t par = it & 1;
+        ++it;
+        uint8_t *img = static_cast<uint8_t *>(p.ws) + ((size_t)h * p.nslots + slot) * kSlotBytes;
 
-    float *sA = reinterpret_cast<float *>(gb + OFF_K);  // the tiles are no longer read
-    if (ok) {
-        // row i of K K^T (warps 0-1) or of Q K^T (warps 2-3) = TMEM lane
-        const int row = threadIdx.x, i = row & 63;
-        const bool rowA = row < 64;
-        const float Gi = sc[SC_G + i];
-        // A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij for j < i;
-        // P_ij = scale e^{G_i - G_j} (Q K^T)_ij for j <= i
-        const float ri = rowA ? -sc[SC_BETA + i] : p.scale;
-        const float ai = ri * sc[SC_AF + i];
-        const int jmax = rowA ? i - 1 : i;
-        const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
-        uint32_t r[32];
+        if (warp == 0) {
+            if (lane == 0) {
+                *okf = 1;
+                mbar_arrive_expect_tx(b_tma, 32768);
+                tma_load_3d(base + OFF_K, &mK, b_tma, 0, hk, (int)t0);
+                tma_load_3d(base + OFF_K + 8192, &mQ, b_tma, 0, hk, (int)t0);
+                tma_load_3d(base + OFF_K + 16384, &mK, b_tma, 64, hk, (int)t0);
+                tma_load_3d(base + OFF_K + 24576, &mQ, b_tma, 64, hk, (int)t0);
+            }
+            chunk_scalars(p, h, t0, L, sc, lane);
+            __syncwarp();
+            if (lane == 0) {
+                bool ok = wait_bounded(b_tma, par);
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            tmem_ld32(tm + ((uint32_t)(32 * warp) << 16) + 32 * hf, r);
-            // D_ij = e^{G_i - G_j}: the product of the two per-chunk factors
-            // when the chunk's log-gate span allows it, else one exponential
-            float dcy[32];
-            if (fact) {
-                const float4 *b4 = reinterpret_cast<const float4 *>(sc + SC_BF + 32 * hf);
+                    for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 bb = b4[q4];
-                    dcy[4 * q4] = ai * bb.x;
-                    dcy[4 * q4 + 1] = ai * bb.y;
-                    dcy[4 * q4 + 2] = ai * bb.z;
-                    dcy[4 * q4 + 3] = ai * bb.w;
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t a = base + OFF_K + kb * 16384 + kk * 32;
+                            mma_ss(tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
+                        }
+                    mma_commit(b_mma);
+                    ok = wait_bounded(b_mma, par);
+                    if (!ok) wait_bounded(b_mma, par);  // drain: the MMA still reads shared memory
+                } else {
+                    wait_bounded(b_tma, par);  // drain: the copy may still land
                 }
-            } else {
-                const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 32 * hf);
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 gg = g4[q4];
-                    const int j = 32 * hf + 4 * q4;
-                    dcy[4 * q4] = ri * __expf(j <= jmax ? Gi - gg.x : -INFINITY);
-                    dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax ? Gi - gg.y : -INFINITY);
-                    dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax ? Gi - gg.z : -INFINITY);
-                    dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax ? Gi - gg.w : -INFINITY);
+                if (!ok) {
+                    *okf = 0;
+                    atomicOr(p.status, kStatusTimeout);
                 }
             }
-            tmem_wait_ld_dep(r);
-            float val[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = 32 * hf + jj;
-                val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
-            }
-            if (rowA) {
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
-                        make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3]);
-            } else {
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    st_shared_v4(base + OFF_PI + sw128(i, 4 * hf + ch), pack_bf16(val[8 * ch], val[8 * ch + 1]),
-                                 pack_bf16(val[8 * ch + 2], val[8 * ch + 3]),
-                                 pack_bf16(val[8 * ch + 4], val[8 * ch + 5]),
-                                 pack_bf16(val[8 * ch + 6], val[8 * ch + 7]));
-            }
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    WY_TRACE_EV(4);
-    if (ok) {
-        float *scr = reinterpret_cast<float *>(gb + OFF_T);
-        solve_T(sA, scr, warp, lane, 1);
-        WY_TRACE_EV(5);
-        // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
-        const int i = threadIdx.x & 63;
-        const bool tp = threadIdx.x < 64;
-        const float *trow = sA + i * LDA;
-        const float *cs = sc + (tp ? SC_BEG : SC_BETA);
-        const uint32_t dst = base + OFF_T + (tp ? 0u : 8192u);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            float tv[32];
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 a = *reinterpret_cast<const float4 *>(trow + 32 * hf + 4 * q4);
-                const float4 cc = *reinterpret_cast<const float4 *>(cs + 32 * hf + 4 * q4);
-                tv[4 * q4] = a.x * cc.x;
-                tv[4 * q4 + 1] = a.y * cc.y;
-                tv[4 * q4 + 2] = a.z * cc.z;
-                tv[4 * q4 + 3] = a.w * cc.w;
-            }
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                st_shared_v4(dst + sw128(i, 4 * hf + ch), pack_bf16(tv[8 * ch], tv[8 * ch + 1]),
-                             pack_bf16(tv[8 * ch + 2], tv[8 * ch + 3]), pack_bf16(tv[8 * ch + 4], tv[8 * ch + 5]),
-                             pack_bf16(tv[8 * ch + 6], tv[8 * ch + 7]));
-        }
+        tc_fence_before();
         __syncthreads();
-        // slot = T' | T'' | P
-        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.ws) +
-                                               ((size_t)h * p.nslots + slot) * kSlotBytes);
-        const uint4 *srcT = reinterpret_cast<const uint4 *>(gb + OFF_T);
-        const uint4 *srcP = reinterpret_cast<const uint4 *>(gb + OFF_PI);
+        tc_fence_after();
+        if (*okf == 0) break;
+
+        {
+            // row i of K K^T (warps 0-1) or of Q K^T (warps 2-3) = TMEM lane
+            const int row = threadIdx.x, i = row & 63;
+            const bool rowA = row < 64;
+            const float Gi = sc[SC_G + i];
+            // A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij for j < i;
+            // P_ij = scale e^{G_i - G_j} (Q K^T)_ij for j <= i
+            const float ri = rowA ? -sc[SC_BETA + i] : p.scale;
+            const float ai = ri * sc[SC_AF + i];
+            const int jmax = rowA ? i - 1 : i;
+            const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
+            uint32_t r[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) out[threadIdx.x + NT * k] = srcT[threadIdx.x + NT * k];
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32(tm + ((uint32_t)(32 * warp) << 16) + 32 * hf, r);
+                // D_ij = e^{G_i - G_j}: the product of the two per-chunk
+                // factors when the chunk's log-gate span allows it, else one
+                // exponential
+                float dcy[32];
+                if (fact) {
+                    const float4 *b4 = reinterpret_cast<const float4 *>(sc + SC_BF + 32 * hf);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) out[1024 + threadIdx.x + NT * k] = srcP[threadIdx.x + NT * k];
-        WY_TRACE_EV(6);
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 bb = b4[q4];
+                        dcy[4 * q4] = ai * bb.x;
+                        dcy[4 * q4 + 1] = ai * bb.y;
+                        dcy[4 * q4 + 2] = ai * bb.z;
+                        dcy[4 * q4 + 3] = ai * bb.w;
+                    }
+                } else {
+                    const float4 *g4 = reinterpret_cast<const float4 *>(sc + SC_G + 32 * hf);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 gg = g4[q4];
+                        const int j = 32 * hf + 4 * q4;
+                        dcy[4 * q4] = ri * __expf(j <= jmax ? Gi - gg.x : -INFINITY);
+                        dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax ? Gi - gg.y : -INFINITY);
+                        dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax ? Gi - gg.z : -INFINITY);
+                        dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax ? Gi - gg.w : -INFINITY);
+                    }
+                }
+                tmem_wait_ld_dep(r);
+                float val[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hf + jj;
+                    val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
+                }
+                if (rowA) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
+                            make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3]);
+                } else {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(val[2 * k], val[2 * k + 1]);
+                    store_image_row(img + 16384, i, hf, pk);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        solve_T(sA, scr, warp, lane, 1);
+        {
+            // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
+            const int i = threadIdx.x & 63;
+            const bool tp = threadIdx.x < 64;
+            const float *trow = sA + i * LDA;
+            const float *cs = sc + (tp ? SC_BEG : SC_BETA);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(trow + 32 * hf + 4 * q4);
+                    const float4 cc = *reinterpret_cast<const float4 *>(cs + 32 * hf + 4 * q4);
+                    pk[2 * q4] = pack_bf16(a.x * cc.x, a.y * cc.y);
+                    pk[2 * q4 + 1] = pack_bf16(a.z * cc.z, a.w * cc.w);
+                }
+                store_image_row(img + (tp ? 0 : 8192), i, hf, pk);
+            }
+        }
+        // A / T and the scratch are read; the next item's TMA rewrites them
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
     }
     if (warp == 0) {
         tc_fence_after();
@@ -492,15 +470,14 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
 
 }  // namespace
 
-size_t wy_smem_bytes() { return SMEM_ALLOC; }
-
 cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
-    const long long grid = p.nslots * p.Nv;
-    if (grid <= 0) return cudaSuccess;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const long long items = p.nslots * p.Nv;
+    if (items <= 0) return cudaSuccess;
     cudaError_t err = cudaFuncSetAttribute(wy_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
-    wy_fwd<<<(unsigned)grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)items;  // one CTA per item
+    wy_fwd<<<grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
     return cudaGetLastError();
 }
 
