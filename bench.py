@@ -244,10 +244,10 @@ def weak_scaling_value(tokens_per_rank: int, world: int, ms_max: float) -> float
     return tokens_per_rank * world / (ms_max / 1e3)
 
 
-def config_of(wl_name, inp, l2):
+def config_of(wl_name, inp, l2, chunk=64):
     B, T, Nk, dk = inp["q"].shape
     Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
-    return dict(workload=wl_name, B=B, T=T, Nk=Nk, Nv=Nv, dk=dk, dv=dv, chunk=64,
+    return dict(workload=wl_name, B=B, T=T, Nk=Nk, Nv=Nv, dk=dk, dv=dv, chunk=chunk,
                 global_batch=B, seq_len=T, gate=inp["g"] is not None,
                 h0=inp["h0"] is not None, l2=l2)
 
@@ -262,6 +262,8 @@ def main():
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--chunk", type=int, default=64, choices=[16, 32, 64],
+                    help="chunk length C (16 and 32 run the CUDA-core kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -298,12 +300,12 @@ def main():
     dt = dn.dtype_code(d["q"].dtype)
     stream = torch.cuda.current_stream(dev)
 
-    ws = dn.workspace_for(d["q"], d["v"], N)
+    ws = dn.workspace_for(d["q"], d["v"], N, args.chunk)
 
     def launch(q=d["q"], k=d["k"], v=d["v"], beta=d["beta"], g=d["g"], h0=d["h0"],
                cu=d["cu_seqlens"], o=o, ht=ht):
         st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
-                             inp["scale"], 64, o, ht, ws, stream=stream)
+                             inp["scale"], args.chunk, o, ht, ws, stream=stream)
         if st != dn.DN_OK:
             raise dn.DnError(st)
 
@@ -408,7 +410,7 @@ def main():
                 n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16"
                 if d["q"].dtype == torch.bfloat16 else "f32", data="synthetic",
-                config=config_of(wl_name, inp, l2="flushed before every timed step "
+                config=config_of(wl_name, inp, chunk=args.chunk, l2="flushed before every timed step "
                                  "(256 MiB write, outside the step's events)"),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
                 gpu_launches=K, roofline=roof,

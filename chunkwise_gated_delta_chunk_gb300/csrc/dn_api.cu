@@ -49,8 +49,16 @@ bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 25
 
 // Bytes of workspace the call with these sizes needs (0: none).  The
 // tensor-core path keeps T' | T'' of every chunk there between its two kernels.
-size_t workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype) {
-    if (tokens <= 0 || !dn::tc_supported(dk, dv, dtype == DN_BF16)) return 0;
+bool chunk_ok(int chunk) { return chunk == 16 || chunk == 32 || chunk == dn::kChunk; }
+
+// The tensor-core path takes bf16, dk = 128, dv a multiple of 128 and 64-token
+// chunks; everything else runs on the CUDA-core kernel.
+bool use_tc(long long tokens, int dk, int dv, dn_dtype dtype, int chunk) {
+    return tokens > 0 && chunk == dn::kChunk && dn::tc_supported(dk, dv, dtype == DN_BF16);
+}
+
+size_t workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype, int chunk) {
+    if (!use_tc(tokens, dk, dv, dtype, chunk)) return 0;
     return dn::tc_workspace_bytes(tokens, n_seqs, Nv);
 }
 
@@ -58,8 +66,8 @@ size_t workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_
 
 DN_EXPORT size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
                                               dn_dtype dtype, int chunk) {
-    if (n_seqs <= 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || chunk != dn::kChunk) return 0;
-    return workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv, dtype);
+    if (n_seqs <= 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || !chunk_ok(chunk)) return 0;
+    return workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv, dtype, chunk);
 }
 
 DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
@@ -83,11 +91,11 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
     // ---- valid, but not built --------------------------------------------
-    if (chunk != dn::kChunk) return DN_ERR_UNSUPPORTED;
+    if (!chunk_ok(chunk)) return DN_ERR_UNSUPPORTED;
     if (!dim_ok(dk) || !dim_ok(dv)) return DN_ERR_UNSUPPORTED;
     if (dtype == DN_F32 && dk > 128) return DN_ERR_UNSUPPORTED;
     if (n_seqs == 0) return DN_OK;
-    const size_t ws_need = workspace_bytes(tokens, n_seqs, Nv, dk, dv, dtype);
+    const size_t ws_need = workspace_bytes(tokens, n_seqs, Nv, dk, dv, dtype, chunk);
     if (ws_need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes_ < ws_need))
         return DN_ERR_INVALID_ARG;
 
@@ -99,12 +107,13 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
     p.ws = workspace;
     p.nslots = tokens / dn::kChunk + n_seqs;
+    p.chunk = chunk;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
 
     const char *name = "";
     const bool bf16 = dtype == DN_BF16;
     cudaError_t err;
-    if (tokens > 0 && dn::tc_supported(dk, dv, bf16))
+    if (use_tc(tokens, dk, dv, dtype, chunk))
         err = dn::tc_launch(p, (cudaStream_t)stream, &name);
     else
         err = dn::simt_launch(p, bf16, (cudaStream_t)stream, &name);

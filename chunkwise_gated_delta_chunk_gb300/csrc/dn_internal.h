@@ -6,7 +6,7 @@
 
 namespace dn {
 
-constexpr int kChunk = 64;  // C: tokens per chunk
+constexpr int kChunk = 64;  // C: tokens per chunk of the tensor-core path; tile size of both paths
 
 // Bits of the per-device status word (see dn_check in the public header).
 constexpr unsigned kStatusTimeout = 1u;   // a bounded mbarrier wait ran out
@@ -23,8 +23,9 @@ struct Params {
     long long tokens;          // B*T
     float scale;
     unsigned *status;          // per-device status word
-    void *ws;                  // workspace: nslots x Nv slots of T' | T'' (tensor-core path)
+    void *ws;                  // workspace: nslots x Nv slots of T' | T'' | P (tensor-core path)
     long long nslots;          // floor(tokens / C) + N
+    int chunk;                 // chunk length: 64 (both paths) or 16 / 32 (CUDA-core path)
 };
 
 // CUDA-core kernel: fp32 arithmetic for every product; any supported shape.

@@ -9,7 +9,8 @@
 //
 // One CTA owns one (sequence, value head, 32-column value tile) and walks the
 // sequence's chunks in order, keeping its fp32 state tile S[dk][32] in shared
-// memory.  Per chunk of L <= 64 tokens:
+// memory.  Chunks are p.chunk = 16, 32 or 64 tokens long; every chunk uses
+// 64-row tiles whose rows past its length L are zero.  Per chunk:
 //   a1  G = inclusive prefix sum of g (warp scan), e^{G_i}, e^{G_L - G_i}
 //   a2  A_ij = -beta_i (k_i.k_j) e^{G_i-G_j} (j < i),
 //       P_ij = scale (q_i.k_j) e^{G_i-G_j} (j <= i)
@@ -146,8 +147,9 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         sS[idx] = (p.h0 && c < bvw) ? p.h0[sbase + (size_t)d * dv + v0 + c] : 0.0f;
     }
 
-    for (long long t0 = bos; t0 < eos; t0 += C) {
-        const int L = (eos - t0) < C ? (int)(eos - t0) : C;
+    const int CH = p.chunk;  // 16, 32 or 64 (<= C)
+    for (long long t0 = bos; t0 < eos; t0 += CH) {
+        const int L = (eos - t0) < CH ? (int)(eos - t0) : CH;
         __syncthreads();  // previous chunk fully consumed
 
         // ---- load the chunk --------------------------------------------

@@ -86,7 +86,10 @@ typedef enum {
  *   dtype       DN_BF16 or DN_F32.  With DN_F32 every product is computed in
  *               fp32 on CUDA cores (no TF32), and dk must be <= 128.
  *   scale       multiplies q in the output; scale <= 0 selects 1/sqrt(dk).
- *   chunk       chunk length C; only 64 is built (others: DN_ERR_UNSUPPORTED).
+ *   chunk       chunk length C: 16, 32 or 64 ([WY] §5 chunk_size; the result
+ *               is the same up to rounding, [WY] §6).  64 runs the tensor-core
+ *               path where it applies; 16 and 32 run the CUDA-core kernel.
+ *               Other values: DN_ERR_UNSUPPORTED.
  *   o           [B, T, Nv, dv]  dtype       output, written for every token of
  *                                           every sequence (rounded to nearest
  *                                           even from fp32 for DN_BF16).
@@ -101,11 +104,11 @@ typedef enum {
  *
  * Returns DN_OK once the work is enqueued; DN_ERR_INVALID_ARG also when the
  * workspace is missing, misaligned or too small.  The tensor-core path
- * (bf16, dk = 128, dv a multiple of 128) launches two kernels per call: the
- * per-chunk WY inverse T and causal scores of every chunk in parallel
- * ([WY] §2.3-§2.4), then
- * the sequential state scan and output ([CGDR] §3.2-§3.3).  Other shapes
- * launch one CUDA-core kernel.
+ * (bf16, dk = 128, dv a multiple of 128, chunk 64) launches two kernels per
+ * call: the per-chunk WY inverse T and causal scores of every chunk in
+ * parallel ([WY] §2.3-§2.4), then the sequential state scan and output
+ * ([CGDR] §3.2-§3.3).  Other shapes and chunk sizes launch one CUDA-core
+ * kernel.
  */
 dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,

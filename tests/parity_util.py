@@ -17,12 +17,12 @@ TOL = {
 }
 
 
-def run_gpu(inp: dict, device="cuda", output_final_state=True, scale=None):
+def run_gpu(inp: dict, device="cuda", output_final_state=True, scale=None, chunk=64):
     import chunkwise_gated_delta_chunk_gb300 as dn
     d = workloads.to_device(inp, device)
     o, ht = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
                          scale=inp["scale"] if scale is None else scale,
-                         output_final_state=output_final_state)
+                         output_final_state=output_final_state, chunk=chunk)
     st = dn.dn_check()
     assert st == dn.DN_OK, dn.dn_status_str(st)
     return o, ht

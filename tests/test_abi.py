@@ -86,7 +86,8 @@ def call(clib, **over):
     (dict(dtype=7), dn.DN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), dn.DN_ERR_INVALID_ARG),
     (dict(chunk=0), dn.DN_ERR_INVALID_ARG),
-    (dict(chunk=32), dn.DN_ERR_UNSUPPORTED),             # only C = 64 is built
+    (dict(chunk=48), dn.DN_ERR_UNSUPPORTED),             # C in {16, 32, 64} is built
+    (dict(chunk=128), dn.DN_ERR_UNSUPPORTED),
     (dict(dk=96), dn.DN_ERR_UNSUPPORTED),
     (dict(dv=512), dn.DN_ERR_UNSUPPORTED),
     (dict(dtype=dn.DN_F32, dk=256), dn.DN_ERR_UNSUPPORTED),
@@ -104,7 +105,8 @@ def test_workspace_size(clib):
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
     assert ws(0, 0, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0
-    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 32) == 0     # rejected chunk size
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 32) == 0     # chunk 32: CUDA-core path
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 48) == 0     # rejected chunk size
 
 
 @pytest.mark.parametrize("ws,wsb", [(None, 0), (A, 1024), (A + 8, 1 << 30), (None, 1 << 30)])

@@ -46,6 +46,31 @@ def test_lengths(lib, T):
     check(inp, o, ht, label="T=%d" % T)
 
 
+@pytest.mark.parametrize("chunk", [16, 32])
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.bfloat16, 64, 256),
+                                         (torch.float32, 64, 64)])
+def test_chunk_sizes(lib, chunk, dtype, dk, dv):
+    """C = 16 and 32 ([WY] §5 chunk_size) give the recurrence's result: ragged
+    tails, a varlen GQA batch with empty and length-1 sequences."""
+    inp = inputs(B=2, T=150, dk=dk, dv=dv, dtype=dtype, seed=400 + chunk + dk)
+    o, ht = run_gpu(inp, chunk=chunk)
+    check(inp, o, ht, label="C=%d %s %dx%d" % (chunk, dtype, dk, dv))
+    inp = inputs(B=1, Nk=2, Nv=4, dk=dk, dv=dv, dtype=dtype, lengths=[1, 0, 33, 64, 97],
+                 seed=450 + chunk + dk)
+    o, ht = run_gpu(inp, chunk=chunk)
+    check(inp, o, ht, label="C=%d varlen" % chunk)
+
+
+def test_chunk_sizes_agree(lib):
+    """The same inputs at C = 16, 32 and 64 agree with each other to the
+    rounding of the two paths (the chunk form is exact, [WY] §6)."""
+    inp = inputs(B=2, T=300, dk=128, dv=128, seed=460)
+    outs = [run_gpu(inp, chunk=c) for c in (16, 32, 64)]
+    for (o, ht) in outs[1:]:
+        assert (o.float() - outs[0][0].float()).abs().max().item() <= 2e-2
+        assert (ht - outs[0][1]).abs().max().item() <= 2e-2
+
+
 @pytest.mark.parametrize("nv_per_nk", [1, 2, 4])
 def test_varlen_gqa(lib, nv_per_nk):
     lengths = [1, 63, 64, 65, 0, 200, 128, 3]
