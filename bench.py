@@ -264,6 +264,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunk", type=int, default=64, choices=[16, 32, 64],
                     help="chunk length C (16 and 32 run the CUDA-core kernel)")
+    ap.add_argument("--mode", default="chunk", choices=["chunk", "recurrent"],
+                    help="dn_chunk_fwd (default) or the token-serial dn_recurrent_fwd")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -304,8 +306,12 @@ def main():
 
     def launch(q=d["q"], k=d["k"], v=d["v"], beta=d["beta"], g=d["g"], h0=d["h0"],
                cu=d["cu_seqlens"], o=o, ht=ht):
-        st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
-                             inp["scale"], args.chunk, o, ht, ws, stream=stream)
+        if args.mode == "recurrent":
+            st = dn.dn_recurrent_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
+                                     inp["scale"], o, ht, stream=stream)
+        else:
+            st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
+                                 inp["scale"], args.chunk, o, ht, ws, stream=stream)
         if st != dn.DN_OK:
             raise dn.DnError(st)
 
@@ -410,8 +416,8 @@ def main():
                 n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16"
                 if d["q"].dtype == torch.bfloat16 else "f32", data="synthetic",
-                config=config_of(wl_name, inp, chunk=args.chunk, l2="flushed before every timed step "
-                                 "(256 MiB write, outside the step's events)"),
+                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2="flushed before every timed step "
+                                      "(256 MiB write, outside the step's events)"), mode=args.mode),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
                 gpu_launches=K, roofline=roof,
                 e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,

@@ -7,7 +7,9 @@ PyTorch supplies device memory and streams.
 
 Names follow the C ABI: :func:`dn_chunk_fwd`,
 :func:`dn_chunk_fwd_workspace_bytes`, :func:`dn_chunk_fwd_noalloc`,
-:func:`dn_check`, :func:`dn_status_str`, :func:`dn_last_kernel`.  :func:`chunk_fwd` is a convenience that allocates
+:func:`dn_recurrent_fwd`, :func:`dn_check`, :func:`dn_status_str`,
+:func:`dn_last_kernel`.  :func:`recurrent_fwd` is the same convenience for
+the token-serial entry point.  :func:`chunk_fwd` is a convenience that allocates
 ``o``, ``ht`` and the workspace with torch and calls :func:`dn_chunk_fwd`.
 """
 from __future__ import annotations
@@ -29,8 +31,8 @@ DN_BF16 = 0
 DN_F32 = 1
 
 # Every symbol the public header declares.
-ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_chunk_fwd_noalloc", "dn_check",
-               "dn_status_str", "dn_last_kernel")
+ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_chunk_fwd_noalloc",
+               "dn_recurrent_fwd", "dn_check", "dn_status_str", "dn_last_kernel")
 
 # Size of the library's fixed scratch array used by dn_chunk_fwd_noalloc.
 DN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -65,6 +67,8 @@ def load(path: str | None = None):
         lib.dn_chunk_fwd_workspace_bytes.restype = Z
         lib.dn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P]
         lib.dn_chunk_fwd_noalloc.restype = I
+        lib.dn_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P]
+        lib.dn_recurrent_fwd.restype = I
         lib.dn_check.argtypes = [P]
         lib.dn_check.restype = I
         lib.dn_status_str.argtypes = [I]
@@ -123,6 +127,36 @@ def dn_chunk_fwd_noalloc(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv,
                                     _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk),
                                     int(Nv), int(dk), int(dv), int(dtype), float(scale), int(chunk),
                                     _ptr(o), _ptr(ht), _stream(stream))
+
+
+def dn_recurrent_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
+                     scale, o, ht, stream=None) -> int:
+    """Call the token-serial C entry point as is; returns its status code."""
+    lib = load()
+    return lib.dn_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                                _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
+                                int(dk), int(dv), int(dtype), float(scale), _ptr(o), _ptr(ht),
+                                _stream(stream))
+
+
+def recurrent_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
+                  output_final_state=True, stream=None, o=None, ht=None):
+    """Allocate ``o`` (and ``ht``) and run :func:`dn_recurrent_fwd` (shapes as
+    for :func:`chunk_fwd`)."""
+    import torch
+    B, T, Nk, dk = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if o is None:
+        o = torch.empty(B, T, Nv, dv, dtype=q.dtype, device=q.device)
+    if ht is None and output_final_state:
+        ht = torch.empty(N, Nv, dk, dv, dtype=torch.float32, device=q.device)
+    st = dn_recurrent_fwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
+                          dtype_code(q.dtype), 0.0 if scale is None else scale, o,
+                          ht if output_final_state else None, stream)
+    if st != DN_OK:
+        raise DnError(st, "dn_recurrent_fwd")
+    return o, (ht if output_final_state else None)
 
 
 def dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype, chunk=64) -> int:

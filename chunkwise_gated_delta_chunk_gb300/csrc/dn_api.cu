@@ -122,6 +122,39 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     return DN_OK;
 }
 
+DN_EXPORT dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v,
+                                     const float *beta, const float *g, const float *h0,
+                                     const int64_t *cu_seqlens, int n_seqs,
+                                     int B, int T, int Nk, int Nv, int dk, int dv,
+                                     dn_dtype dtype, float scale,
+                                     void *o, float *ht, dn_stream_t stream) {
+    if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
+    if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
+        return DN_ERR_INVALID_ARG;
+    if (Nv % Nk != 0) return DN_ERR_INVALID_ARG;
+    if (cu_seqlens ? B != 1 : n_seqs != B) return DN_ERR_INVALID_ARG;
+    if (isnan(scale) || isinf(scale)) return DN_ERR_INVALID_ARG;
+    const long long tokens = (long long)B * T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, g, h0, cu_seqlens, o, ht};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
+    if (!dim_ok(dk) || !dim_ok(dv)) return DN_ERR_UNSUPPORTED;
+    if (n_seqs == 0) return DN_OK;
+
+    dn::Params p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.cu = cu_seqlens;
+    p.o = o; p.ht = ht;
+    p.N = n_seqs; p.B = B; p.T = T; p.Nk = Nk; p.Nv = Nv; p.dk = dk; p.dv = dv;
+    p.tokens = tokens;
+    p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
+    if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
+    const char *name = "";
+    if (dn::recurrent_launch(p, dtype == DN_BF16, (cudaStream_t)stream, &name) != cudaSuccess) return DN_ERR_CUDA;
+    t_last_kernel = name;
+    return DN_OK;
+}
+
 DN_EXPORT dn_status dn_check(dn_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DN_ERR_CUDA;
     unsigned *dptr = nullptr;

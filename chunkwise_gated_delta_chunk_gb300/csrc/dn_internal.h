@@ -33,4 +33,7 @@ struct Params {
 cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
 size_t simt_smem_bytes(int dk, bool bf16);
 
+// Token-serial kernel (decode / short sequences): any supported shape.
+cudaError_t recurrent_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
+
 }  // namespace dn

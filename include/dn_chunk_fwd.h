@@ -131,6 +131,25 @@ size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, in
                                     dn_dtype dtype, int chunk);
 
 /*
+ * dn_recurrent_fwd -- the same forward evaluated token by token ("fused
+ * recurrent", "flash linear attention" notes, Attention section: the
+ * recurrent mode the RetNet layer there picks for query lengths up to 64).
+ * It suits decoding (T = 1 with h0 in and ht out) and short prompts.
+ *
+ * Arguments as for dn_chunk_fwd without chunk and workspace; any dtype and
+ * dk, dv in {16, 32, 64, 128, 256} (fp32 included up to 256).  Per token,
+ * in fp32: S <- e^{g_t} S; d = beta_t (v_t - S^T k_t); S <- S + k_t d^T;
+ * o_t = scale S^T q_t ([CGDR] §1).  One CUDA-core kernel launch per call; it
+ * allocates nothing and needs no workspace.  Errors as for dn_chunk_fwd.
+ */
+dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v,
+                           const float *beta, const float *g, const float *h0,
+                           const int64_t *cu_seqlens, int n_seqs,
+                           int B, int T, int Nk, int Nv, int dk, int dv,
+                           dn_dtype dtype, float scale,
+                           void *o, float *ht, dn_stream_t stream);
+
+/*
  * dn_chunk_fwd_noalloc -- dn_chunk_fwd for callers that cannot allocate
  * device memory where they call it (for example a plugin host whose execute
  * path may not allocate because the host owns every device buffer, or a

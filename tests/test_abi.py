@@ -115,6 +115,35 @@ def test_workspace_checked_on_host(clib, ws, wsb):
     assert call(clib, dk=128, dv=128, Nk=2, Nv=4, ws=ws, wsb=wsb) == dn.DN_ERR_INVALID_ARG
 
 
+def rec_call(clib, **over):
+    args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, o=A, ht=None)
+    args.update(over)
+    return clib.dn_recurrent_fwd(args["q"], args["k"], args["v"], args["beta"], args["g"],
+                                 args["h0"], args["cu"], args["n"], args["B"], args["T"], args["Nk"],
+                                 args["Nv"], args["dk"], args["dv"], args["dtype"], args["scale"],
+                                 args["o"], args["ht"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Nv=3), dn.DN_ERR_INVALID_ARG),
+    (dict(n=3), dn.DN_ERR_INVALID_ARG),
+    (dict(cu=A, n=2, B=2), dn.DN_ERR_INVALID_ARG),
+    (dict(k=None), dn.DN_ERR_INVALID_ARG),
+    (dict(v=A + 8), dn.DN_ERR_INVALID_ARG),
+    (dict(dtype=3), dn.DN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), dn.DN_ERR_INVALID_ARG),
+    (dict(dk=96), dn.DN_ERR_UNSUPPORTED),
+    (dict(dv=512), dn.DN_ERR_UNSUPPORTED),
+])
+def test_recurrent_invalid_arguments_rejected_on_host(clib, over, code):
+    assert rec_call(clib, **over) == code
+
+
+def test_recurrent_zero_sequences_is_a_noop(clib):
+    assert rec_call(clib, n=0, B=0, T=0, q=None, k=None, v=None, beta=None, o=None) == dn.DN_OK
+
+
 def test_zero_sequences_is_a_noop(clib):
     assert call(clib, n=0, B=0, T=0, q=None, k=None, v=None, beta=None, o=None) == dn.DN_OK
     assert call(clib, n=0, B=1, T=5, cu=A) == dn.DN_OK

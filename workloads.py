@@ -14,8 +14,9 @@ Recipe (all draws on a CPU ``torch.Generator`` seeded per workload):
 * h0 ~ N(0, 0.02^2) in fp32 (standard deviation 0.02);
 * varlen: sequence lengths uniform in [1, 4096], drawn from the same seed.
 
-The five named workloads follow the pages' shapes: plain DeltaNet in fp32,
-gated DeltaNet at H=16/T=2048/d=128, GQA + varlen, long context and wide heads.
+The named workloads follow the pages' shapes: plain DeltaNet in fp32, gated
+DeltaNet at H=16/T=2048/d=128, GQA + varlen, long context and wide heads, and
+one decoding step (T = 1, state in and out) for the token-serial path.
 """
 from __future__ import annotations
 
@@ -57,6 +58,9 @@ WORKLOADS = {
                  dv=128, dtype=torch.bfloat16, gate_mu=5.0, h0=False, seed=4),
         Workload("gdn_wide_bf16_b8_h8_t8192_d256", B=8, T=8192, Nk=8, Nv=8, dk=256, dv=256,
                  dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=5),
+        # one decoding step of 64 sequences: the state comes in and goes out
+        Workload("gdn_decode_bf16_b64_h16_t1_d128", B=64, T=1, Nk=16, Nv=16, dk=128, dv=128,
+                 dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=6),
     ]
 }
 
