@@ -178,7 +178,8 @@ def oracle_time(inp: dict, units, threads: int = 0) -> float:
     import oracle
     t0 = time.perf_counter()
     oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
-                     inp["cu_seqlens"], inp["scale"], units=units, threads=threads)
+                     inp["cu_seqlens"], inp["scale"], units=units, threads=threads,
+                     use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     return time.perf_counter() - t0
 
 
@@ -249,7 +250,7 @@ def config_of(wl_name, inp, l2, chunk=64):
     Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
     return dict(workload=wl_name, B=B, T=T, Nk=Nk, Nv=Nv, dk=dk, dv=dv, chunk=chunk,
                 global_batch=B, seq_len=T, gate=inp["g"] is not None,
-                h0=inp["h0"] is not None, l2=l2)
+                h0=inp["h0"] is not None, qk_l2norm_in_kernel=bool(inp.get("qk_l2norm")), l2=l2)
 
 
 # --------------------------------------------------------------------------
@@ -303,15 +304,16 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     ws = dn.workspace_for(d["q"], d["v"], N, args.chunk)
+    flags = dn.DN_QK_L2NORM if inp.get("qk_l2norm") else 0
 
     def launch(q=d["q"], k=d["k"], v=d["v"], beta=d["beta"], g=d["g"], h0=d["h0"],
                cu=d["cu_seqlens"], o=o, ht=ht):
         if args.mode == "recurrent":
             st = dn.dn_recurrent_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
-                                     inp["scale"], o, ht, stream=stream)
+                                     inp["scale"], o, ht, stream=stream, flags=flags)
         else:
             st = dn.dn_chunk_fwd(q, k, v, beta, g, h0, cu, N, B, T, Nk, Nv, dk, dv, dt,
-                                 inp["scale"], args.chunk, o, ht, ws, stream=stream)
+                                 inp["scale"], args.chunk, o, ht, ws, stream=stream, flags=flags)
         if st != dn.DN_OK:
             raise dn.DnError(st)
 

@@ -30,6 +30,9 @@ DN_ERR_DEVICE_ARG = 5
 DN_BF16 = 0
 DN_F32 = 1
 
+# Option bits of the ``flags`` argument.
+DN_QK_L2NORM = 1
+
 # Every symbol the public header declares.
 ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_chunk_fwd_noalloc",
                "dn_recurrent_fwd", "dn_check", "dn_status_str", "dn_last_kernel")
@@ -60,14 +63,16 @@ def load(path: str | None = None):
                 "g.build()\"` -- there is no fallback path" % p)
         lib = ctypes.CDLL(p)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        Z = ctypes.c_size_t
-        lib.dn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P, Z, P]
+        Z, U = ctypes.c_size_t, ctypes.c_uint
+        lib.dn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, U, I, P, P, P, Z,
+                                     P]
         lib.dn_chunk_fwd.restype = I
         lib.dn_chunk_fwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
         lib.dn_chunk_fwd_workspace_bytes.restype = Z
-        lib.dn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P, P, P]
+        lib.dn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, U, I, P,
+                                             P, P]
         lib.dn_chunk_fwd_noalloc.restype = I
-        lib.dn_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, P, P, P]
+        lib.dn_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, U, P, P, P]
         lib.dn_recurrent_fwd.restype = I
         lib.dn_check.argtypes = [P]
         lib.dn_check.restype = I
@@ -101,11 +106,13 @@ def _stream(stream):
 
 
 def dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
-                 scale, chunk, o, ht, workspace=None, workspace_bytes=None, stream=None) -> int:
+                 scale, chunk, o, ht, workspace=None, workspace_bytes=None, stream=None,
+                 flags=0) -> int:
     """Call the C entry point as is; returns its status code.
 
     ``workspace`` is a device tensor (its byte size is passed unless
-    ``workspace_bytes`` is given), an int address, or None.
+    ``workspace_bytes`` is given), an int address, or None.  ``flags`` is the
+    C argument of that name (0 or :data:`DN_QK_L2NORM`).
     """
     lib = load()
     if workspace_bytes is None:
@@ -114,35 +121,37 @@ def dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv,
             workspace_bytes = workspace.numel() * workspace.element_size()
     return lib.dn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                             _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
-                            int(dk), int(dv), int(dtype), float(scale), int(chunk), _ptr(o),
-                            _ptr(ht), _ptr(workspace), int(workspace_bytes), _stream(stream))
+                            int(dk), int(dv), int(dtype), float(scale), int(flags), int(chunk),
+                            _ptr(o), _ptr(ht), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
 
 
 def dn_chunk_fwd_noalloc(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
-                         scale, chunk, o, ht, stream=None) -> int:
+                         scale, chunk, o, ht, stream=None, flags=0) -> int:
     """Call the C entry point that takes no workspace (it uses the library's
     fixed scratch array and allocates nothing); returns its status code."""
     lib = load()
     return lib.dn_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                                     _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk),
-                                    int(Nv), int(dk), int(dv), int(dtype), float(scale), int(chunk),
-                                    _ptr(o), _ptr(ht), _stream(stream))
+                                    int(Nv), int(dk), int(dv), int(dtype), float(scale), int(flags),
+                                    int(chunk), _ptr(o), _ptr(ht), _stream(stream))
 
 
 def dn_recurrent_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype,
-                     scale, o, ht, stream=None) -> int:
+                     scale, o, ht, stream=None, flags=0) -> int:
     """Call the token-serial C entry point as is; returns its status code."""
     lib = load()
     return lib.dn_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
                                 _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
-                                int(dk), int(dv), int(dtype), float(scale), _ptr(o), _ptr(ht),
-                                _stream(stream))
+                                int(dk), int(dv), int(dtype), float(scale), int(flags), _ptr(o),
+                                _ptr(ht), _stream(stream))
 
 
 def recurrent_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
-                  output_final_state=True, stream=None, o=None, ht=None):
-    """Allocate ``o`` (and ``ht``) and run :func:`dn_recurrent_fwd` (shapes as
-    for :func:`chunk_fwd`)."""
+                  output_final_state=True, stream=None, o=None, ht=None,
+                  use_qk_l2norm_in_kernel=False):
+    """Allocate ``o`` (and ``ht``) and run :func:`dn_recurrent_fwd` (shapes
+    and options as for :func:`chunk_fwd`)."""
     import torch
     B, T, Nk, dk = q.shape
     Nv, dv = v.shape[2], v.shape[3]
@@ -153,7 +162,8 @@ def recurrent_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
         ht = torch.empty(N, Nv, dk, dv, dtype=torch.float32, device=q.device)
     st = dn_recurrent_fwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
                           dtype_code(q.dtype), 0.0 if scale is None else scale, o,
-                          ht if output_final_state else None, stream)
+                          ht if output_final_state else None, stream,
+                          flags=DN_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
     if st != DN_OK:
         raise DnError(st, "dn_recurrent_fwd")
     return o, (ht if output_final_state else None)
@@ -200,12 +210,15 @@ def dtype_code(dtype) -> int:
 
 
 def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
-              output_final_state=True, chunk=64, stream=None, o=None, ht=None, workspace=None):
+              output_final_state=True, chunk=64, stream=None, o=None, ht=None, workspace=None,
+              use_qk_l2norm_in_kernel=False):
     """Allocate ``o`` (and ``ht``, and the workspace) and run :func:`dn_chunk_fwd`.
 
     q, k ``[B, T, Nk, dk]``; v ``[B, T, Nv, dv]``; beta, g ``[B, T, Nv]`` fp32;
     h0 ``[N, Nv, dk, dv]`` fp32; cu_seqlens int64 ``[N+1]`` on the device.
-    Returns ``(o, ht)`` (``ht`` is None unless ``output_final_state``).
+    ``use_qk_l2norm_in_kernel`` sets :data:`DN_QK_L2NORM` (the kernels
+    normalise every q and k row).  Returns ``(o, ht)`` (``ht`` is None unless
+    ``output_final_state``).
     """
     import torch
     B, T, Nk, dk = q.shape
@@ -219,7 +232,8 @@ def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
         workspace = workspace_for(q, v, N, chunk)
     st = dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
                       dtype_code(q.dtype), 0.0 if scale is None else scale, chunk, o,
-                      ht if output_final_state else None, workspace, stream=stream)
+                      ht if output_final_state else None, workspace, stream=stream,
+                      flags=DN_QK_L2NORM if use_qk_l2norm_in_kernel else 0)
     if st != DN_OK:
         raise DnError(st)
     return o, (ht if output_final_state else None)

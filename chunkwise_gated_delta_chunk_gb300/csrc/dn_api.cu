@@ -47,6 +47,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128 || d == 256; }
 
+bool flags_ok(unsigned flags) { return (flags & ~DN_QK_L2NORM) == 0; }
+static_assert(DN_QK_L2NORM == dn::kQkL2Norm, "public and internal flag bits agree");
+
 // Bytes of workspace the call with these sizes needs (0: none).  The
 // tensor-core path keeps T' | T'' of every chunk there between its two kernels.
 bool chunk_ok(int chunk) { return chunk == 16 || chunk == 32 || chunk == dn::kChunk; }
@@ -74,7 +77,7 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                                  const float *beta, const float *g, const float *h0,
                                  const int64_t *cu_seqlens, int n_seqs,
                                  int B, int T, int Nk, int Nv, int dk, int dv,
-                                 dn_dtype dtype, float scale, int chunk,
+                                 dn_dtype dtype, float scale, unsigned flags, int chunk,
                                  void *o, float *ht, void *workspace, size_t workspace_bytes_,
                                  dn_stream_t stream) {
     // ---- arguments that are wrong whatever is built ----------------------
@@ -84,6 +87,7 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     if (Nv % Nk != 0) return DN_ERR_INVALID_ARG;
     if (cu_seqlens ? B != 1 : n_seqs != B) return DN_ERR_INVALID_ARG;
     if (isnan(scale) || isinf(scale)) return DN_ERR_INVALID_ARG;
+    if (!flags_ok(flags)) return DN_ERR_INVALID_ARG;
     if (chunk <= 0) return DN_ERR_INVALID_ARG;
     const long long tokens = (long long)B * T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
@@ -108,6 +112,7 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     p.ws = workspace;
     p.nslots = tokens / dn::kChunk + n_seqs;
     p.chunk = chunk;
+    p.flags = flags;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
 
     const char *name = "";
@@ -126,7 +131,7 @@ DN_EXPORT dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v
                                      const float *beta, const float *g, const float *h0,
                                      const int64_t *cu_seqlens, int n_seqs,
                                      int B, int T, int Nk, int Nv, int dk, int dv,
-                                     dn_dtype dtype, float scale,
+                                     dn_dtype dtype, float scale, unsigned flags,
                                      void *o, float *ht, dn_stream_t stream) {
     if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
     if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
@@ -134,6 +139,7 @@ DN_EXPORT dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v
     if (Nv % Nk != 0) return DN_ERR_INVALID_ARG;
     if (cu_seqlens ? B != 1 : n_seqs != B) return DN_ERR_INVALID_ARG;
     if (isnan(scale) || isinf(scale)) return DN_ERR_INVALID_ARG;
+    if (!flags_ok(flags)) return DN_ERR_INVALID_ARG;
     const long long tokens = (long long)B * T;
     if (tokens > 0 && (!q || !k || !v || !beta || !o)) return DN_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, beta, g, h0, cu_seqlens, o, ht};
@@ -148,6 +154,7 @@ DN_EXPORT dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v
     p.N = n_seqs; p.B = B; p.T = T; p.Nk = Nk; p.Nv = Nv; p.dk = dk; p.dv = dv;
     p.tokens = tokens;
     p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
+    p.flags = flags;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
     const char *name = "";
     if (dn::recurrent_launch(p, dtype == DN_BF16, (cudaStream_t)stream, &name) != cudaSuccess) return DN_ERR_CUDA;

@@ -22,8 +22,13 @@ constexpr float kSpanMax = 80.f;
 // Bytes of one workspace slot: T' = T diag(beta e^G), T'' = T diag(beta) and
 // P = tril(scale QK^T . D), each a 64 x 64 bf16 matrix stored as the
 // 128-byte-swizzled K-major image the MMAs read (row i at 128 i, 16-byte
-// chunk c at (c ^ (i & 7)) * 16), in that order.
-constexpr uint32_t kSlotBytes = 24576;
+// chunk c at (c ^ (i & 7)) * 16), in that order; then, with kQkL2Norm, the
+// fp32 factors 1 / max(||k_i||, 1e-12) and 1 / max(||q_i||, 1e-12) of the
+// chunk's 64 rows (the WY kernel folds them into T' and P; the scan kernel
+// folds them into its per-token factors).
+constexpr uint32_t kImageBytes = 8192;
+constexpr uint32_t kSlotNormOff = 3 * kImageBytes;  // 64 key factors, then 64 query factors
+constexpr uint32_t kSlotBytes = kSlotNormOff + 2 * 64 * 4;
 
 __device__ __forceinline__ long long seq_bos(const Params &p, int n) {
     return p.cu ? p.cu[n] : (long long)n * p.T;
@@ -42,6 +47,7 @@ __device__ __forceinline__ long long wy_slot(long long t0, int n) { return t0 / 
 struct ChunkScalars {
     float ga, gb, ba, bb;      // G and beta of the lane's two tokens
     float GL, G0, span;        // G at the last token and at the first, max - min of G
+    float ka, kb, qa, qb;      // inverse key / query norms of the two tokens (1: no normalisation)
     int L;
 };
 
@@ -85,11 +91,24 @@ __device__ __forceinline__ ChunkScalars chunk_scalars_load(const Params &p, int 
     r.gb = gb;
     r.ba = ba;
     r.bb = bb;
+    r.ka = r.kb = r.qa = r.qb = 1.f;
     r.L = L;
     return r;
 }
 
-// Writes the scalar block of a chunk (see the SC_ offsets) into `sc`.
+// The chunk's inverse key and query norms from its workspace slot (written
+// by the WY kernel), for the lane's two tokens.
+__device__ __forceinline__ void chunk_norms_load(ChunkScalars &r, const uint8_t *slot, int lane) {
+    const float *f = reinterpret_cast<const float *>(slot + kSlotNormOff);
+    r.ka = f[lane];
+    r.kb = f[lane + 32];
+    r.qa = f[64 + lane];
+    r.qb = f[64 + lane + 32];
+}
+
+// Writes the scalar block of a chunk (see the SC_ offsets) into `sc`.  The
+// inverse norms, where set, ride on e^{G_L - G_i} (which multiplies k_i's
+// contribution to the state) and on scale e^{G_i} (which multiplies q_i).
 __device__ __forceinline__ void chunk_scalars_store(const Params &p, const ChunkScalars &r, float *sc, int lane) {
     const int ia = lane, ib = lane + 32;
     sc[SC_G + ia] = r.ga;
@@ -98,10 +117,10 @@ __device__ __forceinline__ void chunk_scalars_store(const Params &p, const Chunk
     sc[SC_BETA + ib] = r.bb;
     sc[SC_BEG + ia] = r.ba * __expf(r.ga);
     sc[SC_BEG + ib] = r.bb * __expf(r.gb);
-    sc[SC_DEC + ia] = ia < r.L ? __expf(r.GL - r.ga) : 0.f;
-    sc[SC_DEC + ib] = ib < r.L ? __expf(r.GL - r.gb) : 0.f;
-    sc[SC_OSC + ia] = p.scale * __expf(r.ga);
-    sc[SC_OSC + ib] = p.scale * __expf(r.gb);
+    sc[SC_DEC + ia] = ia < r.L ? __expf(r.GL - r.ga) * r.ka : 0.f;
+    sc[SC_DEC + ib] = ib < r.L ? __expf(r.GL - r.gb) * r.kb : 0.f;
+    sc[SC_OSC + ia] = p.scale * __expf(r.ga) * r.qa;
+    sc[SC_OSC + ib] = p.scale * __expf(r.gb) * r.qb;
     // e^{G_i - G_j} = e^{G_i - G_0} e^{G_0 - G_j} is safe when the chunk's
     // log-gate span is small enough that neither factor leaves fp32 range
     sc[SC_AF + ia] = __expf(r.ga - r.G0);

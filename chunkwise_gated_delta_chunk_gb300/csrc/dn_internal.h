@@ -12,6 +12,9 @@ constexpr int kChunk = 64;  // C: tokens per chunk of the tensor-core path; tile
 constexpr unsigned kStatusTimeout = 1u;   // a bounded mbarrier wait ran out
 constexpr unsigned kStatusBadSeq = 2u;    // cu_seqlens out of order / out of range
 
+// Option bits of Params::flags (the public DN_ flags of the same value).
+constexpr unsigned kQkL2Norm = 1u;        // q and k rows divided by max(||x||_2, 1e-12)
+
 struct Params {
     const void *q, *k, *v;     // [tokens, Nk, dk], [tokens, Nk, dk], [tokens, Nv, dv]
     const float *beta, *g;     // [tokens, Nv]; g may be null
@@ -26,6 +29,7 @@ struct Params {
     void *ws;                  // workspace: nslots x Nv slots of T' | T'' | P (tensor-core path)
     long long nslots;          // floor(tokens / C) + N
     int chunk;                 // chunk length: 64 (both paths) or 16 / 32 (CUDA-core path)
+    unsigned flags;            // kQkL2Norm
 };
 
 // CUDA-core kernel: fp32 arithmetic for every product; any supported shape.

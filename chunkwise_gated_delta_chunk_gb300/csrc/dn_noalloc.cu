@@ -59,12 +59,12 @@ DN_EXPORT dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const voi
                                          const float *beta, const float *g, const float *h0,
                                          const int64_t *cu_seqlens, int n_seqs,
                                          int B, int T, int Nk, int Nv, int dk, int dv,
-                                         dn_dtype dtype, float scale, int chunk,
+                                         dn_dtype dtype, float scale, unsigned flags, int chunk,
                                          void *o, float *ht, dn_stream_t stream) {
     const size_t need = dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype, chunk);
     if (need > kNoAllocScratchBytes) return DN_ERR_UNSUPPORTED;
     void *ws = nullptr;
     if (need > 0 && scratch_ptr(&ws) != cudaSuccess) return DN_ERR_CUDA;
     return dn_chunk_fwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype, scale,
-                        chunk, o, ht, ws, need > 0 ? kNoAllocScratchBytes : 0, stream);
+                        flags, chunk, o, ht, ws, need > 0 ? kNoAllocScratchBytes : 0, stream);
 }

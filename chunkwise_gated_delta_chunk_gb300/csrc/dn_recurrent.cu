@@ -14,7 +14,10 @@
 //     d   <- beta_t (v_t - S^T k_t)
 //     S   <- S + k_t d^T
 //     o_t <- scale S^T q_t
-// in fp32, the same recurrence the chunk form evaluates blockwise.
+// in fp32, the same recurrence the chunk form evaluates blockwise.  With
+// kQkL2Norm, k_t and q_t enter divided by max(||x||, 1e-12): the two factors
+// ride on the dot products and on d, and the rows in shared memory stay as
+// loaded.
 //
 // One 128-thread CTA per (sequence, value head, 32-column value tile).  The
 // fp32 state tile S[dk][32] lives in registers: lane c owns value column
@@ -89,6 +92,22 @@ __global__ void __launch_bounds__(RT) rec_fwd(Params p) {
         const float decay = p.g ? __expf(p.g[t * p.Nv + h]) : 1.f;
         const float vc = col ? ld_f(v, (t * p.Nv + h) * (long long)p.dv + v0 + c) : 0.f;
         __syncthreads();
+        // inverse norms of k_t and q_t (every warp computes both, in the same order)
+        float nk = 1.f, nq = 1.f;
+        if (p.flags & kQkL2Norm) {
+            float a = 0.f, b = 0.f;
+            for (int d = c; d < DK; d += 32) {
+                a = fmaf(sk[d], sk[d], a);
+                b = fmaf(sq[d], sq[d], b);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                b += __shfl_xor_sync(0xffffffffu, b, off);
+            }
+            nk = rsqrtf(fmaxf(a, 1e-24f));
+            nq = rsqrtf(fmaxf(b, 1e-24f));
+        }
         // S <- e^g S; this warp's share of (S^T k)_c
         float part = 0.f;
 #pragma unroll
@@ -98,8 +117,8 @@ __global__ void __launch_bounds__(RT) rec_fwd(Params p) {
         }
         red[0][w][c] = part;
         __syncthreads();
-        const float skc = (red[0][0][c] + red[0][1][c]) + (red[0][2][c] + red[0][3][c]);
-        const float delta = beta * (vc - skc);
+        const float skc = nk * ((red[0][0][c] + red[0][1][c]) + (red[0][2][c] + red[0][3][c]));
+        const float delta = beta * (vc - skc) * nk;  // k^ d = k (d / ||k||)
         // S <- S + k d^T; this warp's share of (S^T q)_c
         float op = 0.f;
 #pragma unroll
@@ -111,7 +130,7 @@ __global__ void __launch_bounds__(RT) rec_fwd(Params p) {
         __syncthreads();
         if (w == 0 && col)
             st_o(o, (t * p.Nv + h) * (long long)p.dv + v0 + c,
-                 p.scale * ((red[1][0][c] + red[1][1][c]) + (red[1][2][c] + red[1][3][c])));
+                 p.scale * nq * ((red[1][0][c] + red[1][1][c]) + (red[1][2][c] + red[1][3][c])));
     }
     if (p.ht && col) {
 #pragma unroll

@@ -21,6 +21,9 @@
 //        cheaper than the 64 x dk matrix W on CUDA cores)
 //   a6  o = scale e^{G} (Q S_in) + P v_new
 //   a5  S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T
+// With kQkL2Norm every product that reads a row k_i or q_i also takes the
+// row's factor 1 / max(||x||, 1e-12), computed in a1; the rows in shared
+// memory stay as loaded.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -47,7 +50,7 @@ __host__ __device__ constexpr int kq_ld(int dk) { return sizeof(Tin) == 2 ? dk +
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 struct Layout {
-    size_t k, q, s, a, t, p, v, r, vn, g, eg, dec, beta, end;
+    size_t k, q, s, a, t, p, v, r, vn, g, eg, dec, beta, rk, rq, end;
 };
 
 template <typename Tin>
@@ -69,6 +72,8 @@ __host__ __device__ inline Layout layout(int dk) {
     L.dec = off; off += C * 4;
     L.beta = off; off += C * 4;
     off += 16;  // G_L and spare
+    L.rk = off; off += C * 4;
+    L.rq = off; off += C * 4;
     L.end = off;
     return L;
 }
@@ -120,6 +125,9 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     float *sDec = reinterpret_cast<float *>(smem + lay.dec);
     float *sBeta = reinterpret_cast<float *>(smem + lay.beta);
     float *sGL = reinterpret_cast<float *>(smem + lay.beta + C * 4);
+    float *sRK = reinterpret_cast<float *>(smem + lay.rk);  // inverse key norms (1 without kQkL2Norm)
+    float *sRQ = reinterpret_cast<float *>(smem + lay.rq);  // inverse query norms
+    const bool qkn = (p.flags & kQkL2Norm) != 0;
     const int ldkq = kq_ld<Tin>(dk);
 
     const Tin *q = static_cast<const Tin *>(p.q);
@@ -185,6 +193,22 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             sDec[lane] = lane < L ? expf(GL - a) : 0.0f;
             sDec[lane + 32] = lane + 32 < L ? expf(GL - b) : 0.0f;
             if (lane == 0) sGL[0] = GL;
+        } else {
+            // warps 1-7: 1 / max(||x||, 1e-12) of every key and query row
+            for (int rr = warp - 1; rr < 2 * C; rr += 7) {
+                const int i = rr & (C - 1);
+                float ss = 0.0f;
+                if (qkn) {
+                    const Tin *x = (rr < C ? sK : sQ) + i * ldkq;
+                    for (int d = lane; d < dk; d += 32) {
+                        const float f = to_f(x[d]);
+                        ss = fmaf(f, f, ss);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                }
+                if (lane == 0) (rr < C ? sRK : sRQ)[i] = qkn ? rsqrtf(fmaxf(ss, 1e-24f)) : 1.0f;
+            }
         }
         __syncthreads();
 
@@ -200,9 +224,9 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                     sk = fmaf(to_f(ki[d]), kjd, sk);
                     sq = fmaf(to_f(qi[d]), kjd, sq);
                 }
-                const float dec = expf(sG[i] - sG[j]);
-                if (j < i) a = -sBeta[i] * dec * sk;
-                pv = p.scale * dec * sq;
+                const float dec = expf(sG[i] - sG[j]) * sRK[j];
+                if (j < i) a = -sBeta[i] * sRK[i] * dec * sk;
+                pv = p.scale * sRQ[i] * dec * sq;
             }
             sA[i * LDC + j] = a;
             sP[i * LDC + j] = pv;
@@ -248,7 +272,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
-                sR[i * BV + c] = i < L ? sBeta[i] * (sV[i * BV + c] - sEG[i] * ks[r]) : 0.0f;
+                sR[i * BV + c] = i < L ? sBeta[i] * (sV[i * BV + c] - sEG[i] * sRK[i] * ks[r]) : 0.0f;
             }
         }
         __syncthreads();
@@ -285,7 +309,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
                 if (i < L && c < bvw) {
-                    const float out = fmaf(p.scale * sEG[i], qs[r], acc[r]);
+                    const float out = fmaf(p.scale * sEG[i] * sRQ[i], qs[r], acc[r]);
                     put(o + ((t0 + i) * Nv + h) * (long long)dv + v0 + c, out);
                 }
             }
@@ -302,7 +326,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                     acc[r] = d < dk ? eGL * sS[d * BV + c] : 0.0f;
                 }
                 for (int i = 0; i < L; ++i) {
-                    const float w = sDec[i] * sVn[i * BV + c];
+                    const float w = sDec[i] * sRK[i] * sVn[i * BV + c];
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
                         const int d = d0 + 8 * r;

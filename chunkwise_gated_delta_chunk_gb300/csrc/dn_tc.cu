@@ -19,6 +19,10 @@
 //   O   S^T Q~^T         -> inter-chunk output, Q~ = diag(scale e^G) Q  (a6)
 //   PV  += v_new^T P^T   -> intra-chunk output, same accumulator   (a6)
 //
+// With in-kernel q / k normalisation (kQkL2Norm) the K and Q tiles stay as
+// loaded: T' and P already carry the inverse norms, and the loader folds the
+// per-token factors 1/||k_i|| into v~ and 1/||q_i|| into Q~.
+//
 // Warp roles (14 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
 // group of four consecutive warps covers all 128 lanes):
 //   0      loader: TMA for the K, Q, V tiles of a chunk, bulk copies of the
@@ -260,8 +264,12 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         const int s = c % NS;
         const long long t0 = u.bos + (long long)c * C;
         const int L = (int)min((long long)C, u.eos - t0);
-        // the gates come from global memory while the stage is still in use
-        const ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
+        // the gates (and the WY kernel's inverse q / k norms) come from
+        // global memory while the stage is still in use
+        ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
+        if (p.flags & kQkL2Norm)
+            chunk_norms_load(cs, static_cast<const uint8_t *>(p.ws) +
+                                     ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n)) * kSlotBytes, lane);
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
         DN_TRACE_EV(0, c);
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;

@@ -55,10 +55,11 @@ constexpr uint32_t OFF_K = 0;                    // K0 Q0 K1 Q1 (8 KB each): col
 constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases the tiles)
 constexpr uint32_t OFF_SCR = 64 * LDA * 4;       // solve scratch (aliases the tiles)
 constexpr uint32_t OFF_SC = 32768;               // gate scalars
-constexpr uint32_t OFF_BAR = OFF_SC + SCAL_FLOATS * 4;
+constexpr uint32_t OFF_NRM = OFF_SC + SCAL_FLOATS * 4;  // 64 inverse key norms, 64 inverse query norms
+constexpr uint32_t OFF_BAR = OFF_NRM + 512;
 constexpr uint32_t SMEM_USED = OFF_BAR + 32;     // 2 mbarriers, TMEM base, flag
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(kSlotBytes == 3 * 8192, "slot = T' | T'' | P");
+static_assert(kSlotNormOff == 3 * kImageBytes && kImageBytes == 8192, "slot = T' | T'' | P | norms");
 
 constexpr uint32_t TM_COLS = 64;
 constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);  // A, B K-major
@@ -283,6 +284,9 @@ __device__ __forceinline__ void store_image_row(uint8_t *img, int i, int hf, con
     }
 }
 
+// QKN: in-kernel q / k normalisation (kQkL2Norm); a template parameter so
+// that the plain instantiation carries none of its registers.
+template <bool QKN>
 __global__ void __launch_bounds__(NT, 6)
 wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ Params p) {
@@ -373,6 +377,38 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         tc_fence_after();
         if (*okf == 0) break;
 
+        float *nrm = reinterpret_cast<float *>(gb + OFF_NRM);
+        constexpr bool qkn = QKN;
+        if (qkn) {
+            // 1 / max(||x||, 1e-12) of key row i (threads 0-63) or query row
+            // i (64-127), from the two column halves of the tile.  The sum
+            // of squares does not depend on the order of the row's 16-byte
+            // chunks, so the swizzle is ignored; each lane starts at chunk
+            // (i & 7) so that eight lanes of a phase hit eight bank groups.
+            const int i = threadIdx.x & 63;
+            const uint8_t *row = gb + OFF_K + (threadIdx.x < 64 ? 0 : 8192) + i * 128;
+            float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + hb * 16384 + (((cc + i) & 7) << 4));
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(wv[e] << 16), hi = __uint_as_float(wv[e] & 0xffff0000u);
+                        ss0 = fmaf(lo, lo, ss0);
+                        ss1 = fmaf(hi, hi, ss1);
+                    }
+                }
+            const float rn = rsqrtf(fmaxf(ss0 + ss1, 1e-24f));
+            nrm[threadIdx.x] = rn;
+            reinterpret_cast<float *>(img + kSlotNormOff)[threadIdx.x] = rn;
+            // T' = T diag(beta e^G / ||k||)
+            if (threadIdx.x < 64) sc[SC_BEG + i] *= rn;
+            __syncthreads();
+        }
+
         {
             // row i of K K^T (warps 0-1) or of Q K^T (warps 2-3) = TMEM lane
             const int row = threadIdx.x, i = row & 63;
@@ -380,7 +416,8 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
             const float Gi = sc[SC_G + i];
             // A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij for j < i;
             // P_ij = scale e^{G_i - G_j} (Q K^T)_ij for j <= i
-            const float ri = rowA ? -sc[SC_BETA + i] : p.scale;
+            // with kQkL2Norm: times 1/||k_i|| or 1/||q_i||, and 1/||k_j|| per column
+            const float ri = (rowA ? -sc[SC_BETA + i] : p.scale) * (qkn ? nrm[row] : 1.f);
             const float ai = ri * sc[SC_AF + i];
             const int jmax = rowA ? i - 1 : i;
             const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
@@ -412,6 +449,17 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
                         dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax ? Gi - gg.y : -INFINITY);
                         dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax ? Gi - gg.z : -INFINITY);
                         dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax ? Gi - gg.w : -INFINITY);
+                    }
+                }
+                if (qkn) {
+                    const float4 *n4 = reinterpret_cast<const float4 *>(nrm + 32 * hf);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        const float4 nn = n4[q4];
+                        dcy[4 * q4] *= nn.x;
+                        dcy[4 * q4 + 1] *= nn.y;
+                        dcy[4 * q4 + 2] *= nn.z;
+                        dcy[4 * q4 + 3] *= nn.w;
                     }
                 }
                 tmem_wait_ld_dep(r);
@@ -473,11 +521,16 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
 cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
     const long long items = p.nslots * p.Nv;
     if (items <= 0) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(wy_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
-    if (err != cudaSuccess) return err;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)items;  // one CTA per item
-    wy_fwd<<<grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
+    const bool qkn = (p.flags & kQkL2Norm) != 0;
+    cudaError_t err = cudaFuncSetAttribute(qkn ? wy_fwd<true> : wy_fwd<false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    if (err != cudaSuccess) return err;
+    if (qkn)
+        wy_fwd<true><<<grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
+    else
+        wy_fwd<false><<<grid, NT, SMEM_ALLOC, stream>>>(mK, mQ, p);
     return cudaGetLastError();
 }
 

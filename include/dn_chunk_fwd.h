@@ -55,6 +55,18 @@ typedef enum {
     DN_ERR_DEVICE_ARG = 5    /* the device found a malformed cu_seqlens (dn_check) */
 } dn_status;
 
+/*
+ * Option bits (the `flags` argument of the forward entry points; other bits
+ * are rejected with DN_ERR_INVALID_ARG).
+ *   DN_QK_L2NORM  the kernels replace every query and key row (one token,
+ *                 one head, length dk) by x / max(||x||_2, 1e-12) before
+ *                 using it, in fp32, without writing the normalised rows
+ *                 anywhere ([WY] §5 use_qk_l2norm_in_kernel: the same
+ *                 normalisation the pages' tests apply to k beforehand,
+ *                 [WY] §6, done inside the kernels to save memory).
+ */
+#define DN_QK_L2NORM 1u
+
 /* Element type of q, k, v and o (one dtype for all four, as in [WY] §5). */
 typedef enum {
     DN_BF16 = 0,
@@ -86,6 +98,7 @@ typedef enum {
  *   dtype       DN_BF16 or DN_F32.  With DN_F32 every product is computed in
  *               fp32 on CUDA cores (no TF32), and dk must be <= 128.
  *   scale       multiplies q in the output; scale <= 0 selects 1/sqrt(dk).
+ *   flags       0 or DN_QK_L2NORM (q and k rows normalised in the kernels).
  *   chunk       chunk length C: 16, 32 or 64 ([WY] §5 chunk_size; the result
  *               is the same up to rounding, [WY] §6).  64 runs the tensor-core
  *               path where it applies; 16 and 32 run the CUDA-core kernel.
@@ -114,17 +127,19 @@ dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,
                        const int64_t *cu_seqlens, int n_seqs,
                        int B, int T, int Nk, int Nv, int dk, int dv,
-                       dn_dtype dtype, float scale, int chunk,
+                       dn_dtype dtype, float scale, unsigned flags, int chunk,
                        void *o, float *ht, void *workspace, size_t workspace_bytes,
                        dn_stream_t stream);
 
 /*
  * dn_chunk_fwd_workspace_bytes -- bytes of workspace dn_chunk_fwd needs for
  * these sizes (same meaning as there).  For the tensor-core path it is
- * (floor(B*T / 64) + n_seqs) * Nv * 24576: one 24 KB slot per chunk and value
- * head holding three bf16 64 x 64 matrices of the chunk, T diag(beta e^G) and
+ * (floor(B*T / 64) + n_seqs) * Nv * 25088: one slot per chunk and value head
+ * holding three bf16 64 x 64 matrices of the chunk, T diag(beta e^G) and
  * T diag(beta) of its WY representation ([WY] §2.4) and its causal score
- * matrix tril(scale QK^T . D) ([CGDR] §3.2).  Returns 0 when no workspace is
+ * matrix tril(scale QK^T . D) ([CGDR] §3.2), then the chunk's 64 key and 64
+ * query inverse norms (fp32; written only with DN_QK_L2NORM).  The size does
+ * not depend on the flags.  Returns 0 when no workspace is
  * needed, and for sizes dn_chunk_fwd would reject.  Host-only; no CUDA call.
  */
 size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
@@ -136,7 +151,8 @@ size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, in
  * recurrent mode the RetNet layer there picks for query lengths up to 64).
  * It suits decoding (T = 1 with h0 in and ht out) and short prompts.
  *
- * Arguments as for dn_chunk_fwd without chunk and workspace; any dtype and
+ * Arguments as for dn_chunk_fwd (flags included) without chunk and
+ * workspace; any dtype and
  * dk, dv in {16, 32, 64, 128, 256} (fp32 included up to 256).  Per token,
  * in fp32: S <- e^{g_t} S; d = beta_t (v_t - S^T k_t); S <- S + k_t d^T;
  * o_t = scale S^T q_t ([CGDR] §1).  One CUDA-core kernel launch per call; it
@@ -146,7 +162,7 @@ dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v,
                            const float *beta, const float *g, const float *h0,
                            const int64_t *cu_seqlens, int n_seqs,
                            int B, int T, int Nk, int Nv, int dk, int dv,
-                           dn_dtype dtype, float scale,
+                           dn_dtype dtype, float scale, unsigned flags,
                            void *o, float *ht, dn_stream_t stream);
 
 /*
@@ -165,7 +181,7 @@ dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v,
  *   - Sizes whose dn_chunk_fwd_workspace_bytes() exceeds
  *     DN_NOALLOC_SCRATCH_BYTES are rejected with DN_ERR_UNSUPPORTED before
  *     anything is launched (64 MiB covers (floor(B*T/64) + n_seqs) * Nv <=
- *     2730, e.g. B = 4, T = 2048, Nv = 16).
+ *     2674, e.g. B = 4, T = 2048, Nv = 16).
  *   - The first call with a given device current looks up the array's device
  *     address there (a host query that allocates nothing); make that first
  *     call before any stream capture on that device.
@@ -179,7 +195,7 @@ dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                const float *beta, const float *g, const float *h0,
                                const int64_t *cu_seqlens, int n_seqs,
                                int B, int T, int Nk, int Nv, int dk, int dv,
-                               dn_dtype dtype, float scale, int chunk,
+                               dn_dtype dtype, float scale, unsigned flags, int chunk,
                                void *o, float *ht, dn_stream_t stream);
 
 /*

@@ -13,8 +13,12 @@ Functions follow the pages' notation:
   §2.3-§2.4 and §3.1-§3.3), with a dense forward-substitution solve.
 * :func:`wy_chunk` -- steps a1-a4 of one chunk (G, T, W, U), exposed so the
   tests can check W and U against brute-force Householder-like products.
+* :func:`l2norm` -- the row normalisation that ``use_qk_l2norm_in_kernel``
+  applies to q and k ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与
+  Triton 内核实现" §5, §6); :func:`recurrent` and :func:`chunked` take the
+  same option and normalise q and k with it before anything else.
 
-All arithmetic is fp64 in ``dn_oracle.c``.  Every function here is pinned by
+All arithmetic is fp64 (``dn_oracle.c``; :func:`l2norm` in numpy).  Every function here is pinned by
 ``tests/test_oracle_pins.py``; none is marked "parity unpinned".
 """
 from __future__ import annotations
@@ -107,8 +111,22 @@ def _units(units):
     return u, len(u)
 
 
+def l2norm(x):
+    """Each row (last axis) of ``x`` divided by ``max(||row||_2, 1e-12)``, fp64.
+
+    The pages' tests L2-normalise k along the head dimension with
+    ``F.normalize(p=2, dim=-1)`` (whose guard is 1e-12), and the option
+    ``use_qk_l2norm_in_kernel`` moves that normalisation, for q and k, into
+    the kernels ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton
+    内核实现" §5 parameter table, §6).
+    """
+    x = _f64(x)
+    norm = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return x / np.maximum(norm, 1e-12)
+
+
 def recurrent(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
-              units=None, threads=0, read_mode=0):
+              units=None, threads=0, read_mode=0, use_qk_l2norm_in_kernel=False):
     """Token recurrence in fp64.
 
     Shapes: q, k ``[B, T, Nk, dk]``; v ``[B, T, Nv, dv]``; beta, g ``[B, T, Nv]``;
@@ -116,9 +134,12 @@ def recurrent(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
     in fp64.  ``units`` restricts the work to the listed ``n * Nv + h``
     (sequence, v-head) pairs; other outputs stay NaN.  ``read_mode=1`` is the
     literal undecayed read, kept only to show the chunk form rejects it.
+    ``use_qk_l2norm_in_kernel`` first replaces q and k by :func:`l2norm` of them.
     """
     lib = _load()
     q, k, v, beta, g, h0 = map(_f64, (q, k, v, beta, g, h0))
+    if use_qk_l2norm_in_kernel:
+        q, k = l2norm(q), l2norm(k)
     B, T, Nk, dk, Nv, dv, cu, N = _shapes(q, v, cu_seqlens)
     if scale is None:
         scale = dk ** -0.5
@@ -134,10 +155,13 @@ def recurrent(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
 
 
 def chunked(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, chunk=64,
-            units=None, threads=0):
-    """Chunk algorithm in fp64 (steps a1-a6); same shapes as :func:`recurrent`."""
+            units=None, threads=0, use_qk_l2norm_in_kernel=False):
+    """Chunk algorithm in fp64 (steps a1-a6); same shapes and options as
+    :func:`recurrent`."""
     lib = _load()
     q, k, v, beta, g, h0 = map(_f64, (q, k, v, beta, g, h0))
+    if use_qk_l2norm_in_kernel:
+        q, k = l2norm(q), l2norm(k)
     B, T, Nk, dk, Nv, dv, cu, N = _shapes(q, v, cu_seqlens)
     if scale is None:
         scale = dk ** -0.5

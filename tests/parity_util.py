@@ -18,11 +18,14 @@ TOL = {
 
 
 def run_gpu(inp: dict, device="cuda", output_final_state=True, scale=None, chunk=64):
+    """dn_chunk_fwd on the inputs (with in-kernel q / k normalisation when the
+    inputs ask for it), then dn_check."""
     import chunkwise_gated_delta_chunk_gb300 as dn
     d = workloads.to_device(inp, device)
     o, ht = dn.chunk_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
                          scale=inp["scale"] if scale is None else scale,
-                         output_final_state=output_final_state, chunk=chunk)
+                         output_final_state=output_final_state, chunk=chunk,
+                         use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     st = dn.dn_check()
     assert st == dn.DN_OK, dn.dn_status_str(st)
     return o, ht
@@ -54,7 +57,8 @@ def check(inp: dict, o_gpu, ht_gpu, units=None, threads=0, tol=None, label=""):
     tol = tol or TOL[dtype]
     o_ref, ht_ref = oracle.recurrent(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"],
                                      inp["h0"], inp["cu_seqlens"], inp["scale"], units=units,
-                                     threads=threads)
+                                     threads=threads,
+                                     use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     o_g = o_gpu.detach().to("cpu", torch.float64).numpy()
     ht_g = None if ht_gpu is None else ht_gpu.detach().to("cpu", torch.float64).numpy()
     Nv = inp["v"].shape[2]

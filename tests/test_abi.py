@@ -63,13 +63,13 @@ A = 1 << 20
 
 def call(clib, **over):
     args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
-                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, chunk=64, o=A, ht=None, ws=None,
-                wsb=0)
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, flags=0, chunk=64, o=A, ht=None,
+                ws=None, wsb=0)
     args.update(over)
     return clib.dn_chunk_fwd(args["q"], args["k"], args["v"], args["beta"], args["g"], args["h0"],
                              args["cu"], args["n"], args["B"], args["T"], args["Nk"], args["Nv"],
-                             args["dk"], args["dv"], args["dtype"], args["scale"], args["chunk"],
-                             args["o"], args["ht"], args["ws"], args["wsb"], None)
+                             args["dk"], args["dv"], args["dtype"], args["scale"], args["flags"],
+                             args["chunk"], args["o"], args["ht"], args["ws"], args["wsb"], None)
 
 
 @pytest.mark.parametrize("over,code", [
@@ -85,6 +85,8 @@ def call(clib, **over):
     (dict(T=-1), dn.DN_ERR_INVALID_ARG),
     (dict(dtype=7), dn.DN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), dn.DN_ERR_INVALID_ARG),
+    (dict(flags=2), dn.DN_ERR_INVALID_ARG),              # unknown option bit
+    (dict(flags=dn.DN_QK_L2NORM | 4), dn.DN_ERR_INVALID_ARG),
     (dict(chunk=0), dn.DN_ERR_INVALID_ARG),
     (dict(chunk=48), dn.DN_ERR_UNSUPPORTED),             # C in {16, 32, 64} is built
     (dict(chunk=128), dn.DN_ERR_UNSUPPORTED),
@@ -97,10 +99,10 @@ def test_invalid_arguments_rejected_on_host(clib, over, code):
 
 
 def test_workspace_size(clib):
-    """One 24 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
+    """One 24.5 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
     ws = clib.dn_chunk_fwd_workspace_bytes
-    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 24576
-    assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 24576
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 25088
+    assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 25088
     assert ws(2, 2, 64, 2, 4, 64, 64, dn.DN_BF16, 64) == 0       # CUDA-core path
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
@@ -117,12 +119,12 @@ def test_workspace_checked_on_host(clib, ws, wsb):
 
 def rec_call(clib, **over):
     args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
-                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, o=A, ht=None)
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, flags=0, o=A, ht=None)
     args.update(over)
     return clib.dn_recurrent_fwd(args["q"], args["k"], args["v"], args["beta"], args["g"],
                                  args["h0"], args["cu"], args["n"], args["B"], args["T"], args["Nk"],
                                  args["Nv"], args["dk"], args["dv"], args["dtype"], args["scale"],
-                                 args["o"], args["ht"], None)
+                                 args["flags"], args["o"], args["ht"], None)
 
 
 @pytest.mark.parametrize("over,code", [
@@ -133,6 +135,7 @@ def rec_call(clib, **over):
     (dict(v=A + 8), dn.DN_ERR_INVALID_ARG),
     (dict(dtype=3), dn.DN_ERR_INVALID_ARG),
     (dict(scale=float("inf")), dn.DN_ERR_INVALID_ARG),
+    (dict(flags=8), dn.DN_ERR_INVALID_ARG),
     (dict(dk=96), dn.DN_ERR_UNSUPPORTED),
     (dict(dv=512), dn.DN_ERR_UNSUPPORTED),
 ])

@@ -291,3 +291,71 @@ def test_empty_sequence_keeps_h0():
     o, ht = _call(oracle.recurrent, inp)
     h0 = inp["h0"].double().numpy()
     assert np.array_equal(ht[0], h0[0]) and np.array_equal(ht[2], h0[2])
+
+
+# --------------------------------------------------------------------------
+# In-kernel q / k normalisation ([WY] §5 use_qk_l2norm_in_kernel; [WY] §6:
+# the tests L2-normalise k along the head dimension, F.normalize(p=2,
+# dim=-1), or leave it to the kernels with the option on).
+# --------------------------------------------------------------------------
+def test_l2norm_closed_forms():
+    """Pythagorean rows by hand, the zero row, and a row below the 1e-12 guard
+    (divided by the guard, not by its own norm)."""
+    x = np.array([[3.0, 4.0, 0.0], [1.0, 2.0, 2.0], [0.0, 0.0, 0.0], [-1e-13, 0.0, 0.0],
+                  [0.0, -12.0, 5.0]])
+    want = np.array([[0.6, 0.8, 0.0], [1 / 3, 2 / 3, 2 / 3], [0.0, 0.0, 0.0], [-0.1, 0.0, 0.0],
+                     [0.0, -12 / 13, 5 / 13]])
+    assert np.allclose(oracle.l2norm(x), want, rtol=0, atol=1e-15)
+
+
+def test_l2norm_unit_rows_same_direction():
+    """Random rows of every head size come out with norm 1 and a positive
+    multiple of the input (x^ . x = ||x||), over arbitrary leading axes."""
+    rng = np.random.default_rng(5)
+    for d in (1, 16, 128, 256):
+        x = rng.standard_normal((3, 7, 2, d)) * np.exp(rng.standard_normal((3, 7, 2, 1)))
+        y = oracle.l2norm(x)
+        assert y.shape == x.shape
+        assert np.allclose(np.sqrt((y * y).sum(-1)), 1.0, rtol=0, atol=1e-14)
+        assert np.allclose((y * x).sum(-1), np.sqrt((x * x).sum(-1)), rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("fn", ["recurrent", "chunked"])
+def test_qk_l2norm_ignores_row_scale(fn):
+    """With the option on, rescaling every q row and every k row by its own
+    positive factor leaves o and ht unchanged; with it off they change.  A
+    normalisation that misses q or k, or normalises along the wrong axis,
+    fails this."""
+    f = getattr(oracle, fn)
+    inp = _small(B=1, Nk=2, Nv=4, dk=8, dv=5, lengths=[9, 70, 1], seed=91)
+    rng = np.random.default_rng(91)
+    sq = torch.tensor(np.exp(rng.standard_normal(inp["q"].shape[:-1] + (1,))))
+    sk = torch.tensor(np.exp(rng.standard_normal(inp["k"].shape[:-1] + (1,))))
+    scaled = dict(inp, q=inp["q"].double() * sq, k=inp["k"].double() * sk)
+    o1, h1 = _call(f, inp, use_qk_l2norm_in_kernel=True)
+    o2, h2 = _call(f, scaled, use_qk_l2norm_in_kernel=True)
+    assert _rel(o2, o1) < 1e-12 and _rel(h2, h1) < 1e-12
+    o3, _ = _call(f, scaled)
+    assert _rel(o3, o1) > 1e-2
+
+
+def test_qk_l2norm_reduces_to_plain_on_unit_rows():
+    """Rows that already have unit norm are left alone: the option changes
+    nothing (up to fp64 rounding) when q and k are unit rows."""
+    inp = _small(B=2, T=40, Nk=1, Nv=2, dk=16, dv=4, seed=92)
+    q, k = inp["q"].double(), inp["k"].double()
+    inp = dict(inp, q=q / q.norm(dim=-1, keepdim=True), k=k / k.norm(dim=-1, keepdim=True))
+    o1, h1 = _call(oracle.recurrent, inp)
+    o2, h2 = _call(oracle.recurrent, inp, use_qk_l2norm_in_kernel=True)
+    assert _rel(o2, o1) < 1e-13 and _rel(h2, h1) < 1e-13
+
+
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_qk_l2norm_chunk_equals_recurrent(chunk):
+    """The chunk form and the token recurrence agree with the option on, on
+    raw (unnormalised, widely scaled) q and k."""
+    inp = workloads.make_inputs(1, 0, 2, 4, 16, 8, dtype=torch.float32, gate_mu=3.0, h0=True,
+                                seed=93, lengths=[5, 64, 100], raw_qk=True)
+    o_r, h_r = _call(oracle.recurrent, inp, use_qk_l2norm_in_kernel=True)
+    o_c, h_c = _call(oracle.chunked, inp, chunk=chunk, use_qk_l2norm_in_kernel=True)
+    assert _rel(o_c, o_r) < 1e-12 and _rel(h_c, h_r) < 1e-12

@@ -222,6 +222,7 @@ SAMPLES = {
     "gdn_long_bf16_b1_h32_t32768_d128": [0, 31],
     "gdn_wide_bf16_b8_h8_t8192_d256": [0, 63],
     "gdn_decode_bf16_b64_h16_t1_d128": None,
+    "gdn_l2norm_bf16_b4_h16_t2048_d128": [0, 33, 63],
 }
 
 

@@ -22,7 +22,8 @@ def run(inp, output_final_state=True):
     import chunkwise_gated_delta_chunk_gb300 as dn
     d = workloads.to_device(inp, "cuda")
     o, ht = dn.recurrent_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
-                             scale=inp["scale"], output_final_state=output_final_state)
+                             scale=inp["scale"], output_final_state=output_final_state,
+                             use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     assert dn.dn_check() == dn.DN_OK
     return o, ht
 

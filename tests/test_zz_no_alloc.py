@@ -51,7 +51,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     import chunkwise_gated_delta_chunk_gb300 as dn
     dn.load()
     Nv = 16
-    slots = dn.DN_NOALLOC_SCRATCH_BYTES // (24576 * Nv)  # whole slots per value head that fit
+    slots = dn.DN_NOALLOC_SCRATCH_BYTES // (25088 * Nv)  # whole slots per value head that fit
     T = slots * 64  # floor(T / 64) + N = slots + 1 slots: one too many
     assert dn.dn_chunk_fwd_workspace_bytes(1, 1, T, Nv, Nv, 128, 128, dn.DN_BF16) > \
         dn.DN_NOALLOC_SCRATCH_BYTES

@@ -8,6 +8,9 @@ Recipe (all draws on a CPU ``torch.Generator`` seeded per workload):
 
 * q, v ~ N(0, 1), drawn in fp32 and cast to the workload dtype (RNE);
 * k ~ N(0, 1) in fp32, L2-normalised per (token, head) in fp32, then cast;
+  for the in-kernel normalisation workloads (``qk_l2norm``) k is left as
+  drawn, and every q and k row is multiplied by exp(0.5 z), z ~ N(0, 1), so
+  the row norms spread over about a factor of e around sqrt(d);
 * beta = sigmoid(N(0, 1)) in fp32;
 * g = log(sigmoid(N(mu, 1))) in fp32 (mu = 3, or 5 for the long-context
   workload), so every per-token decay e^g lies in (0, 1);
@@ -43,6 +46,7 @@ class Workload:
     n_varlen: int = 0          # > 0: that many packed sequences, B must be 1
     max_len: int = 4096
     chunk: int = 64
+    qk_l2norm: bool = False    # q and k left raw; the kernels normalise them
 
 
 WORKLOADS = {
@@ -61,6 +65,9 @@ WORKLOADS = {
         # one decoding step of 64 sequences: the state comes in and goes out
         Workload("gdn_decode_bf16_b64_h16_t1_d128", B=64, T=1, Nk=16, Nv=16, dk=128, dv=128,
                  dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=6),
+        # the gated DeltaNet shapes with raw q / k normalised inside the kernels
+        Workload("gdn_l2norm_bf16_b4_h16_t2048_d128", B=4, T=2048, Nk=16, Nv=16, dk=128,
+                 dv=128, dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=7, qk_l2norm=True),
     ]
 }
 
@@ -76,12 +83,13 @@ def make_inputs(B: int, T: int, Nk: int, Nv: int, dk: int, dv: int,
                 dtype: torch.dtype = torch.bfloat16, gate_mu: Optional[float] = 3.0,
                 h0: bool = True, seed: int = 0,
                 lengths: Optional[Sequence[int]] = None,
-                beta_range: Optional[tuple] = None) -> dict:
+                beta_range: Optional[tuple] = None, raw_qk: bool = False) -> dict:
     """Draw one input set on the CPU.
 
     With ``lengths`` the sequences are packed (B must be 1, T = sum(lengths))
     and ``cu_seqlens`` (int64, ``[N+1]``) is returned.  Keys: q, k, v, beta,
-    g (or None), h0 (or None), cu_seqlens (or None), scale, N.
+    g (or None), h0 (or None), cu_seqlens (or None), scale, N, qk_l2norm
+    (= ``raw_qk``: q and k are not normalised and need the in-kernel option).
     """
     gen = torch.Generator().manual_seed(seed)
     cu = None
@@ -97,7 +105,8 @@ def make_inputs(B: int, T: int, Nk: int, Nv: int, dk: int, dv: int,
         N = B
     q = torch.randn(B, T, Nk, dk, generator=gen)
     k = torch.randn(B, T, Nk, dk, generator=gen)
-    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+    if not raw_qk:
+        k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-12)
     v = torch.randn(B, T, Nv, dv, generator=gen)
     beta = torch.sigmoid(torch.randn(B, T, Nv, generator=gen))
     if beta_range is not None:
@@ -109,9 +118,12 @@ def make_inputs(B: int, T: int, Nk: int, Nv: int, dk: int, dv: int,
     s0 = None
     if h0:
         s0 = 0.02 * torch.randn(N, Nv, dk, dv, generator=gen)
+    if raw_qk:
+        q = q * torch.exp(0.5 * torch.randn(B, T, Nk, 1, generator=gen))
+        k = k * torch.exp(0.5 * torch.randn(B, T, Nk, 1, generator=gen))
     return dict(q=q.to(dtype), k=k.to(dtype), v=v.to(dtype), beta=beta.float(),
                 g=None if g is None else g.float(), h0=s0, cu_seqlens=cu,
-                scale=1.0 / math.sqrt(dk), N=N)
+                scale=1.0 / math.sqrt(dk), N=N, qk_l2norm=bool(raw_qk))
 
 
 def workload_inputs(name: str) -> dict:
@@ -123,7 +135,8 @@ def workload_inputs(name: str) -> dict:
         lengths = varlen_lengths(w.n_varlen, w.max_len, gen)
         # separate stream for the tensors so the lengths do not shift them
     return make_inputs(w.B, w.T, w.Nk, w.Nv, w.dk, w.dv, dtype=w.dtype, gate_mu=w.gate_mu,
-                       h0=w.h0, seed=w.seed + (1000 if w.n_varlen else 0), lengths=lengths)
+                       h0=w.h0, seed=w.seed + (1000 if w.n_varlen else 0), lengths=lengths,
+                       raw_qk=w.qk_l2norm)
 
 
 def to_device(inp: dict, device) -> dict:
