@@ -13,6 +13,8 @@ Functions follow the pages' notation:
   §2.3-§2.4 and §3.1-§3.3), with a dense forward-substitution solve.
 * :func:`wy_chunk` -- steps a1-a4 of one chunk (G, T, W, U), exposed so the
   tests can check W and U against brute-force Householder-like products.
+* :func:`recurrent_bwd` -- the gradient of :func:`recurrent` (reverse mode
+  through the token recurrence) for given output and final-state gradients.
 * :func:`l2norm` -- the row normalisation that ``use_qk_l2norm_in_kernel``
   applies to q and k ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与
   Triton 内核实现" §5, §6); :func:`recurrent` and :func:`chunked` take the
@@ -68,6 +70,9 @@ def _load():
             lib.dn_oracle_wy_chunk.argtypes = [I, I, I, P, ctypes.c_long, P, ctypes.c_long,
                                                P, ctypes.c_long, P, ctypes.c_long, P, P, P, P]
             lib.dn_oracle_wy_chunk.restype = None
+            lib.dn_oracle_recurrent_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
+                                                    P, P, P, P, P, P, P, P, P, I, I]
+            lib.dn_oracle_recurrent_bwd.restype = I
             lib.dn_oracle_default_threads.argtypes = []
             lib.dn_oracle_default_threads.restype = I
             _lib = lib
@@ -193,3 +198,36 @@ def wy_chunk(k, v, beta, g=None):
     lib.dn_oracle_wy_chunk(L, dk, dv, _ptr(k), dk, _ptr(v), dv, _ptr(beta), 1,
                            _ptr(g), 1, _ptr(G), _ptr(Tm), _ptr(W), _ptr(U))
     return G, Tm, W, U
+
+
+def recurrent_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, do=None,
+                  dht=None, groups=None, threads=0):
+    """Gradient of the forward in fp64, reverse mode through the token recurrence.
+
+    For the loss ``sum(do * o) + sum(dht * ht)`` of :func:`recurrent` (same
+    shapes; ``do`` like o, ``dht`` like ht or None), returns a dict with
+    ``dq``, ``dk`` (``[B, T, Nk, dk]``), ``dv`` (like v), ``dbeta``, ``dg``
+    (``[B, T, Nv]``) and ``dh0`` (``[N, Nv, dk, dv]``).  ``groups`` restricts
+    the work to the listed ``n * Nk + hk`` (sequence, key head) groups, each
+    with all value heads that read key head hk; other entries stay NaN.
+    ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §3.4
+    lists these gradients; the pages print no formula for them, so this is
+    the chain rule through each step of the definition.)
+    """
+    lib = _load()
+    q, k, v, beta, g, h0, do, dht = map(_f64, (q, k, v, beta, g, h0, do, dht))
+    B, T, Nk, dk, Nv, dv, cu, N = _shapes(q, v, cu_seqlens)
+    if scale is None:
+        scale = dk ** -0.5
+    out = dict(dq=np.full(q.shape, np.nan), dk=np.full(k.shape, np.nan),
+               dv=np.full(v.shape, np.nan), dbeta=np.full(beta.shape, np.nan),
+               dg=np.full(beta.shape, np.nan), dh0=np.full((N, Nv, dk, dv), np.nan))
+    gr, ng = _units(groups)
+    rc = lib.dn_oracle_recurrent_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                                     _ptr(cu), N, B, T, Nk, Nv, dk, dv, float(scale),
+                                     _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]),
+                                     _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dg"]),
+                                     _ptr(out["dh0"]), _ptr(gr), ng, int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (rc=%d)" % rc)
+    return out

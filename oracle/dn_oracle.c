@@ -12,7 +12,7 @@
  *   [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么"
  *          (what the ChunkGatedDeltaRule operator computes)
  *
- * Two independent forms are implemented:
+ * Two independent forms of the forward are implemented:
  *
  *   dn_oracle_recurrent  -- the definition: a token-by-token recurrence
  *                           ([WY] §1, [CGDR] §1), written out plainly.
@@ -20,6 +20,18 @@
  *                           prefix sum, WY matrix A, T = (I-A)^-1, W and U,
  *                           v_new, output, state ([CGDR] §3.1-§3.3,
  *                           [WY] §2.3-§2.4).  Used to pin the chunk algebra.
+ *
+ * and the gradient of the forward:
+ *
+ *   dn_oracle_recurrent_bwd -- reverse-mode differentiation of the token
+ *                           recurrence, token by token in reverse order
+ *                           ([WY] §3.4 names the gradients dq, dk, dv,
+ *                           dbeta and dh0 of the backward, and [WY] §6 its
+ *                           tests; dg is the gradient of the gated form).
+ *                           The pages print no backward formula, so this is
+ *                           the chain rule applied to each step of the
+ *                           definition; the tests pin it by finite
+ *                           differences of dn_oracle_recurrent.
  *
  * Readings taken where the pages are silent or garbled:
  *   - decay placement: the state is decayed *before* the delta read, i.e.
@@ -360,4 +372,258 @@ int dn_oracle_chunked(const double *q, const double *k, const double *v,
     J.o = o; J.ht = ht; J.chunk = chunk; J.read_mode = 0;
     J.units = units; J.n_units = n_units;
     return run(&J, n_threads);
+}
+
+/* ---------------------------------------------------------------------- */
+/* Gradient of the token recurrence (reverse mode).                        */
+/* ---------------------------------------------------------------------- */
+/*
+ * For the loss l = sum(do . o) + sum(dht . ht) of one forward, given do and
+ * dht (dht may be NULL: zero), the gradients of l with respect to q, k, v,
+ * beta, g and h0.  Per token of the forward (decayed read, reading 1):
+ *     a = e^{g_t};  S' = a S_{t-1};  p = S'^T k_t;  d = beta_t (v_t - p);
+ *     S_t = S' + k_t d^T;  o_t = scale S_t^T q_t.
+ * Walking the tokens backwards with dS = dl/dS_t (dht after the last one):
+ *     dS     += scale q_t do_t^T          dq_t  += scale S_t do_t
+ *     dd      = dS^T k_t                  dk_t  += dS d
+ *     dbeta_t = dd . (v_t - p)            dv_t   = beta_t dd
+ *     dp      = -beta_t dd                dS    += k_t dp^T     dk_t += S' dp
+ *     dg_t    = <dS, S'>                  dS     = a dS         (= dl/dS_{t-1})
+ * and dh0 = dS after the first token.  The states are recomputed from
+ * checkpoints taken every CK tokens of a forward pass.
+ *
+ * Work is split over (sequence, key head) groups, so that one thread owns
+ * every value head that reads a key head and sums their dq and dk.
+ */
+typedef struct {
+    const double *q, *k, *v, *beta, *g, *h0, *dout, *dht;
+    const int64_t *cu;
+    int n_seqs, B, T, Nk, Nv, dk, dv;
+    double scale;
+    double *dq, *dk_, *dv_, *dbeta, *dg, *dh0;
+    const int32_t *groups; /* group u = n * Nk + hk */
+    int n_groups;
+    int next, failed;
+    pthread_mutex_t lock;
+} bjob_t;
+
+enum { CK = 64 };
+
+static void bwd_unit(const bjob_t *J, int n, int h, double *ck, double *St, double *dS,
+                     double *Sp, double *tmp)
+{
+    const int dk = J->dk, dv = J->dv, Nk = J->Nk, Nv = J->Nv;
+    const int hk = h / (Nv / Nk);
+    const size_t sz = (size_t)dk * dv;
+    int64_t bos, eos;
+    if (J->cu) {
+        bos = J->cu[n];
+        eos = J->cu[n + 1];
+    } else {
+        bos = (int64_t)n * J->T;
+        eos = (int64_t)(n + 1) * J->T;
+    }
+    const int64_t len = eos - bos;
+    const int64_t nck = (len + CK - 1) / CK;
+
+    /* forward pass: the state before each block of CK tokens */
+    double *S = St;  /* scratch for the running state */
+    if (J->h0)
+        memcpy(S, J->h0 + ((size_t)n * Nv + h) * sz, sizeof(double) * sz);
+    else
+        memset(S, 0, sizeof(double) * sz);
+    for (int64_t c = 0; c < nck; ++c) {
+        memcpy(ck + (size_t)c * sz, S, sizeof(double) * sz);
+        const int64_t t1 = bos + (c + 1) * CK < eos ? bos + (c + 1) * CK : eos;
+        for (int64_t t = bos + c * CK; t < t1; ++t) {
+            const double *kt = J->k + ((size_t)t * Nk + hk) * dk;
+            const double *vt = J->v + ((size_t)t * Nv + h) * dv;
+            const double bt = J->beta[(size_t)t * Nv + h];
+            const double a = J->g ? exp(J->g[(size_t)t * Nv + h]) : 1.0;
+            for (size_t i = 0; i < sz; ++i) S[i] *= a;
+            for (int c2 = 0; c2 < dv; ++c2) {
+                double r = 0.0;
+                for (int d = 0; d < dk; ++d) r += kt[d] * S[d * dv + c2];
+                tmp[c2] = bt * (vt[c2] - r);
+            }
+            for (int d = 0; d < dk; ++d)
+                for (int c2 = 0; c2 < dv; ++c2) S[d * dv + c2] += kt[d] * tmp[c2];
+        }
+    }
+
+    /* backward pass */
+    if (J->dht)
+        memcpy(dS, J->dht + ((size_t)n * Nv + h) * sz, sizeof(double) * sz);
+    else
+        memset(dS, 0, sizeof(double) * sz);
+    double *p = tmp, *dlt = tmp + dv, *ddl = tmp + 2 * dv, *dp = tmp + 3 * dv;
+    for (int64_t c = nck - 1; c >= 0; --c) {
+        const int64_t t0 = bos + c * CK;
+        const int L = (int)((eos - t0) < CK ? (eos - t0) : CK);
+        /* states S_{t0-1} .. S_{t0+L-1} of this block: St[j] = state before token t0 + j */
+        memcpy(St, ck + (size_t)c * sz, sizeof(double) * sz);
+        for (int j = 0; j < L; ++j) {
+            const int64_t t = t0 + j;
+            const double *kt = J->k + ((size_t)t * Nk + hk) * dk;
+            const double *vt = J->v + ((size_t)t * Nv + h) * dv;
+            const double bt = J->beta[(size_t)t * Nv + h];
+            const double a = J->g ? exp(J->g[(size_t)t * Nv + h]) : 1.0;
+            const double *Sa = St + (size_t)j * sz;
+            double *Sb = St + (size_t)(j + 1) * sz;
+            for (size_t i = 0; i < sz; ++i) Sb[i] = a * Sa[i];
+            for (int c2 = 0; c2 < dv; ++c2) {
+                double r = 0.0;
+                for (int d = 0; d < dk; ++d) r += kt[d] * Sb[d * dv + c2];
+                dlt[c2] = bt * (vt[c2] - r);
+            }
+            for (int d = 0; d < dk; ++d)
+                for (int c2 = 0; c2 < dv; ++c2) Sb[d * dv + c2] += kt[d] * dlt[c2];
+        }
+        for (int j = L - 1; j >= 0; --j) {
+            const int64_t t = t0 + j;
+            const double *qt = J->q + ((size_t)t * Nk + hk) * dk;
+            const double *kt = J->k + ((size_t)t * Nk + hk) * dk;
+            const double *vt = J->v + ((size_t)t * Nv + h) * dv;
+            const double *dot = J->dout + ((size_t)t * Nv + h) * dv;
+            const double bt = J->beta[(size_t)t * Nv + h];
+            const double a = J->g ? exp(J->g[(size_t)t * Nv + h]) : 1.0;
+            const double *Sprev = St + (size_t)j * sz, *Snow = St + (size_t)(j + 1) * sz;
+            double *dqt = J->dq + ((size_t)t * Nk + hk) * dk;
+            double *dkt = J->dk_ + ((size_t)t * Nk + hk) * dk;
+            double *dvt = J->dv_ + ((size_t)t * Nv + h) * dv;
+            /* recompute S', p and d of this token */
+            for (size_t i = 0; i < sz; ++i) Sp[i] = a * Sprev[i];
+            for (int c2 = 0; c2 < dv; ++c2) {
+                double r = 0.0;
+                for (int d = 0; d < dk; ++d) r += kt[d] * Sp[d * dv + c2];
+                p[c2] = r;
+                dlt[c2] = bt * (vt[c2] - r);
+            }
+            /* o_t = scale S_t^T q_t */
+            for (int d = 0; d < dk; ++d) {
+                double r = 0.0;
+                for (int c2 = 0; c2 < dv; ++c2) {
+                    dS[d * dv + c2] += J->scale * qt[d] * dot[c2];
+                    r += Snow[d * dv + c2] * dot[c2];
+                }
+                dqt[d] += J->scale * r;
+            }
+            /* S_t = S' + k d^T */
+            for (int c2 = 0; c2 < dv; ++c2) {
+                double r = 0.0;
+                for (int d = 0; d < dk; ++d) r += dS[d * dv + c2] * kt[d];
+                ddl[c2] = r;
+            }
+            for (int d = 0; d < dk; ++d) {
+                double r = 0.0;
+                for (int c2 = 0; c2 < dv; ++c2) r += dS[d * dv + c2] * dlt[c2];
+                dkt[d] += r;
+            }
+            /* d = beta (v - p) */
+            double db = 0.0;
+            for (int c2 = 0; c2 < dv; ++c2) {
+                db += ddl[c2] * (vt[c2] - p[c2]);
+                dvt[c2] = bt * ddl[c2];
+                dp[c2] = -bt * ddl[c2];
+            }
+            J->dbeta[(size_t)t * Nv + h] = db;
+            /* p = S'^T k */
+            for (int d = 0; d < dk; ++d) {
+                double r = 0.0;
+                for (int c2 = 0; c2 < dv; ++c2) {
+                    dS[d * dv + c2] += kt[d] * dp[c2];
+                    r += Sp[d * dv + c2] * dp[c2];
+                }
+                dkt[d] += r;
+            }
+            /* S' = a S_{t-1} */
+            double dgt = 0.0;
+            for (size_t i = 0; i < sz; ++i) dgt += dS[i] * Sp[i];
+            if (J->dg) J->dg[(size_t)t * Nv + h] = dgt;
+            for (size_t i = 0; i < sz; ++i) dS[i] *= a;
+        }
+    }
+    if (J->dh0) memcpy(J->dh0 + ((size_t)n * Nv + h) * sz, dS, sizeof(double) * sz);
+}
+
+static void *bwd_worker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    const size_t sz = (size_t)J->dk * J->dv;
+    int64_t maxlen = J->T;
+    if (J->cu)
+        for (int n = 0; n < J->n_seqs; ++n)
+            if (J->cu[n + 1] - J->cu[n] > maxlen) maxlen = J->cu[n + 1] - J->cu[n];
+    const int64_t nck = (maxlen + CK - 1) / CK + 1;
+    double *ck = (double *)malloc(sizeof(double) * sz * nck);
+    double *St = (double *)malloc(sizeof(double) * sz * (CK + 1));
+    double *dS = (double *)malloc(sizeof(double) * sz);
+    double *Sp = (double *)malloc(sizeof(double) * sz);
+    double *tmp = (double *)malloc(sizeof(double) * 4 * J->dv);
+    if (!ck || !St || !dS || !Sp || !tmp) {
+        pthread_mutex_lock(&J->lock);
+        J->failed = 1;
+        pthread_mutex_unlock(&J->lock);
+    } else {
+        const int total = J->groups ? J->n_groups : J->n_seqs * J->Nk;
+        const int r = J->Nv / J->Nk;
+        for (;;) {
+            pthread_mutex_lock(&J->lock);
+            const int w = J->next++;
+            pthread_mutex_unlock(&J->lock);
+            if (w >= total) break;
+            const int u = J->groups ? J->groups[w] : w;
+            const int n = u / J->Nk, hk = u % J->Nk;
+            /* zero this group's dq and dk rows, then add every value head's share */
+            int64_t bos, eos;
+            if (J->cu) {
+                bos = J->cu[n];
+                eos = J->cu[n + 1];
+            } else {
+                bos = (int64_t)n * J->T;
+                eos = (int64_t)(n + 1) * J->T;
+            }
+            for (int64_t t = bos; t < eos; ++t) {
+                memset(J->dq + ((size_t)t * J->Nk + hk) * J->dk, 0, sizeof(double) * J->dk);
+                memset(J->dk_ + ((size_t)t * J->Nk + hk) * J->dk, 0, sizeof(double) * J->dk);
+            }
+            for (int h = hk * r; h < (hk + 1) * r; ++h) bwd_unit(J, n, h, ck, St, dS, Sp, tmp);
+        }
+    }
+    free(ck); free(St); free(dS); free(Sp); free(tmp);
+    return NULL;
+}
+
+int dn_oracle_recurrent_bwd(const double *q, const double *k, const double *v,
+                            const double *beta, const double *g, const double *h0,
+                            const int64_t *cu_seqlens, int n_seqs, int B, int T,
+                            int Nk, int Nv, int dk, int dv, double scale,
+                            const double *dout, const double *dht,
+                            double *dq, double *dk_out, double *dv_out, double *dbeta,
+                            double *dg, double *dh0,
+                            const int32_t *groups, int n_groups, int n_threads)
+{
+    if (Nk <= 0 || Nv <= 0 || Nv % Nk != 0 || dk <= 0 || dv <= 0) return 1;
+    if (cu_seqlens && B != 1) return 1;
+    if (!cu_seqlens && n_seqs != B) return 1;
+    bjob_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.g = g; J.h0 = h0; J.dout = dout; J.dht = dht;
+    J.cu = cu_seqlens; J.n_seqs = n_seqs; J.B = B; J.T = T;
+    J.Nk = Nk; J.Nv = Nv; J.dk = dk; J.dv = dv; J.scale = scale;
+    J.dq = dq; J.dk_ = dk_out; J.dv_ = dv_out; J.dbeta = dbeta; J.dg = dg; J.dh0 = dh0;
+    J.groups = groups; J.n_groups = n_groups;
+    if (n_threads <= 0) n_threads = dn_oracle_default_threads();
+    const int total = groups ? n_groups : n_seqs * Nk;
+    if (n_threads > total) n_threads = total > 0 ? total : 1;
+    pthread_mutex_init(&J.lock, NULL);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * n_threads);
+    int started = 0;
+    for (int i = 0; i < n_threads; ++i)
+        if (pthread_create(&th[i], NULL, bwd_worker, &J) == 0) ++started;
+    if (started == 0) bwd_worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    return J.failed ? 2 : 0;
 }

@@ -359,3 +359,67 @@ def test_qk_l2norm_chunk_equals_recurrent(chunk):
     o_r, h_r = _call(oracle.recurrent, inp, use_qk_l2norm_in_kernel=True)
     o_c, h_c = _call(oracle.chunked, inp, chunk=chunk, use_qk_l2norm_in_kernel=True)
     assert _rel(o_c, o_r) < 1e-12 and _rel(h_c, h_r) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Gradient of the forward ([WY] §3.4 lists dq, dk, dv, dbeta and dh0; the
+# gated form adds dg).  The pages print no backward formula, so the oracle's
+# reverse pass is pinned by central finite differences of the forward oracle
+# (the definition), element by element, on tiny inputs that cross the
+# reverse pass's 64-token checkpoints.
+# --------------------------------------------------------------------------
+def _loss(inp, do, dht, **over):
+    d = dict(inp, **over)
+    o, ht = oracle.recurrent(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                             d["cu_seqlens"], d["scale"], threads=1)
+    return float((o * do).sum() + (0.0 if dht is None else (ht * dht).sum()))
+
+
+@pytest.mark.parametrize("gate,h0,with_dht", [(True, True, True), (False, False, True),
+                                              (True, True, False)])
+def test_bwd_matches_finite_differences(gate, h0, with_dht):
+    inp = _small(B=1, Nk=2, Nv=4, dk=5, dv=3, gate=gate, h0=h0, lengths=[7, 0, 70, 2], seed=95)
+    inp = {key: (val.double().numpy().copy() if hasattr(val, "numpy") and key != "cu_seqlens"
+                 else val) for key, val in inp.items()}
+    if inp["g"] is None:
+        inp["g"] = np.zeros_like(inp["beta"])   # differentiate at g = 0
+    if inp["h0"] is None:
+        inp["h0"] = np.zeros((4, 4, 5, 3))
+    rng = np.random.default_rng(95)
+    o, ht = _call(oracle.recurrent, inp)
+    do = rng.standard_normal(o.shape)
+    dht = rng.standard_normal(ht.shape) if with_dht else None
+    gr = oracle.recurrent_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
+                              inp["cu_seqlens"], inp["scale"], do=do, dht=dht)
+    eps = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("g", "dg"),
+                        ("h0", "dh0")):
+        x = inp[name].copy()
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(inp, do, dht, **{name: x})
+            x[idx] = old - eps
+            lm = _loss(inp, do, dht, **{name: x})
+            x[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        an = gr[gname]
+        assert np.abs(fd - an).max() <= 1e-7 * max(np.abs(an).max(), 1.0), (name, gate, h0)
+
+
+def test_bwd_groups_subset_matches_full():
+    """Restricting the work to (sequence, key head) groups gives those groups'
+    gradients bit for bit and leaves the rest NaN."""
+    inp = _small(B=2, T=30, Nk=2, Nv=4, dk=6, dv=4, seed=96)
+    rng = np.random.default_rng(96)
+    o, ht = _call(oracle.recurrent, inp)
+    do, dht = rng.standard_normal(o.shape), rng.standard_normal(ht.shape)
+    args = (inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"], inp["cu_seqlens"],
+            inp["scale"])
+    full = oracle.recurrent_bwd(*args, do=do, dht=dht)
+    part = oracle.recurrent_bwd(*args, do=do, dht=dht, groups=[3])  # n = 1, hk = 1
+    assert np.array_equal(part["dq"][1, :, 1], full["dq"][1, :, 1])
+    assert np.array_equal(part["dv"][1, :, 2:], full["dv"][1, :, 2:])
+    assert np.array_equal(part["dh0"][1, 2:], full["dh0"][1, 2:])
+    assert np.isnan(part["dq"][0]).all() and np.isnan(part["dbeta"][1, :, :2]).all()
