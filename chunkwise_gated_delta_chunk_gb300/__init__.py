@@ -7,9 +7,11 @@ PyTorch supplies device memory and streams.
 
 Names follow the C ABI: :func:`dn_chunk_fwd`,
 :func:`dn_chunk_fwd_workspace_bytes`, :func:`dn_chunk_fwd_noalloc`,
-:func:`dn_recurrent_fwd`, :func:`dn_check`, :func:`dn_status_str`,
-:func:`dn_last_kernel`.  :func:`recurrent_fwd` is the same convenience for
-the token-serial entry point.  :func:`chunk_fwd` is a convenience that allocates
+:func:`dn_recurrent_fwd`, :func:`dn_chunk_bwd`,
+:func:`dn_chunk_bwd_workspace_bytes`, :func:`dn_check`,
+:func:`dn_status_str`, :func:`dn_last_kernel`.  :func:`recurrent_fwd` and
+:func:`chunk_bwd` are conveniences for the token-serial entry point and the
+backward.  :func:`chunk_fwd` is a convenience that allocates
 ``o``, ``ht`` and the workspace with torch and calls :func:`dn_chunk_fwd`.
 """
 from __future__ import annotations
@@ -35,7 +37,8 @@ DN_QK_L2NORM = 1
 
 # Every symbol the public header declares.
 ABI_SYMBOLS = ("dn_chunk_fwd", "dn_chunk_fwd_workspace_bytes", "dn_chunk_fwd_noalloc",
-               "dn_recurrent_fwd", "dn_check", "dn_status_str", "dn_last_kernel")
+               "dn_recurrent_fwd", "dn_chunk_bwd", "dn_chunk_bwd_workspace_bytes", "dn_check",
+               "dn_status_str", "dn_last_kernel")
 
 # Size of the library's fixed scratch array used by dn_chunk_fwd_noalloc.
 DN_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
@@ -74,6 +77,11 @@ def load(path: str | None = None):
         lib.dn_chunk_fwd_noalloc.restype = I
         lib.dn_recurrent_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, U, P, P, P]
         lib.dn_recurrent_fwd.restype = I
+        lib.dn_chunk_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, U, P, P, P, P,
+                                     P, P, P, P, P, Z, P]
+        lib.dn_chunk_bwd.restype = I
+        lib.dn_chunk_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+        lib.dn_chunk_bwd_workspace_bytes.restype = Z
         lib.dn_check.argtypes = [P]
         lib.dn_check.restype = I
         lib.dn_status_str.argtypes = [I]
@@ -237,3 +245,53 @@ def chunk_fwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None,
     if st != DN_OK:
         raise DnError(st)
     return o, (ht if output_final_state else None)
+
+
+def dn_chunk_bwd(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv, dk, dv, dtype, scale,
+                 flags, d_o, d_ht, d_q, d_k, d_v, d_beta, d_g, d_h0, workspace,
+                 workspace_bytes=None, stream=None) -> int:
+    """Call the backward C entry point as is; returns its status code."""
+    lib = load()
+    if workspace_bytes is None:
+        workspace_bytes = 0
+        if workspace is not None and not isinstance(workspace, int):
+            workspace_bytes = workspace.numel() * workspace.element_size()
+    return lib.dn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g), _ptr(h0),
+                            _ptr(cu_seqlens), int(n_seqs), int(B), int(T), int(Nk), int(Nv),
+                            int(dk), int(dv), int(dtype), float(scale), int(flags), _ptr(d_o),
+                            _ptr(d_ht), _ptr(d_q), _ptr(d_k), _ptr(d_v), _ptr(d_beta), _ptr(d_g),
+                            _ptr(d_h0), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def dn_chunk_bwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype) -> int:
+    return int(load().dn_chunk_bwd_workspace_bytes(int(n_seqs), int(B), int(T), int(Nk),
+                                                   int(Nv), int(dk), int(dv), int(dtype)))
+
+
+def chunk_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, do=None, dht=None,
+              stream=None, workspace=None):
+    """Gradients of :func:`chunk_fwd`'s loss ``sum(do * o) + sum(dht * ht)``.
+
+    Allocates the fp32 gradients and the workspace with torch and runs
+    :func:`dn_chunk_bwd`.  Returns a dict with ``dq``, ``dk``, ``dv``,
+    ``dbeta``, ``dg`` (None when g is None) and ``dh0`` (None when h0 is None).
+    """
+    import torch
+    B, T, Nk, dk = q.shape
+    Nv, dv = v.shape[2], v.shape[3]
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32),
+               dv=torch.empty(v.shape, **f32), dbeta=torch.empty(beta.shape, **f32),
+               dg=None if g is None else torch.empty(beta.shape, **f32),
+               dh0=None if h0 is None else torch.empty(N, Nv, dk, dv, **f32))
+    if workspace is None:
+        nbytes = dn_chunk_bwd_workspace_bytes(N, B, T, Nk, Nv, dk, dv, dtype_code(q.dtype))
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    st = dn_chunk_bwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
+                      dtype_code(q.dtype), 0.0 if scale is None else scale, 0, do, dht,
+                      out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dh0"],
+                      workspace, stream=stream)
+    if st != DN_OK:
+        raise DnError(st, "dn_chunk_bwd")
+    return out

@@ -162,6 +162,71 @@ DN_EXPORT dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v
     return DN_OK;
 }
 
+namespace {
+
+// Sizes the backward takes: dk <= 128 (its shared-memory tiles), dv any.
+bool bwd_dims_ok(int dk, int dv) { return dim_ok(dk) && dk <= 128 && dim_ok(dv); }
+
+size_t bwd_workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv) {
+    return (size_t)(tokens / dn::kChunk + n_seqs) * (size_t)Nv * (size_t)dk * (size_t)dv * 4u;
+}
+
+}  // namespace
+
+DN_EXPORT size_t dn_chunk_bwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
+                                              dn_dtype dtype) {
+    if (n_seqs <= 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0) return 0;
+    if (dtype != DN_BF16 && dtype != DN_F32) return 0;
+    if (!bwd_dims_ok(dk, dv)) return 0;
+    return bwd_workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv);
+}
+
+DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
+                                 const float *beta, const float *g, const float *h0,
+                                 const int64_t *cu_seqlens, int n_seqs,
+                                 int B, int T, int Nk, int Nv, int dk, int dv,
+                                 dn_dtype dtype, float scale, unsigned flags,
+                                 const void *d_o, const float *d_ht,
+                                 float *d_q, float *d_k, float *d_v, float *d_beta, float *d_g,
+                                 float *d_h0, void *workspace, size_t workspace_bytes_,
+                                 dn_stream_t stream) {
+    if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
+    if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
+        return DN_ERR_INVALID_ARG;
+    if (Nv % Nk != 0) return DN_ERR_INVALID_ARG;
+    if (cu_seqlens ? B != 1 : n_seqs != B) return DN_ERR_INVALID_ARG;
+    if (isnan(scale) || isinf(scale)) return DN_ERR_INVALID_ARG;
+    if (!flags_ok(flags)) return DN_ERR_INVALID_ARG;
+    const long long tokens = (long long)B * T;
+    if (tokens > 0 && (!q || !k || !v || !beta || !d_o || !d_q || !d_k || !d_v || !d_beta))
+        return DN_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, beta, g, h0, cu_seqlens, d_o, d_ht, d_q, d_k, d_v, d_beta, d_g, d_h0};
+    for (const void *ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
+    if (flags & DN_QK_L2NORM) return DN_ERR_UNSUPPORTED;
+    if (!bwd_dims_ok(dk, dv)) return DN_ERR_UNSUPPORTED;
+    if (n_seqs == 0) return DN_OK;
+    const size_t ws_need = bwd_workspace_bytes(tokens, n_seqs, Nv, dk, dv);
+    if (!workspace || !aligned16(workspace) || workspace_bytes_ < ws_need) return DN_ERR_INVALID_ARG;
+
+    dn::Params p{};
+    p.q = q; p.k = k; p.v = v; p.beta = beta; p.g = g; p.h0 = h0; p.cu = cu_seqlens;
+    p.N = n_seqs; p.B = B; p.T = T; p.Nk = Nk; p.Nv = Nv; p.dk = dk; p.dv = dv;
+    p.tokens = tokens;
+    p.scale = scale > 0.0f ? scale : 1.0f / sqrtf((float)dk);
+    p.nslots = tokens / dn::kChunk + n_seqs;
+    p.chunk = dn::kChunk;
+    p.flags = flags;
+    p.hs = static_cast<float *>(workspace);
+    p.dout = d_o; p.dht = d_ht;
+    p.dq = d_q; p.dkk = d_k; p.dvv = d_v; p.dbeta = d_beta; p.dg = d_g; p.dh0 = d_h0;
+    if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
+    const char *name = "";
+    if (dn::bwd_launch(p, dtype == DN_BF16, (cudaStream_t)stream, &name) != cudaSuccess) return DN_ERR_CUDA;
+    t_last_kernel = name;
+    return DN_OK;
+}
+
 DN_EXPORT dn_status dn_check(dn_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DN_ERR_CUDA;
     unsigned *dptr = nullptr;

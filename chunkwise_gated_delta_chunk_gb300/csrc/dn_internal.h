@@ -30,12 +30,25 @@ struct Params {
     long long nslots;          // floor(tokens / C) + N
     int chunk;                 // chunk length: 64 (both paths) or 16 / 32 (CUDA-core path)
     unsigned flags;            // kQkL2Norm
+    // backward (dn_chunk_bwd) only; null elsewhere
+    float *hs;                 // [Nv][nslots][dk][dv]: state before each 64-token chunk (slot t0/64 + n)
+    const void *dout;          // [tokens, Nv, dv] gradient of o (dtype of q)
+    const float *dht;          // [N, Nv, dk, dv] gradient of ht or null
+    float *dq, *dkk, *dvv;     // [tokens, Nk, dk], [tokens, Nk, dk], [tokens, Nv, dv]
+    float *dbeta, *dg;         // [tokens, Nv]; dg may be null
+    float *dh0;                // [N, Nv, dk, dv] or null
 };
 
 // CUDA-core kernel: fp32 arithmetic for every product; any supported shape.
 // `bf16` selects bf16 q/k/v/o, else fp32.  Returns the launch error.
 cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
 size_t simt_smem_bytes(int dk, bool bf16);
+
+// Backward: zero the accumulated gradients, rerun the CUDA-core forward
+// saving each chunk's start state in p.hs (p.o and p.ht null), then walk the
+// chunks in reverse.  dk <= 128.
+cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
+size_t bwd_smem_bytes(int dk, bool bf16);
 
 // Token-serial kernel (decode / short sequences): any supported shape.
 cudaError_t recurrent_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);

@@ -160,6 +160,15 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         const int L = (eos - t0) < CH ? (int)(eos - t0) : CH;
         __syncthreads();  // previous chunk fully consumed
 
+        // backward's forward pass: keep the state this chunk starts from
+        if (p.hs) {
+            float *dst = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
+            for (int idx = tid; idx < dk * BV; idx += NT) {
+                const int d = idx / BV, c = idx - d * BV;
+                if (c < bvw) dst[(size_t)d * dv + c] = sS[idx];
+            }
+        }
+
         // ---- load the chunk --------------------------------------------
         load_rows<Tin>(sK, k, t0, L, Nk, hk, dk, tid);
         load_rows<Tin>(sQ, q, t0, L, Nk, hk, dk, tid);
@@ -308,7 +317,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
-                if (i < L && c < bvw) {
+                if (i < L && c < bvw && o) {
                     const float out = fmaf(p.scale * sEG[i] * sRQ[i], qs[r], acc[r]);
                     put(o + ((t0 + i) * Nv + h) * (long long)dv + v0 + c, out);
                 }

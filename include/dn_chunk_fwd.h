@@ -199,6 +199,55 @@ dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                void *o, float *ht, dn_stream_t stream);
 
 /*
+ * dn_chunk_bwd -- gradient of dn_chunk_fwd ([WY] §3.4: the backward
+ * recomputes each chunk's WY quantities and walks the chunks in reverse; it
+ * gives dq, dk, dv, dbeta and dh0, and the gated form dg).
+ *
+ * For the loss l = sum(d_o . o) + sum(d_ht . ht) of the forward with the same
+ * inputs, writes the gradients of l:
+ *   d_q, d_k   [B, T, Nk, dk]  float32   (summed over the Nv/Nk value heads
+ *                                          that read each key head)
+ *   d_v        [B, T, Nv, dv]  float32
+ *   d_beta     [B, T, Nv]      float32
+ *   d_g        [B, T, Nv]      float32 or NULL (not computed); with g NULL it
+ *                                          is the gradient at g = 0
+ *   d_h0       [N, Nv, dk, dv] float32 or NULL; with h0 NULL it is the
+ *                                          gradient at h0 = 0
+ * from
+ *   d_o        [B, T, Nv, dv]  dtype     gradient of o (required)
+ *   d_ht       [N, Nv, dk, dv] float32   gradient of ht; NULL means zero.
+ * The other arguments are those of dn_chunk_fwd (the chunk length is 64).
+ * All arithmetic is fp32 on CUDA cores.  dk must be at most 128
+ * (DN_ERR_UNSUPPORTED otherwise); flags must be 0 (DN_QK_L2NORM is
+ * DN_ERR_UNSUPPORTED).  Rows of tokens outside every sequence are 0 in d_q,
+ * d_k, d_beta and d_g and not written in d_v.  The sums over value tiles and
+ * value heads use fp32 atomic adds, so the last bits of d_q, d_k, d_beta
+ * and d_g may differ from run to run.
+ *
+ * workspace: at least dn_chunk_bwd_workspace_bytes() bytes, 16-byte
+ * aligned, owned by the caller (it holds the state at the start of every
+ * 64-token chunk).  Launches a zero fill, the CUDA-core forward (saving those
+ * states) and the backward kernel.  Errors as for dn_chunk_fwd.
+ */
+dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
+                       const float *beta, const float *g, const float *h0,
+                       const int64_t *cu_seqlens, int n_seqs,
+                       int B, int T, int Nk, int Nv, int dk, int dv,
+                       dn_dtype dtype, float scale, unsigned flags,
+                       const void *d_o, const float *d_ht,
+                       float *d_q, float *d_k, float *d_v, float *d_beta, float *d_g,
+                       float *d_h0, void *workspace, size_t workspace_bytes,
+                       dn_stream_t stream);
+
+/*
+ * dn_chunk_bwd_workspace_bytes -- bytes of workspace dn_chunk_bwd needs:
+ * (floor(B*T / 64) + n_seqs) * Nv * dk * dv * 4 (one fp32 state per chunk and
+ * value head).  0 for sizes dn_chunk_bwd would reject.  Host-only.
+ */
+size_t dn_chunk_bwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
+                                    dn_dtype dtype);
+
+/*
  * dn_check -- wait for `stream`, then read and clear the device status word
  * of the current device.  Returns DN_ERR_TIMEOUT or DN_ERR_DEVICE_ARG if a
  * kernel of this library recorded one since the last check, DN_ERR_CUDA if
@@ -210,8 +259,9 @@ dn_status dn_check(dn_stream_t stream);
 const char *dn_status_str(dn_status status);
 
 /*
- * dn_last_kernel -- name of the kernel the last successful dn_chunk_fwd call
- * on this host thread launched ("" before any call).  Static storage.
+ * dn_last_kernel -- name of the kernel(s) the last successful call of a
+ * compute entry point on this host thread launched ("" before any call).
+ * Static storage.
  */
 const char *dn_last_kernel(void);
 

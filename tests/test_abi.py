@@ -156,3 +156,42 @@ def test_product_path_has_no_fallback(tmp_path):
     """The binding refuses to run without the CUDA library (no CPU path)."""
     with pytest.raises(RuntimeError, match="no fallback"):
         dn.load(str(tmp_path / "missing.so"))
+
+
+def bwd_call(clib, **over):
+    args = dict(q=A, k=A, v=A, beta=A, g=None, h0=None, cu=None, n=2, B=2, T=64, Nk=2, Nv=4,
+                dk=64, dv=64, dtype=dn.DN_BF16, scale=0.0, flags=0, do=A, dht=None, dq=A, dkk=A,
+                dvv=A, dbeta=A, dg=None, dh0=None, ws=A, wsb=1 << 30)
+    args.update(over)
+    return clib.dn_chunk_bwd(args["q"], args["k"], args["v"], args["beta"], args["g"], args["h0"],
+                             args["cu"], args["n"], args["B"], args["T"], args["Nk"], args["Nv"],
+                             args["dk"], args["dv"], args["dtype"], args["scale"], args["flags"],
+                             args["do"], args["dht"], args["dq"], args["dkk"], args["dvv"],
+                             args["dbeta"], args["dg"], args["dh0"], args["ws"], args["wsb"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(Nv=3), dn.DN_ERR_INVALID_ARG),
+    (dict(n=3), dn.DN_ERR_INVALID_ARG),
+    (dict(do=None), dn.DN_ERR_INVALID_ARG),              # gradient of o is required
+    (dict(dq=None), dn.DN_ERR_INVALID_ARG),
+    (dict(dbeta=A + 4), dn.DN_ERR_INVALID_ARG),          # misaligned
+    (dict(flags=2), dn.DN_ERR_INVALID_ARG),
+    (dict(ws=None), dn.DN_ERR_INVALID_ARG),              # the workspace is required
+    (dict(wsb=1024), dn.DN_ERR_INVALID_ARG),             # and must be large enough
+    (dict(flags=dn.DN_QK_L2NORM), dn.DN_ERR_UNSUPPORTED),
+    (dict(dk=256), dn.DN_ERR_UNSUPPORTED),
+    (dict(dv=48), dn.DN_ERR_UNSUPPORTED),
+    (dict(n=0, B=0), dn.DN_OK),                           # nothing to do, nothing launched
+])
+def test_bwd_host_validation(clib, over, code):
+    """dn_chunk_bwd rejects bad arguments on the host before any CUDA call."""
+    assert bwd_call(clib, **over) == code
+
+
+def test_bwd_workspace_bytes(clib):
+    """One fp32 dk x dv state per (floor(tokens/64) + N) x Nv; 0 for rejected sizes."""
+    ws = clib.dn_chunk_bwd_workspace_bytes
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16) == (4 * 2048 // 64 + 4) * 16 * 128 * 128 * 4
+    assert ws(3, 1, 300, 2, 8, 64, 32, dn.DN_F32) == (300 // 64 + 3) * 8 * 64 * 32 * 4
+    assert ws(1, 1, 64, 1, 1, 256, 64, dn.DN_BF16) == 0
