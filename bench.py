@@ -231,6 +231,11 @@ def reference_arm(args, inp, wl_name, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def launches_per_call(kernel: str) -> int:
+    """Kernels one call launches: dn_last_kernel() lists them joined by '+'."""
+    return len([k for k in kernel.split("+") if k])
+
+
 def max_over_ranks(x: float, dist=None, device="cpu") -> float:
     """The largest value of `x` over all ranks (the slowest rank's time)."""
     if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
@@ -254,6 +259,176 @@ def config_of(wl_name, inp, l2, chunk=64):
 
 
 # --------------------------------------------------------------------------
+# Backward (dn_chunk_bwd): same timing rules, its own algorithmic work.
+# --------------------------------------------------------------------------
+BWD_METRIC = "bwd tokens/s & % of roofline, gated delta rule H=16 d=128 T=2048 (1 GB300)"
+
+
+def algorithmic_bwd(inp: dict) -> dict:
+    """Work of one backward: the forward it reruns plus the products of the
+    chunk-form gradient (per chunk and value head: eight C x dk x dv products,
+    five C x C x dv, four C x C x dk; per key head K K^T and Q K^T again).
+    Bytes: q, k, v, dO, beta, g in; dq, dk, dv (fp32), dbeta, dg out; h0,
+    dht in and dh0 out."""
+    B, T, Nk, dk = inp["q"].shape
+    Nv, dv = inp["v"].shape[2], inp["v"].shape[3]
+    C = 64
+    tok = B * T
+    e = inp["q"].element_size()
+    has_g = inp["g"] is not None
+    has_h0 = inp["h0"] is not None
+    N = inp["N"]
+    fwd = algorithmic(inp)
+    flops = fwd["flops"] + tok * (Nv * (16 * dk * dv + 10 * C * dv + 8 * C * dk) + Nk * 4 * C * dk)
+    bytes_ = (tok * (2 * Nk * dk * e + 2 * Nv * dv * e + Nv * 4 * (1 + has_g)
+                     + 4 * (2 * Nk * dk + Nv * dv) + Nv * 4 * (1 + has_g))
+              + N * Nv * dk * dv * 4 * (2 * has_h0 + 1))
+    return dict(flops=flops, bytes=bytes_, tokens=tok)
+
+
+def fp32_alu_peak_tflops(sm_mhz: float) -> float:
+    """fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flop x clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
+    d = workloads.to_device(inp, dev)
+    B, T, Nk, dk = d["q"].shape
+    Nv, dv = d["v"].shape[2], d["v"].shape[3]
+    N = inp["N"]
+    gen = torch.Generator().manual_seed(1234)
+    inp = dict(inp)
+    inp["do"] = torch.randn(inp["v"].shape, generator=gen).to(inp["v"].dtype)
+    inp["dht"] = torch.randn(N, Nv, dk, dv, generator=gen)
+    d["do"], d["dht"] = inp["do"].to(dev), inp["dht"].to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = dict(dq=torch.empty(d["q"].shape, **f32), dk=torch.empty(d["k"].shape, **f32),
+                 dv=torch.empty(d["v"].shape, **f32), dbeta=torch.empty(d["beta"].shape, **f32),
+                 dg=None if d["g"] is None else torch.empty(d["beta"].shape, **f32),
+                 dh0=None if d["h0"] is None else torch.empty(N, Nv, dk, dv, **f32))
+    dt = dn.dtype_code(d["q"].dtype)
+    ws = torch.empty(max(dn.dn_chunk_bwd_workspace_bytes(N, B, T, Nk, Nv, dk, dv, dt), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(src=d):
+        st = dn.dn_chunk_bwd(src["q"], src["k"], src["v"], src["beta"], src["g"], src["h0"],
+                             src["cu_seqlens"], N, B, T, Nk, Nv, dk, dv, dt, inp["scale"], 0,
+                             src["do"], src["dht"], grads["dq"], grads["dk"], grads["dv"],
+                             grads["dbeta"], grads["dg"], grads["dh0"], ws, stream=stream)
+        if st != dn.DN_OK:
+            raise dn.DnError(st, "dn_chunk_bwd")
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    if dn.dn_check(stream) != dn.DN_OK:
+        raise RuntimeError("warm-up reported a device error")
+    kernel = dn.dn_last_kernel()
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(smi_gpu_id(dev, int(os.environ.get("LOCAL_RANK", "0")))) as clk:
+        for i in range(K):
+            flush.zero_()
+            ev0[i].record(stream)
+            launch()
+            ev1[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1)) / K
+    if dn.dn_check(stream) != dn.DN_OK:
+        raise RuntimeError("timed region reported a device error")
+    ms_max = max_over_ranks(ms, dist, dev)
+
+    # end to end: inputs and output gradient from pinned host memory, every
+    # gradient back to the host
+    host = {key: inp[key].contiguous().pin_memory() for key in
+            ("q", "k", "v", "beta", "g", "h0", "cu_seqlens", "do", "dht") if inp[key] is not None}
+    dbuf = {key: torch.empty_like(val, device=dev) for key, val in host.items()}
+    ghost = {key: torch.empty(val.shape, dtype=val.dtype).pin_memory()
+             for key, val in grads.items() if val is not None}
+    h2d = sum(val.numel() * val.element_size() for val in host.values())
+    d2h = sum(val.numel() * val.element_size() for val in ghost.values())
+    src = dict(d)
+
+    def e2e_step():
+        for key, val in host.items():
+            dbuf[key].copy_(val, non_blocking=True)
+        src.update({key: dbuf[key] for key in dbuf})
+        launch(src)
+        for key, val in ghost.items():
+            val.copy_(grads[key], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    E = max(1, min(args.e2e_steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, dist, dev)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    alg = algorithmic_bwd(inp)
+    clocks = clk.summary()
+    sec = ms / 1e3
+    mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
+    peak = fp32_alu_peak_tflops(mhz)
+    achieved = alg["flops"] / sec / 1e12
+    peaks, peak_src = load_peaks()
+    roof = dict(bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
+                traffic=measured_traffic(kernel, wl_name + ":bwd"),
+                peak_source="derived: 152 SMs x 128 fp32 lanes x 2 flop x %.0f MHz" % mhz,
+                roofline_time_us=1e6 * max(alg["flops"] / (peak * 1e12),
+                                           alg["bytes"] / (peaks["hbm_gbs"] * 1e9)),
+                algorithmic_bytes=alg["bytes"], algorithmic_flops=alg["flops"],
+                hbm_gbs=alg["bytes"] / sec / 1e9, kernel=kernel)
+    line = dict(metric=BWD_METRIC, value=weak_scaling_value(alg["tokens"], world, ms_max), unit=UNIT,
+                n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
+                higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f32 (inputs %s)" % ("bf16" if d["q"].dtype == torch.bfloat16 else "f32"),
+                data="synthetic",
+                config=dict(config_of(wl_name, inp, l2="flushed before every timed step "
+                                      "(256 MiB write, outside the step's events)"), mode="bwd"),
+                parallelism="dp%d (independent sequences per GPU, no collective)" % world,
+                gpu_launches=K * launches_per_call(kernel), roofline=roof,
+                e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,
+                         h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, ms_per_step=e2e_ms),
+                clocks=clocks)
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        cores = oracle.default_threads()
+        groups = list(range(min(N * Nk, cores)))
+        t0 = time.perf_counter()
+        oracle.recurrent_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
+                             inp["cu_seqlens"], inp["scale"], do=inp["do"], dht=inp["dht"],
+                             groups=groups)
+        secs = time.perf_counter() - t0
+        toks = workloads.tokens(inp) * len(groups) / (N * Nk)
+        line["cpu_baseline"] = dict(
+            value=toks / secs, unit=UNIT, cores=cores, kind="oracle",
+            sample="%d of %d (sequence, key head) groups of the workload, one pass (%.1f s)" % (
+                len(groups), N * Nk, secs))
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -265,8 +440,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--chunk", type=int, default=64, choices=[16, 32, 64],
                     help="chunk length C (16 and 32 run the CUDA-core kernel)")
-    ap.add_argument("--mode", default="chunk", choices=["chunk", "recurrent"],
-                    help="dn_chunk_fwd (default) or the token-serial dn_recurrent_fwd")
+    ap.add_argument("--mode", default="chunk", choices=["chunk", "recurrent", "bwd"],
+                    help="dn_chunk_fwd (default), the token-serial dn_recurrent_fwd, or the "
+                         "backward dn_chunk_bwd")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -294,6 +470,9 @@ def main():
     dn.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.mode == "bwd":
+        bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist)
+        return
     d = workloads.to_device(inp, dev)
     B, T, Nk, dk = d["q"].shape
     Nv, dv = d["v"].shape[2], d["v"].shape[3]
@@ -421,7 +600,7 @@ def main():
                 config=dict(config_of(wl_name, inp, chunk=args.chunk, l2="flushed before every timed step "
                                       "(256 MiB write, outside the step's events)"), mode=args.mode),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
-                gpu_launches=K, roofline=roof,
+                gpu_launches=K * launches_per_call(kernel), roofline=roof,
                 e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
                          ms_per_step=e2e_ms),

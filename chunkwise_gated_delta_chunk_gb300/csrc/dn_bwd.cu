@@ -41,23 +41,25 @@
 #include <math.h>
 
 #include "dn_internal.h"
+#include "dn_simt_common.cuh"
 
 namespace dn {
 namespace {
 
-constexpr int C = kChunk;  // 64
-constexpr int BV = 32;     // value columns per CTA
-constexpr int NT = 256;    // 8 warps
-constexpr int LDC = C + 1; // row stride of the C x C matrices
-constexpr int LDV = BV + 1;  // row stride of the C x BV and dk x BV tiles (conflict-free row-per-lane reads)
+using simt::kq_ld;
+using simt::ld4;
+using simt::to_f;
+using simt::align16;
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+constexpr int C = kChunk;    // 64
+constexpr int BV = 32;       // value columns per CTA
+constexpr int NT = 256;      // 8 warps
+constexpr int LDC = C + 1;   // row stride of the C x C matrices
+constexpr int LDV = BV + 1;  // row stride of the C x BV tiles (conflict-free row-per-lane reads)
 
-template <typename Tin>
-__host__ __device__ constexpr int kq_ld(int dk) { return sizeof(Tin) == 2 ? dk + 2 : dk + 1; }
-
-__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+// Row stride (floats) of the transposed state tiles S^T, dS^T ([BV][dk]):
+// 16-byte rows, consecutive rows 4 banks apart.
+__host__ __device__ inline int st_ld(int dk) { return dk + 4; }
 
 struct Layout {
     size_t k, q, s, ds, m0, m1, m2, u, dO, ks, vn, dv, kds, sc, end;
@@ -73,8 +75,8 @@ __host__ __device__ inline Layout layout(int dk) {
     const size_t kq = align16(size_t(C) * kq_ld<Tin>(dk) * sizeof(Tin));
     L.k = off; off += kq;
     L.q = off; off += kq;
-    L.s = off; off += align16(size_t(dk) * LDV * 4);
-    L.ds = off; off += align16(size_t(dk) * LDV * 4);
+    L.s = off; off += align16(size_t(BV) * st_ld(dk) * 4);
+    L.ds = off; off += align16(size_t(BV) * st_ld(dk) * 4);
     L.m0 = off; off += align16(size_t(C) * LDC * 4);
     L.m1 = off; off += align16(size_t(C) * LDC * 4);
     L.m2 = off; off += align16(size_t(C) * LDC * 4);
@@ -87,22 +89,6 @@ __host__ __device__ inline Layout layout(int dk) {
     L.sc = off; off += size_t(R_COUNT) * C * 4 + 64;  // + G_L, block partial sums
     L.end = off;
     return L;
-}
-
-template <typename Tin>
-__device__ __forceinline__ void load_rows(Tin *dst, const Tin *src, long long t0, int L, int H, int hh,
-                                          int d, int tid) {
-    constexpr int VEC = 16 / sizeof(Tin);
-    const int ld = kq_ld<Tin>(d);
-    const int per_row = d / VEC;
-    for (int idx = tid; idx < L * per_row; idx += NT) {
-        const int i = idx / per_row, cv = idx - i * per_row;
-        const uint4 w = *reinterpret_cast<const uint4 *>(src + ((t0 + i) * H + hh) * (long long)d + cv * VEC);
-        const Tin *e = reinterpret_cast<const Tin *>(&w);
-#pragma unroll
-        for (int x = 0; x < VEC; ++x) dst[i * ld + cv * VEC + x] = e[x];
-    }
-    for (int idx = L * ld + tid; idx < C * ld; idx += NT) dst[idx] = Tin(0.0f);
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -123,13 +109,14 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     const int v0 = vt * BV;
     const int bvw = min(BV, dv - v0);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = lane;  // value column of the C x BV tiles
+    const int c = lane;  // value column of the C x BV tiles in the row-per-warp loops
+    const int SLD = st_ld(dk);
 
     const Layout lay = layout<Tin>(dk);
     Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);
     Tin *sQ = reinterpret_cast<Tin *>(smem + lay.q);
-    float *sS = reinterpret_cast<float *>(smem + lay.s);     // [dk][LDV] state the chunk starts from
-    float *sdS = reinterpret_cast<float *>(smem + lay.ds);   // [dk][LDV] gradient of the state it hands on
+    float *sSt = reinterpret_cast<float *>(smem + lay.s);    // [BV][SLD]: S^T, S = state the chunk starts from
+    float *sdSt = reinterpret_cast<float *>(smem + lay.ds);  // [BV][SLD]: dS'^T, gradient of the state it hands on
     float *sM0 = reinterpret_cast<float *>(smem + lay.m0);   // -(K K^T . D), then M
     float *sM1 = reinterpret_cast<float *>(smem + lay.m1);   // T, then scale D . dP
     float *sM2 = reinterpret_cast<float *>(smem + lay.m2);   // P, then E
@@ -169,7 +156,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     const size_t sbase = ((size_t)n * Nv + h) * dk * dv;
     for (int idx = tid; idx < dk * BV; idx += NT) {
         const int d = idx / BV, cc = idx - d * BV;
-        sdS[d * LDV + cc] = (p.dht && cc < bvw) ? p.dht[sbase + (size_t)d * dv + v0 + cc] : 0.0f;
+        sdSt[cc * SLD + d] = (p.dht && cc < bvw) ? p.dht[sbase + (size_t)d * dv + v0 + cc] : 0.0f;
     }
 
     const long long nch = (eos - bos + C - 1) / C;
@@ -179,8 +166,8 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         __syncthreads();  // the previous (later) chunk is done with every buffer
 
         // ---- load --------------------------------------------------------
-        load_rows<Tin>(sK, k, t0, L, Nk, hk, dk, tid);
-        load_rows<Tin>(sQ, q, t0, L, Nk, hk, dk, tid);
+        simt::load_rows<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
+        simt::load_rows<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
         for (int idx = tid; idx < C * BV; idx += NT) {
             const int i = idx / BV, cc = idx - i * BV;
             const bool in = i < L && cc < bvw;
@@ -192,7 +179,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             const float *hs = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
             for (int idx = tid; idx < dk * BV; idx += NT) {
                 const int d = idx / BV, cc = idx - d * BV;
-                sS[d * LDV + cc] = cc < bvw ? hs[(size_t)d * dv + cc] : 0.0f;
+                sSt[cc * SLD + d] = cc < bvw ? hs[(size_t)d * dv + cc] : 0.0f;
             }
         }
         if (tid < C) {
@@ -225,8 +212,8 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         {
             float part = 0.0f;
             for (int idx = tid; idx < dk * BV; idx += NT) {
-                const int d = idx / BV, cc = idx - d * BV;
-                part = fmaf(sS[d * LDV + cc], sdS[d * LDV + cc], part);
+                const int cc = idx / dk, d = idx - cc * dk;
+                part = fmaf(sSt[cc * SLD + d], sdSt[cc * SLD + d], part);
             }
             part = warp_sum(part);
             if (lane == 0) sRed[warp] = part;
@@ -234,24 +221,16 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         __syncthreads();
 
         // ---- -(K K^T . D) (strictly lower) and P (lower) ------------------
-        for (int idx = tid; idx < C * C; idx += NT) {
-            const int i = idx >> 6, j = idx & 63;
+        simt::kq_products<NT>(sK, sQ, ldkq, dk, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
             if (i < L && j <= i) {
-                const Tin *ki = sK + i * ldkq, *kj = sK + j * ldkq, *qi = sQ + i * ldkq;
-                float skk = 0.0f, sqk = 0.0f;
-                for (int d = 0; d < dk; ++d) {
-                    const float kjd = to_f(kj[d]);
-                    skk = fmaf(to_f(ki[d]), kjd, skk);
-                    sqk = fmaf(to_f(qi[d]), kjd, sqk);
-                }
-                const float dec = expf(sG[i] - sG[j]);
-                if (j < i) a = -skk * dec;
-                pv = p.scale * sqk * dec;
+                const float D = expf(sG[i] - sG[j]);
+                if (j < i) a = -kk * D;
+                pv = p.scale * qk * D;
             }
             sM0[i * LDC + j] = a;
             sM2[i * LDC + j] = pv;
-        }
+        });
         __syncthreads();
 
         // ---- T = (I - A)^-1, A_im = beta_i sM0_im; column j by 4 lanes ----
@@ -270,29 +249,50 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             }
         }
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
+        // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         {
-            float ks[8], qs[8], kd[8];
+            const int i0 = 2 * (tid >> 3), cg = tid & 7;
+            float ks[2][4], qs[2][4], kd[2][4];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) { ks[r] = 0.0f; qs[r] = 0.0f; kd[r] = 0.0f; }
-            for (int d = 0; d < dk; ++d) {
-                const float s = sS[d * LDV + c], ds = sdS[d * LDV + c];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int i = warp + 8 * r;
-                    const float kv = to_f(sK[i * ldkq + d]);
-                    ks[r] = fmaf(kv, s, ks[r]);
-                    kd[r] = fmaf(kv, ds, kd[r]);
-                    qs[r] = fmaf(to_f(sQ[i * ldkq + d]), s, qs[r]);
+                for (int x = 0; x < 4; ++x) ks[r][x] = qs[r][x] = kd[r][x] = 0.0f;
+            for (int d = 0; d < dk; d += 4) {
+                float4 kr[2], qr[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    kr[r] = ld4(sK + (i0 + r) * ldkq + d);
+                    qr[r] = ld4(sQ + (i0 + r) * ldkq + d);
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float4 s4 = *reinterpret_cast<const float4 *>(sSt + (cg + 8 * x) * SLD + d);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sdSt + (cg + 8 * x) * SLD + d);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        ks[r][x] = fmaf(kr[r].x, s4.x, fmaf(kr[r].y, s4.y, fmaf(kr[r].z, s4.z, fmaf(kr[r].w, s4.w, ks[r][x]))));
+                        qs[r][x] = fmaf(qr[r].x, s4.x, fmaf(qr[r].y, s4.y, fmaf(qr[r].z, s4.z, fmaf(qr[r].w, s4.w, qs[r][x]))));
+                        kd[r][x] = fmaf(kr[r].x, d4.x, fmaf(kr[r].y, d4.y, fmaf(kr[r].z, d4.z, fmaf(kr[r].w, d4.w, kd[r][x]))));
+                    }
                 }
             }
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = warp + 8 * r;
-                sKS[i * LDV + c] = ks[r];
-                sKdS[i * LDV + c] = kd[r];
-                sU[i * LDV + c] = i < L ? sU[i * LDV + c] - sEG[i] * ks[r] : 0.0f;
-                const float qd = warp_sum(qs[r] * sdO[i * LDV + c]);
-                if (lane == 0) sQSdO[i] = qd;
+            for (int r = 0; r < 2; ++r) {
+                const int i = i0 + r;
+                float qd = 0.0f;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int cc = cg + 8 * x;
+                    sKS[i * LDV + cc] = ks[r][x];
+                    sKdS[i * LDV + cc] = kd[r][x];
+                    sU[i * LDV + cc] = i < L ? sU[i * LDV + cc] - sEG[i] * ks[r][x] : 0.0f;
+                    qd = fmaf(qs[r][x], sdO[i * LDV + cc], qd);
+                }
+                // the eight threads of a row pair are lanes 8 m .. 8 m + 7
+                qd += __shfl_xor_sync(0xffffffffu, qd, 1);
+                qd += __shfl_xor_sync(0xffffffffu, qd, 2);
+                qd += __shfl_xor_sync(0xffffffffu, qd, 4);
+                if (cg == 0) sQSdO[i] = qd;
             }
         }
         __syncthreads();
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        // ---- warp 0: dbeta, dG and dg; warps 1-7: dq, dk ------------------
+        // ---- warp 0: dbeta, dG and dg ------------------------------------
         if (warp == 0) {
             float dG[2], db[2];
             float esum = 0.0f;
@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) red += sRed[w];
             const float extra = esum + expf(sGL[0]) * red;
-            if (lane == ((L - 1) & 31)) dG[(L - 1) >> 5] += extra;
+            if (lane == ((L - 1) & 31)) {
+                if ((L - 1) >> 5) dG[1] += extra; else dG[0] += extra;
+            }
             // dg_t = sum_{i >= t} dG_i: suffix sums over the 64 rows
             float a = dG[0], b = dG[1];
 #pragma unroll
@@ -434,48 +436,121 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                     if (p.dg) atomicAdd(p.dg + (t0 + i) * Nv + h, hj ? b : a);
                 }
             }
-        } else {
-            // rows i = (warp - 1) + 7 m, columns d = lane + 32 x
-            for (int i = warp - 1; i < L; i += 7) {
-                const float eg = sEG[i], dec = sDec[i], bi = sBeta[i];
-                for (int d = lane; d < dk; d += 32) {
-                    float sdo = 0.0f, sdr = 0.0f, dsv = 0.0f;
-#pragma unroll 8
+        }
+        // ---- dq, dk: 4-row x 8-column register tiles ----------------------
+        //   dq_i = scale e^{G_i} S dO_i + sum_j WP_ij k_j
+        //   dk_i = dec_i dS' Vn_i - beta_i e^{G_i} S dR_i
+        //          + sum_j (M_ij + M_ji) k_j + sum_j WP_ji q_j
+        {
+            const int ndg = dk >> 3;
+            for (int tile = tid; tile < 16 * ndg; tile += NT) {
+                const int i0 = 4 * (tile / ndg), d0 = 8 * (tile % ndg);
+                if (i0 >= L) continue;
+                float gq[4][8], gk[4][8];
+                {
+                    float a1[4][8], a2[4][8], a3[4][8];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) a1[r][x] = a2[r][x] = a3[r][x] = 0.0f;
                     for (int cc = 0; cc < BV; ++cc) {
-                        const float s = sS[d * LDV + cc];
-                        sdo = fmaf(s, sdO[i * LDV + cc], sdo);
-                        sdr = fmaf(s, sdV[i * LDV + cc], sdr);
-                        dsv = fmaf(sdS[d * LDV + cc], sVn[i * LDV + cc], dsv);
+                        const float4 s0 = *reinterpret_cast<const float4 *>(sSt + cc * SLD + d0);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(sSt + cc * SLD + d0 + 4);
+                        const float4 t0v = *reinterpret_cast<const float4 *>(sdSt + cc * SLD + d0);
+                        const float4 t1v = *reinterpret_cast<const float4 *>(sdSt + cc * SLD + d0 + 4);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const float o = sdO[(i0 + r) * LDV + cc], vn = sVn[(i0 + r) * LDV + cc],
+                                        dr = sdV[(i0 + r) * LDV + cc];
+                            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                            const float tv[8] = {t0v.x, t0v.y, t0v.z, t0v.w, t1v.x, t1v.y, t1v.z, t1v.w};
+#pragma unroll
+                            for (int x = 0; x < 8; ++x) {
+                                a1[r][x] = fmaf(o, sv[x], a1[r][x]);
+                                a2[r][x] = fmaf(vn, tv[x], a2[r][x]);
+                                a3[r][x] = fmaf(dr, sv[x], a3[r][x]);
+                            }
+                        }
                     }
-                    float gq = p.scale * eg * sdo;
-                    float gk = dec * dsv - bi * eg * sdr;
-                    for (int j = 0; j <= i; ++j) {
-                        const float kj = to_f(sK[j * ldkq + d]);
-                        gq = fmaf(sM1[i * LDC + j], kj, gq);   // scale D_ij dP_ij k_j
-                        gk = fmaf(sM0[i * LDC + j], kj, gk);   // M_ij k_j (j < i; M_ii = 0)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int i = i0 + r;
+                        const float fq = p.scale * sEG[i], fd = sDec[i], fr = sBeta[i] * sEG[i];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            gq[r][x] = fq * a1[r][x];
+                            gk[r][x] = fd * a2[r][x] - fr * a3[r][x];
+                        }
                     }
-                    for (int j = i; j < L; ++j) {
-                        gk = fmaf(sM0[j * LDC + i], to_f(sK[j * ldkq + d]), gk);  // M_ji k_j
-                        gk = fmaf(sM1[j * LDC + i], to_f(sQ[j * ldkq + d]), gk);  // scale D_ji dP_ji q_j
+                }
+                for (int j = 0; j < L; ++j) {
+                    const float4 k0v = ld4(sK + j * ldkq + d0), k1v = ld4(sK + j * ldkq + d0 + 4);
+                    const float4 q0v = ld4(sQ + j * ldkq + d0), q1v = ld4(sQ + j * ldkq + d0 + 4);
+                    const float kv[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
+                    const float qv[8] = {q0v.x, q0v.y, q0v.z, q0v.w, q1v.x, q1v.y, q1v.z, q1v.w};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int i = i0 + r;
+                        const float wq = sM1[i * LDC + j];                       // WP_ij (0 for j > i)
+                        const float mk = sM0[i * LDC + j] + sM0[j * LDC + i];    // M_ij + M_ji
+                        const float wt = sM1[j * LDC + i];                       // WP_ji (0 for j < i)
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            gq[r][x] = fmaf(wq, kv[x], gq[r][x]);
+                            gk[r][x] = fmaf(mk, kv[x], fmaf(wt, qv[x], gk[r][x]));
+                        }
                     }
-                    atomicAdd(p.dq + ((t0 + i) * Nk + hk) * (long long)dk + d, gq);
-                    atomicAdd(p.dkk + ((t0 + i) * Nk + hk) * (long long)dk + d, gk);
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r;
+                    if (i >= L) continue;
+                    float *pq = p.dq + ((t0 + i) * Nk + hk) * (long long)dk + d0;
+                    float *pk = p.dkk + ((t0 + i) * Nk + hk) * (long long)dk + d0;
+                    atomicAdd(reinterpret_cast<float4 *>(pq), make_float4(gq[r][0], gq[r][1], gq[r][2], gq[r][3]));
+                    atomicAdd(reinterpret_cast<float4 *>(pq + 4), make_float4(gq[r][4], gq[r][5], gq[r][6], gq[r][7]));
+                    atomicAdd(reinterpret_cast<float4 *>(pk), make_float4(gk[r][0], gk[r][1], gk[r][2], gk[r][3]));
+                    atomicAdd(reinterpret_cast<float4 *>(pk + 4), make_float4(gk[r][4], gk[r][5], gk[r][6], gk[r][7]));
                 }
             }
         }
         __syncthreads();
 
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
+        // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
         {
             const float eGL = expf(sGL[0]);
-            for (int d = warp; d < dk; d += 8) {
-                float acc = eGL * sdS[d * LDV + c];
-                for (int i = 0; i < L; ++i) {
-                    const float eg = sEG[i];
-                    acc = fmaf(p.scale * eg * to_f(sQ[i * ldkq + d]), sdO[i * LDV + c], acc);
-                    acc = fmaf(-sBeta[i] * eg * to_f(sK[i * ldkq + d]), sdV[i * LDV + c], acc);
+            const int ndg = dk >> 3;
+            for (int tile = tid; tile < 16 * ndg; tile += NT) {
+                const int c0 = 2 * (tile / ndg), d0 = 8 * (tile % ndg);
+                float acc[2][8];
+#pragma unroll
+                for (int y = 0; y < 2; ++y) {
+                    const float4 a = *reinterpret_cast<const float4 *>(sdSt + (c0 + y) * SLD + d0);
+                    const float4 b = *reinterpret_cast<const float4 *>(sdSt + (c0 + y) * SLD + d0 + 4);
+                    acc[y][0] = eGL * a.x; acc[y][1] = eGL * a.y; acc[y][2] = eGL * a.z; acc[y][3] = eGL * a.w;
+                    acc[y][4] = eGL * b.x; acc[y][5] = eGL * b.y; acc[y][6] = eGL * b.z; acc[y][7] = eGL * b.w;
                 }
-                sdS[d * LDV + c] = acc;
+                for (int i = 0; i < L; ++i) {
+                    const float fq = p.scale * sEG[i], fk = -sBeta[i] * sEG[i];
+                    const float4 q0v = ld4(sQ + i * ldkq + d0), q1v = ld4(sQ + i * ldkq + d0 + 4);
+                    const float4 k0v = ld4(sK + i * ldkq + d0), k1v = ld4(sK + i * ldkq + d0 + 4);
+                    const float qv[8] = {q0v.x, q0v.y, q0v.z, q0v.w, q1v.x, q1v.y, q1v.z, q1v.w};
+                    const float kv[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const float a = fq * sdO[i * LDV + c0 + y], b = fk * sdV[i * LDV + c0 + y];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) acc[y][x] = fmaf(a, qv[x], fmaf(b, kv[x], acc[y][x]));
+                    }
+                }
+#pragma unroll
+                for (int y = 0; y < 2; ++y) {
+                    *reinterpret_cast<float4 *>(sdSt + (c0 + y) * SLD + d0) =
+                        make_float4(acc[y][0], acc[y][1], acc[y][2], acc[y][3]);
+                    *reinterpret_cast<float4 *>(sdSt + (c0 + y) * SLD + d0 + 4) =
+                        make_float4(acc[y][4], acc[y][5], acc[y][6], acc[y][7]);
+                }
             }
         }
     }
@@ -484,22 +559,25 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     if (p.dh0) {
         for (int idx = tid; idx < dk * BV; idx += NT) {
             const int d = idx / BV, cc = idx - d * BV;
-            if (cc < bvw) p.dh0[sbase + (size_t)d * dv + v0 + cc] = sdS[d * LDV + cc];
+            if (cc < bvw) p.dh0[sbase + (size_t)d * dv + v0 + cc] = sdSt[cc * SLD + d];
         }
     }
 }
 
-__global__ void fill_zero(float *p, long long n) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-        p[i] = 0.0f;
-}
+// Zero-fills up to four fp32 buffers in one launch (null pointers skipped).
+struct ZeroArgs {
+    float *ptr[4];
+    long long n[4];
+};
 
-cudaError_t zero(float *ptr, long long n, cudaStream_t stream) {
-    if (!ptr || n <= 0) return cudaSuccess;
-    long long blocks = (n + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    fill_zero<<<(unsigned)blocks, 256, 0, stream>>>(ptr, n);
-    return cudaGetLastError();
+__global__ void fill_zero(ZeroArgs z) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (!z.ptr[b]) continue;
+        for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < z.n[b]; i += stride)
+            z.ptr[b][i] = 0.0f;
+    }
 }
 
 }  // namespace
@@ -514,10 +592,16 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaError_t err;
-    if ((err = zero(p.dq, p.tokens * p.Nk * p.dk, stream)) != cudaSuccess) return err;
-    if ((err = zero(p.dkk, p.tokens * p.Nk * p.dk, stream)) != cudaSuccess) return err;
-    if ((err = zero(p.dbeta, p.tokens * p.Nv, stream)) != cudaSuccess) return err;
-    if ((err = zero(p.dg, p.tokens * p.Nv, stream)) != cudaSuccess) return err;
+    {
+        const ZeroArgs z{{p.dq, p.dkk, p.dbeta, p.dg},
+                         {p.tokens * p.Nk * p.dk, p.tokens * p.Nk * p.dk, p.tokens * p.Nv, p.tokens * p.Nv}};
+        const long long most = p.tokens * p.Nk * p.dk;
+        long long blocks = (most + 255) / 256;
+        if (blocks > 152 * 8) blocks = 152 * 8;
+        if (blocks < 1) blocks = 1;
+        fill_zero<<<(unsigned)blocks, 256, 0, stream>>>(z);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
     // forward pass at chunk 64, saving the chunk-start states
     Params f = p;
     f.o = nullptr;

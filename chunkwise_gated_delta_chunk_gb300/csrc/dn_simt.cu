@@ -28,26 +28,22 @@
 #include <math.h>
 
 #include "dn_internal.h"
+#include "dn_simt_common.cuh"
 
 namespace dn {
 namespace {
+
+using simt::align16;
+using simt::kq_ld;
+using simt::to_f;
 
 constexpr int C = kChunk;
 constexpr int BV = 32;   // value columns per CTA
 constexpr int NT = 256;  // threads per CTA (8 warps)
 constexpr int LDC = C + 1;
 
-__device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void put(float *p, float x) { *p = x; }
 __device__ __forceinline__ void put(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
-
-// Row stride (elements) of the shared K/Q copies: odd in 4-byte words, so
-// lanes reading one column of 32 different rows hit 32 different banks.
-template <typename Tin>
-__host__ __device__ constexpr int kq_ld(int dk) { return sizeof(Tin) == 2 ? dk + 2 : dk + 1; }
-
-__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 struct Layout {
     size_t k, q, s, a, t, p, v, r, vn, g, eg, dec, beta, rk, rq, end;
@@ -76,24 +72,6 @@ __host__ __device__ inline Layout layout(int dk) {
     L.rq = off; off += C * 4;
     L.end = off;
     return L;
-}
-
-// Copy L rows of a [tokens, H, d] tensor (head `hh`, tokens from t0) into a
-// padded shared tile, zero-filling rows L..C-1.
-template <typename Tin>
-__device__ __forceinline__ void load_rows(Tin *dst, const Tin *src, long long t0, int L, int H,
-                                          int hh, int d, int tid) {
-    constexpr int VEC = 16 / sizeof(Tin);
-    const int ld = kq_ld<Tin>(d);
-    const int per_row = d / VEC;
-    for (int idx = tid; idx < L * per_row; idx += NT) {
-        const int i = idx / per_row, cv = idx - i * per_row;
-        const uint4 w = *reinterpret_cast<const uint4 *>(src + ((t0 + i) * H + hh) * (long long)d + cv * VEC);
-        const Tin *e = reinterpret_cast<const Tin *>(&w);
-#pragma unroll
-        for (int x = 0; x < VEC; ++x) dst[i * ld + cv * VEC + x] = e[x];
-    }
-    for (int idx = L * ld + tid; idx < C * ld; idx += NT) dst[idx] = Tin(0.0f);
 }
 
 template <typename Tin>
@@ -170,8 +148,8 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         }
 
         // ---- load the chunk --------------------------------------------
-        load_rows<Tin>(sK, k, t0, L, Nk, hk, dk, tid);
-        load_rows<Tin>(sQ, q, t0, L, Nk, hk, dk, tid);
+        simt::load_rows<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
+        simt::load_rows<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
         for (int idx = tid; idx < C * BV; idx += NT) {
             const int i = idx / BV, c = idx - i * BV;
             sV[idx] = (i < L && c < bvw) ? to_f(v[((t0 + i) * Nv + h) * (long long)dv + v0 + c]) : 0.0f;
@@ -222,24 +200,16 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         __syncthreads();
 
         // ---- a2: A (strictly lower) and P (lower incl. diagonal) ---------
-        for (int idx = tid; idx < C * C; idx += NT) {
-            const int i = idx >> 6, j = idx & 63;
+        simt::kq_products<NT>(sK, sQ, ldkq, dk, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
             if (i < L && j <= i) {
-                const Tin *ki = sK + i * ldkq, *kj = sK + j * ldkq, *qi = sQ + i * ldkq;
-                float sk = 0.0f, sq = 0.0f;
-                for (int d = 0; d < dk; ++d) {
-                    const float kjd = to_f(kj[d]);
-                    sk = fmaf(to_f(ki[d]), kjd, sk);
-                    sq = fmaf(to_f(qi[d]), kjd, sq);
-                }
                 const float dec = expf(sG[i] - sG[j]) * sRK[j];
-                if (j < i) a = -sBeta[i] * sRK[i] * dec * sk;
-                pv = p.scale * sRQ[i] * dec * sq;
+                if (j < i) a = -sBeta[i] * sRK[i] * dec * kk;
+                pv = p.scale * sRQ[i] * dec * qk;
             }
             sA[i * LDC + j] = a;
             sP[i * LDC + j] = pv;
-        }
+        });
         __syncthreads();
 
         // ---- a3: T = (I - A)^-1, column j by the 4 lanes 4j..4j+3 ---------
