@@ -40,13 +40,17 @@ using simt::to_f;
 constexpr int C = kChunk;
 constexpr int BV = 32;   // value columns per CTA
 constexpr int NT = 256;  // threads per CTA (8 warps)
-constexpr int LDC = C + 1;
+constexpr int LDC = C + 4;   // row stride of the C x C matrices (16-byte rows)
+
+// Row stride (floats) of the transposed state tile S^T ([BV][dk]): 16-byte
+// rows, consecutive rows 4 banks apart.
+__host__ __device__ inline int st_ld(int dk) { return dk + 4; }
 
 __device__ __forceinline__ void put(float *p, float x) { *p = x; }
 __device__ __forceinline__ void put(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
 
 struct Layout {
-    size_t k, q, s, a, t, p, v, r, vn, g, eg, dec, beta, rk, rq, end;
+    size_t k, q, s, a, t, p, v, r, vn, oi, g, eg, dec, beta, rk, rq, end;
 };
 
 template <typename Tin>
@@ -56,13 +60,14 @@ __host__ __device__ inline Layout layout(int dk) {
     const size_t kq = align16(size_t(C) * kq_ld<Tin>(dk) * sizeof(Tin));
     L.k = off; off += kq;
     L.q = off; off += kq;
-    L.s = off; off += align16(size_t(dk) * BV * 4);
+    L.s = off; off += align16(size_t(BV) * st_ld(dk) * 4);
     L.a = off; off += align16(size_t(C) * LDC * 4);
     L.t = off; off += align16(size_t(C) * LDC * 4);
     L.p = off; off += align16(size_t(C) * LDC * 4);
     L.v = off; off += size_t(C) * BV * 4;
     L.r = off; off += size_t(C) * BV * 4;
     L.vn = off; off += size_t(C) * BV * 4;
+    L.oi = off; off += size_t(C) * BV * 4;
     L.g = off; off += C * 4;
     L.eg = off; off += C * 4;
     L.dec = off; off += C * 4;
@@ -91,13 +96,14 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     const Layout lay = layout<Tin>(dk);
     Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);
     Tin *sQ = reinterpret_cast<Tin *>(smem + lay.q);
-    float *sS = reinterpret_cast<float *>(smem + lay.s);
+    float *sSt = reinterpret_cast<float *>(smem + lay.s);  // [BV][SLD]: S^T
     float *sA = reinterpret_cast<float *>(smem + lay.a);
     float *sT = reinterpret_cast<float *>(smem + lay.t);
     float *sP = reinterpret_cast<float *>(smem + lay.p);
     float *sV = reinterpret_cast<float *>(smem + lay.v);
     float *sR = reinterpret_cast<float *>(smem + lay.r);
     float *sVn = reinterpret_cast<float *>(smem + lay.vn);
+    float *sOi = reinterpret_cast<float *>(smem + lay.oi);  // scale e^G (Q S_in), the inter-chunk output
     float *sG = reinterpret_cast<float *>(smem + lay.g);
     float *sEG = reinterpret_cast<float *>(smem + lay.eg);
     float *sDec = reinterpret_cast<float *>(smem + lay.dec);
@@ -112,6 +118,8 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     const Tin *k = static_cast<const Tin *>(p.k);
     const Tin *v = static_cast<const Tin *>(p.v);
     Tin *o = static_cast<Tin *>(p.o);
+    const bool want_o = o != nullptr;  // the backward's forward pass needs only the states
+    const int SLD = st_ld(dk);
 
     long long bos, eos;
     if (p.cu) {
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     const size_t sbase = ((size_t)n * Nv + h) * dk * dv;
     for (int idx = tid; idx < dk * BV; idx += NT) {
         const int d = idx / BV, c = idx - d * BV;
-        sS[idx] = (p.h0 && c < bvw) ? p.h0[sbase + (size_t)d * dv + v0 + c] : 0.0f;
+        sSt[c * SLD + d] = (p.h0 && c < bvw) ? p.h0[sbase + (size_t)d * dv + v0 + c] : 0.0f;
     }
 
     const int CH = p.chunk;  // 16, 32 or 64 (<= C)
@@ -143,7 +151,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             float *dst = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
             for (int idx = tid; idx < dk * BV; idx += NT) {
                 const int d = idx / BV, c = idx - d * BV;
-                if (c < bvw) dst[(size_t)d * dv + c] = sS[idx];
+                if (c < bvw) dst[(size_t)d * dv + c] = sSt[c * SLD + d];
             }
         }
 
@@ -233,38 +241,60 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         __syncthreads();
 
         // ---- a4/a5: R = diag(beta)(V - diag(e^G) K S_in); also Q S_in -----
-        const int c = lane;
-        float qs[8];
+        // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         {
-            float ks[8];
+            const int i0 = 2 * (tid >> 3), cg = tid & 7;
+            float ks[2][4], qs[2][4];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) { ks[r] = 0.0f; qs[r] = 0.0f; }
-            for (int d = 0; d < dk; ++d) {
-                const float s = sS[d * BV + c];
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int i = warp + 8 * r;
-                    ks[r] = fmaf(to_f(sK[i * ldkq + d]), s, ks[r]);
-                    qs[r] = fmaf(to_f(sQ[i * ldkq + d]), s, qs[r]);
+                for (int x = 0; x < 4; ++x) ks[r][x] = qs[r][x] = 0.0f;
+            for (int d = 0; d < dk; d += 4) {
+                float4 kr[2], qr[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    kr[r] = simt::ld4(sK + (i0 + r) * ldkq + d);
+                    if (want_o) qr[r] = simt::ld4(sQ + (i0 + r) * ldkq + d);
+                }
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float4 s4 = *reinterpret_cast<const float4 *>(sSt + (cg + 8 * x) * SLD + d);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        ks[r][x] = fmaf(kr[r].x, s4.x, fmaf(kr[r].y, s4.y, fmaf(kr[r].z, s4.z, fmaf(kr[r].w, s4.w, ks[r][x]))));
+                        if (want_o)
+                            qs[r][x] = fmaf(qr[r].x, s4.x, fmaf(qr[r].y, s4.y, fmaf(qr[r].z, s4.z, fmaf(qr[r].w, s4.w, qs[r][x]))));
+                    }
                 }
             }
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int i = warp + 8 * r;
-                sR[i * BV + c] = i < L ? sBeta[i] * (sV[i * BV + c] - sEG[i] * sRK[i] * ks[r]) : 0.0f;
+            for (int r = 0; r < 2; ++r) {
+                const int i = i0 + r;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int cc = cg + 8 * x;
+                    sR[i * BV + cc] = i < L ? sBeta[i] * (sV[i * BV + cc] - sEG[i] * sRK[i] * ks[r][x]) : 0.0f;
+                    sOi[i * BV + cc] = p.scale * sEG[i] * sRQ[i] * qs[r][x];
+                }
             }
         }
         __syncthreads();
 
-        // ---- a5: v_new = T R --------------------------------------------
+        // ---- a5: v_new = T R (row i per warp, lane = column) ---------------
+        const int c = lane;
         {
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-            for (int j = 0; j < L; ++j) {
-                const float rj = sR[j * BV + c];
+            for (int j = 0; j < L; j += 4) {
+                float rj[4];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = fmaf(sT[(warp + 8 * r) * LDC + j], rj, acc[r]);
+                for (int x = 0; x < 4; ++x) rj[x] = sR[(j + x) * BV + c];  // rows past L are zero
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(sT + (warp + 8 * r) * LDC + j);
+                    acc[r] = fmaf(t4.x, rj[0], fmaf(t4.y, rj[1], fmaf(t4.z, rj[2], fmaf(t4.w, rj[3], acc[r]))));
+                }
             }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -275,47 +305,59 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         __syncthreads();
 
         // ---- a6: o = scale e^G (Q S_in) + P v_new ------------------------
-        {
+        if (want_o) {
             float acc[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
-            for (int j = 0; j < L; ++j) {
-                const float vj = sVn[j * BV + c];
+            for (int r = 0; r < 8; ++r) acc[r] = sOi[(warp + 8 * r) * BV + c];
+            for (int j = 0; j < L; j += 4) {
+                float vj[4];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = fmaf(sP[(warp + 8 * r) * LDC + j], vj, acc[r]);
+                for (int x = 0; x < 4; ++x) vj[x] = sVn[(j + x) * BV + c];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float4 p4 = *reinterpret_cast<const float4 *>(sP + (warp + 8 * r) * LDC + j);
+                    acc[r] = fmaf(p4.x, vj[0], fmaf(p4.y, vj[1], fmaf(p4.z, vj[2], fmaf(p4.w, vj[3], acc[r]))));
+                }
             }
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
-                if (i < L && c < bvw && o) {
-                    const float out = fmaf(p.scale * sEG[i] * sRQ[i], qs[r], acc[r]);
-                    put(o + ((t0 + i) * Nv + h) * (long long)dv + v0 + c, out);
-                }
+                if (i < L && c < bvw) put(o + ((t0 + i) * Nv + h) * (long long)dv + v0 + c, acc[r]);
             }
         }
 
         // ---- a5: S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T ----
+        // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of S
         {
             const float eGL = expf(sGL[0]);
-            for (int d0 = warp; d0 < dk; d0 += 8 * 8) {
-                float acc[8];
+            const int ndg = dk >> 3;
+            for (int tile = tid; tile < 16 * ndg; tile += NT) {
+                const int c0 = 2 * (tile / ndg), d0 = 8 * (tile % ndg);
+                float acc[2][8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int d = d0 + 8 * r;
-                    acc[r] = d < dk ? eGL * sS[d * BV + c] : 0.0f;
+                for (int y = 0; y < 2; ++y) {
+                    const float4 a = *reinterpret_cast<const float4 *>(sSt + (c0 + y) * SLD + d0);
+                    const float4 b = *reinterpret_cast<const float4 *>(sSt + (c0 + y) * SLD + d0 + 4);
+                    acc[y][0] = eGL * a.x; acc[y][1] = eGL * a.y; acc[y][2] = eGL * a.z; acc[y][3] = eGL * a.w;
+                    acc[y][4] = eGL * b.x; acc[y][5] = eGL * b.y; acc[y][6] = eGL * b.z; acc[y][7] = eGL * b.w;
                 }
                 for (int i = 0; i < L; ++i) {
-                    const float w = sDec[i] * sRK[i] * sVn[i * BV + c];
+                    const float f = sDec[i] * sRK[i];
+                    const float4 k0v = simt::ld4(sK + i * ldkq + d0), k1v = simt::ld4(sK + i * ldkq + d0 + 4);
+                    const float kv[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const int d = d0 + 8 * r;
-                        if (d < dk) acc[r] = fmaf(to_f(sK[i * ldkq + d]), w, acc[r]);
+                    for (int y = 0; y < 2; ++y) {
+                        const float w = f * sVn[i * BV + c0 + y];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) acc[y][x] = fmaf(w, kv[x], acc[y][x]);
                     }
                 }
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int d = d0 + 8 * r;
-                    if (d < dk) sS[d * BV + c] = acc[r];
+                for (int y = 0; y < 2; ++y) {
+                    *reinterpret_cast<float4 *>(sSt + (c0 + y) * SLD + d0) =
+                        make_float4(acc[y][0], acc[y][1], acc[y][2], acc[y][3]);
+                    *reinterpret_cast<float4 *>(sSt + (c0 + y) * SLD + d0 + 4) =
+                        make_float4(acc[y][4], acc[y][5], acc[y][6], acc[y][7]);
                 }
             }
         }
@@ -325,7 +367,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     if (p.ht) {
         for (int idx = tid; idx < dk * BV; idx += NT) {
             const int d = idx / BV, c = idx - d * BV;
-            if (c < bvw) p.ht[sbase + (size_t)d * dv + v0 + c] = sS[idx];
+            if (c < bvw) p.ht[sbase + (size_t)d * dv + v0 + c] = sSt[c * SLD + d];
         }
     }
 }
