@@ -14,7 +14,8 @@ Functions follow the pages' notation:
 * :func:`wy_chunk` -- steps a1-a4 of one chunk (G, T, W, U), exposed so the
   tests can check W and U against brute-force Householder-like products.
 * :func:`recurrent_bwd` -- the gradient of :func:`recurrent` (reverse mode
-  through the token recurrence) for given output and final-state gradients.
+  through the token recurrence) for given output and final-state gradients;
+  :func:`l2norm_bwd` is the gradient of :func:`l2norm`.
 * :func:`l2norm` -- the row normalisation that ``use_qk_l2norm_in_kernel``
   applies to q and k ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与
   Triton 内核实现" §5, §6); :func:`recurrent` and :func:`chunked` take the
@@ -200,8 +201,23 @@ def wy_chunk(k, v, beta, g=None):
     return G, Tm, W, U
 
 
+def l2norm_bwd(x, dy):
+    """Gradient with respect to ``x`` of ``sum(dy * l2norm(x))``, row by row, fp64.
+
+    For a row with ``||x|| > 1e-12``: ``(dy - y (y . dy)) / ||x||`` with
+    ``y = x / ||x||`` (the derivative of x / ||x||); below the guard the
+    divisor is the constant 1e-12, so the gradient is ``dy / 1e-12``.
+    """
+    x, dy = _f64(x), _f64(dy)
+    norm = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    big = norm > 1e-12
+    y = x / np.where(big, norm, 1.0)
+    proj = np.sum(y * dy, axis=-1, keepdims=True)
+    return np.where(big, (dy - y * proj) / np.where(big, norm, 1.0), dy / 1e-12)
+
+
 def recurrent_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, do=None,
-                  dht=None, groups=None, threads=0):
+                  dht=None, groups=None, threads=0, use_qk_l2norm_in_kernel=False):
     """Gradient of the forward in fp64, reverse mode through the token recurrence.
 
     For the loss ``sum(do * o) + sum(dht * ht)`` of :func:`recurrent` (same
@@ -212,10 +228,18 @@ def recurrent_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, d
     with all value heads that read key head hk; other entries stay NaN.
     ("flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §3.4
     lists these gradients; the pages print no formula for them, so this is
-    the chain rule through each step of the definition.)
+    the chain rule through each step of the definition.)  With
+    ``use_qk_l2norm_in_kernel`` the forward normalises q and k first
+    (:func:`l2norm`), and dq, dk go back through :func:`l2norm_bwd`.
     """
     lib = _load()
     q, k, v, beta, g, h0, do, dht = map(_f64, (q, k, v, beta, g, h0, do, dht))
+    if use_qk_l2norm_in_kernel:
+        out = recurrent_bwd(l2norm(q), l2norm(k), v, beta, g, h0, cu_seqlens, scale, do, dht,
+                            groups, threads)
+        out["dq"] = l2norm_bwd(q, out["dq"])
+        out["dk"] = l2norm_bwd(k, out["dk"])
+        return out
     B, T, Nk, dk, Nv, dv, cu, N = _shapes(q, v, cu_seqlens)
     if scale is None:
         scale = dk ** -0.5

@@ -368,10 +368,10 @@ def test_qk_l2norm_chunk_equals_recurrent(chunk):
 # (the definition), element by element, on tiny inputs that cross the
 # reverse pass's 64-token checkpoints.
 # --------------------------------------------------------------------------
-def _loss(inp, do, dht, **over):
+def _loss(inp, do, dht, l2=False, **over):
     d = dict(inp, **over)
     o, ht = oracle.recurrent(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
-                             d["cu_seqlens"], d["scale"], threads=1)
+                             d["cu_seqlens"], d["scale"], threads=1, use_qk_l2norm_in_kernel=l2)
     return float((o * do).sum() + (0.0 if dht is None else (ht * dht).sum()))
 
 
@@ -423,3 +423,46 @@ def test_bwd_groups_subset_matches_full():
     assert np.array_equal(part["dv"][1, :, 2:], full["dv"][1, :, 2:])
     assert np.array_equal(part["dh0"][1, 2:], full["dh0"][1, 2:])
     assert np.isnan(part["dq"][0]).all() and np.isnan(part["dbeta"][1, :, :2]).all()
+
+
+def test_bwd_l2norm_matches_finite_differences():
+    """With in-kernel q / k normalisation, dq and dk (through the normalisation)
+    and the other gradients against central differences of the normalised
+    forward, on raw q / k rows of widely varying norm."""
+    inp = workloads.make_inputs(1, 0, 2, 4, 5, 3, dtype=torch.float32, gate_mu=1.0, h0=True,
+                                seed=97, lengths=[7, 0, 70, 2], raw_qk=True)
+    inp = {key: (val.double().numpy().copy() if hasattr(val, "numpy") and key != "cu_seqlens"
+                 else val) for key, val in inp.items()}
+    rng = np.random.default_rng(97)
+    o, ht = _call(oracle.recurrent, inp, use_qk_l2norm_in_kernel=True)
+    do, dht = rng.standard_normal(o.shape), rng.standard_normal(ht.shape)
+    gr = oracle.recurrent_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
+                              inp["cu_seqlens"], inp["scale"], do=do, dht=dht,
+                              use_qk_l2norm_in_kernel=True)
+    eps = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("beta", "dbeta"), ("g", "dg")):
+        x = inp[name].copy()
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(inp, do, dht, True, **{name: x})
+            x[idx] = old - eps
+            lm = _loss(inp, do, dht, True, **{name: x})
+            x[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        an = gr[gname]
+        assert np.abs(fd - an).max() <= 1e-7 * max(np.abs(an).max(), 1.0), name
+
+
+def test_l2norm_bwd_closed_forms():
+    """The gradient of x / ||x|| is orthogonal to x and scales as 1 / ||x||;
+    below the guard it is dy / 1e-12."""
+    rng = np.random.default_rng(98)
+    x = rng.standard_normal((5, 7))
+    dy = rng.standard_normal((5, 7))
+    g = oracle.l2norm_bwd(x, dy)
+    assert np.allclose((g * x).sum(-1), 0.0, atol=1e-13)
+    assert np.allclose(oracle.l2norm_bwd(3.0 * x, dy), g / 3.0, rtol=1e-13)
+    tiny = np.array([[1e-14, 0.0, 0.0]])
+    assert np.allclose(oracle.l2norm_bwd(tiny, np.array([[1.0, 2.0, 3.0]])), [[1e12, 2e12, 3e12]])
