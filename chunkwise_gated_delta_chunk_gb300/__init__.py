@@ -269,8 +269,9 @@ def dn_chunk_bwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype) -> int:
 
 
 def chunk_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, do=None, dht=None,
-              stream=None, workspace=None):
-    """Gradients of :func:`chunk_fwd`'s loss ``sum(do * o) + sum(dht * ht)``.
+              stream=None, workspace=None, use_qk_l2norm_in_kernel=False):
+    """Gradients of :func:`chunk_fwd`'s loss ``sum(do * o) + sum(dht * ht)``
+    (with the same ``use_qk_l2norm_in_kernel``).
 
     Allocates the fp32 gradients and the workspace with torch and runs
     :func:`dn_chunk_bwd`.  Returns a dict with ``dq``, ``dk``, ``dv``,
@@ -289,7 +290,8 @@ def chunk_bwd(q, k, v, beta, g=None, h0=None, cu_seqlens=None, scale=None, do=No
         nbytes = dn_chunk_bwd_workspace_bytes(N, B, T, Nk, Nv, dk, dv, dtype_code(q.dtype))
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
     st = dn_chunk_bwd(q, k, v, beta, g, h0, cu_seqlens, N, B, T, Nk, Nv, dk, dv,
-                      dtype_code(q.dtype), 0.0 if scale is None else scale, 0, do, dht,
+                      dtype_code(q.dtype), 0.0 if scale is None else scale,
+                      DN_QK_L2NORM if use_qk_l2norm_in_kernel else 0, do, dht,
                       out["dq"], out["dk"], out["dv"], out["dbeta"], out["dg"], out["dh0"],
                       workspace, stream=stream)
     if st != DN_OK:

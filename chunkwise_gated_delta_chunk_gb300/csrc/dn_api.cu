@@ -203,7 +203,6 @@ DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
     const void *ptrs[] = {q, k, v, beta, g, h0, cu_seqlens, d_o, d_ht, d_q, d_k, d_v, d_beta, d_g, d_h0};
     for (const void *ptr : ptrs)
         if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
-    if (flags & DN_QK_L2NORM) return DN_ERR_UNSUPPORTED;
     if (!bwd_dims_ok(dk, dv)) return DN_ERR_UNSUPPORTED;
     if (n_seqs == 0) return DN_OK;
     const size_t ws_need = bwd_workspace_bytes(tokens, n_seqs, Nv, dk, dv);

@@ -66,7 +66,7 @@ struct Layout {
 };
 
 // Per-row scalars (C floats each) at Layout::sc.
-enum { R_G, R_EG, R_DEC, R_BETA, R_QSDO, R_DBU, R_DGAM, R_E, R_ROWE, R_DBA, R_COUNT };
+enum { R_G, R_EG, R_DEC, R_BETA, R_QSDO, R_DBU, R_DGAM, R_E, R_ROWE, R_DBA, R_RK, R_RQ, R_COUNT };
 
 template <typename Tin>
 __host__ __device__ inline Layout layout(int dk) {
@@ -130,6 +130,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     float *sG = sc + R_G * C, *sEG = sc + R_EG * C, *sDec = sc + R_DEC * C, *sBeta = sc + R_BETA * C;
     float *sQSdO = sc + R_QSDO * C, *sDBU = sc + R_DBU * C, *sDGam = sc + R_DGAM * C;
     float *sE = sc + R_E * C, *sRowE = sc + R_ROWE * C, *sDBA = sc + R_DBA * C;
+    // inverse key / query norms of the chunk's rows (1 without kQkL2Norm):
+    // every product below that reads a k or q row takes the row's factor, so
+    // the gradients the CTA adds up are those of the normalised rows
+    float *sRK = sc + R_RK * C, *sRQ = sc + R_RQ * C;
+    const bool qkn = (p.flags & kQkL2Norm) != 0;
     float *sGL = sc + R_COUNT * C;      // [0]: G_L
     float *sRed = sGL + 4;              // [8]: per-warp partial <S, dS'>
     const int ldkq = kq_ld<Tin>(dk);
@@ -208,6 +213,20 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             sDec[lane] = lane < L ? expf(GL - a) : 0.0f;
             sDec[lane + 32] = lane + 32 < L ? expf(GL - b) : 0.0f;
             if (lane == 0) sGL[0] = GL;
+        } else {
+            for (int rr = warp - 1; rr < 2 * C; rr += 7) {
+                const int i = rr & (C - 1);
+                float ss = 0.0f;
+                if (qkn) {
+                    const Tin *x = (rr < C ? sK : sQ) + i * ldkq;
+                    for (int d = lane; d < dk; d += 32) {
+                        const float f = to_f(x[d]);
+                        ss = fmaf(f, f, ss);
+                    }
+                    ss = warp_sum(ss);
+                }
+                if (lane == 0) (rr < C ? sRK : sRQ)[i] = qkn ? rsqrtf(fmaxf(ss, 1e-24f)) : 1.0f;
+            }
         }
         {
             float part = 0.0f;
@@ -224,9 +243,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         simt::kq_products<NT>(sK, sQ, ldkq, dk, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
             if (i < L && j <= i) {
-                const float D = expf(sG[i] - sG[j]);
-                if (j < i) a = -kk * D;
-                pv = p.scale * qk * D;
+                const float D = expf(sG[i] - sG[j]) * sRK[j];
+                if (j < i) a = -kk * D * sRK[i];
+                pv = p.scale * qk * D * sRQ[i];
             }
             sM0[i * LDC + j] = a;
             sM2[i * LDC + j] = pv;
@@ -279,14 +298,16 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int i = i0 + r;
+                const float rk = sRK[i], rq = sRQ[i];
                 float qd = 0.0f;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     const int cc = cg + 8 * x;
-                    sKS[i * LDV + cc] = ks[r][x];
-                    sKdS[i * LDV + cc] = kd[r][x];
-                    sU[i * LDV + cc] = i < L ? sU[i * LDV + cc] - sEG[i] * ks[r][x] : 0.0f;
-                    qd = fmaf(qs[r][x], sdO[i * LDV + cc], qd);
+                    const float ksv = rk * ks[r][x];
+                    sKS[i * LDV + cc] = ksv;
+                    sKdS[i * LDV + cc] = rk * kd[r][x];
+                    sU[i * LDV + cc] = i < L ? sU[i * LDV + cc] - sEG[i] * ksv : 0.0f;
+                    qd = fmaf(rq * qs[r][x], sdO[i * LDV + cc], qd);
                 }
                 // the eight threads of a row pair are lanes 8 m .. 8 m + 7
                 qd += __shfl_xor_sync(0xffffffffu, qd, 1);
@@ -488,12 +509,13 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                     const float4 q0v = ld4(sQ + j * ldkq + d0), q1v = ld4(sQ + j * ldkq + d0 + 4);
                     const float kv[8] = {k0v.x, k0v.y, k0v.z, k0v.w, k1v.x, k1v.y, k1v.z, k1v.w};
                     const float qv[8] = {q0v.x, q0v.y, q0v.z, q0v.w, q1v.x, q1v.y, q1v.z, q1v.w};
+                    const float rkj = sRK[j], rqj = sRQ[j];
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const int i = i0 + r;
-                        const float wq = sM1[i * LDC + j];                       // WP_ij (0 for j > i)
-                        const float mk = sM0[i * LDC + j] + sM0[j * LDC + i];    // M_ij + M_ji
-                        const float wt = sM1[j * LDC + i];                       // WP_ji (0 for j < i)
+                        const float wq = rkj * sM1[i * LDC + j];                       // WP_ij (0 for j > i)
+                        const float mk = rkj * (sM0[i * LDC + j] + sM0[j * LDC + i]);  // M_ij + M_ji
+                        const float wt = rqj * sM1[j * LDC + i];                       // WP_ji (0 for j < i)
 #pragma unroll
                         for (int x = 0; x < 8; ++x) {
                             gq[r][x] = fmaf(wq, kv[x], gq[r][x]);
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                     acc[y][4] = eGL * b.x; acc[y][5] = eGL * b.y; acc[y][6] = eGL * b.z; acc[y][7] = eGL * b.w;
                 }
                 for (int i = 0; i < L; ++i) {
-                    const float fq = p.scale * sEG[i], fk = -sBeta[i] * sEG[i];
+                    const float fq = p.scale * sEG[i] * sRQ[i], fk = -sBeta[i] * sEG[i] * sRK[i];
                     const float4 q0v = ld4(sQ + i * ldkq + d0), q1v = ld4(sQ + i * ldkq + d0 + 4);
                     const float4 k0v = ld4(sK + i * ldkq + d0), k1v = ld4(sK + i * ldkq + d0 + 4);
                     const float qv[8] = {q0v.x, q0v.y, q0v.z, q0v.w, q1v.x, q1v.y, q1v.z, q1v.w};
@@ -561,6 +583,42 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             const int d = idx / BV, cc = idx - d * BV;
             if (cc < bvw) p.dh0[sbase + (size_t)d * dv + v0 + cc] = sdSt[cc * SLD + d];
         }
+    }
+}
+
+// With kQkL2Norm the backward kernel's dq and dk are the gradients of the
+// normalised rows y = x r, r = 1 / max(||x||, 1e-12).  This maps each row
+// back: dx = r (dy - y (y . dy)) where ||x|| > 1e-12, else dx = r dy (the
+// divisor is the constant 1e-12 there).  One warp per row; rows of q, then k.
+template <typename Tin>
+__global__ void l2norm_bwd_rows(const Tin *q, const Tin *k, float *dq, float *dk, long long rows, int d) {
+    const long long wid = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (wid >= 2 * rows) return;
+    const bool isq = wid < rows;
+    const long long row = isq ? wid : wid - rows;
+    const Tin *x = (isq ? q : k) + row * d;
+    float *g = (isq ? dq : dk) + row * d;
+    float xv[8], gv[8];  // d <= 256
+    float ss = 0.0f, xg = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int e = lane + 32 * m;
+        xv[m] = e < d ? to_f(x[e]) : 0.0f;
+        gv[m] = e < d ? g[e] : 0.0f;
+        ss = fmaf(xv[m], xv[m], ss);
+        xg = fmaf(xv[m], gv[m], xg);
+    }
+    ss = warp_sum(ss);
+    xg = warp_sum(xg);
+    const bool big = ss > 1e-24f;
+    const float r = rsqrtf(fmaxf(ss, 1e-24f));
+    // y . dy = r (x . dy);  r (dy - y (y . dy)) = r dy - r^3 (x . dy) x
+    const float c = big ? r * r * r * xg : 0.0f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int e = lane + 32 * m;
+        if (e < d) g[e] = r * gv[m] - c * xv[m];
     }
 }
 
@@ -610,16 +668,28 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     const char *fname = "";
     if ((err = simt_launch(f, bf16, stream, &fname)) != cudaSuccess) return err;
     const size_t smem = bwd_smem_bytes(p.dk, bf16);
+    const bool qkn = (p.flags & kQkL2Norm) != 0;
+    const long long rows = p.tokens * p.Nk;  // q (and k) rows
+    const unsigned nblk = (unsigned)((2 * rows * 32 + 255) / 256);
     if (bf16) {
         err = cudaFuncSetAttribute(simt_bwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         simt_bwd<__nv_bfloat16><<<(unsigned)grid, NT, smem, stream>>>(p);
-        *name = "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>";
+        if (qkn && rows > 0)
+            l2norm_bwd_rows<__nv_bfloat16><<<nblk, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), p.dq, p.dkk, rows,
+                p.dk);
+        *name = qkn ? "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
+                    : "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>";
     } else {
         err = cudaFuncSetAttribute(simt_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
         simt_bwd<float><<<(unsigned)grid, NT, smem, stream>>>(p);
-        *name = "fill_zero+simt_fwd<f32>+simt_bwd<f32>";
+        if (qkn && rows > 0)
+            l2norm_bwd_rows<float><<<nblk, 256, 0, stream>>>(static_cast<const float *>(p.q),
+                                                             static_cast<const float *>(p.k), p.dq, p.dkk, rows, p.dk);
+        *name = qkn ? "fill_zero+simt_fwd<f32>+simt_bwd<f32>+l2norm_bwd_rows<f32>"
+                    : "fill_zero+simt_fwd<f32>+simt_bwd<f32>";
     }
     return cudaGetLastError();
 }

@@ -218,8 +218,10 @@ dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *   d_ht       [N, Nv, dk, dv] float32   gradient of ht; NULL means zero.
  * The other arguments are those of dn_chunk_fwd (the chunk length is 64).
  * All arithmetic is fp32 on CUDA cores.  dk must be at most 128
- * (DN_ERR_UNSUPPORTED otherwise); flags must be 0 (DN_QK_L2NORM is
- * DN_ERR_UNSUPPORTED).  Rows of tokens outside every sequence are 0 in d_q,
+ * (DN_ERR_UNSUPPORTED otherwise).  With DN_QK_L2NORM the forward it
+ * differentiates normalises q and k in the kernels, and d_q, d_k are the
+ * gradients of the raw rows (through the normalisation; a fourth launch maps
+ * them row by row).  Rows of tokens outside every sequence are 0 in d_q,
  * d_k, d_beta and d_g and not written in d_v.  The sums over value tiles and
  * value heads use fp32 atomic adds, so the last bits of d_q, d_k, d_beta
  * and d_g may differ from run to run.

@@ -179,7 +179,6 @@ def bwd_call(clib, **over):
     (dict(flags=2), dn.DN_ERR_INVALID_ARG),
     (dict(ws=None), dn.DN_ERR_INVALID_ARG),              # the workspace is required
     (dict(wsb=1024), dn.DN_ERR_INVALID_ARG),             # and must be large enough
-    (dict(flags=dn.DN_QK_L2NORM), dn.DN_ERR_UNSUPPORTED),
     (dict(dk=256), dn.DN_ERR_UNSUPPORTED),
     (dict(dv=48), dn.DN_ERR_UNSUPPORTED),
     (dict(n=0, B=0), dn.DN_OK),                           # nothing to do, nothing launched

@@ -23,9 +23,9 @@ NAMES = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
 
 
 def inputs(B=2, T=150, Nk=2, Nv=2, dk=64, dv=64, dtype=torch.bfloat16, gate=3.0, h0=True,
-           seed=0, lengths=None, dht=True):
+           seed=0, lengths=None, dht=True, raw_qk=False):
     inp = workloads.make_inputs(B, T, Nk, Nv, dk, dv, dtype=dtype, gate_mu=gate, h0=h0,
-                                seed=seed, lengths=lengths)
+                                seed=seed, lengths=lengths, raw_qk=raw_qk)
     gen = torch.Generator().manual_seed(seed + 99)
     inp["do"] = torch.randn(inp["v"].shape, generator=gen).to(dtype)
     N = inp["N"]
@@ -37,7 +37,8 @@ def run(inp):
     import chunkwise_gated_delta_chunk_gb300 as dn
     d = workloads.to_device(inp, "cuda")
     out = dn.chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], d["cu_seqlens"],
-                       scale=inp["scale"], do=d["do"], dht=d["dht"])
+                       scale=inp["scale"], do=d["do"], dht=d["dht"],
+                       use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     assert dn.dn_check() == dn.DN_OK
     return out
 
@@ -45,7 +46,8 @@ def run(inp):
 def check(inp, out, groups=None, label=""):
     ref = oracle.recurrent_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
                                inp["cu_seqlens"], inp["scale"], do=inp["do"], dht=inp["dht"],
-                               groups=groups)
+                               groups=groups,
+                               use_qk_l2norm_in_kernel=inp.get("qk_l2norm", False))
     res = {}
     for name in NAMES:
         if out[name] is None:
@@ -138,3 +140,21 @@ def test_repeatable(lib):
     for name in NAMES:
         assert torch.allclose(a[name], b[name], rtol=1e-5, atol=1e-5), name
     assert torch.equal(a["dv"], b["dv"]) and torch.equal(a["dh0"], b["dh0"])
+
+
+@pytest.mark.parametrize("dtype,dk,dv,lengths", [(torch.bfloat16, 128, 128, None),
+                                                 (torch.float32, 64, 32, None),
+                                                 (torch.bfloat16, 64, 64, [1, 0, 64, 65, 130])])
+def test_qk_l2norm(lib, dtype, dk, dv, lengths):
+    """DN_QK_L2NORM: the gradient of the forward that normalises raw q / k rows
+    in the kernels; dq and dk go back through the normalisation."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    if lengths is None:
+        inp = inputs(B=2, T=150, dk=dk, dv=dv, dtype=dtype, seed=900 + dk, raw_qk=True)
+    else:
+        inp = inputs(B=1, Nk=2, Nv=4, dk=dk, dv=dv, dtype=dtype, lengths=lengths, seed=905,
+                     raw_qk=True)
+    out = run(inp)
+    assert dn.dn_last_kernel().endswith("l2norm_bwd_rows<%s>" % ("bf16" if dtype == torch.bfloat16
+                                                                 else "f32"))
+    check(inp, out, label="bwd l2norm %s %dx%d" % (dtype, dk, dv))
