@@ -5,7 +5,7 @@ chunkwise gated delta rule, gated DeltaNet at B=4, H=16, T=2048, d=128, bf16.
 
 One step = one dn_chunk_fwd call over the whole workload (all chunk steps of
 the path in one launch).  Inputs are resident in HBM before the timed region;
-L2 is flushed (a 256 MiB write) before every timed step, outside the events
+L2 is flushed before every timed step, outside the events
 that time the step.  Each rank runs its own copy of the workload (independent
 sequences, no exchange between GPUs), so scaling is weak and `value` is the
 tokens all ranks processed per second of the slowest rank.
@@ -36,6 +36,23 @@ import workloads  # noqa: E402
 METRIC = "fwd tokens/s & % of roofline, gated delta rule H=16 d=128 T=2048 (1 GB300)"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed before every timed step, outside the step's events: a 256 MiB write, then a "
+           "256 MiB read of another buffer so the written lines are back in HBM and L2 holds "
+           "only clean unrelated lines")
+
+
+class L2Flush:
+    """Before each timed step: write a buffer larger than L2, then read another
+    one, so that neither the step's inputs nor dirty lines of the flush itself
+    are in L2 when the step starts."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        torch.sum(self.r)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = os.path.join(ROOT, "chunkwise_gated_delta_chunk_gb300", "csrc")
 
@@ -319,9 +336,9 @@ def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
         if st != dn.DN_OK:
             raise dn.DnError(st, "dn_chunk_bwd")
 
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         launch()
     torch.cuda.synchronize(dev)
     if dn.dn_check(stream) != dn.DN_OK:
@@ -335,7 +352,7 @@ def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
     torch.cuda.synchronize(dev)
     with ClockSampler(smi_gpu_id(dev, int(os.environ.get("LOCAL_RANK", "0")))) as clk:
         for i in range(K):
-            flush.zero_()
+            flush()
             ev0[i].record(stream)
             launch()
             ev1[i].record(stream)
@@ -402,8 +419,7 @@ def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
                 higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="f32 (inputs %s)" % ("bf16" if d["q"].dtype == torch.bfloat16 else "f32"),
                 data="synthetic",
-                config=dict(config_of(wl_name, inp, l2="flushed before every timed step "
-                                      "(256 MiB write, outside the step's events)"), mode="bwd"),
+                config=dict(config_of(wl_name, inp, l2=L2_NOTE), mode="bwd"),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
                 gpu_launches=K * launches_per_call(kernel), roofline=roof,
                 e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,
@@ -496,9 +512,9 @@ def main():
         if st != dn.DN_OK:
             raise dn.DnError(st)
 
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         launch()
     torch.cuda.synchronize(dev)
     st = dn.dn_check(stream)
@@ -517,7 +533,7 @@ def main():
     with ClockSampler(gpu_id) as clk:
         w0 = time.perf_counter()
         for i in range(K):
-            flush.zero_()
+            flush()
             ev0[i].record(stream)
             launch()
             ev1[i].record(stream)
@@ -597,8 +613,7 @@ def main():
                 n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16"
                 if d["q"].dtype == torch.bfloat16 else "f32", data="synthetic",
-                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2="flushed before every timed step "
-                                      "(256 MiB write, outside the step's events)"), mode=args.mode),
+                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2=L2_NOTE), mode=args.mode),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,
                 gpu_launches=K * launches_per_call(kernel), roofline=roof,
                 e2e=dict(value=weak_scaling_value(alg["tokens"], world, e2e_ms), unit=UNIT,
