@@ -28,13 +28,14 @@
 //   0      loader: TMA for the K, Q, V tiles of a chunk, bulk copies of the
 //          chunk's T', T'' and P into three two-deep rings, and the gate
 //          scalars (prefix sum G, e^G, decays) computed with warp shuffles;
-//   1      chain MMA issuer (one thread: U, VN, O, DS, PV) and TMEM owner;
+//   1      chain MMA issuer (one thread: U, VN, DS) and TMEM owner;
 //   2-5    prep: one thread issues W of the next chunk as soon as its tiles
 //          and T' have landed; the warpgroup turns W^T into the bf16 -W^T
 //          operand, running ahead of the state scan;
 //   6-9    state: v_new and v~ operands, the fp32 state update, ht;
-//   10-13  output: o = scale e^{G} (S^T Q^T) + P v_new, transposed through
-//          shared memory and stored as bf16 rows.
+//   10-13  output: its leader issues O and PV of each chunk once DS is done;
+//          the warpgroup reads o = scale e^{G} (S^T Q^T) + P v_new,
+//          transposes it through shared memory and stores bf16 rows.
 //
 // Every wait is bounded: after kTimeoutNs a CTA records kStatusTimeout in the
 // status word, raises a shared abort flag so the other roles stop too, drains
@@ -116,6 +117,7 @@ enum {
     B_O_EMPTY,
     B_DRAIN,
     B_DRAIN2,
+    B_DRAIN3,                   // the output leader's own MMAs
     B_COUNT
 };
 static_assert(B_COUNT <= NBARS, "barrier space");
@@ -327,13 +329,14 @@ __device__ __forceinline__ void issue_o(const Ctx &x, uint32_t tm, int c) {
 }
 
 // ---------------------------------------------------------------------------
-// Chain MMA issuer (one thread).  The tensor pipe runs MMAs in issue order,
-// so the state-dependent VN and DS go first and the others fill the gaps
-// while the state warpgroup converts operands:
-//   VN(c); U(c+1) while v_new^T is converted; DS(c);
-//   O(c) and PV(c) while S^T is converted (into the other S^T buffer).
-// It also refills the T'' and P rings as their buffers free up (W and the
-// T' ring belong to the prep warpgroup).
+// Chain MMA issuer (one thread): the MMAs on the serial chain of the scan,
+//   VN(c); U(c+1) while v_new^T is converted; DS(c).
+// Issuing a tcgen05 MMA holds the issuing thread for tens of cycles, so O(c)
+// and PV(c), which are off the chain, have their own issuer (the output
+// warpgroup's leader); they enter the in-order tensor pipe after DS(c) and
+// run while the state warpgroup converts S^T.  This thread also refills the
+// T'' and P rings as their buffers free up (W and the T' ring belong to the
+// prep warpgroup).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool wait_tiles(const Ctx &x, int c, int ring) {
     return wait(x, bar(x, B_FULL + c % NS), (c / NS) & 1) &&
@@ -402,21 +405,6 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
             load_ring(x, p, u, 1, c + 2);
             loaded[1] = c + 2;
         }
-        // output: inter-chunk part O (reads S^T buffer c & 1, which the state
-        // warpgroup rewrites only after DS of the next chunk, a later commit
-        // of this thread) and the intra-chunk part PV on top, once the output
-        // of chunk c - 1 has read acc_o
-        if (!wait(x, bar(x, B_O_EMPTY), par ^ 1)) break;
-        if (!wait(x, bar(x, B_QS + s), (c / NS) & 1)) break;
-        if (!wait(x, bar(x, B_PF + t), (c >> 1) & 1)) break;
-        tc_fence_after();
-        issue_o(x, tm, c);
-        const uint32_t pbuf = x.base + OFF_PR + t * 8192;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tm + TM_O, av + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, 1);
-        mma_commit(bar(x, B_D_FULL));
-        mma_commit(bar(x, B_EMPTY + s));
         DN_TRACE_EV(3, c);
     }
     // every MMA issued by this thread completes before tensor memory is
@@ -441,7 +429,30 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     const uint32_t buf = x.base + OFF_OST;
     const uint8_t *gbuf = x.gbase + OFF_OST;
     const long long rstride = (long long)p.Nv * p.dv * 2;  // bytes between tokens
+    const bool leader = tid == 0;
+    bool issued = false;  // the leader has MMAs in flight to drain at exit
     for (int c = 0; c < u.nc; ++c) {
+        if (leader) {
+            // O(c) = S_in(c)^T Q~^T and PV(c) = v_new(c)^T P(c)^T into acc_o.
+            // S_UPD(c): DS(c) is done, so these follow it in the tensor pipe
+            // (and VSM(c), hence v_new^T(c), was ready before DS(c) was
+            // issued).  O_EMPTY: acc_o of chunk c - 1 has been read.
+            const int s = c % NS, t = c & 1;
+            if (wait(x, bar(x, B_S_UPD), c & 1) && wait(x, bar(x, B_O_EMPTY), (c & 1) ^ 1) &&
+                wait(x, bar(x, B_QS + s), (c / NS) & 1) && wait(x, bar(x, B_PF + t), (c >> 1) & 1)) {
+                tc_fence_after();
+                issue_o(x, tm, c);
+                const uint32_t av = tm + TM_V + 64 * t;
+                const uint32_t pbuf = x.base + OFF_PR + t * 8192;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tm + TM_O, av + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, 1);
+                mma_commit(bar(x, B_D_FULL));
+                mma_commit(bar(x, B_EMPTY + s));  // the last reader of the stage
+                issued = true;
+            }
+        }
+        __syncwarp();
         // Every exit is taken by the whole warpgroup together (bar_red_or), so
         // no warp is left waiting at one of its named barriers.
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
@@ -486,6 +497,11 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
             named_bar_sync(2, 128);
         }
         DN_TRACE_EV(1, c);
+    }
+    // the leader's MMAs complete before tensor memory is freed
+    if (leader && issued) {
+        mma_commit(bar(x, B_DRAIN3));
+        wait_drain(bar(x, B_DRAIN3), 0);
     }
 }
 
@@ -638,6 +654,11 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         // 0..31 and v~^T packed in columns 32..63; a column is rewritten only
         // after it has been read.
         if (!wwait(x, bar(x, B_V_FULL), par)) return;
+        // O(c - 1), the last reader of the bf16 S^T buffer this chunk's state
+        // pass rewrites, comes from the output leader: wait for its commit.
+        // (D_FULL(c) needs this warpgroup's VSM(c), so the barrier is at most
+        // one phase ahead here.)
+        if (c > 0 && !wwait(x, bar(x, B_D_FULL), (c - 1) & 1)) return;
         DN_TRACE_EV(0, c);
         tc_fence_after();
         {
@@ -684,8 +705,6 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
         // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
         const bool last = (c + 1 == u.nc);
-        // (S_UPD also covers O of the chunk before, the last reader of the
-        // bf16 S^T buffer this pass overwrites)
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         DN_TRACE_EV(2, c);
         tc_fence_after();
@@ -745,6 +764,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     x.status = p.status;
     const int warp = threadIdx.x >> 5;
     const Unit u = unit_of(p);
+    DN_TRACE_EV(15, 1023);  // kernel start (per warp)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -767,6 +787,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         mbar_init(bar(x, B_O_EMPTY), 4);
         mbar_init(bar(x, B_DRAIN), 1);
         mbar_init(bar(x, B_DRAIN2), 1);
+        mbar_init(bar(x, B_DRAIN3), 1);
         *x.abort_flag = 0;
         fence_barrier_init();
     }
@@ -804,10 +825,12 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     } else {
         output_role(x, p, u, tm);
     }
+    DN_TRACE_EV(13, 1023);  // role done (per warp)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tm, TM_COLS);
+    DN_TRACE_EV(14, 1023);  // kernel end (per warp)
 }
 
 }  // namespace
