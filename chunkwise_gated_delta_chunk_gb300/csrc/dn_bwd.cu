@@ -252,21 +252,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         });
         __syncthreads();
 
-        // ---- T = (I - A)^-1, A_im = beta_i sM0_im; column j by 4 lanes ----
-        {
-            const int j = tid >> 2, pl = tid & 3;
-            for (int i = pl; i < C; i += 4) sM1[i * LDC + j] = (i == j) ? 1.0f : 0.0f;
-            __syncwarp();
-            for (int i = 1; i < L; ++i) {
-                float part = 0.0f;
-                if (i > j) {
-                    for (int m = j + pl; m < i; m += 4) part = fmaf(sM0[i * LDC + m], sM1[m * LDC + j], part);
-                }
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                if (i > j && ((i - j) & 3) == pl) sM1[i * LDC + j] = sBeta[i] * part;
-            }
-        }
+        // ---- T = (I - A)^-1, A_im = beta_i sM0_im (blocked; sVn, written
+        // later, is its scratch) ---------------------------------------------
+        simt::solve_T_blocked<NT>(sM0, LDC, sBeta, sM1, LDC, sVn, L, tid);
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         {

@@ -14,7 +14,8 @@
 //   a1  G = inclusive prefix sum of g (warp scan), e^{G_i}, e^{G_L - G_i}
 //   a2  A_ij = -beta_i (k_i.k_j) e^{G_i-G_j} (j < i),
 //       P_ij = scale (q_i.k_j) e^{G_i-G_j} (j <= i)
-//   a3  T = (I - A)^-1 by forward substitution, one column per 4 lanes
+//   a3  T = (I - A)^-1: the diagonal 16 x 16 blocks by forward substitution,
+//       the rest from block products (dn_simt_common.cuh)
 //   a4+a5  v_new = U - W S_in = T diag(beta) (V - diag(e^G) K S_in)
 //       (the same product as T diag(beta) V - T diag(beta e^G) K S_in, grouped
 //        so that W = T diag(beta e^G) K is never formed: K S_in is 64 x 32,
@@ -220,25 +221,9 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         });
         __syncthreads();
 
-        // ---- a3: T = (I - A)^-1, column j by the 4 lanes 4j..4j+3 ---------
-        // Column j of T solves (I - A) x = e_j:  x_j = 1 and
-        // x_i = sum_{j <= m < i} A_im x_m for i > j.  Lane p sums the terms
-        // with m = j + p (mod 4) and keeps those x_m itself.
-        {
-            const int j = tid >> 2, pl = tid & 3;
-            for (int i = pl; i < C; i += 4) sT[i * LDC + j] = (i == j) ? 1.0f : 0.0f;
-            __syncwarp();  // the solve below reads rows other lanes initialised
-            for (int i = 1; i < L; ++i) {
-                float part = 0.0f;
-                if (i > j) {
-                    for (int m = j + pl; m < i; m += 4) part = fmaf(sA[i * LDC + m], sT[m * LDC + j], part);
-                }
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                if (i > j && ((i - j) & 3) == pl) sT[i * LDC + j] = part;
-            }
-        }
-        __syncthreads();
+        // ---- a3: T = (I - A)^-1, blocked over 16 x 16 blocks ----------------
+        // (sVn, written only in a5, is the solve's scratch)
+        simt::solve_T_blocked<NT>(sA, LDC, nullptr, sT, LDC, sVn, L, tid);
 
         // ---- a4/a5: R = diag(beta)(V - diag(e^G) K S_in); also Q S_in -----
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)

@@ -129,3 +129,193 @@ __device__ __forceinline__ void kq_products(const float *sK, const float *sQ, in
 
 }  // namespace simt
 }  // namespace dn
+
+namespace dn {
+namespace simt {
+
+// T = (I - A)^-1 of the chunk's 64 x 64 strictly lower A, in fp32 on CUDA
+// cores, blocked over 16 x 16 blocks (all NT threads call it; it synchronises
+// with __syncthreads):
+//   A_im = rs[i] * sA[i * lda + m] (rs null: 1), zero on and above the diagonal;
+//   T_D = the inverses of the four diagonal blocks I - A_bb (forward
+//   substitution, one column per thread), N = T_D A_O (A_O: the blocks below
+//   the diagonal), N^4 = 0, and
+//       T = (I + N + N^2 + N^3) T_D,
+//   i.e. T10 = N10 T00, T21 = N21 T11, T32 = N32 T22,
+//        T20 = (N20 + N21 N10) T00, T31 = (N31 + N32 N21) T11,
+//        T30 = (N30 + N31 N10 + N32 N20 + N32 N21 N10) T00.
+// sT (row stride ldt) gets T, zero above the diagonal; scr holds 3 x 256
+// floats of scratch.  Rows and columns past the chunk's length L have A = 0
+// and so come out as the identity's; with L <= 32 only T10 = N10 T00 is
+// formed off the diagonal (the other blocks are zero).
+template <int NT>
+__device__ __forceinline__ void solve_T_blocked(const float *sA, int lda, const float *rs, float *sT, int ldt,
+                                                float *scr, int L, int tid) {
+    static_assert(NT >= 96, "enough threads for the block rows");
+    auto A = [&](int i, int m) { return (rs ? rs[i] : 1.0f) * sA[i * lda + m]; };
+    auto Tb = [&](int bi, int bj) { return sT + 16 * bi * ldt + 16 * bj; };
+    // phase 0: diagonal blocks (threads 0-63: block t / 16, column t % 16);
+    // the others zero the blocks above the diagonal
+    if (tid < 64) {
+        const int b = tid >> 4, col = tid & 15, o = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = (r == col) ? 1.0f : 0.0f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) s = fmaf(A(o + r, o + m), x[m], s);
+            x[r] = s;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(o + r) * ldt + o + col] = x[r];
+    } else {
+        for (int e = tid - 64; e < 6 * 256; e += NT - 64) {
+            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            // upper blocks (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            Tb(bi, bj)[r * ldt + c] = 0.0f;
+        }
+    }
+    __syncthreads();
+    if (L <= 32) {  // (uniform) two diagonal blocks at most
+        if (tid < 16) {
+            // N10 = T11 A10, then T10 = N10 T00
+            const int r = tid;
+            float n[16], out[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) n[c] = 0.0f;
+            for (int k = 0; k <= r; ++k) {
+                const float t = Tb(1, 1)[r * ldt + k];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) n[c] = fmaf(t, A(16 + k, c), n[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+#pragma unroll
+                for (int c = 0; c <= k; ++c) out[c] = fmaf(n[k], Tb(0, 0)[k * ldt + c], out[c]);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) Tb(1, 0)[r * ldt + c] = out[c];
+        } else {
+            for (int e = tid - 16; e < 5 * 256; e += NT - 16) {
+                const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                // lower blocks (2,0) (2,1) (3,0) (3,1) (3,2)
+                const int bi = blk < 2 ? 2 : 3;
+                const int bj = blk < 2 ? blk : blk - 2;
+                Tb(bi, bj)[r * ldt + c] = 0.0f;
+            }
+        }
+        __syncthreads();
+        return;
+    }
+    // phase 1: N_ij = T_ii A_ij into block (i, j) of sT
+    if (tid < 96) {
+        const int task = tid >> 4, r = tid & 15;
+        const int bi = task == 0 ? 1 : (task < 3 ? 2 : 3);
+        const int bj = task == 0 ? 0 : (task < 3 ? task - 1 : task - 3);
+        const float *Tii = Tb(bi, bi);
+        float out[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) out[c] = 0.0f;
+        for (int k = 0; k <= r; ++k) {
+            const float t = Tii[r * ldt + k];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = fmaf(t, A(16 * bi + k, 16 * bj + c), out[c]);
+        }
+        float *dst = Tb(bi, bj) + r * ldt;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = out[c];
+    }
+    __syncthreads();
+    // phase 2: P20 = N21 N10, S31 = N31 + N32 N21, S30 = N30 + N31 N10 + N32 N20
+    if (tid < 48) {
+        const int task = tid >> 4, r = tid & 15;
+        float out[16];
+        auto mul_add = [&](const float *X, const float *Y) {  // out += X[r, :] Y
+            for (int k = 0; k < 16; ++k) {
+                const float xv = X[r * ldt + k];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) out[c] = fmaf(xv, Y[k * ldt + c], out[c]);
+            }
+        };
+        if (task == 0) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = 0.0f;
+            mul_add(Tb(2, 1), Tb(1, 0));
+        } else if (task == 1) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = Tb(3, 1)[r * ldt + c];
+            mul_add(Tb(3, 2), Tb(2, 1));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = Tb(3, 0)[r * ldt + c];
+            mul_add(Tb(3, 1), Tb(1, 0));
+            mul_add(Tb(3, 2), Tb(2, 0));
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) scr[task * 256 + r * 16 + c] = out[c];
+    }
+    __syncthreads();
+    // phase 3: S30 += N32 P20; T31 = S31 T11; T20 = (N20 + P20) T00;
+    // T10 = N10 T00; T21 = N21 T11 (a thread reads its own row of an
+    // in-place block before it writes it, and no one else reads that row)
+    if (tid < 80) {
+        const int task = tid >> 4, r = tid & 15;
+        float x[16], out[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) out[c] = 0.0f;
+        if (task == 0) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) out[c] = scr[2 * 256 + r * 16 + c];
+            for (int k = 0; k < 16; ++k) {
+                const float xv = Tb(3, 2)[r * ldt + k];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) out[c] = fmaf(xv, scr[k * 16 + c], out[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) scr[2 * 256 + r * 16 + c] = out[c];
+        } else {
+            // X T_jj with X = S31 (task 1), N20 + P20 (2), N10 (3), N21 (4)
+            const int bi = task == 1 ? 3 : (task == 2 ? 2 : (task == 3 ? 1 : 2));
+            const int bj = task == 1 ? 1 : (task == 2 ? 0 : (task == 3 ? 0 : 1));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                x[k] = task == 1 ? scr[256 + r * 16 + k] : Tb(bi, bj)[r * ldt + k];
+                if (task == 2) x[k] += scr[r * 16 + k];
+            }
+            const float *Tjj = Tb(bj, bj);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+#pragma unroll
+                for (int c = 0; c <= k; ++c) out[c] = fmaf(x[k], Tjj[k * ldt + c], out[c]);
+            float *dst = Tb(bi, bj) + r * ldt;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) dst[c] = out[c];
+        }
+    }
+    __syncthreads();
+    // phase 4: T30 = S30 T00; T32 = N32 T22 (in place)
+    if (tid < 32) {
+        const int task = tid >> 4, r = tid & 15;
+        float x[16], out[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            x[k] = task == 0 ? scr[2 * 256 + r * 16 + k] : Tb(3, 2)[r * ldt + k];
+            out[k] = 0.0f;
+        }
+        const float *Tjj = task == 0 ? Tb(0, 0) : Tb(2, 2);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+#pragma unroll
+            for (int c = 0; c <= k; ++c) out[c] = fmaf(x[k], Tjj[k * ldt + c], out[c]);
+        float *dst = Tb(3, task == 0 ? 0 : 2) + r * ldt;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) dst[c] = out[c];
+    }
+    __syncthreads();
+}
+
+}  // namespace simt
+}  // namespace dn
