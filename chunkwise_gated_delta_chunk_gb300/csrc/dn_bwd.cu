@@ -43,6 +43,13 @@
 #include "dn_internal.h"
 #include "dn_simt_common.cuh"
 
+#ifdef DN_TRACE
+__device__ unsigned long long g_bwd_ph[64][16];
+extern "C" __attribute__((visibility("default"))) int dn_trace_dump_bwd(void *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_bwd_ph, sizeof(g_bwd_ph));
+}
+#endif
+
 namespace dn {
 namespace {
 
@@ -167,9 +174,12 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     const long long nch = (eos - bos + C - 1) / C;
     for (long long ci = nch - 1; ci >= 0; --ci) {
         const long long t0 = bos + ci * C;
+        const int pc = (int)(nch - 1 - ci);  // position in the walk (phase stamps)
+        (void)pc;
         const int L = (eos - t0) < C ? (int)(eos - t0) : C;
         __syncthreads();  // the previous (later) chunk is done with every buffer
 
+        DN_PHASE(g_bwd_ph, pc, 0);
         // ---- load --------------------------------------------------------
         simt::load_rows<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
         simt::load_rows<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
@@ -193,6 +203,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 1);
         // ---- gate prefix sum (warp 0); <S, dS'> partials (every warp) ----
         if (warp == 0) {
             float a = sG[lane], b = sG[lane + 32];
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 2);
         // ---- -(K K^T . D) (strictly lower) and P (lower) ------------------
         simt::kq_products<NT>(sK, sQ, ldkq, dk, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
@@ -252,9 +264,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         });
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 3);
         // ---- T = (I - A)^-1, A_im = beta_i sM0_im (blocked; sVn, written
         // later, is its scratch) ---------------------------------------------
         simt::solve_T_blocked<NT>(sM0, LDC, sBeta, sM1, LDC, sVn, L, tid);
+        DN_PHASE(g_bwd_ph, pc, 4);
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         {
@@ -306,6 +320,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 5);
         // ---- Vn = T diag(beta) U ------------------------------------------
         {
             float acc[8];
@@ -324,6 +339,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 6);
         // ---- dVn = diag(dec) K dS' + P^T dO; e_i --------------------------
         {
 #pragma unroll
@@ -338,6 +354,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 7);
         // ---- dR = T^T dVn; dv = diag(beta) dR ------------------------------
         {
             float acc[8];
@@ -365,6 +382,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 8);
         // ---- dA, dP and E (row i per warp, columns j = lane, lane + 32) ----
         {
 #pragma unroll 1
@@ -407,6 +425,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 9);
         // ---- warp 0: dbeta, dG and dg ------------------------------------
         if (warp == 0) {
             float dG[2], db[2];
@@ -526,6 +545,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
+        DN_PHASE(g_bwd_ph, pc, 10);
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
         {
@@ -563,6 +583,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                 }
             }
         }
+        DN_PHASE(g_bwd_ph, pc, 11);
     }
 
     __syncthreads();

@@ -23,7 +23,7 @@
 // loaded: T' and P already carry the inverse norms, and the loader folds the
 // per-token factors 1/||k_i|| into v~ and 1/||q_i|| into Q~.
 //
-// Warp roles (14 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
+// Warp roles (15 warps; warp w reaches TMEM lanes 32 (w % 4) .. +31, so each
 // group of four consecutive warps covers all 128 lanes):
 //   0      loader: TMA for the K, Q, V tiles of a chunk, bulk copies of the
 //          chunk's T', T'' and P into three two-deep rings, and the gate
@@ -32,10 +32,11 @@
 //   2-5    prep: one thread issues W of the next chunk as soon as its tiles
 //          and T' have landed; the warpgroup turns W^T into the bf16 -W^T
 //          operand, running ahead of the state scan;
-//   6-9    state: v_new and v~ operands, the fp32 state update, ht;
-//   10-13  output: its leader issues O and PV of each chunk once DS is done;
-//          the warpgroup reads o = scale e^{G} (S^T Q^T) + P v_new,
-//          transposes it through shared memory and stores bf16 rows.
+//   6-9    state: v_new and v~ operands; key blocks 0-1 of the state passes;
+//   10-13  output: key blocks 2-3 of each state pass (the S^T operand, the
+//          alpha scaling, ht); then reads o = scale e^{G} (S^T Q^T) +
+//          P v_new, transposes it through shared memory, stores bf16 rows;
+//   14     output MMA issuer (one thread: O, PV).
 //
 // Every wait is bounded: after kTimeoutNs a CTA records kStatusTimeout in the
 // status word, raises a shared abort flag so the other roles stop too, drains
@@ -53,7 +54,7 @@
 // Optional per-chunk event trace of CTA 0 (SM clock), compiled in only with
 // -DDN_TRACE for profiling builds; the default build contains no trace code.
 #ifdef DN_TRACE
-__device__ unsigned long long g_dn_trace[14][1024][16];
+__device__ unsigned long long g_dn_trace[16][1024][16];  // [warp][chunk][event]
 #define DN_TRACE_EV(ev, c)                                                    \
     do {                                                                      \
         if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (c) < 1024)         \
@@ -77,7 +78,7 @@ constexpr int C = kChunk;      // 64
 constexpr int DK = 128;
 constexpr int BVT = 128;       // value columns per CTA
 constexpr int NS = 3;          // pipeline stages of K/Q/V tiles
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 480;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
@@ -117,7 +118,7 @@ enum {
     B_O_EMPTY,
     B_DRAIN,
     B_DRAIN2,
-    B_DRAIN3,                   // the output leader's own MMAs
+    B_DRAIN3,                   // the output issuer's own MMAs
     B_COUNT
 };
 static_assert(B_COUNT <= NBARS, "barrier space");
@@ -332,9 +333,9 @@ __device__ __forceinline__ void issue_o(const Ctx &x, uint32_t tm, int c) {
 // Chain MMA issuer (one thread): the MMAs on the serial chain of the scan,
 //   VN(c); U(c+1) while v_new^T is converted; DS(c).
 // Issuing a tcgen05 MMA holds the issuing thread for tens of cycles, so O(c)
-// and PV(c), which are off the chain, have their own issuer (the output
-// warpgroup's leader); they enter the in-order tensor pipe after DS(c) and
-// run while the state warpgroup converts S^T.  This thread also refills the
+// and PV(c), which are off the chain, have their own issuer thread (warp
+// 14); they enter the in-order tensor pipe after DS(c) and run while the
+// state is converted.  This thread also refills the
 // T'' and P rings as their buffers free up (W and the T' ring belong to the
 // prep warpgroup).
 // ---------------------------------------------------------------------------
@@ -418,6 +419,69 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 }
 
 // ---------------------------------------------------------------------------
+// The fp32 state acc_s (TMEM lane = value column, 128 columns = key index d)
+// is handled in 32-column blocks: blocks 0-1 by the state warpgroup, blocks
+// 2-3 by the output warpgroup, which is otherwise idle in the window after
+// DS.  Halving each pass halves the S^T conversion on the scan's serial
+// chain.  `lb` is the thread's TMEM lane base; `hb` its element of h0 / ht at
+// key index 0 (row stride dv).
+// ---------------------------------------------------------------------------
+// acc_s = alpha_0 h0^T and SB[0] = bf16(h0^T), blocks [b0, b1).
+__device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, size_t hb, float alpha, int b0,
+                                                  int b1) {
+    uint32_t r[32], pk[16];
+    for (int blk = b0; blk < b1; ++blk) {
+        float f[32];
+        const float *hp = p.h0 ? p.h0 + hb + (size_t)(32 * blk) * p.dv : nullptr;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            f[k] = hp ? *hp : 0.f;
+            if (hp) hp += p.dv;
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
+        tmem_st16(lb + TM_SB + 16 * blk, pk);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * f[k]);
+        tmem_st32(lb + TM_S + 32 * blk, r);
+    }
+}
+
+// After DS(c): SB[(c+1) & 1] = bf16(acc_s), or for the last chunk ht = acc_s.
+__device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t lb, size_t hb, int c, bool last,
+                                                     int b0, int b1) {
+    uint32_t r[32], pk[16];
+    for (int blk = b0; blk < b1; ++blk) {
+        tmem_ld32(lb + TM_S + 32 * blk, r);
+        tmem_wait_ld_dep(r);
+        if (!last) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+            tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
+        } else if (p.ht) {
+            float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                *hp = __uint_as_float(r[k]);
+                hp += p.dv;
+            }
+        }
+    }
+}
+
+// acc_s *= alpha(c+1) before DS(c+1).
+__device__ __forceinline__ void state_scale_blocks(uint32_t lb, float alpha, int b0, int b1) {
+    uint32_t r[32];
+    for (int blk = b0; blk < b1; ++blk) {
+        tmem_ld32(lb + TM_S + 32 * blk, r);
+        tmem_wait_ld_dep(r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * __uint_as_float(r[k]));
+        tmem_st32(lb + TM_S + 32 * blk, r);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Output warpgroup: o[i][v] = (S^T Q~^T + v_new^T P^T)[v][i] for value column
 // v = this thread's TMEM lane, chunk by chunk once O and PV are done.
 // ---------------------------------------------------------------------------
@@ -429,32 +493,40 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     const uint32_t buf = x.base + OFF_OST;
     const uint8_t *gbuf = x.gbase + OFF_OST;
     const long long rstride = (long long)p.Nv * p.dv * 2;  // bytes between tokens
-    const bool leader = tid == 0;
-    bool issued = false;  // the leader has MMAs in flight to drain at exit
-    for (int c = 0; c < u.nc; ++c) {
-        if (leader) {
-            // O(c) = S_in(c)^T Q~^T and PV(c) = v_new(c)^T P(c)^T into acc_o.
-            // S_UPD(c): DS(c) is done, so these follow it in the tensor pipe
-            // (and VSM(c), hence v_new^T(c), was ready before DS(c) was
-            // issued).  O_EMPTY: acc_o of chunk c - 1 has been read.
-            const int s = c % NS, t = c & 1;
-            if (wait(x, bar(x, B_S_UPD), c & 1) && wait(x, bar(x, B_O_EMPTY), (c & 1) ^ 1) &&
-                wait(x, bar(x, B_QS + s), (c / NS) & 1) && wait(x, bar(x, B_PF + t), (c >> 1) & 1)) {
-                tc_fence_after();
-                issue_o(x, tm, c);
-                const uint32_t av = tm + TM_V + 64 * t;
-                const uint32_t pbuf = x.base + OFF_PR + t * 8192;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tm + TM_O, av + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, 1);
-                mma_commit(bar(x, B_D_FULL));
-                mma_commit(bar(x, B_EMPTY + s));  // the last reader of the stage
-                issued = true;
-            }
+    const size_t hb = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;  // h0 / ht of this lane
+    if (u.nc > 0) {
+        // blocks 2-3 of the initial state; then acc_s is ready for DS(0)
+        if (!bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + 0), 0))) {
+            state_init_blocks(p, lb, hb, scal(x, 0)[SC_ALPHA], 2, 4);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(bar(x, B_S_FULL));
+            warp_arrive(bar(x, B_VSM_FULL));
         }
-        __syncwarp();
+    }
+    for (int c = 0; c < u.nc; ++c) {
         // Every exit is taken by the whole warpgroup together (bar_red_or), so
         // no warp is left waiting at one of its named barriers.
+        // Blocks 2-3 of the state: the S^T operand of chunk c + 1 (or ht),
+        // then acc_s *= alpha(c+1), which DS(c+1) waits for (VSM_FULL).
+        const bool last = c + 1 == u.nc;
+        if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
+        DN_TRACE_EV(4, c);
+        tc_fence_after();
+        state_convert_blocks(p, lb, hb, c, last, 2, 4);
+        if (!last) {
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(bar(x, B_S_FULL));
+            DN_TRACE_EV(5, c);
+            const int s1 = (c + 1) % NS;
+            if (bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1))) break;
+            state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 2, 4);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(bar(x, B_VSM_FULL));
+            DN_TRACE_EV(6, c);
+        }
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
         tc_fence_after();
         const long long t0 = u.bos + (long long)c * C;
@@ -498,8 +570,36 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         }
         DN_TRACE_EV(1, c);
     }
-    // the leader's MMAs complete before tensor memory is freed
-    if (leader && issued) {
+}
+
+// ---------------------------------------------------------------------------
+// Output MMA issuer (warp 14, one thread): O(c) = S_in(c)^T Q~^T and
+// PV(c) = v_new(c)^T P(c)^T into acc_o.  S_UPD(c): DS(c) is done, so these
+// follow it in the tensor pipe and run while the state is converted (VSM(c),
+// hence v_new^T(c), was ready before DS(c) was issued).  O_EMPTY: acc_o of
+// chunk c - 1 has been read.  Issuing holds the issuing thread for tens of
+// cycles per MMA, which is why neither the chain thread nor a thread of a
+// converting warpgroup does it.
+// ---------------------------------------------------------------------------
+__device__ void out_mma_role(const Ctx x, const Unit u, uint32_t tm) {
+    bool issued = false;
+    for (int c = 0; c < u.nc; ++c) {
+        const int s = c % NS, t = c & 1;
+        if (!(wait(x, bar(x, B_S_UPD), c & 1) && wait(x, bar(x, B_O_EMPTY), (c & 1) ^ 1) &&
+              wait(x, bar(x, B_QS + s), (c / NS) & 1) && wait(x, bar(x, B_PF + t), (c >> 1) & 1)))
+            break;
+        tc_fence_after();
+        issue_o(x, tm, c);
+        const uint32_t av = tm + TM_V + 64 * t;
+        const uint32_t pbuf = x.base + OFF_PR + t * 8192;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ts(tm + TM_O, av + kk * 8, sdesc(pbuf + kk * 32, 16, 1024), ID_PV, 1);
+        mma_commit(bar(x, B_D_FULL));
+        mma_commit(bar(x, B_EMPTY + s));  // the last reader of the stage
+        issued = true;
+    }
+    // every MMA this thread issued completes before tensor memory is freed
+    if (issued) {
         mma_commit(bar(x, B_DRAIN3));
         wait_drain(bar(x, B_DRAIN3), 0);
     }
@@ -616,36 +716,19 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
     const uint32_t lb = lane_base(tm, warp);
     const size_t sbase = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;
     const int dv = p.dv;
-    uint32_t r[32], pk[16];
 
     if (u.nc == 0) {  // empty sequence: ht = h0
         if (p.ht)
             for (int d = 0; d < DK; ++d) p.ht[sbase + (size_t)d * dv] = p.h0 ? p.h0[sbase + (size_t)d * dv] : 0.f;
         return;
     }
-    // initial state: acc_s = alpha_0 h0^T, SB = bf16(h0^T)
+    // initial state: acc_s = alpha_0 h0^T, SB = bf16(h0^T) (blocks 0-1 here,
+    // 2-3 in the output warpgroup)
     if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
-    {
-        const float alpha = scal(x, 0)[SC_ALPHA];
-        for (int blk = 0; blk < 4; ++blk) {
-            float f[32];
-            const float *hp = p.h0 ? p.h0 + sbase + (size_t)(32 * blk) * dv : nullptr;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                f[k] = hp ? *hp : 0.f;
-                if (hp) hp += dv;
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
-            tmem_st16(lb + TM_SB + 16 * blk, pk);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * f[k]);
-            tmem_st32(lb + TM_S + 32 * blk, r);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(bar(x, B_S_FULL));
-    }
+    state_init_blocks(p, lb, sbase, scal(x, 0)[SC_ALPHA], 0, 2);
+    tmem_wait_st();
+    tc_fence_before();
+    warp_arrive(bar(x, B_S_FULL));
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const uint32_t par = c & 1;
@@ -655,7 +738,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         // after it has been read.
         if (!wwait(x, bar(x, B_V_FULL), par)) return;
         // O(c - 1), the last reader of the bf16 S^T buffer this chunk's state
-        // pass rewrites, comes from the output leader: wait for its commit.
+        // pass rewrites, comes from the output issuer: wait for its commit.
         // (D_FULL(c) needs this warpgroup's VSM(c), so the barrier is at most
         // one phase ahead here.)
         if (c > 0 && !wwait(x, bar(x, B_D_FULL), (c - 1) & 1)) return;
@@ -708,23 +791,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         DN_TRACE_EV(2, c);
         tc_fence_after();
-        for (int blk = 0; blk < 4; ++blk) {
-            tmem_ld32(lb + TM_S + 32 * blk, r);
-            tmem_wait_ld_dep(r);
-            if (!last) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
-                tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
-            } else if (p.ht) {
-                float *hp = p.ht + sbase + (size_t)(32 * blk) * dv;
-#pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    *hp = __uint_as_float(r[k]);
-                    hp += dv;
-                }
-            }
-        }
+        state_convert_blocks(p, lb, sbase, c, last, 0, 2);
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
@@ -736,14 +803,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         const int s1 = (c + 1) % NS;
         if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
         DN_TRACE_EV(6, c);
-        const float alpha = scal(x, s1)[SC_ALPHA];
-        for (int blk = 0; blk < 4; ++blk) {
-            tmem_ld32(lb + TM_S + 32 * blk, r);
-            tmem_wait_ld_dep(r);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * __uint_as_float(r[k]));
-            tmem_st32(lb + TM_S + 32 * blk, r);
-        }
+        state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 0, 2);
         tmem_wait_st();  // ordered before the next v~ arrive (fence there)
         DN_TRACE_EV(4, c);
     }
@@ -779,9 +839,9 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         }
         mbar_init(bar(x, B_WF), 1);
         mbar_init(bar(x, B_WSM_FULL), 4);
-        mbar_init(bar(x, B_S_FULL), 4);
+        mbar_init(bar(x, B_S_FULL), 8);    // state and output warpgroups, half the state each
         mbar_init(bar(x, B_V_FULL), 1);
-        mbar_init(bar(x, B_VSM_FULL), 4);
+        mbar_init(bar(x, B_VSM_FULL), 8);  // state (v_new^T, v~^T) and output (acc_s scaled)
         mbar_init(bar(x, B_S_UPD), 1);
         mbar_init(bar(x, B_D_FULL), 1);
         mbar_init(bar(x, B_O_EMPTY), 4);
@@ -822,8 +882,11 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         prep_role(x, p, u, tm);
     } else if (warp < 10) {
         state_role(x, p, u, tm);
-    } else {
+    } else if (warp < 14) {
         output_role(x, p, u, tm);
+    } else {
+        if ((threadIdx.x & 31) == 0) out_mma_role(x, u, tm);
+        __syncwarp();
     }
     DN_TRACE_EV(13, 1023);  // role done (per warp)
     tc_fence_before();
