@@ -167,8 +167,16 @@ namespace {
 // Sizes the backward takes: dk <= 128 (its shared-memory tiles), dv any.
 bool bwd_dims_ok(int dk, int dv) { return dim_ok(dk) && dk <= 128 && dim_ok(dv); }
 
-size_t bwd_workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv) {
+// The backward keeps the fp32 state every 64-token chunk starts from; where
+// the forward runs on the tensor cores, that forward's WY slots follow.
+size_t bwd_states_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv) {
     return (size_t)(tokens / dn::kChunk + n_seqs) * (size_t)Nv * (size_t)dk * (size_t)dv * 4u;
+}
+
+size_t bwd_workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype) {
+    size_t b = bwd_states_bytes(tokens, n_seqs, Nv, dk, dv);
+    if (use_tc(tokens, dk, dv, dtype, dn::kChunk)) b += dn::tc_workspace_bytes(tokens, n_seqs, Nv);
+    return b;
 }
 
 }  // namespace
@@ -178,7 +186,7 @@ DN_EXPORT size_t dn_chunk_bwd_workspace_bytes(int n_seqs, int B, int T, int Nk, 
     if (n_seqs <= 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0) return 0;
     if (dtype != DN_BF16 && dtype != DN_F32) return 0;
     if (!bwd_dims_ok(dk, dv)) return 0;
-    return bwd_workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv);
+    return bwd_workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv, dtype);
 }
 
 DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
@@ -205,7 +213,7 @@ DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
         if (ptr && !aligned16(ptr)) return DN_ERR_INVALID_ARG;
     if (!bwd_dims_ok(dk, dv)) return DN_ERR_UNSUPPORTED;
     if (n_seqs == 0) return DN_OK;
-    const size_t ws_need = bwd_workspace_bytes(tokens, n_seqs, Nv, dk, dv);
+    const size_t ws_need = bwd_workspace_bytes(tokens, n_seqs, Nv, dk, dv, dtype);
     if (!workspace || !aligned16(workspace) || workspace_bytes_ < ws_need) return DN_ERR_INVALID_ARG;
 
     dn::Params p{};
@@ -217,6 +225,8 @@ DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
     p.chunk = dn::kChunk;
     p.flags = flags;
     p.hs = static_cast<float *>(workspace);
+    if (use_tc(tokens, dk, dv, dtype, dn::kChunk))
+        p.ws = static_cast<uint8_t *>(workspace) + bwd_states_bytes(tokens, n_seqs, Nv, dk, dv);
     p.dout = d_o; p.dht = d_ht;
     p.dq = d_q; p.dkk = d_k; p.dvv = d_v; p.dbeta = d_beta; p.dg = d_g; p.dh0 = d_h0;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;

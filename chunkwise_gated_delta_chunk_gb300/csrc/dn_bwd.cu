@@ -1,4 +1,4 @@
-// Backward of the chunkwise gated delta rule forward (CUDA cores, fp32).
+// Backward of the chunkwise gated delta rule forward (CUDA cores, fp32 arithmetic).
 //
 // Sources: [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现"
 //                 §3.4 (the backward recomputes the chunk's WY quantities
@@ -32,8 +32,11 @@
 // and dg is the reverse prefix sum of dG over the chunk (G_i = sum_{j<=i} g_j).
 //
 // One CTA per (sequence, value head, 32-column value tile), as in the
-// CUDA-core forward.  The chunk-start states come from a forward pass of that
-// kernel (saved per 64-token chunk).  Every quantity above that sums over
+// CUDA-core forward.  The chunk-start states come from a forward pass at
+// chunk 64 that saves them: the tensor-core forward where it applies (bf16,
+// dk = 128, dv a multiple of 128; its states carry the bf16 rounding of its
+// MMA operands, like the pages' backward, which recomputes them with the
+// forward kernels), else the CUDA-core forward in fp32.  Every quantity above that sums over
 // value columns (dq, dk, dbeta, dg, and dA, dP through them) is linear in the
 // tile's columns, so each CTA adds its share to zero-initialised fp32 outputs
 // with atomics; dv and dh0 belong to one tile and are stored directly.
@@ -42,6 +45,7 @@
 
 #include "dn_internal.h"
 #include "dn_simt_common.cuh"
+#include "dn_tc.h"
 
 #ifdef DN_TRACE
 __device__ unsigned long long g_bwd_ph[64][16];
@@ -669,13 +673,17 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
         fill_zero<<<(unsigned)blocks, 256, 0, stream>>>(z);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    // forward pass at chunk 64, saving the chunk-start states
+    // forward pass at chunk 64 with no output, saving the chunk-start states:
+    // the tensor-core forward where it applies (its WY slots in p.ws), else
+    // the CUDA-core one
     Params f = p;
     f.o = nullptr;
     f.ht = nullptr;
     f.chunk = kChunk;
+    const bool tc = p.tokens > 0 && tc_supported(p.dk, p.dv, bf16);
+    if (tc && !p.ws) return cudaErrorInvalidValue;
     const char *fname = "";
-    if ((err = simt_launch(f, bf16, stream, &fname)) != cudaSuccess) return err;
+    if ((err = tc ? tc_launch(f, stream, &fname) : simt_launch(f, bf16, stream, &fname)) != cudaSuccess) return err;
     const size_t smem = bwd_smem_bytes(p.dk, bf16);
     const bool qkn = (p.flags & kQkL2Norm) != 0;
     const long long rows = p.tokens * p.Nk;  // q (and k) rows
@@ -688,8 +696,12 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
             l2norm_bwd_rows<__nv_bfloat16><<<nblk, 256, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), p.dq, p.dkk, rows,
                 p.dk);
-        *name = qkn ? "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
-                    : "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>";
+        if (tc)
+            *name = qkn ? "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
+                        : "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16>";
+        else
+            *name = qkn ? "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
+                        : "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>";
     } else {
         err = cudaFuncSetAttribute(simt_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;

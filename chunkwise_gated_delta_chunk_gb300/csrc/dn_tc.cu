@@ -427,8 +427,16 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 // key index 0 (row stride dv).
 // ---------------------------------------------------------------------------
 // acc_s = alpha_0 h0^T and SB[0] = bf16(h0^T), blocks [b0, b1).
+// Column of this lane's value column v in the saved state of chunk c (row
+// d = 0, rows dv apart), or null when the states are not saved.
+__device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, int v) {
+    if (!p.hs) return nullptr;
+    const long long slot = wy_slot(u.bos + (long long)c * C, u.n);
+    return p.hs + ((size_t)u.h * p.nslots + (size_t)slot) * DK * p.dv + u.v0 + v;
+}
+
 __device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, size_t hb, float alpha, int b0,
-                                                  int b1) {
+                                                  int b1, float *hsd) {
     uint32_t r[32], pk[16];
     for (int blk = b0; blk < b1; ++blk) {
         float f[32];
@@ -437,6 +445,14 @@ __device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, 
         for (int k = 0; k < 32; ++k) {
             f[k] = hp ? *hp : 0.f;
             if (hp) hp += p.dv;
+        }
+        if (hsd) {
+            float *dp = hsd + (size_t)(32 * blk) * p.dv;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                *dp = f[k];
+                dp += p.dv;
+            }
         }
 #pragma unroll
         for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
@@ -447,9 +463,10 @@ __device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, 
     }
 }
 
-// After DS(c): SB[(c+1) & 1] = bf16(acc_s), or for the last chunk ht = acc_s.
+// After DS(c): SB[(c+1) & 1] = bf16(acc_s) (and, with hsd, the fp32 state
+// chunk c + 1 starts from), or for the last chunk ht = acc_s.
 __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t lb, size_t hb, int c, bool last,
-                                                     int b0, int b1) {
+                                                     int b0, int b1, float *hsd) {
     uint32_t r[32], pk[16];
     for (int blk = b0; blk < b1; ++blk) {
         tmem_ld32(lb + TM_S + 32 * blk, r);
@@ -458,6 +475,14 @@ __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t l
 #pragma unroll
             for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
             tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
+            if (hsd) {
+                float *dp = hsd + (size_t)(32 * blk) * p.dv;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    *dp = __uint_as_float(r[k]);
+                    dp += p.dv;
+                }
+            }
         } else if (p.ht) {
             float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
 #pragma unroll
@@ -497,7 +522,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     if (u.nc > 0) {
         // blocks 2-3 of the initial state; then acc_s is ready for DS(0)
         if (!bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + 0), 0))) {
-            state_init_blocks(p, lb, hb, scal(x, 0)[SC_ALPHA], 2, 4);
+            state_init_blocks(p, lb, hb, scal(x, 0)[SC_ALPHA], 2, 4, hs_col(p, u, 0, v));
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
@@ -513,7 +538,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
         DN_TRACE_EV(4, c);
         tc_fence_after();
-        state_convert_blocks(p, lb, hb, c, last, 2, 4);
+        state_convert_blocks(p, lb, hb, c, last, 2, 4, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
@@ -532,19 +557,23 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         const long long t0 = u.bos + (long long)c * C;
         const int L = (int)min((long long)C, u.eos - t0);
         // the chunk's output column v as packed bf16 pairs (tokens 2k, 2k + 1)
+        // (with no o, as in the backward's state pass, only the hand-off)
         uint32_t ob[32];
+        if (p.o) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t ra[32];
-            tmem_ld32(lb + TM_O + 32 * hf, ra);
-            tmem_wait_ld_dep(ra);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t ra[32];
+                tmem_ld32(lb + TM_O + 32 * hf, ra);
+                tmem_wait_ld_dep(ra);
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                ob[16 * hf + k] = pack_bf16(__uint_as_float(ra[2 * k]), __uint_as_float(ra[2 * k + 1]));
+                for (int k = 0; k < 16; ++k)
+                    ob[16 * hf + k] = pack_bf16(__uint_as_float(ra[2 * k]), __uint_as_float(ra[2 * k + 1]));
+            }
         }
         tc_fence_before();
         warp_arrive(bar(x, B_O_EMPTY));
         DN_TRACE_EV(0, c);
+        if (!p.o) continue;
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
@@ -612,10 +641,12 @@ __device__ void out_mma_role(const Ctx x, const Unit u, uint32_t tm) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool issue_w_mma(const Ctx &x, uint32_t tm, int c) {
     const bool ok = wait_tiles(x, c, 0);
+    DN_TRACE_EV(8, c);
     if (ok) {
         tc_fence_after();
         issue_w(x, tm, c);
         mma_commit(bar(x, B_WF));
+        DN_TRACE_EV(9, c);
     }
     return ok;
 }
@@ -628,6 +659,7 @@ __device__ __forceinline__ bool issue_w_mma(const Ctx &x, uint32_t tm, int c) {
 __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     const int s = c % NS;
     if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return false;
+    DN_TRACE_EV(10, c);
     const float *sc = scal(x, s);
     const int tid = threadIdx.x - 64;
 #pragma unroll
@@ -647,6 +679,7 @@ __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     }
     fence_proxy_async_smem();
     warp_arrive(bar(x, B_QS + s));
+    DN_TRACE_EV(12, c);
     return true;
 }
 
@@ -658,9 +691,9 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
     int loaded = min(u.nc, 2) - 1;  // last chunk whose T' copy was issued
     bool lok = true;                // the leader's own waits
     if (leader && u.nc > 0) lok = issue_w_mma(x, tm, 0);
-    if (u.nc > 0 && !scale_q(x, 0)) return;
     for (int c = 0; c < u.nc; ++c) {
         if (!wwait(x, bar(x, B_WF), c & 1) || !__all_sync(0xffffffffu, lok)) break;
+        DN_TRACE_EV(11, c);
         // W of chunk c is done with its T' buffer: it takes chunk c + 2's
         if (leader && c + 2 < u.nc) {
             load_ring(x, p, u, 0, c + 2);
@@ -696,7 +729,9 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
         // the next chunk's W, once all four warps have read acc_w (their
         // WSM arrivals)
         if (leader && c + 1 < u.nc) lok = wait(x, bar(x, B_WSM_FULL), c & 1) && issue_w_mma(x, tm, c + 1);
-        if (c + 1 < u.nc && !scale_q(x, c + 1)) break;
+        // this chunk's Q rows, which only O(c) reads (after DS(c)): off the
+        // path from the stage's arrival to -W^T
+        if (!scale_q(x, c)) break;
     }
     if (leader) {
         // W completes before tensor memory is freed; the last T' copies it
@@ -725,7 +760,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
     // initial state: acc_s = alpha_0 h0^T, SB = bf16(h0^T) (blocks 0-1 here,
     // 2-3 in the output warpgroup)
     if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
-    state_init_blocks(p, lb, sbase, scal(x, 0)[SC_ALPHA], 0, 2);
+    state_init_blocks(p, lb, sbase, scal(x, 0)[SC_ALPHA], 0, 2, hs_col(p, u, 0, v));
     tmem_wait_st();
     tc_fence_before();
     warp_arrive(bar(x, B_S_FULL));
@@ -791,7 +826,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         DN_TRACE_EV(2, c);
         tc_fence_after();
-        state_convert_blocks(p, lb, sbase, c, last, 0, 2);
+        state_convert_blocks(p, lb, sbase, c, last, 0, 2, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();

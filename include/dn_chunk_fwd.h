@@ -217,7 +217,11 @@ dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  *   d_o        [B, T, Nv, dv]  dtype     gradient of o (required)
  *   d_ht       [N, Nv, dk, dv] float32   gradient of ht; NULL means zero.
  * The other arguments are those of dn_chunk_fwd (the chunk length is 64).
- * All arithmetic is fp32 on CUDA cores.  dk must be at most 128
+ * The reverse walk is fp32 arithmetic on CUDA cores.  The chunk-start states
+ * it reads come from a forward pass with no output: for bf16 with dk = 128
+ * and dv a multiple of 128, the tensor-core forward (bf16 MMA operands, fp32
+ * state), as the [WY] §3.4 backward recomputes them with the forward
+ * kernels; otherwise the fp32 CUDA-core forward.  dk must be at most 128
  * (DN_ERR_UNSUPPORTED otherwise).  With DN_QK_L2NORM the forward it
  * differentiates normalises q and k in the kernels, and d_q, d_k are the
  * gradients of the raw rows (through the normalisation; a fourth launch maps
@@ -227,9 +231,10 @@ dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
  * and d_g may differ from run to run.
  *
  * workspace: at least dn_chunk_bwd_workspace_bytes() bytes, 16-byte
- * aligned, owned by the caller (it holds the state at the start of every
- * 64-token chunk).  Launches a zero fill, the CUDA-core forward (saving those
- * states) and the backward kernel.  Errors as for dn_chunk_fwd.
+ * aligned, owned by the caller (it holds the fp32 state at the start of every
+ * 64-token chunk, then, on the tensor-core forward, that forward's
+ * workspace).  Launches a zero fill, the forward (one or two launches,
+ * saving those states) and the backward kernel.  Errors as for dn_chunk_fwd.
  */
 dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,
@@ -244,7 +249,10 @@ dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
 /*
  * dn_chunk_bwd_workspace_bytes -- bytes of workspace dn_chunk_bwd needs:
  * (floor(B*T / 64) + n_seqs) * Nv * dk * dv * 4 (one fp32 state per chunk and
- * value head).  0 for sizes dn_chunk_bwd would reject.  Host-only.
+ * value head), plus dn_chunk_fwd_workspace_bytes() of the same sizes at
+ * chunk 64 where the backward's forward pass runs on the tensor cores (bf16,
+ * dk = 128, dv a multiple of 128).  0 for sizes dn_chunk_bwd would reject.
+ * Host-only.
  */
 size_t dn_chunk_bwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
                                     dn_dtype dtype);

@@ -189,8 +189,12 @@ def test_bwd_host_validation(clib, over, code):
 
 
 def test_bwd_workspace_bytes(clib):
-    """One fp32 dk x dv state per (floor(tokens/64) + N) x Nv; 0 for rejected sizes."""
+    """One fp32 dk x dv state per (floor(tokens/64) + N) x Nv, plus the forward's
+    WY slots where that forward runs on the tensor cores; 0 for rejected sizes."""
     ws = clib.dn_chunk_bwd_workspace_bytes
-    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16) == (4 * 2048 // 64 + 4) * 16 * 128 * 128 * 4
+    slots = 4 * 2048 // 64 + 4
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16) == slots * 16 * (128 * 128 * 4 + 25088)
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_F32) == slots * 16 * 128 * 128 * 4
+    assert ws(4, 4, 2048, 16, 16, 64, 128, dn.DN_BF16) == slots * 16 * 64 * 128 * 4
     assert ws(3, 1, 300, 2, 8, 64, 32, dn.DN_F32) == (300 // 64 + 3) * 8 * 64 * 32 * 4
     assert ws(1, 1, 64, 1, 1, 256, 64, dn.DN_BF16) == 0

@@ -4,10 +4,16 @@ dg of the gated form) against the fp64 oracle's reverse pass, through the C
 ABI.  The oracle's gradient is itself pinned by finite differences of the
 forward definition (tests/test_oracle_pins.py).
 
-Tolerance.  The kernels compute in fp32 from the same (exactly upcast) inputs
-the oracle sees, so the only error is fp32 rounding through the chunk algebra
+Tolerance.  The reverse walk computes in fp32 from the same (exactly upcast)
+inputs the oracle sees.  Where the chunk-start states come from the fp32
+CUDA-core forward, the only error is fp32 rounding through the chunk algebra
 and the cross-tile atomic sums: rel-L2 <= 1e-4 per gradient tensor (the fp32
-forward bound) and max-abs <= 1e-3 * max(1, max |reference|).
+forward bound) and max-abs <= 1e-3 * max(1, max |reference|).  For bf16 with
+dk = 128 and dv a multiple of 128 the states come from the tensor-core
+forward, as the page's backward recomputes them with its forward kernels
+(§3.4); they carry that forward's bf16 operand rounding, so these cases take
+the forward's bf16 bound, rel-L2 <= 5e-3, with max-abs <= 2e-2 * max(1, max
+|reference|) (the page's own gradient checks allow 0.006-0.008, §6).
 """
 import numpy as np
 import pytest
@@ -43,6 +49,12 @@ def run(inp):
     return out
 
 
+def tc_states(inp):
+    """True where the backward's forward pass runs on the tensor cores."""
+    dk, dv = inp["q"].shape[-1], inp["v"].shape[-1]
+    return inp["q"].dtype == torch.bfloat16 and dk == 128 and dv % 128 == 0
+
+
 def check(inp, out, groups=None, label=""):
     ref = oracle.recurrent_bwd(inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], inp["h0"],
                                inp["cu_seqlens"], inp["scale"], do=inp["do"], dht=inp["dht"],
@@ -62,8 +74,10 @@ def check(inp, out, groups=None, label=""):
         rel = float(np.linalg.norm(err) / max(np.linalg.norm(w), 1e-30))
         mx = float(np.abs(err).max())
         res[name] = (mx, rel)
-        assert rel <= 1e-4, (label, name, mx, rel)
-        assert mx <= 1e-3 * max(1.0, float(np.abs(w).max())), (label, name, mx, rel)
+        rel_tol, max_tol = (5e-3, 2e-2) if tc_states(inp) else (1e-4, 1e-3)
+        assert rel <= rel_tol, (label, name, mx, rel)
+        assert mx <= max_tol * max(1.0, float(np.abs(w).max())), (label, name, mx, rel)
+    print(label, {k: "%.1e / %.1e" % v for k, v in res.items()})
     return res
 
 
@@ -72,8 +86,11 @@ def check(inp, out, groups=None, label=""):
                                          (torch.bfloat16, 64, 256), (torch.bfloat16, 128, 32),
                                          (torch.float32, 64, 64), (torch.float32, 16, 32)])
 def test_dims(lib, dtype, dk, dv):
+    import chunkwise_gated_delta_chunk_gb300 as dn
     inp = inputs(dk=dk, dv=dv, dtype=dtype, seed=800 + dk + dv)
-    check(inp, run(inp), label="bwd %s %dx%d" % (dtype, dk, dv))
+    out = run(inp)
+    assert ("tc_fwd" in dn.dn_last_kernel()) == tc_states(inp), dn.dn_last_kernel()
+    check(inp, out, label="bwd %s %dx%d" % (dtype, dk, dv))
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 130])
@@ -82,13 +99,14 @@ def test_lengths(lib, T):
     check(inp, run(inp), label="bwd T=%d" % T)
 
 
-@pytest.mark.parametrize("nv_per_nk", [1, 4])
-def test_varlen_gqa(lib, nv_per_nk):
+@pytest.mark.parametrize("nv_per_nk,d", [(1, 64), (4, 64), (2, 128)])
+def test_varlen_gqa(lib, nv_per_nk, d):
     """Packed sequences (empty, length 1, one chunk, ragged) with value heads
-    sharing a key head: dq and dk sum over those heads."""
-    inp = inputs(B=1, Nk=2, Nv=2 * nv_per_nk, dk=64, dv=64, lengths=[1, 0, 64, 65, 130, 3],
-                 seed=840 + nv_per_nk)
-    check(inp, run(inp), label="bwd varlen r=%d" % nv_per_nk)
+    sharing a key head: dq and dk sum over those heads.  d = 128 takes the
+    tensor-core forward for the states (its slots follow the packed layout)."""
+    inp = inputs(B=1, Nk=2, Nv=2 * nv_per_nk, dk=d, dv=d, lengths=[1, 0, 64, 65, 130, 3],
+                 seed=840 + nv_per_nk + d)
+    check(inp, run(inp), label="bwd varlen r=%d d=%d" % (nv_per_nk, d))
 
 
 @pytest.mark.parametrize("gate,h0,dht", [(None, False, False), (None, True, True),
