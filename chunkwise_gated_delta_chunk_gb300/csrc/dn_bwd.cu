@@ -108,7 +108,381 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-template <typename Tin>
+// ---- TF32 tensor-core tiles for the products of the reverse walk ------------
+// Used where the chunk-start states come from the tensor-core forward (bf16,
+// dk = 128, dv a multiple of 128): every product of a phase below is one
+// m16n8k8 mma.sync chain with fp32 accumulation; fp32 operands are rounded to
+// TF32 (bf16 inputs are exact in it).  Fragments, lane = 4 g + t:
+//   A (16 x 8, m x k): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
+//   B (8 x 8,  k x n): b0 (t, g), b1 (t + 4, g)
+//   C (16 x 8, m x n): c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1)
+namespace tf32 {
+__device__ __forceinline__ uint32_t cvt(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+// a bf16 value is exact in tf32: its bits, widened
+__device__ __forceinline__ uint32_t bf(__nv_bfloat16 x) { return (uint32_t)__bfloat16_as_ushort(x) << 16; }
+__device__ __forceinline__ float f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                    uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// sum over the four lanes t of a fragment row (lanes 4 g .. 4 g + 3)
+__device__ __forceinline__ float row_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+}  // namespace tf32
+
+// The chunk's shared-memory operands, as the tensor-core phases see them.
+struct BwdChunk {
+    const __nv_bfloat16 *K, *Q;          // [C][ldkq]
+    float *St, *dSt;                     // [BV][SLD]
+    float *M0, *M1, *M2;                 // [C][LDC]
+    float *U, *dO, *KS, *Vn, *dV, *KdS;  // [C][LDV]
+    const float *G, *EG, *Dec, *Beta, *RK, *RQ;
+    float *QSdO, *DBU, *DGam, *E, *RowE, *DBA;
+    int ldkq, SLD, L;
+    float scale;
+};
+
+// K S, Q S, K dS' (M = 64 rows i, N = 32 columns, K = dk = 128) and from
+// them KS, KdS, U = V - e^G KS and the row sums (Q S . dO) into QSdO
+// (zeroed before).  Warp w: row tile w % 4, column tiles 2 (w / 4) + {0, 1}.
+__device__ __forceinline__ void mma_ks(const BwdChunk &s, int warp, int lane) {
+    const int g = lane >> 2, t = lane & 3, nh = warp >> 2;
+    const int r0 = 16 * (warp & 3) + g;
+    float aks[2][4] = {}, aqs[2][4] = {}, akd[2][4] = {};
+#pragma unroll 4
+    for (int ks = 0; ks < 16; ++ks) {
+        const int d = 8 * ks + t;
+        const uint32_t k0 = tf32::bf(s.K[r0 * s.ldkq + d]), k1 = tf32::bf(s.K[(r0 + 8) * s.ldkq + d]),
+                       k2 = tf32::bf(s.K[r0 * s.ldkq + d + 4]), k3 = tf32::bf(s.K[(r0 + 8) * s.ldkq + d + 4]);
+        const uint32_t q0 = tf32::bf(s.Q[r0 * s.ldkq + d]), q1 = tf32::bf(s.Q[(r0 + 8) * s.ldkq + d]),
+                       q2 = tf32::bf(s.Q[r0 * s.ldkq + d + 4]), q3 = tf32::bf(s.Q[(r0 + 8) * s.ldkq + d + 4]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int cc = 16 * nh + 8 * n + g;
+            const uint32_t sb0 = tf32::cvt(s.St[cc * s.SLD + d]), sb1 = tf32::cvt(s.St[cc * s.SLD + d + 4]);
+            const uint32_t db0 = tf32::cvt(s.dSt[cc * s.SLD + d]), db1 = tf32::cvt(s.dSt[cc * s.SLD + d + 4]);
+            tf32::mma(aks[n], k0, k1, k2, k3, sb0, sb1);
+            tf32::mma(aqs[n], q0, q1, q2, q3, sb0, sb1);
+            tf32::mma(akd[n], k0, k1, k2, k3, db0, db1);
+        }
+    }
+    float qd[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = r0 + 8 * (e >> 1), cc = 16 * nh + 8 * n + 2 * t + (e & 1);
+            const float rk = s.RK[i], ksv = rk * aks[n][e];
+            s.KS[i * LDV + cc] = ksv;
+            s.KdS[i * LDV + cc] = rk * akd[n][e];
+            s.U[i * LDV + cc] = i < s.L ? s.U[i * LDV + cc] - s.EG[i] * ksv : 0.0f;
+            qd[e >> 1] = fmaf(s.RQ[i] * aqs[n][e], s.dO[i * LDV + cc], qd[e >> 1]);
+        }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const float v = tf32::row_sum(qd[hf]);
+        if (t == 0) atomicAdd(s.QSdO + r0 + 8 * hf, v);
+    }
+}
+
+// Vn = T diag(beta) U (T lower triangular: column tiles up to the diagonal).
+__device__ __forceinline__ void mma_vn(const BwdChunk &s, int warp, int lane) {
+    const int g = lane >> 2, t = lane & 3, nh = warp >> 2, mt = warp & 3;
+    const int r0 = 16 * mt + g;
+    float acc[2][4] = {};
+    for (int ks = 0; ks < 2 * mt + 2; ++ks) {
+        const int j = 8 * ks + t;
+        const uint32_t a0 = tf32::cvt(s.M1[r0 * LDC + j]), a1 = tf32::cvt(s.M1[(r0 + 8) * LDC + j]),
+                       a2 = tf32::cvt(s.M1[r0 * LDC + j + 4]), a3 = tf32::cvt(s.M1[(r0 + 8) * LDC + j + 4]);
+        const float bj0 = s.Beta[j], bj1 = s.Beta[j + 4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int cc = 16 * nh + 8 * n + g;
+            tf32::mma(acc[n], a0, a1, a2, a3, tf32::cvt(bj0 * s.U[j * LDV + cc]),
+                      tf32::cvt(bj1 * s.U[(j + 4) * LDV + cc]));
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = r0 + 8 * (e >> 1), cc = 16 * nh + 8 * n + 2 * t + (e & 1);
+            s.Vn[i * LDV + cc] = i < s.L ? acc[n][e] : 0.0f;
+        }
+}
+
+// dVn = diag(dec) KdS + P^T dO (P lower: row tiles from the diagonal down)
+// and e_i = dec_i (KdS_i . Vn_i) into E (zeroed before).
+__device__ __forceinline__ void mma_dvn(const BwdChunk &s, int warp, int lane) {
+    const int g = lane >> 2, t = lane & 3, nh = warp >> 2, mt = warp & 3;
+    const int r0 = 16 * mt + g;
+    float acc[2][4];
+    float part[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = r0 + 8 * (e >> 1), cc = 16 * nh + 8 * n + 2 * t + (e & 1);
+            const float kd = s.KdS[i * LDV + cc];
+            acc[n][e] = s.Dec[i] * kd;
+            part[e >> 1] = fmaf(kd, s.Vn[i * LDV + cc], part[e >> 1]);
+        }
+    for (int ks = 2 * mt; ks < 8; ++ks) {
+        const int j = 8 * ks + t;
+        const uint32_t a0 = tf32::cvt(s.M2[j * LDC + r0]), a1 = tf32::cvt(s.M2[j * LDC + r0 + 8]),
+                       a2 = tf32::cvt(s.M2[(j + 4) * LDC + r0]), a3 = tf32::cvt(s.M2[(j + 4) * LDC + r0 + 8]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int cc = 16 * nh + 8 * n + g;
+            tf32::mma(acc[n], a0, a1, a2, a3, tf32::cvt(s.dO[j * LDV + cc]), tf32::cvt(s.dO[(j + 4) * LDV + cc]));
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = r0 + 8 * (e >> 1), cc = 16 * nh + 8 * n + 2 * t + (e & 1);
+            s.dV[i * LDV + cc] = i < s.L ? acc[n][e] : 0.0f;
+        }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const float v = tf32::row_sum(part[hf]);
+        if (t == 0) atomicAdd(s.E + r0 + 8 * hf, s.Dec[r0 + 8 * hf] * v);
+    }
+}
+
+// dR = T^T dVn, written over dVn (every warp reads dVn before any writes);
+// dv = diag(beta) dR to global memory; row sums dR . U into DBU (zeroed
+// before) and -beta (dR . KS) into DGam (holding scale (Q S . dO) before).
+// Called by every thread of the CTA (it holds a barrier).  dv0: dv of the
+// chunk's first row at the tile's first column; rows dvs apart.
+__device__ __forceinline__ void mma_dr(const BwdChunk &s, int warp, int lane, float *dv0, long long dvs) {
+    const int g = lane >> 2, t = lane & 3, nh = warp >> 2, mt = warp & 3;
+    const int r0 = 16 * mt + g;
+    float acc[2][4] = {};
+    for (int ks = 2 * mt; ks < 8; ++ks) {
+        const int j = 8 * ks + t;
+        const uint32_t a0 = tf32::cvt(s.M1[j * LDC + r0]), a1 = tf32::cvt(s.M1[j * LDC + r0 + 8]),
+                       a2 = tf32::cvt(s.M1[(j + 4) * LDC + r0]), a3 = tf32::cvt(s.M1[(j + 4) * LDC + r0 + 8]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int cc = 16 * nh + 8 * n + g;
+            tf32::mma(acc[n], a0, a1, a2, a3, tf32::cvt(s.dV[j * LDV + cc]), tf32::cvt(s.dV[(j + 4) * LDV + cc]));
+        }
+    }
+    __syncthreads();  // every warp has read dVn
+    float bu[2] = {0.0f, 0.0f}, bk[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = r0 + 8 * hf, cc = 16 * nh + 8 * n + 2 * t;
+            const float d0 = i < s.L ? acc[n][2 * hf] : 0.0f, d1 = i < s.L ? acc[n][2 * hf + 1] : 0.0f;
+            s.dV[i * LDV + cc] = d0;
+            s.dV[i * LDV + cc + 1] = d1;
+            if (i < s.L)
+                *reinterpret_cast<float2 *>(dv0 + i * dvs + cc) = make_float2(s.Beta[i] * d0, s.Beta[i] * d1);
+            bu[hf] = fmaf(d0, s.U[i * LDV + cc], fmaf(d1, s.U[i * LDV + cc + 1], bu[hf]));
+            bk[hf] = fmaf(d0, s.KS[i * LDV + cc], fmaf(d1, s.KS[i * LDV + cc + 1], bk[hf]));
+        }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const float u = tf32::row_sum(bu[hf]), k = tf32::row_sum(bk[hf]);
+        if (t == 0) {
+            const int i = r0 + 8 * hf;
+            atomicAdd(s.DBU + i, u);
+            atomicAdd(s.DGam + i, -s.Beta[i] * k);
+        }
+    }
+}
+
+// Of the tile (mt, nt) of the lower band (nt <= 2 mt + 1) numbered k in
+// row-tile order: k = mt (mt + 1) + nt.
+__device__ __forceinline__ int band_mt(int k) { return k < 2 ? 0 : (k < 6 ? 1 : (k < 12 ? 2 : 3)); }
+
+// dA = dR Vn^T, dP = dO Vn^T over the band of 16 x 8 tiles that holds j <= i
+// (20 tiles, M = 64, N = 64, K = 32), then per element (j <= i < L)
+//   M_ij = -beta_i D_ij dA_ij,  WP_ij = scale D_ij dP_ij,
+//   E_ij = beta_i dA_ij A'_ij + dP_ij P_ij   (A' = -(K K^T . D), dA_ii = 0)
+// over M0, M1, M2 (zero elsewhere), with row sums of E into RowE and of
+// dA . A' into DBA (both zeroed before).
+__device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int tid) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int k = warp; k < 20; k += 8) {
+        const int mt = band_mt(k), nt = k - mt * (mt + 1);
+        const int r0 = 16 * mt + g, jb = 8 * nt + g;
+        float da[4] = {}, dp[4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int cc = 8 * ks + t;
+            const uint32_t b0 = tf32::cvt(s.Vn[jb * LDV + cc]), b1 = tf32::cvt(s.Vn[jb * LDV + cc + 4]);
+            tf32::mma(da, tf32::cvt(s.dV[r0 * LDV + cc]), tf32::cvt(s.dV[(r0 + 8) * LDV + cc]),
+                      tf32::cvt(s.dV[r0 * LDV + cc + 4]), tf32::cvt(s.dV[(r0 + 8) * LDV + cc + 4]), b0, b1);
+            tf32::mma(dp, tf32::cvt(s.dO[r0 * LDV + cc]), tf32::cvt(s.dO[(r0 + 8) * LDV + cc]),
+                      tf32::cvt(s.dO[r0 * LDV + cc + 4]), tf32::cvt(s.dO[(r0 + 8) * LDV + cc + 4]), b0, b1);
+        }
+        float rowe[2] = {0.0f, 0.0f}, dba[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = r0 + 8 * (e >> 1), j = 8 * nt + 2 * t + (e & 1);
+            float m = 0.0f, wp = 0.0f, ee = 0.0f;
+            if (i < s.L && j <= i) {
+                const float dav = j == i ? 0.0f : da[e];
+                const float ap = s.M0[i * LDC + j], pp = s.M2[i * LDC + j];
+                const float D = expf(s.G[i] - s.G[j]);
+                ee = dav * s.Beta[i] * ap + dp[e] * pp;
+                dba[e >> 1] = fmaf(dav, ap, dba[e >> 1]);
+                m = -s.Beta[i] * D * dav;
+                wp = s.scale * D * dp[e];
+                rowe[e >> 1] += ee;
+            }
+            s.M0[i * LDC + j] = m;
+            s.M1[i * LDC + j] = wp;
+            s.M2[i * LDC + j] = ee;
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const float re = tf32::row_sum(rowe[hf]), db = tf32::row_sum(dba[hf]);
+            if (t == 0) {
+                atomicAdd(s.RowE + r0 + 8 * hf, re);
+                atomicAdd(s.DBA + r0 + 8 * hf, db);
+            }
+        }
+    }
+    // the tiles right of the band are zero
+    for (int idx = tid; idx < C * C; idx += NT) {
+        const int i = idx >> 6, j = idx & (C - 1);
+        if ((j >> 3) > 2 * (i >> 4) + 1) s.M0[i * LDC + j] = s.M1[i * LDC + j] = s.M2[i * LDC + j] = 0.0f;
+    }
+}
+
+// dq, dk of the chunk's rows (M = 64 rows i, N = dk = 128 columns d):
+//   dq_i = scale e^{G_i} S dO_i + sum_j WP_ij rk_j k_j
+//   dk_i = dec_i dS' Vn_i - beta_i e^{G_i} S dR_i + sum_j (M_ij + M_ji) rk_j k_j
+//          + sum_j WP_ji rq_j q_j
+// added into dq0 / dk0 (the chunk's first row, rows dqs apart) with fp32
+// atomics.  Warp w: row tile w % 4, columns 64 (w / 4) .. + 63.
+__device__ __forceinline__ void mma_dqdk(const BwdChunk &s, int warp, int lane, float *dq0, float *dk0,
+                                         long long dqs) {
+    const int g = lane >> 2, t = lane & 3, mt = warp & 3, nq = warp >> 2;
+    const int i0 = 16 * mt + g, i1 = i0 + 8;
+    float gq[8][4] = {}, gk[8][4] = {};
+    {
+        const float fq0 = s.scale * s.EG[i0], fq1 = s.scale * s.EG[i1];
+        const float fd0 = s.Dec[i0], fd1 = s.Dec[i1];
+        const float fr0 = -s.Beta[i0] * s.EG[i0], fr1 = -s.Beta[i1] * s.EG[i1];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int cc = 8 * ks + t;
+            const uint32_t o0 = tf32::cvt(fq0 * s.dO[i0 * LDV + cc]), o1 = tf32::cvt(fq1 * s.dO[i1 * LDV + cc]),
+                           o2 = tf32::cvt(fq0 * s.dO[i0 * LDV + cc + 4]), o3 = tf32::cvt(fq1 * s.dO[i1 * LDV + cc + 4]);
+            const uint32_t v0 = tf32::cvt(fd0 * s.Vn[i0 * LDV + cc]), v1 = tf32::cvt(fd1 * s.Vn[i1 * LDV + cc]),
+                           v2 = tf32::cvt(fd0 * s.Vn[i0 * LDV + cc + 4]), v3 = tf32::cvt(fd1 * s.Vn[i1 * LDV + cc + 4]);
+            const uint32_t r0 = tf32::cvt(fr0 * s.dV[i0 * LDV + cc]), r1 = tf32::cvt(fr1 * s.dV[i1 * LDV + cc]),
+                           r2 = tf32::cvt(fr0 * s.dV[i0 * LDV + cc + 4]), r3 = tf32::cvt(fr1 * s.dV[i1 * LDV + cc + 4]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int d = 64 * nq + 8 * nt + g;
+                const uint32_t sb0 = tf32::cvt(s.St[cc * s.SLD + d]), sb1 = tf32::cvt(s.St[(cc + 4) * s.SLD + d]);
+                const uint32_t db0 = tf32::cvt(s.dSt[cc * s.SLD + d]), db1 = tf32::cvt(s.dSt[(cc + 4) * s.SLD + d]);
+                tf32::mma(gq[nt], o0, o1, o2, o3, sb0, sb1);
+                tf32::mma(gk[nt], v0, v1, v2, v3, db0, db1);
+                tf32::mma(gk[nt], r0, r1, r2, r3, sb0, sb1);
+            }
+        }
+    }
+    for (int ks = 0; ks < 8; ++ks) {
+        const int j = 8 * ks + t;
+        const float rk0 = s.RK[j], rk1 = s.RK[j + 4], rq0 = s.RQ[j], rq1 = s.RQ[j + 4];
+        const bool lower = ks <= 2 * mt + 1, upper = ks >= 2 * mt;  // WP_ij, WP_ji can be nonzero
+        const uint32_t w0 = tf32::cvt(rk0 * s.M1[i0 * LDC + j]), w1 = tf32::cvt(rk0 * s.M1[i1 * LDC + j]),
+                       w2 = tf32::cvt(rk1 * s.M1[i0 * LDC + j + 4]), w3 = tf32::cvt(rk1 * s.M1[i1 * LDC + j + 4]);
+        const uint32_t m0 = tf32::cvt(rk0 * (s.M0[i0 * LDC + j] + s.M0[j * LDC + i0])),
+                       m1 = tf32::cvt(rk0 * (s.M0[i1 * LDC + j] + s.M0[j * LDC + i1])),
+                       m2 = tf32::cvt(rk1 * (s.M0[i0 * LDC + j + 4] + s.M0[(j + 4) * LDC + i0])),
+                       m3 = tf32::cvt(rk1 * (s.M0[i1 * LDC + j + 4] + s.M0[(j + 4) * LDC + i1]));
+        const uint32_t x0 = tf32::cvt(rq0 * s.M1[j * LDC + i0]), x1 = tf32::cvt(rq0 * s.M1[j * LDC + i1]),
+                       x2 = tf32::cvt(rq1 * s.M1[(j + 4) * LDC + i0]), x3 = tf32::cvt(rq1 * s.M1[(j + 4) * LDC + i1]);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int d = 64 * nq + 8 * nt + g;
+            const uint32_t kb0 = tf32::bf(s.K[j * s.ldkq + d]), kb1 = tf32::bf(s.K[(j + 4) * s.ldkq + d]);
+            if (lower) tf32::mma(gq[nt], w0, w1, w2, w3, kb0, kb1);
+            tf32::mma(gk[nt], m0, m1, m2, m3, kb0, kb1);
+            if (upper) tf32::mma(gk[nt], x0, x1, x2, x3, tf32::bf(s.Q[j * s.ldkq + d]), tf32::bf(s.Q[(j + 4) * s.ldkq + d]));
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = hf ? i1 : i0;
+            if (i >= s.L) continue;
+            const int d = 64 * nq + 8 * nt + 2 * t;
+            atomicAdd(reinterpret_cast<float2 *>(dq0 + i * dqs + d), make_float2(gq[nt][2 * hf], gq[nt][2 * hf + 1]));
+            atomicAdd(reinterpret_cast<float2 *>(dk0 + i * dqs + d), make_float2(gk[nt][2 * hf], gk[nt][2 * hf + 1]));
+        }
+}
+
+// dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR, in
+// place over dS'^T (M = dk = 128 rows d, N = 32 columns, K = the chunk's
+// rows).  Warp w: rows 16 w .. 16 w + 15, every column.
+__device__ __forceinline__ void mma_ds(const BwdChunk &s, int warp, int lane, float eGL) {
+    const int g = lane >> 2, t = lane & 3;
+    const int d0 = 16 * warp + g, d1 = d0 + 8;
+    float acc[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        const int cc = 8 * n + 2 * t;
+        acc[n][0] = eGL * s.dSt[cc * s.SLD + d0];
+        acc[n][1] = eGL * s.dSt[(cc + 1) * s.SLD + d0];
+        acc[n][2] = eGL * s.dSt[cc * s.SLD + d1];
+        acc[n][3] = eGL * s.dSt[(cc + 1) * s.SLD + d1];
+    }
+    const int kend = (s.L + 7) >> 3;
+    for (int ks = 0; ks < kend; ++ks) {
+        const int i = 8 * ks + t;
+        const float fq0 = s.scale * s.EG[i] * s.RQ[i], fq1 = s.scale * s.EG[i + 4] * s.RQ[i + 4];
+        const float fk0 = -s.Beta[i] * s.EG[i] * s.RK[i], fk1 = -s.Beta[i + 4] * s.EG[i + 4] * s.RK[i + 4];
+        const uint32_t q0 = tf32::cvt(fq0 * tf32::f(s.Q[i * s.ldkq + d0])),
+                       q1 = tf32::cvt(fq0 * tf32::f(s.Q[i * s.ldkq + d1])),
+                       q2 = tf32::cvt(fq1 * tf32::f(s.Q[(i + 4) * s.ldkq + d0])),
+                       q3 = tf32::cvt(fq1 * tf32::f(s.Q[(i + 4) * s.ldkq + d1]));
+        const uint32_t k0 = tf32::cvt(fk0 * tf32::f(s.K[i * s.ldkq + d0])),
+                       k1 = tf32::cvt(fk0 * tf32::f(s.K[i * s.ldkq + d1])),
+                       k2 = tf32::cvt(fk1 * tf32::f(s.K[(i + 4) * s.ldkq + d0])),
+                       k3 = tf32::cvt(fk1 * tf32::f(s.K[(i + 4) * s.ldkq + d1]));
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+            const int cc = 8 * n + g;
+            tf32::mma(acc[n], q0, q1, q2, q3, tf32::cvt(s.dO[i * LDV + cc]), tf32::cvt(s.dO[(i + 4) * LDV + cc]));
+            tf32::mma(acc[n], k0, k1, k2, k3, tf32::cvt(s.dV[i * LDV + cc]), tf32::cvt(s.dV[(i + 4) * LDV + cc]));
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+        const int cc = 8 * n + 2 * t;
+        s.dSt[cc * s.SLD + d0] = acc[n][0];
+        s.dSt[(cc + 1) * s.SLD + d0] = acc[n][1];
+        s.dSt[cc * s.SLD + d1] = acc[n][2];
+        s.dSt[(cc + 1) * s.SLD + d1] = acc[n][3];
+    }
+}
+
+// MMA: the products run as TF32 tensor-core tiles (bf16 inputs, dk = 128,
+// dv a multiple of BV; the states come from the tensor-core forward); else
+// as fp32 FMAs.
+template <typename Tin, bool MMA>
 __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
@@ -149,6 +523,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     float *sGL = sc + R_COUNT * C;      // [0]: G_L
     float *sRed = sGL + 4;              // [8]: per-warp partial <S, dS'>
     const int ldkq = kq_ld<Tin>(dk);
+    BwdChunk bc{reinterpret_cast<const __nv_bfloat16 *>(sK), reinterpret_cast<const __nv_bfloat16 *>(sQ),
+                sSt, sdSt, sM0, sM1, sM2, sU, sdO, sKS, sVn, sdV, sKdS,
+                sG, sEG, sDec, sBeta, sRK, sRQ, sQSdO, sDBU, sDGam, sE, sRowE, sDBA,
+                ldkq, SLD, 0, p.scale};
 
     const Tin *q = static_cast<const Tin *>(p.q);
     const Tin *k = static_cast<const Tin *>(p.k);
@@ -204,7 +582,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         if (tid < C) {
             sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
             sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
+            if (MMA) {  // row sums the tensor-core phases add into
+                sQSdO[tid] = sE[tid] = sRowE[tid] = sDBA[tid] = sDBU[tid] = 0.0f;
+            }
         }
+        bc.L = L;
         __syncthreads();
 
         DN_PHASE(g_bwd_ph, pc, 1);
@@ -275,7 +657,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 4);
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
-        {
+        if constexpr (MMA) {
+            mma_ks(bc, warp, lane);
+        } else {
             const int i0 = 2 * (tid >> 3), cg = tid & 7;
             float ks[2][4], qs[2][4], kd[2][4];
 #pragma unroll
@@ -326,7 +710,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 
         DN_PHASE(g_bwd_ph, pc, 5);
         // ---- Vn = T diag(beta) U ------------------------------------------
-        {
+        if constexpr (MMA) {
+            if (tid < C) sDGam[tid] = p.scale * sQSdO[tid];  // dR's row sums are added to it
+            mma_vn(bc, warp, lane);
+        } else {
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
@@ -345,7 +732,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 
         DN_PHASE(g_bwd_ph, pc, 6);
         // ---- dVn = diag(dec) K dS' + P^T dO; e_i --------------------------
-        {
+        if constexpr (MMA) {
+            mma_dvn(bc, warp, lane);
+        } else {
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
@@ -360,7 +749,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 
         DN_PHASE(g_bwd_ph, pc, 7);
         // ---- dR = T^T dVn; dv = diag(beta) dR ------------------------------
-        {
+        if constexpr (MMA) {
+            mma_dr(bc, warp, lane, p.dvv + (t0 * Nv + h) * (long long)dv + v0, (long long)Nv * dv);
+        } else {
             float acc[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
@@ -388,7 +779,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 
         DN_PHASE(g_bwd_ph, pc, 8);
         // ---- dA, dP and E (row i per warp, columns j = lane, lane + 32) ----
-        {
+        if constexpr (MMA) {
+            mma_e(bc, warp, lane, tid);
+        } else {
 #pragma unroll 1
             for (int r = 0; r < 8; ++r) {
                 const int i = warp + 8 * r;
@@ -473,7 +866,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         //   dq_i = scale e^{G_i} S dO_i + sum_j WP_ij k_j
         //   dk_i = dec_i dS' Vn_i - beta_i e^{G_i} S dR_i
         //          + sum_j (M_ij + M_ji) k_j + sum_j WP_ji q_j
-        {
+        if constexpr (MMA) {
+            mma_dqdk(bc, warp, lane, p.dq + (t0 * Nk + hk) * (long long)dk, p.dkk + (t0 * Nk + hk) * (long long)dk,
+                     (long long)Nk * dk);
+        } else {
             const int ndg = dk >> 3;
             for (int tile = tid; tile < 16 * ndg; tile += NT) {
                 const int i0 = 4 * (tile / ndg), d0 = 8 * (tile % ndg);
@@ -552,7 +948,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 10);
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
-        {
+        if constexpr (MMA) {
+            mma_ds(bc, warp, lane, expf(sGL[0]));
+        } else {
             const float eGL = expf(sGL[0]);
             const int ndg = dk >> 3;
             for (int tile = tid; tile < 16 * ndg; tile += NT) {
@@ -689,23 +1087,26 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     const long long rows = p.tokens * p.Nk;  // q (and k) rows
     const unsigned nblk = (unsigned)((2 * rows * 32 + 255) / 256);
     if (bf16) {
-        err = cudaFuncSetAttribute(simt_bwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // the tensor-core products where the states come from the
+        // tensor-core forward (dk = 128, dv a multiple of 128)
+        auto kern = tc ? simt_bwd<__nv_bfloat16, true> : simt_bwd<__nv_bfloat16, false>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        simt_bwd<__nv_bfloat16><<<(unsigned)grid, NT, smem, stream>>>(p);
+        kern<<<(unsigned)grid, NT, smem, stream>>>(p);
         if (qkn && rows > 0)
             l2norm_bwd_rows<__nv_bfloat16><<<nblk, 256, 0, stream>>>(
                 static_cast<const __nv_bfloat16 *>(p.q), static_cast<const __nv_bfloat16 *>(p.k), p.dq, p.dkk, rows,
                 p.dk);
         if (tc)
-            *name = qkn ? "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
-                        : "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16>";
+            *name = qkn ? "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16,tf32>+l2norm_bwd_rows<bf16>"
+                        : "fill_zero+wy_fwd+tc_fwd+simt_bwd<bf16,tf32>";
         else
             *name = qkn ? "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>+l2norm_bwd_rows<bf16>"
                         : "fill_zero+simt_fwd<bf16>+simt_bwd<bf16>";
     } else {
-        err = cudaFuncSetAttribute(simt_bwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = cudaFuncSetAttribute(simt_bwd<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        simt_bwd<float><<<(unsigned)grid, NT, smem, stream>>>(p);
+        simt_bwd<float, false><<<(unsigned)grid, NT, smem, stream>>>(p);
         if (qkn && rows > 0)
             l2norm_bwd_rows<float><<<nblk, 256, 0, stream>>>(static_cast<const float *>(p.q),
                                                              static_cast<const float *>(p.k), p.dq, p.dkk, rows, p.dk);
