@@ -77,7 +77,7 @@ struct Layout {
 };
 
 // Per-row scalars (C floats each) at Layout::sc.
-enum { R_G, R_EG, R_DEC, R_BETA, R_QSDO, R_DBU, R_DGAM, R_E, R_ROWE, R_DBA, R_RK, R_RQ, R_COUNT };
+enum { R_G, R_EG, R_DEC, R_BETA, R_QSDO, R_DBU, R_DGAM, R_E, R_ROWE, R_DBA, R_RK, R_RQ, R_COLE, R_COUNT };
 
 template <typename Tin>
 __host__ __device__ inline Layout layout(int dk) {
@@ -138,7 +138,26 @@ __device__ __forceinline__ float row_sum(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     return v + __shfl_xor_sync(0xffffffffu, v, 2);
 }
+// sum over the eight lanes g of a fragment column pair (lanes t, t + 4, ..)
+__device__ __forceinline__ float col_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
 }  // namespace tf32
+
+// Asynchronous global -> shared copies (no register staging).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // The chunk's shared-memory operands, as the tensor-core phases see them.
 struct BwdChunk {
@@ -147,7 +166,7 @@ struct BwdChunk {
     float *M0, *M1, *M2;                 // [C][LDC]
     float *U, *dO, *KS, *Vn, *dV, *KdS;  // [C][LDV]
     const float *G, *EG, *Dec, *Beta, *RK, *RQ;
-    float *QSdO, *DBU, *DGam, *E, *RowE, *DBA;
+    float *QSdO, *DBU, *DGam, *E, *RowE, *DBA, *ColE;
     int ldkq, SLD, L;
     float scale;
 };
@@ -314,8 +333,8 @@ __device__ __forceinline__ int band_mt(int k) { return k < 2 ? 0 : (k < 6 ? 1 : 
 // (20 tiles, M = 64, N = 64, K = 32), then per element (j <= i < L)
 //   M_ij = -beta_i D_ij dA_ij,  WP_ij = scale D_ij dP_ij,
 //   E_ij = beta_i dA_ij A'_ij + dP_ij P_ij   (A' = -(K K^T . D), dA_ii = 0)
-// over M0, M1, M2 (zero elsewhere), with row sums of E into RowE and of
-// dA . A' into DBA (both zeroed before).
+// over M0, M1, M2 (zero elsewhere), with row sums of E into RowE, column
+// sums of E into ColE and row sums of dA . A' into DBA (all zeroed before).
 __device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int tid) {
     const int g = lane >> 2, t = lane & 3;
     for (int k = warp; k < 20; k += 8) {
@@ -331,7 +350,7 @@ __device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int
             tf32::mma(dp, tf32::cvt(s.dO[r0 * LDV + cc]), tf32::cvt(s.dO[(r0 + 8) * LDV + cc]),
                       tf32::cvt(s.dO[r0 * LDV + cc + 4]), tf32::cvt(s.dO[(r0 + 8) * LDV + cc + 4]), b0, b1);
         }
-        float rowe[2] = {0.0f, 0.0f}, dba[2] = {0.0f, 0.0f};
+        float rowe[2] = {0.0f, 0.0f}, dba[2] = {0.0f, 0.0f}, cole[2] = {0.0f, 0.0f};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int i = r0 + 8 * (e >> 1), j = 8 * nt + 2 * t + (e & 1);
@@ -345,6 +364,7 @@ __device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int
                 m = -s.Beta[i] * D * dav;
                 wp = s.scale * D * dp[e];
                 rowe[e >> 1] += ee;
+                cole[e & 1] += ee;
             }
             s.M0[i * LDC + j] = m;
             s.M1[i * LDC + j] = wp;
@@ -357,6 +377,8 @@ __device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int
                 atomicAdd(s.RowE + r0 + 8 * hf, re);
                 atomicAdd(s.DBA + r0 + 8 * hf, db);
             }
+            const float ce = tf32::col_sum(cole[hf]);
+            if (g == 0) atomicAdd(s.ColE + 8 * nt + 2 * t + hf, ce);
         }
     }
     // the tiles right of the band are zero
@@ -519,13 +541,14 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     // every product below that reads a k or q row takes the row's factor, so
     // the gradients the CTA adds up are those of the normalised rows
     float *sRK = sc + R_RK * C, *sRQ = sc + R_RQ * C;
+    float *sColE = sc + R_COLE * C;  // column sums of E (tensor-core path)
     const bool qkn = (p.flags & kQkL2Norm) != 0;
     float *sGL = sc + R_COUNT * C;      // [0]: G_L
     float *sRed = sGL + 4;              // [8]: per-warp partial <S, dS'>
     const int ldkq = kq_ld<Tin>(dk);
     BwdChunk bc{reinterpret_cast<const __nv_bfloat16 *>(sK), reinterpret_cast<const __nv_bfloat16 *>(sQ),
                 sSt, sdSt, sM0, sM1, sM2, sU, sdO, sKS, sVn, sdV, sKdS,
-                sG, sEG, sDec, sBeta, sRK, sRQ, sQSdO, sDBU, sDGam, sE, sRowE, sDBA,
+                sG, sEG, sDec, sBeta, sRK, sRQ, sQSdO, sDBU, sDGam, sE, sRowE, sDBA, sColE,
                 ldkq, SLD, 0, p.scale};
 
     const Tin *q = static_cast<const Tin *>(p.q);
@@ -563,8 +586,27 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
 
         DN_PHASE(g_bwd_ph, pc, 0);
         // ---- load --------------------------------------------------------
-        simt::load_rows<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
-        simt::load_rows<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
+        // K, Q rows and the state: asynchronous copies, in flight while V and
+        // dO are converted
+        {
+            constexpr int VEC = 16 / sizeof(Tin);
+            const int per_row = dk / VEC;
+            for (int idx = tid; idx < L * per_row; idx += NT) {
+                const int i = idx / per_row, cv = idx - i * per_row;
+                const long long go = ((t0 + i) * Nk + hk) * (long long)dk + cv * VEC;
+                cp_async16(sK + i * ldkq + cv * VEC, k + go);
+                cp_async16(sQ + i * ldkq + cv * VEC, q + go);
+            }
+            for (int idx = L * ldkq + tid; idx < C * ldkq; idx += NT) sK[idx] = sQ[idx] = Tin(0.0f);
+            const float *hs = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
+            for (int idx = tid; idx < dk * BV; idx += NT) {
+                const int d = idx / BV, cc = idx - d * BV;
+                if (cc < bvw)
+                    cp_async4(sSt + cc * SLD + d, hs + (size_t)d * dv + cc);
+                else
+                    sSt[cc * SLD + d] = 0.0f;
+            }
+        }
         for (int idx = tid; idx < C * BV; idx += NT) {
             const int i = idx / BV, cc = idx - i * BV;
             const bool in = i < L && cc < bvw;
@@ -572,21 +614,15 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             sU[i * LDV + cc] = in ? to_f(v[off]) : 0.0f;
             sdO[i * LDV + cc] = in ? to_f(dout[off]) : 0.0f;
         }
-        {
-            const float *hs = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
-            for (int idx = tid; idx < dk * BV; idx += NT) {
-                const int d = idx / BV, cc = idx - d * BV;
-                sSt[cc * SLD + d] = cc < bvw ? hs[(size_t)d * dv + cc] : 0.0f;
-            }
-        }
         if (tid < C) {
             sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
             sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
             if (MMA) {  // row sums the tensor-core phases add into
-                sQSdO[tid] = sE[tid] = sRowE[tid] = sDBA[tid] = sDBU[tid] = 0.0f;
+                sQSdO[tid] = sE[tid] = sRowE[tid] = sDBA[tid] = sDBU[tid] = sColE[tid] = 0.0f;
             }
         }
         bc.L = L;
+        cp_async_wait_all();
         __syncthreads();
 
         DN_PHASE(g_bwd_ph, pc, 1);
@@ -831,7 +867,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             for (int hj = 0; hj < 2; ++hj) {
                 const int i = lane + 32 * hj;
                 float colE = 0.0f;
-                for (int i2 = i; i2 < L; ++i2) colE += sM2[i2 * LDC + i];
+                if constexpr (MMA)
+                    colE = sColE[i];
+                else
+                    for (int i2 = i; i2 < L; ++i2) colE += sM2[i2 * LDC + i];
                 dG[hj] = i < L ? sEG[i] * sDGam[i] + sRowE[i] - colE - sE[i] : 0.0f;
                 db[hj] = sDBU[i] + sDBA[i];
                 esum += i < L ? sE[i] : 0.0f;
