@@ -333,9 +333,9 @@ __device__ __forceinline__ int band_mt(int k) { return k < 2 ? 0 : (k < 6 ? 1 : 
 // (20 tiles, M = 64, N = 64, K = 32), then per element (j <= i < L)
 //   M_ij = -beta_i D_ij dA_ij,  WP_ij = scale D_ij dP_ij,
 //   E_ij = beta_i dA_ij A'_ij + dP_ij P_ij   (A' = -(K K^T . D), dA_ii = 0)
-// over M0, M1, M2 (zero elsewhere), with row sums of E into RowE, column
+// over M0, M1, M2 within the band, with row sums of E into RowE, column
 // sums of E into ColE and row sums of dA . A' into DBA (all zeroed before).
-__device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int tid) {
+__device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane) {
     const int g = lane >> 2, t = lane & 3;
     for (int k = warp; k < 20; k += 8) {
         const int mt = band_mt(k), nt = k - mt * (mt + 1);
@@ -381,11 +381,8 @@ __device__ __forceinline__ void mma_e(const BwdChunk &s, int warp, int lane, int
             if (g == 0) atomicAdd(s.ColE + 8 * nt + 2 * t + hf, ce);
         }
     }
-    // the tiles right of the band are zero
-    for (int idx = tid; idx < C * C; idx += NT) {
-        const int i = idx >> 6, j = idx & (C - 1);
-        if ((j >> 3) > 2 * (i >> 4) + 1) s.M0[i * LDC + j] = s.M1[i * LDC + j] = s.M2[i * LDC + j] = 0.0f;
-    }
+    // (right of the band, j > i: M0 and M2 hold the zeros of -(K K^T . D)
+    // and P, M1 those of T, as the later phases need)
 }
 
 // dq, dk of the chunk's rows (M = 64 rows i, N = dk = 128 columns d):
@@ -816,7 +813,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 8);
         // ---- dA, dP and E (row i per warp, columns j = lane, lane + 32) ----
         if constexpr (MMA) {
-            mma_e(bc, warp, lane, tid);
+            mma_e(bc, warp, lane);
         } else {
 #pragma unroll 1
             for (int r = 0; r < 8; ++r) {
