@@ -478,12 +478,21 @@ def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
     clocks = clk.summary()
     sec = ms / 1e3
     mhz = (clocks or {}).get("sm_max_mhz") or 2070.0
-    peak = fp32_alu_peak_tflops(mhz)
     achieved = alg["flops"] / sec / 1e12
     peaks, peak_src = load_peaks()
-    roof = dict(bound="alu", achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
+    alu = fp32_alu_peak_tflops(mhz)
+    if "tf32" in kernel:
+        # the reverse walk's products run as TF32 tensor-core tiles: TF32 dense
+        # peak = the bf16 GEMM peak x the nominal TF32 / bf16 ratio (1.1 / 2.25)
+        peak = peaks["bf16_tflops"] * 1.1 / 2.25
+        bound, src = "tensor", ("%s bf16 %.0f TFLOP/s x 1.1 / 2.25 (nominal TF32 / bf16)"
+                                % (peak_src, peaks["bf16_tflops"]))
+    else:
+        peak = alu
+        bound, src = "alu", "derived: 152 SMs x 128 fp32 lanes x 2 flop x %.0f MHz" % mhz
+    roof = dict(bound=bound, achieved=achieved, peak=peak, unit="TFLOP/s", frac=achieved / peak,
                 traffic=measured_traffic(kernel, wl_name + ":bwd"),
-                peak_source="derived: 152 SMs x 128 fp32 lanes x 2 flop x %.0f MHz" % mhz,
+                peak_source=src, fp32_alu_peak=alu, frac_of_fp32_alu=achieved / alu,
                 roofline_time_us=1e6 * max(alg["flops"] / (peak * 1e12),
                                            alg["bytes"] / (peaks["hbm_gbs"] * 1e9)),
                 algorithmic_bytes=alg["bytes"], algorithmic_flops=alg["flops"],
@@ -491,7 +500,8 @@ def bench_bwd(args, inp, wl_name, dn, dev, rank, world, dist):
     line = dict(metric=BWD_METRIC, value=weak_scaling_value(alg["tokens"], world, ms_max), unit=UNIT,
                 n_gpus=world, steps=K, warmup=args.warmup, ms_per_step=ms_max,
                 higher_is_better=True, scaling="weak", vs_baseline=None,
-                dtype="f32 (inputs %s)" % ("bf16" if d["q"].dtype == torch.bfloat16 else "f32"),
+                dtype=("tf32 (fp32 accumulation; inputs bf16)" if "tf32" in kernel
+                       else "f32 (inputs %s)" % ("bf16" if d["q"].dtype == torch.bfloat16 else "f32")),
                 data="synthetic",
                 config=dict(config_of(wl_name, inp, l2=L2_NOTE), mode="bwd"),
                 parallelism="dp%d (independent sequences per GPU, no collective)" % world,

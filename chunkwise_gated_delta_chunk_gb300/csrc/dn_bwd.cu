@@ -65,8 +65,14 @@ using simt::align16;
 constexpr int C = kChunk;    // 64
 constexpr int BV = 32;       // value columns per CTA
 constexpr int NT = 256;      // 8 warps
-constexpr int LDC = C + 1;   // row stride of the C x C matrices
-constexpr int LDV = BV + 1;  // row stride of the C x BV tiles (conflict-free row-per-lane reads)
+// Row strides of the C x C matrices (LDC) and of the C x BV tiles (LDV).
+// FMA code: C + 1 and BV + 1 (conflict-free row-per-lane reads).  Tensor-core
+// code: 4 mod 32, so that a fragment's 8 rows x 4 columns hit 32 banks.
+template <bool MMA>
+struct Strides {
+    static constexpr int LDC = MMA ? C + 4 : C + 1;
+    static constexpr int LDV = MMA ? BV + 4 : BV + 1;
+};
 
 // Row stride (floats) of the transposed state tiles S^T, dS^T ([BV][dk]):
 // 16-byte rows, consecutive rows 4 banks apart.
@@ -79,8 +85,9 @@ struct Layout {
 // Per-row scalars (C floats each) at Layout::sc.
 enum { R_G, R_EG, R_DEC, R_BETA, R_QSDO, R_DBU, R_DGAM, R_E, R_ROWE, R_DBA, R_RK, R_RQ, R_COLE, R_COUNT };
 
-template <typename Tin>
+template <typename Tin, bool MMA>
 __host__ __device__ inline Layout layout(int dk) {
+    constexpr int LDC = Strides<MMA>::LDC, LDV = Strides<MMA>::LDV;
     Layout L{};
     size_t off = 0;
     const size_t kq = align16(size_t(C) * kq_ld<Tin>(dk) * sizeof(Tin));
@@ -158,6 +165,10 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The tensor-core phases (their own strides).
+namespace tcp {
+constexpr int LDC = Strides<true>::LDC, LDV = Strides<true>::LDV;
 
 // The chunk's shared-memory operands, as the tensor-core phases see them.
 struct BwdChunk {
@@ -498,11 +509,14 @@ __device__ __forceinline__ void mma_ds(const BwdChunk &s, int warp, int lane, fl
     }
 }
 
+}  // namespace tcp
+
 // MMA: the products run as TF32 tensor-core tiles (bf16 inputs, dk = 128,
 // dv a multiple of BV; the states come from the tensor-core forward); else
 // as fp32 FMAs.
 template <typename Tin, bool MMA>
 __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
+    constexpr int LDC = Strides<MMA>::LDC, LDV = Strides<MMA>::LDV;
     extern __shared__ __align__(16) unsigned char smem[];
     const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
     const int nvt = (dv + BV - 1) / BV;
@@ -516,7 +530,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     const int c = lane;  // value column of the C x BV tiles in the row-per-warp loops
     const int SLD = st_ld(dk);
 
-    const Layout lay = layout<Tin>(dk);
+    const Layout lay = layout<Tin, MMA>(dk);
     Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);
     Tin *sQ = reinterpret_cast<Tin *>(smem + lay.q);
     float *sSt = reinterpret_cast<float *>(smem + lay.s);    // [BV][SLD]: S^T, S = state the chunk starts from
@@ -543,7 +557,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     float *sGL = sc + R_COUNT * C;      // [0]: G_L
     float *sRed = sGL + 4;              // [8]: per-warp partial <S, dS'>
     const int ldkq = kq_ld<Tin>(dk);
-    BwdChunk bc{reinterpret_cast<const __nv_bfloat16 *>(sK), reinterpret_cast<const __nv_bfloat16 *>(sQ),
+    tcp::BwdChunk bc{reinterpret_cast<const __nv_bfloat16 *>(sK), reinterpret_cast<const __nv_bfloat16 *>(sQ),
                 sSt, sdSt, sM0, sM1, sM2, sU, sdO, sKS, sVn, sdV, sKdS,
                 sG, sEG, sDec, sBeta, sRK, sRQ, sQSdO, sDBU, sDGam, sE, sRowE, sDBA, sColE,
                 ldkq, SLD, 0, p.scale};
@@ -691,7 +705,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         if constexpr (MMA) {
-            mma_ks(bc, warp, lane);
+            tcp::mma_ks(bc, warp, lane);
         } else {
             const int i0 = 2 * (tid >> 3), cg = tid & 7;
             float ks[2][4], qs[2][4], kd[2][4];
@@ -745,7 +759,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         // ---- Vn = T diag(beta) U ------------------------------------------
         if constexpr (MMA) {
             if (tid < C) sDGam[tid] = p.scale * sQSdO[tid];  // dR's row sums are added to it
-            mma_vn(bc, warp, lane);
+            tcp::mma_vn(bc, warp, lane);
         } else {
             float acc[8];
 #pragma unroll
@@ -766,7 +780,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 6);
         // ---- dVn = diag(dec) K dS' + P^T dO; e_i --------------------------
         if constexpr (MMA) {
-            mma_dvn(bc, warp, lane);
+            tcp::mma_dvn(bc, warp, lane);
         } else {
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -783,7 +797,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 7);
         // ---- dR = T^T dVn; dv = diag(beta) dR ------------------------------
         if constexpr (MMA) {
-            mma_dr(bc, warp, lane, p.dvv + (t0 * Nv + h) * (long long)dv + v0, (long long)Nv * dv);
+            tcp::mma_dr(bc, warp, lane, p.dvv + (t0 * Nv + h) * (long long)dv + v0, (long long)Nv * dv);
         } else {
             float acc[8];
 #pragma unroll
@@ -813,7 +827,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 8);
         // ---- dA, dP and E (row i per warp, columns j = lane, lane + 32) ----
         if constexpr (MMA) {
-            mma_e(bc, warp, lane);
+            tcp::mma_e(bc, warp, lane);
         } else {
 #pragma unroll 1
             for (int r = 0; r < 8; ++r) {
@@ -903,7 +917,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         //   dk_i = dec_i dS' Vn_i - beta_i e^{G_i} S dR_i
         //          + sum_j (M_ij + M_ji) k_j + sum_j WP_ji q_j
         if constexpr (MMA) {
-            mma_dqdk(bc, warp, lane, p.dq + (t0 * Nk + hk) * (long long)dk, p.dkk + (t0 * Nk + hk) * (long long)dk,
+            tcp::mma_dqdk(bc, warp, lane, p.dq + (t0 * Nk + hk) * (long long)dk, p.dkk + (t0 * Nk + hk) * (long long)dk,
                      (long long)Nk * dk);
         } else {
             const int ndg = dk >> 3;
@@ -985,7 +999,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
         if constexpr (MMA) {
-            mma_ds(bc, warp, lane, expf(sGL[0]));
+            tcp::mma_ds(bc, warp, lane, expf(sGL[0]));
         } else {
             const float eGL = expf(sGL[0]);
             const int ndg = dk >> 3;
@@ -1087,8 +1101,9 @@ __global__ void fill_zero(ZeroArgs z) {
 
 }  // namespace
 
-size_t bwd_smem_bytes(int dk, bool bf16) {
-    return bf16 ? layout<__nv_bfloat16>(dk).end : layout<float>(dk).end;
+size_t bwd_smem_bytes(int dk, bool bf16, bool mma) {
+    return bf16 ? (mma ? layout<__nv_bfloat16, true>(dk).end : layout<__nv_bfloat16, false>(dk).end)
+                : layout<float, false>(dk).end;
 }
 
 cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name) {
@@ -1118,7 +1133,7 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     if (tc && !p.ws) return cudaErrorInvalidValue;
     const char *fname = "";
     if ((err = tc ? tc_launch(f, stream, &fname) : simt_launch(f, bf16, stream, &fname)) != cudaSuccess) return err;
-    const size_t smem = bwd_smem_bytes(p.dk, bf16);
+    const size_t smem = bwd_smem_bytes(p.dk, bf16, tc);
     const bool qkn = (p.flags & kQkL2Norm) != 0;
     const long long rows = p.tokens * p.Nk;  // q (and k) rows
     const unsigned nblk = (unsigned)((2 * rows * 32 + 255) / 256);

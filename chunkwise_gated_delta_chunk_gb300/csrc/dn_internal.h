@@ -48,7 +48,7 @@ size_t simt_smem_bytes(int dk, bool bf16);
 // saving each chunk's start state in p.hs (p.o and p.ht null), then walk the
 // chunks in reverse.  dk <= 128.
 cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
-size_t bwd_smem_bytes(int dk, bool bf16);
+size_t bwd_smem_bytes(int dk, bool bf16, bool mma);  // mma: the tensor-core instantiation
 
 // Token-serial kernel (decode / short sequences): any supported shape.
 cudaError_t recurrent_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
