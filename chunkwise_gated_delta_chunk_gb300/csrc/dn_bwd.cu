@@ -79,7 +79,7 @@ struct Strides {
 __host__ __device__ inline int st_ld(int dk) { return dk + 4; }
 
 struct Layout {
-    size_t k, q, s, ds, m0, m1, m2, u, dO, ks, vn, dv, kds, sc, end;
+    size_t k, q, k2, q2, s, ds, m0, m1, m2, u, dO, ks, vn, dv, kds, sc, end;
 };
 
 // Per-row scalars (C floats each) at Layout::sc.
@@ -93,6 +93,9 @@ __host__ __device__ inline Layout layout(int dk) {
     const size_t kq = align16(size_t(C) * kq_ld<Tin>(dk) * sizeof(Tin));
     L.k = off; off += kq;
     L.q = off; off += kq;
+    // tensor-core path: second K / Q buffers, filled one chunk ahead
+    L.k2 = off; off += MMA ? kq : 0;
+    L.q2 = off; off += MMA ? kq : 0;
     L.s = off; off += align16(size_t(BV) * st_ld(dk) * 4);
     L.ds = off; off += align16(size_t(BV) * st_ld(dk) * 4);
     L.m0 = off; off += align16(size_t(C) * LDC * 4);
@@ -165,6 +168,9 @@ __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every committed group but the latest one has landed
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // The tensor-core phases (their own strides).
 namespace tcp {
@@ -531,8 +537,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     const int SLD = st_ld(dk);
 
     const Layout lay = layout<Tin, MMA>(dk);
-    Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);
-    Tin *sQ = reinterpret_cast<Tin *>(smem + lay.q);
+    // K / Q buffers (two on the tensor-core path: chunk ci in buffer ci & 1)
+    Tin *const sK0 = reinterpret_cast<Tin *>(smem + lay.k), *const sK1 = reinterpret_cast<Tin *>(smem + lay.k2);
+    Tin *const sQ0 = reinterpret_cast<Tin *>(smem + lay.q), *const sQ1 = reinterpret_cast<Tin *>(smem + lay.q2);
+    Tin *sK = sK0;
+    Tin *sQ = sQ0;
     float *sSt = reinterpret_cast<float *>(smem + lay.s);    // [BV][SLD]: S^T, S = state the chunk starts from
     float *sdSt = reinterpret_cast<float *>(smem + lay.ds);  // [BV][SLD]: dS'^T, gradient of the state it hands on
     float *sM0 = reinterpret_cast<float *>(smem + lay.m0);   // -(K K^T . D), then M
@@ -588,6 +597,37 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     }
 
     const long long nch = (eos - bos + C - 1) / C;
+    // asynchronous copies of chunk cj's K and Q rows (rows past its length
+    // zeroed) and of the state it starts from
+    auto load_kq = [&](long long cj, Tin *dK, Tin *dQ) {
+        constexpr int VEC = 16 / sizeof(Tin);
+        const long long tj = bos + cj * C;
+        const int Lj = (eos - tj) < C ? (int)(eos - tj) : C;
+        const int per_row = dk / VEC;
+        for (int idx = tid; idx < Lj * per_row; idx += NT) {
+            const int i = idx / per_row, cv = idx - i * per_row;
+            const long long go = ((tj + i) * Nk + hk) * (long long)dk + cv * VEC;
+            cp_async16(dK + i * ldkq + cv * VEC, k + go);
+            cp_async16(dQ + i * ldkq + cv * VEC, q + go);
+        }
+        for (int idx = Lj * ldkq + tid; idx < C * ldkq; idx += NT) dK[idx] = dQ[idx] = Tin(0.0f);
+    };
+    auto load_hs = [&](long long cj) {
+        const long long tj = bos + cj * C;
+        const float *hs = p.hs + ((size_t)h * p.nslots + (size_t)(tj / C + n)) * dk * dv + v0;
+        for (int idx = tid; idx < dk * BV; idx += NT) {
+            const int d = idx / BV, cc = idx - d * BV;
+            if (cc < bvw)
+                cp_async4(sSt + cc * SLD + d, hs + (size_t)d * dv + cc);
+            else
+                sSt[cc * SLD + d] = 0.0f;
+        }
+    };
+    if (MMA && nch > 0) {
+        load_kq(nch - 1, ((nch - 1) & 1) ? sK1 : sK0, ((nch - 1) & 1) ? sQ1 : sQ0);
+        load_hs(nch - 1);
+        cp_async_commit();
+    }
     for (long long ci = nch - 1; ci >= 0; --ci) {
         const long long t0 = bos + ci * C;
         const int pc = (int)(nch - 1 - ci);  // position in the walk (phase stamps)
@@ -598,25 +638,21 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 0);
         // ---- load --------------------------------------------------------
         // K, Q rows and the state: asynchronous copies, in flight while V and
-        // dO are converted
-        {
-            constexpr int VEC = 16 / sizeof(Tin);
-            const int per_row = dk / VEC;
-            for (int idx = tid; idx < L * per_row; idx += NT) {
-                const int i = idx / per_row, cv = idx - i * per_row;
-                const long long go = ((t0 + i) * Nk + hk) * (long long)dk + cv * VEC;
-                cp_async16(sK + i * ldkq + cv * VEC, k + go);
-                cp_async16(sQ + i * ldkq + cv * VEC, q + go);
+        // dO are converted.  On the tensor-core path this chunk's were issued
+        // one chunk ahead (K, Q) and during the previous chunk's dS update
+        // (the state); the next chunk's K and Q go out now.
+        if constexpr (MMA) {
+            sK = (ci & 1) ? sK1 : sK0;
+            sQ = (ci & 1) ? sQ1 : sQ0;
+            bc.K = reinterpret_cast<const __nv_bfloat16 *>(sK);
+            bc.Q = reinterpret_cast<const __nv_bfloat16 *>(sQ);
+            if (ci > 0) {
+                load_kq(ci - 1, (ci & 1) ? sK0 : sK1, (ci & 1) ? sQ0 : sQ1);
+                cp_async_commit();
             }
-            for (int idx = L * ldkq + tid; idx < C * ldkq; idx += NT) sK[idx] = sQ[idx] = Tin(0.0f);
-            const float *hs = p.hs + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * dk * dv + v0;
-            for (int idx = tid; idx < dk * BV; idx += NT) {
-                const int d = idx / BV, cc = idx - d * BV;
-                if (cc < bvw)
-                    cp_async4(sSt + cc * SLD + d, hs + (size_t)d * dv + cc);
-                else
-                    sSt[cc * SLD + d] = 0.0f;
-            }
+        } else {
+            load_kq(ci, sK, sQ);
+            load_hs(ci);
         }
         for (int idx = tid; idx < C * BV; idx += NT) {
             const int i = idx / BV, cc = idx - i * BV;
@@ -633,7 +669,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             }
         }
         bc.L = L;
-        cp_async_wait_all();
+        if (MMA && ci > 0)
+            cp_async_wait_prev();
+        else
+            cp_async_wait_all();
         __syncthreads();
 
         DN_PHASE(g_bwd_ph, pc, 1);
@@ -999,6 +1038,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
         if constexpr (MMA) {
+            // S^T is free until the next chunk's K S: its state goes out now
+            if (ci > 0) {
+                load_hs(ci - 1);
+                cp_async_commit();
+            }
             tcp::mma_ds(bc, warp, lane, expf(sGL[0]));
         } else {
             const float eGL = expf(sGL[0]);
