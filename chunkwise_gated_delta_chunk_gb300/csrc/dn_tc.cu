@@ -464,22 +464,29 @@ __device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, 
 }
 
 // After DS(c): SB[(c+1) & 1] = bf16(acc_s) (and, with hsd, the fp32 state
-// chunk c + 1 starts from), or for the last chunk ht = acc_s.
+// chunk c + 1 starts from), or for the last chunk ht = acc_s.  Key blocks b0
+// and b0 + 1: both TMEM loads are in flight before the one wait.
 __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t lb, size_t hb, int c, bool last,
-                                                     int b0, int b1, float *hsd) {
-    uint32_t r[32], pk[16];
-    for (int blk = b0; blk < b1; ++blk) {
-        tmem_ld32(lb + TM_S + 32 * blk, r);
-        tmem_wait_ld_dep(r);
-        if (!last) {
+                                                     int b0, float *hsd) {
+    uint32_t r[2][32];
+    tmem_ld32(lb + TM_S + 32 * b0, r[0]);
+    tmem_ld32(lb + TM_S + 32 * (b0 + 1), r[1]);
+    tmem_wait_ld_dep(r[0]);
+    tmem_ld_dep(r[1]);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+    for (int e = 0; e < 2; ++e) {
+        const int blk = b0 + e;
+        if (!last) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = pack_bf16(__uint_as_float(r[e][2 * k]), __uint_as_float(r[e][2 * k + 1]));
             tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
             if (hsd) {
                 float *dp = hsd + (size_t)(32 * blk) * p.dv;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    *dp = __uint_as_float(r[k]);
+                    *dp = __uint_as_float(r[e][k]);
                     dp += p.dv;
                 }
             }
@@ -487,22 +494,25 @@ __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t l
             float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                *hp = __uint_as_float(r[k]);
+                *hp = __uint_as_float(r[e][k]);
                 hp += p.dv;
             }
         }
     }
 }
 
-// acc_s *= alpha(c+1) before DS(c+1).
-__device__ __forceinline__ void state_scale_blocks(uint32_t lb, float alpha, int b0, int b1) {
-    uint32_t r[32];
-    for (int blk = b0; blk < b1; ++blk) {
-        tmem_ld32(lb + TM_S + 32 * blk, r);
-        tmem_wait_ld_dep(r);
+// acc_s *= alpha(c+1) before DS(c+1), key blocks b0 and b0 + 1.
+__device__ __forceinline__ void state_scale_blocks(uint32_t lb, float alpha, int b0) {
+    uint32_t r[2][32];
+    tmem_ld32(lb + TM_S + 32 * b0, r[0]);
+    tmem_ld32(lb + TM_S + 32 * (b0 + 1), r[1]);
+    tmem_wait_ld_dep(r[0]);
+    tmem_ld_dep(r[1]);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * __uint_as_float(r[k]));
-        tmem_st32(lb + TM_S + 32 * blk, r);
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[e][k] = __float_as_uint(alpha * __uint_as_float(r[e][k]));
+        tmem_st32(lb + TM_S + 32 * (b0 + e), r[e]);
     }
 }
 
@@ -538,7 +548,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
         DN_TRACE_EV(4, c);
         tc_fence_after();
-        state_convert_blocks(p, lb, hb, c, last, 2, 4, last ? nullptr : hs_col(p, u, c + 1, v));
+        state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
@@ -546,7 +556,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
             DN_TRACE_EV(5, c);
             const int s1 = (c + 1) % NS;
             if (bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1))) break;
-            state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 2, 4);
+            state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 2);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_VSM_FULL));
@@ -826,7 +836,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         DN_TRACE_EV(2, c);
         tc_fence_after();
-        state_convert_blocks(p, lb, sbase, c, last, 0, 2, last ? nullptr : hs_col(p, u, c + 1, v));
+        state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
@@ -838,7 +848,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         const int s1 = (c + 1) % NS;
         if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
         DN_TRACE_EV(6, c);
-        state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 0, 2);
+        state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 0);
         tmem_wait_st();  // ordered before the next v~ arrive (fence there)
         DN_TRACE_EV(4, c);
     }
