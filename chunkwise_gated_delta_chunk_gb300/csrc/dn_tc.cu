@@ -331,7 +331,7 @@ __device__ __forceinline__ void issue_o(const Ctx &x, uint32_t tm, int c) {
 
 // ---------------------------------------------------------------------------
 // Chain MMA issuer (one thread): the MMAs on the serial chain of the scan,
-//   VN(c); U(c+1) while v_new^T is converted; DS(c).
+//   VN(c); DS(c); U(c+1).
 // Issuing a tcgen05 MMA holds the issuing thread for tens of cycles, so O(c)
 // and PV(c), which are off the chain, have their own issuer thread (warp
 // 14); they enter the in-order tensor pipe after DS(c) and run while the
@@ -380,14 +380,6 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
                 loaded[2] = c + 1;
             }
         }
-        // (only if its tiles are already in: a late stage must not hold up DS)
-        bool u_next = c + 1 >= u.nc;
-        if (!u_next && mbar_test_wait(bar(x, B_FULL + (c + 1) % NS), ((c + 1) / NS) & 1) &&
-            mbar_test_wait(bar(x, B_TUF + ((c + 1) & 1)), ((c + 1) >> 1) & 1)) {
-            tc_fence_after();
-            issue_u(x, tm, c + 1);
-            u_next = true;
-        }
         // state update (VSM also means VN, hence U, of this chunk is done:
         // its T'' buffer takes chunk c + 2's)
         if (!wait(x, bar(x, B_VSM_FULL), par)) break;
@@ -397,7 +389,9 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
             mma_ts(tm + TM_S, av + 32 + kk * 8, sdesc(st + kk * 2048, 16384, 1024), ID_DS, 1);
         mma_commit(bar(x, B_S_UPD));
         DN_TRACE_EV(1, c);
-        if (!u_next) {
+        // U of the next chunk, behind DS in the tensor pipe: issued while
+        // v_new was converted it slowed that conversion more than it gains
+        if (c + 1 < u.nc) {
             if (!wait_tiles(x, c + 1, 1)) break;
             tc_fence_after();
             issue_u(x, tm, c + 1);
@@ -790,39 +784,31 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         DN_TRACE_EV(0, c);
         tc_fence_after();
         {
-            // quarter qq holds j = 16 qq .. 16 qq + 15 in columns 16 qq ..;
-            // v_new^T pairs go to columns 8 qq .., v~^T pairs to 32 + 8 qq ..
-            // (each destination column has been read before it is written).
             const float4 *dec4 = reinterpret_cast<const float4 *>(scal(x, s) + SC_DEC);
-            const uint32_t lbv = lb + TM_V + 64 * (c & 1);  // acc_v of this chunk
-            uint32_t q16[16], pv8[8], t8[3][8];
+            const uint32_t lbv = lb + TM_V + 64 * (c & 1);
+            uint32_t r[32], tvh[16];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                tmem_ld16(lbv + 16 * qq, q16);
-                tmem_wait_ld_dep16(q16);
-                uint32_t tq[8];
+            for (int hf = 0; hf < 2; ++hf) {
+                tmem_ld32(lbv + 32 * hf, r);
+                tmem_wait_ld_dep(r);
+                if (hf == 1) tmem_st16(lbv + 32, tvh);  // columns 32-47 are loaded now
+                uint32_t pv[16], tv[16];
 #pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const float4 dd = dec4[4 * qq + k4];
-                    const float a0 = __uint_as_float(q16[4 * k4]), a1 = __uint_as_float(q16[4 * k4 + 1]);
-                    const float a2 = __uint_as_float(q16[4 * k4 + 2]), a3 = __uint_as_float(q16[4 * k4 + 3]);
-                    pv8[2 * k4] = pack_bf16(a0, a1);
-                    pv8[2 * k4 + 1] = pack_bf16(a2, a3);
-                    tq[2 * k4] = pack_bf16(a0 * dd.x, a1 * dd.y);
-                    tq[2 * k4 + 1] = pack_bf16(a2 * dd.z, a3 * dd.w);
+                for (int k4 = 0; k4 < 8; ++k4) {
+                    const float4 dd = dec4[8 * hf + k4];
+                    const float a0 = __uint_as_float(r[4 * k4]), a1 = __uint_as_float(r[4 * k4 + 1]);
+                    const float a2 = __uint_as_float(r[4 * k4 + 2]), a3 = __uint_as_float(r[4 * k4 + 3]);
+                    pv[2 * k4] = pack_bf16(a0, a1);
+                    pv[2 * k4 + 1] = pack_bf16(a2, a3);
+                    tv[2 * k4] = pack_bf16(a0 * dd.x, a1 * dd.y);
+                    tv[2 * k4 + 1] = pack_bf16(a2 * dd.z, a3 * dd.w);
                 }
-                tmem_st8(lbv + 8 * qq, pv8);
-                if (qq < 2) {
+                tmem_st16(lbv + 16 * hf, pv);
+                if (hf == 0) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) t8[qq][k] = tq[k];
-                } else if (qq == 2) {
-                    tmem_st8(lbv + 32, t8[0]);
-                    tmem_st8(lbv + 40, t8[1]);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) t8[2][k] = tq[k];
+                    for (int k = 0; k < 16; ++k) tvh[k] = tv[k];
                 } else {
-                    tmem_st8(lbv + 48, t8[2]);
-                    tmem_st8(lbv + 56, tq);
+                    tmem_st16(lbv + 48, tv);
                 }
             }
             tmem_wait_st();
