@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         DN_PHASE(g_bwd_ph, pc, 2);
         // ---- -(K K^T . D) (strictly lower) and P (lower) ------------------
         // (dk = 128 at compile time on the tensor-core path: the k loop unrolls)
-        simt::kq_products<NT>(sK, sQ, ldkq, MMA ? 128 : dk, tid, [&](int i, int j, float kk, float qk) {
+        simt::kq_products<NT>(sK, sQ, ldkq, MMA ? 128 : dk, L, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
             if (i < L && j <= i) {
                 const float D = expf(sG[i] - sG[j]) * sRK[j];

@@ -28,6 +28,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "dn_internal.h"
 #include "dn_simt_common.cuh"
 
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
 
         DN_PHASE(g_simt_ph, ci, 2);
         // ---- a2: A (strictly lower) and P (lower incl. diagonal) ---------
-        simt::kq_products<NT>(sK, sQ, ldkq, dk, tid, [&](int i, int j, float kk, float qk) {
+        simt::kq_products<NT>(sK, sQ, ldkq, dk, L, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
             if (i < L && j <= i) {
                 const float dec = expf(sG[i] - sG[j]) * sRK[j];
@@ -241,18 +243,20 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
 
         DN_PHASE(g_simt_ph, ci, 4);
         // ---- a4/a5: R = diag(beta)(V - diag(e^G) K S_in); also Q S_in -----
-        // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
-        {
-            const int i0 = 2 * (tid >> 3), cg = tid & 7;
-            float ks[2][4], qs[2][4];
+        // thread: RP rows from i0; columns cg + 8 x (x < 4).  RP = 2 covers
+        // 64 rows, RP = 1 the first 32 (enough for chunks of up to 32 tokens)
+        auto ks_qs = [&](auto rows) {
+            constexpr int RP = decltype(rows)::value;
+            const int i0 = RP * (tid >> 3), cg = tid & 7;
+            float ks[RP][4], qs[RP][4];
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int r = 0; r < RP; ++r)
 #pragma unroll
                 for (int x = 0; x < 4; ++x) ks[r][x] = qs[r][x] = 0.0f;
             for (int d = 0; d < dk; d += 4) {
-                float4 kr[2], qr[2];
+                float4 kr[RP], qr[RP];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < RP; ++r) {
                     kr[r] = simt::ld4(sK + (i0 + r) * ldkq + d);
                     if (want_o) qr[r] = simt::ld4(sQ + (i0 + r) * ldkq + d);
                 }
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                 for (int x = 0; x < 4; ++x) {
                     const float4 s4 = *reinterpret_cast<const float4 *>(sSt + (cg + 8 * x) * SLD + d);
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
+                    for (int r = 0; r < RP; ++r) {
                         ks[r][x] = fmaf(kr[r].x, s4.x, fmaf(kr[r].y, s4.y, fmaf(kr[r].z, s4.z, fmaf(kr[r].w, s4.w, ks[r][x]))));
                         if (want_o)
                             qs[r][x] = fmaf(qr[r].x, s4.x, fmaf(qr[r].y, s4.y, fmaf(qr[r].z, s4.z, fmaf(qr[r].w, s4.w, qs[r][x]))));
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                 }
             }
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
+            for (int r = 0; r < RP; ++r) {
                 const int i = i0 + r;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
@@ -277,7 +281,11 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                     sOi[i * BV + cc] = p.scale * sEG[i] * sRQ[i] * qs[r][x];
                 }
             }
-        }
+        };
+        if (L <= 32)
+            ks_qs(std::integral_constant<int, 1>{});
+        else
+            ks_qs(std::integral_constant<int, 2>{});
         __syncthreads();
 
         DN_PHASE(g_simt_ph, ci, 5);

@@ -78,21 +78,22 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 
 // The chunk's (K K^T)_ij and (Q K^T)_ij, handed to epi(i, j, kk, qk) for every
 // (i, j) of the 64 x 64 grid: computed where j <= i (up to the 8-column tile
-// that holds the diagonal), zero elsewhere.  Rows past the chunk's length are
-// zero in the tiles and so give zero.  bf16: tensor-core tiles (the products
-// of bf16 values are exact in fp32, accumulation is fp32); one warp per
-// (16-row, 8-column) tile pair.
+// that holds the diagonal) and i < L, zero elsewhere.  Rows past the chunk's
+// length L are zero in the tiles, so skipping them changes nothing.  bf16:
+// tensor-core tiles (the products of bf16 values are exact in fp32,
+// accumulation is fp32); one warp per (16-row, 8-column) tile pair.
 template <int NT, typename Epi>
 __device__ __forceinline__ void kq_products(const __nv_bfloat16 *sK, const __nv_bfloat16 *sQ, int ld, int dk,
-                                            int tid, Epi epi) {
+                                            int L, int tid, Epi epi) {
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    // 20 tiles hold the lower triangle: 16-row tile mt pairs with 8-column tiles 0 .. 2 mt + 1
+    // 20 tiles hold the lower triangle: 16-row tile mt pairs with 8-column
+    // tiles 0 .. 2 mt + 1; the row tiles below L come first in this order
     for (int pidx = warp; pidx < 20; pidx += NT / 32) {
         const int mt = pidx < 2 ? 0 : (pidx < 6 ? 1 : (pidx < 12 ? 2 : 3));
         const int nt = pidx - (mt == 0 ? 0 : (mt == 1 ? 2 : (mt == 2 ? 6 : 12)));
         const int r0 = 16 * mt + g, j0 = 8 * nt + g;
         float ck[4] = {0.f, 0.f, 0.f, 0.f}, cq[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k0 = 0; k0 < dk; k0 += 16) {
+        for (int k0 = 0; 16 * mt < L && k0 < dk; k0 += 16) {
             const int kc = k0 + 2 * t;
             uint32_t a[4], aq[4], b[2];
             a[0] = *reinterpret_cast<const uint32_t *>(sK + r0 * ld + kc);
@@ -125,11 +126,12 @@ __device__ __forceinline__ void kq_products(const __nv_bfloat16 *sK, const __nv_
 
 // fp32: one (i, j) pair per thread and step, fp32 FMAs over d.
 template <int NT, typename Epi>
-__device__ __forceinline__ void kq_products(const float *sK, const float *sQ, int ld, int dk, int tid, Epi epi) {
+__device__ __forceinline__ void kq_products(const float *sK, const float *sQ, int ld, int dk, int L, int tid,
+                                            Epi epi) {
     for (int idx = tid; idx < C * C; idx += NT) {
         const int i = idx >> 6, j = idx & 63;
         float kk = 0.f, qk = 0.f;
-        if (j <= i) {
+        if (j <= i && i < L) {
             const float *ki = sK + i * ld, *kj = sK + j * ld, *qi = sQ + i * ld;
             for (int d = 0; d < dk; d += 4) {
                 const float4 a = ld4(ki + d), b = ld4(kj + d), q = ld4(qi + d);
