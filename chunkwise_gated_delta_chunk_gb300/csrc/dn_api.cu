@@ -121,7 +121,7 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     if (use_tc(tokens, dk, dv, dtype, chunk))
         err = dn::tc_launch(p, (cudaStream_t)stream, &name);
     else
-        err = dn::simt_launch(p, bf16, (cudaStream_t)stream, &name);
+        err = dn::simt_launch(p, bf16, bf16, (cudaStream_t)stream, &name);
     if (err != cudaSuccess) return DN_ERR_CUDA;
     t_last_kernel = name;
     return DN_OK;

@@ -1177,7 +1177,7 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     const bool tc = p.tokens > 0 && tc_supported(p.dk, p.dv, bf16);
     if (tc && !p.ws) return cudaErrorInvalidValue;
     const char *fname = "";
-    if ((err = tc ? tc_launch(f, stream, &fname) : simt_launch(f, bf16, stream, &fname)) != cudaSuccess) return err;
+    if ((err = tc ? tc_launch(f, stream, &fname) : simt_launch(f, bf16, false, stream, &fname)) != cudaSuccess) return err;
     const size_t smem = bwd_smem_bytes(p.dk, bf16, tc);
     const bool qkn = (p.flags & kQkL2Norm) != 0;
     const long long rows = p.tokens * p.Nk;  // q (and k) rows

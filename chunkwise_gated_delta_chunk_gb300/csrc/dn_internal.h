@@ -39,9 +39,10 @@ struct Params {
     float *dh0;                // [N, Nv, dk, dv] or null
 };
 
-// CUDA-core kernel: fp32 arithmetic for every product; any supported shape.
-// `bf16` selects bf16 q/k/v/o, else fp32.  Returns the launch error.
-cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
+// CUDA-core kernel: any supported shape.  `bf16` selects bf16 q/k/v/o, else
+// fp32.  `tf32` (bf16 only): the state products as TF32 tensor-core tiles;
+// otherwise every product is an fp32 FMA.  Returns the launch error.
+cudaError_t simt_launch(const Params &p, bool bf16, bool tf32, cudaStream_t stream, const char **name);
 size_t simt_smem_bytes(int dk, bool bf16);
 
 // Backward: zero the accumulated gradients, rerun the CUDA-core forward

@@ -89,7 +89,34 @@ __host__ __device__ inline Layout layout(int dk) {
     return L;
 }
 
-template <typename Tin>
+// TF32 tensor-core tiles (m16n8k8 mma.sync, fp32 accumulation) for the
+// state products of bf16 inputs; fp32 operands are rounded to TF32, bf16
+// inputs are exact in it.  Fragments, lane = 4 g + t: A (16 x 8) a0 (g, t),
+// a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4); B (8 x 8, k x n) b0 (t, g),
+// b1 (t + 4, g); C (16 x 8) c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t),
+// c3 (g + 8, 2t + 1).
+namespace mmat {
+__device__ __forceinline__ uint32_t cvt(float f) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(f));
+    return r;
+}
+__device__ __forceinline__ uint32_t bf(__nv_bfloat16 x) { return (uint32_t)__bfloat16_as_ushort(x) << 16; }
+__device__ __forceinline__ void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                    uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+}  // namespace mmat
+
+// MMA: the state products (K S, Q S and the state update) as TF32
+// tensor-core tiles; used by the forward for bf16 inputs (its bf16 parity
+// bound).  Without it every product is an fp32 FMA (the fp32 configuration
+// and the backward's state pass).
+template <typename Tin, bool MMA>
 __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
@@ -282,10 +309,34 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
                 }
             }
         };
-        if (L <= 32)
+        if constexpr (MMA) {
+            // 16 x 8 tiles of K S and Q S over the chunk's row tiles
+            const int g = lane >> 2, t = lane & 3;
+            const int mtiles = (L + 15) >> 4;
+            for (int tile = warp; tile < 4 * mtiles; tile += NT / 32) {
+                const int mt = tile >> 2, nt = tile & 3;
+                const int r0 = 16 * mt + g, cb = 8 * nt + g;
+                float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int d = t; d < dk; d += 8) {
+                    const uint32_t b0 = mmat::cvt(sSt[cb * SLD + d]), b1 = mmat::cvt(sSt[cb * SLD + d + 4]);
+                    mmat::mma(ks, mmat::bf(sK[r0 * ldkq + d]), mmat::bf(sK[(r0 + 8) * ldkq + d]),
+                              mmat::bf(sK[r0 * ldkq + d + 4]), mmat::bf(sK[(r0 + 8) * ldkq + d + 4]), b0, b1);
+                    if (want_o)
+                        mmat::mma(qs, mmat::bf(sQ[r0 * ldkq + d]), mmat::bf(sQ[(r0 + 8) * ldkq + d]),
+                                  mmat::bf(sQ[r0 * ldkq + d + 4]), mmat::bf(sQ[(r0 + 8) * ldkq + d + 4]), b0, b1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = r0 + 8 * (e >> 1), cc = 8 * nt + 2 * t + (e & 1);
+                    sR[i * BV + cc] = i < L ? sBeta[i] * (sV[i * BV + cc] - sEG[i] * sRK[i] * ks[e]) : 0.0f;
+                    sOi[i * BV + cc] = p.scale * sEG[i] * sRQ[i] * qs[e];
+                }
+            }
+        } else if (L <= 32) {
             ks_qs(std::integral_constant<int, 1>{});
-        else
+        } else {
             ks_qs(std::integral_constant<int, 2>{});
+        }
         __syncthreads();
 
         DN_PHASE(g_simt_ph, ci, 5);
@@ -339,7 +390,31 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         DN_PHASE(g_simt_ph, ci, 7);
         // ---- a5: S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T ----
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of S
-        {
+        if constexpr (MMA) {
+            // S^T[c][d] += sum_i (dec_i rk_i v_new[i][c]) k_i[d]: 16 x 8 tiles
+            // of (value column, key index) over the chunk's rows
+            const int g = lane >> 2, t = lane & 3;
+            const float eGL = expf(sGL[0]);
+            const int kend = (L + 7) >> 3;
+            for (int tile = warp; tile < 2 * (dk >> 3); tile += NT / 32) {
+                const int mt = tile & 1, nt = tile >> 1;
+                const int c0 = 16 * mt + g, dn = 8 * nt + g;
+                float acc[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[e] = eGL * sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)];
+                for (int kk = 0; kk < kend; ++kk) {
+                    const int i = 8 * kk + t;
+                    const float f0 = sDec[i] * sRK[i], f1 = sDec[i + 4] * sRK[i + 4];
+                    mmat::mma(acc, mmat::cvt(f0 * sVn[i * BV + c0]), mmat::cvt(f0 * sVn[i * BV + c0 + 8]),
+                              mmat::cvt(f1 * sVn[(i + 4) * BV + c0]), mmat::cvt(f1 * sVn[(i + 4) * BV + c0 + 8]),
+                              mmat::bf(sK[i * ldkq + dn]), mmat::bf(sK[(i + 4) * ldkq + dn]));
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)] = acc[e];
+            }
+        } else {
             const float eGL = expf(sGL[0]);
             const int ndg = dk >> 3;
             for (int tile = tid; tile < 16 * ndg; tile += NT) {
@@ -389,7 +464,7 @@ size_t simt_smem_bytes(int dk, bool bf16) {
     return bf16 ? layout<__nv_bfloat16>(dk).end : layout<float>(dk).end;
 }
 
-cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name) {
+cudaError_t simt_launch(const Params &p, bool bf16, bool tf32, cudaStream_t stream, const char **name) {
     const int nvt = (p.dv + BV - 1) / BV;
     const long long grid = (long long)p.N * p.Nv * nvt;
     if (grid <= 0) return cudaSuccess;
@@ -397,14 +472,15 @@ cudaError_t simt_launch(const Params &p, bool bf16, cudaStream_t stream, const c
     const size_t smem = simt_smem_bytes(p.dk, bf16);
     cudaError_t err;
     if (bf16) {
-        err = cudaFuncSetAttribute(simt_fwd<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        auto kern = tf32 ? simt_fwd<__nv_bfloat16, true> : simt_fwd<__nv_bfloat16, false>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        simt_fwd<__nv_bfloat16><<<(unsigned)grid, NT, smem, stream>>>(p);
-        *name = "simt_fwd<bf16>";
+        kern<<<(unsigned)grid, NT, smem, stream>>>(p);
+        *name = tf32 ? "simt_fwd<bf16,tf32>" : "simt_fwd<bf16>";
     } else {
-        err = cudaFuncSetAttribute(simt_fwd<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = cudaFuncSetAttribute(simt_fwd<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (err != cudaSuccess) return err;
-        simt_fwd<float><<<(unsigned)grid, NT, smem, stream>>>(p);
+        simt_fwd<float, false><<<(unsigned)grid, NT, smem, stream>>>(p);
         *name = "simt_fwd<f32>";
     }
     return cudaGetLastError();
