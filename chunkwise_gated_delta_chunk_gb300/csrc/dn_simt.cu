@@ -196,9 +196,9 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         }
 
         DN_PHASE(g_simt_ph, ci, 0);
-        // ---- load the chunk --------------------------------------------
-        simt::load_rows<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
-        simt::load_rows<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
+        // ---- load the chunk (K and Q rows asynchronously, beside V) --------
+        simt::load_rows_async<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
+        simt::load_rows_async<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
         for (int idx = tid; idx < C * BV; idx += NT) {
             const int i = idx / BV, c = idx - i * BV;
             sV[idx] = (i < L && c < bvw) ? to_f(v[((t0 + i) * Nv + h) * (long long)dv + v0 + c]) : 0.0f;
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
             sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
         }
+        simt::cp_async_wait_all();
         __syncthreads();
 
         DN_PHASE(g_simt_ph, ci, 1);
@@ -310,26 +311,36 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             }
         };
         if constexpr (MMA) {
-            // 16 x 8 tiles of K S and Q S over the chunk's row tiles
-            const int g = lane >> 2, t = lane & 3;
-            const int mtiles = (L + 15) >> 4;
-            for (int tile = warp; tile < 4 * mtiles; tile += NT / 32) {
-                const int mt = tile >> 2, nt = tile & 3;
-                const int r0 = 16 * mt + g, cb = 8 * nt + g;
-                float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int d = t; d < dk; d += 8) {
-                    const uint32_t b0 = mmat::cvt(sSt[cb * SLD + d]), b1 = mmat::cvt(sSt[cb * SLD + d + 4]);
-                    mmat::mma(ks, mmat::bf(sK[r0 * ldkq + d]), mmat::bf(sK[(r0 + 8) * ldkq + d]),
+            // 16 x 8 tiles of K S and Q S over the chunk's row tiles: warp w
+            // takes column tile w % 4 and row tiles w / 4, w / 4 + 2 (below
+            // L), loading each S^T fragment once for both
+            const int g = lane >> 2, t = lane & 3, nt = warp & 3;
+            const int mtiles = (L + 15) >> 4, m0 = warp >> 2;
+            const int cb = 8 * nt + g;
+            float ks[2][4] = {}, qs[2][4] = {};
+            for (int d = t; d < dk; d += 8) {
+                const uint32_t b0 = mmat::cvt(sSt[cb * SLD + d]), b1 = mmat::cvt(sSt[cb * SLD + d + 4]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int mt = m0 + 2 * j;
+                    if (mt >= mtiles) break;
+                    const int r0 = 16 * mt + g;
+                    mmat::mma(ks[j], mmat::bf(sK[r0 * ldkq + d]), mmat::bf(sK[(r0 + 8) * ldkq + d]),
                               mmat::bf(sK[r0 * ldkq + d + 4]), mmat::bf(sK[(r0 + 8) * ldkq + d + 4]), b0, b1);
                     if (want_o)
-                        mmat::mma(qs, mmat::bf(sQ[r0 * ldkq + d]), mmat::bf(sQ[(r0 + 8) * ldkq + d]),
+                        mmat::mma(qs[j], mmat::bf(sQ[r0 * ldkq + d]), mmat::bf(sQ[(r0 + 8) * ldkq + d]),
                                   mmat::bf(sQ[r0 * ldkq + d + 4]), mmat::bf(sQ[(r0 + 8) * ldkq + d + 4]), b0, b1);
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int mt = m0 + 2 * j;
+                if (mt >= mtiles) break;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int i = r0 + 8 * (e >> 1), cc = 8 * nt + 2 * t + (e & 1);
-                    sR[i * BV + cc] = i < L ? sBeta[i] * (sV[i * BV + cc] - sEG[i] * sRK[i] * ks[e]) : 0.0f;
-                    sOi[i * BV + cc] = p.scale * sEG[i] * sRQ[i] * qs[e];
+                    const int i = 16 * mt + g + 8 * (e >> 1), cc = 8 * nt + 2 * t + (e & 1);
+                    sR[i * BV + cc] = i < L ? sBeta[i] * (sV[i * BV + cc] - sEG[i] * sRK[i] * ks[j][e]) : 0.0f;
+                    sOi[i * BV + cc] = p.scale * sEG[i] * sRQ[i] * qs[j][e];
                 }
             }
         } else if (L <= 32) {
@@ -393,26 +404,41 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         if constexpr (MMA) {
             // S^T[c][d] += sum_i (dec_i rk_i v_new[i][c]) k_i[d]: 16 x 8 tiles
             // of (value column, key index) over the chunk's rows
+            // warp w: value-column tile w % 2, key-index tiles w / 2 + 4 j;
+            // each A fragment (v_new rows) is built once for all of them
             const int g = lane >> 2, t = lane & 3;
             const float eGL = expf(sGL[0]);
             const int kend = (L + 7) >> 3;
-            for (int tile = warp; tile < 2 * (dk >> 3); tile += NT / 32) {
-                const int mt = tile & 1, nt = tile >> 1;
-                const int c0 = 16 * mt + g, dn = 8 * nt + g;
-                float acc[4];
+            const int c0 = 16 * (warp & 1) + g, n0 = warp >> 1, ntn = dk >> 3;
+            float acc[8][4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int nt = n0 + 4 * j;
+                if (nt >= ntn) break;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    acc[e] = eGL * sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)];
-                for (int kk = 0; kk < kend; ++kk) {
-                    const int i = 8 * kk + t;
-                    const float f0 = sDec[i] * sRK[i], f1 = sDec[i + 4] * sRK[i + 4];
-                    mmat::mma(acc, mmat::cvt(f0 * sVn[i * BV + c0]), mmat::cvt(f0 * sVn[i * BV + c0 + 8]),
-                              mmat::cvt(f1 * sVn[(i + 4) * BV + c0]), mmat::cvt(f1 * sVn[(i + 4) * BV + c0 + 8]),
-                              mmat::bf(sK[i * ldkq + dn]), mmat::bf(sK[(i + 4) * ldkq + dn]));
+                    acc[j][e] = eGL * sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)];
+            }
+            for (int kk = 0; kk < kend; ++kk) {
+                const int i = 8 * kk + t;
+                const float f0 = sDec[i] * sRK[i], f1 = sDec[i + 4] * sRK[i + 4];
+                const uint32_t a0 = mmat::cvt(f0 * sVn[i * BV + c0]), a1 = mmat::cvt(f0 * sVn[i * BV + c0 + 8]),
+                               a2 = mmat::cvt(f1 * sVn[(i + 4) * BV + c0]), a3 = mmat::cvt(f1 * sVn[(i + 4) * BV + c0 + 8]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int nt = n0 + 4 * j;
+                    if (nt >= ntn) break;
+                    const int dn = 8 * nt + g;
+                    mmat::mma(acc[j], a0, a1, a2, a3, mmat::bf(sK[i * ldkq + dn]), mmat::bf(sK[(i + 4) * ldkq + dn]));
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int nt = n0 + 4 * j;
+                if (nt >= ntn) break;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)] = acc[e];
+                    sSt[(c0 + 8 * (e >> 1)) * SLD + 8 * nt + 2 * t + (e & 1)] = acc[j][e];
             }
         } else {
             const float eGL = expf(sGL[0]);

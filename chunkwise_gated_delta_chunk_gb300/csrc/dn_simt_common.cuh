@@ -67,6 +67,27 @@ __device__ __forceinline__ void load_rows(Tin *dst, const Tin *src, long long t0
     for (int idx = L * ld + tid; idx < C * ld; idx += NT) dst[idx] = Tin(0.0f);
 }
 
+// The same rows as load_rows, as asynchronous copies (cp.async, 16 bytes
+// each) that land while the caller does other work; cp_async_wait_all() then
+// a barrier before the rows are read.  Rows past L are zeroed with stores.
+template <typename Tin, int NT>
+__device__ __forceinline__ void load_rows_async(Tin *dst, const Tin *src, long long t0, int L, int H, int hh,
+                                                int d, int tid) {
+    constexpr int VEC = 16 / sizeof(Tin);
+    const int ld = kq_ld<Tin>(d);
+    const int per_row = d / VEC;
+    for (int idx = tid; idx < L * per_row; idx += NT) {
+        const int i = idx / per_row, cv = idx - i * per_row;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(dst + i * ld + cv * VEC)),
+                     "l"(src + ((t0 + i) * H + hh) * (long long)d + cv * VEC)
+                     : "memory");
+    }
+    for (int idx = L * ld + tid; idx < C * ld; idx += NT) dst[idx] = Tin(0.0f);
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // bf16 m16n8k16 tensor-core product with fp32 accumulation: d += a b.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
