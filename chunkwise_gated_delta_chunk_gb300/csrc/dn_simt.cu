@@ -1,8 +1,13 @@
-// CUDA-core kernel of the chunkwise gated delta rule forward.
+// CUDA-core kernel of the chunkwise gated delta rule forward: every shape
+// the tensor-core scan does not take (fp32 inputs, chunks of 16 or 32 tokens,
+// d other than 128).
 //
-// Every product is an fp32 FMA (no TF32), so this kernel serves fp32 inputs,
-// whose tolerance leaves no room for reduced-precision tensor-core products,
-// and every shape the tensor-core kernel does not take.
+// Two kinds of instantiation.  simt_fwd<T, false>: every product an fp32
+// FMA, for fp32 inputs (whose tolerance leaves no room for reduced-precision
+// products) and the backward's state pass.  simt_fwd<bf16, true>: K S, Q S
+// and the state update as TF32 tensor-core tiles (mma.sync, fp32
+// accumulation), within the bf16 bound.  K K^T and Q K^T of bf16 inputs are
+// bf16 tensor-core tiles in both (products of bf16 values are exact in fp32).
 //
 // Sources: [CGDR] "01 · 数学原理:ChunkGatedDeltaRule 在算什么" §3.1-§3.3;
 //          [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现" §2.3-§2.4.
