@@ -12,7 +12,7 @@
 // index d), for the whole sequence.  Every contraction is a tcgen05 MMA with
 // M = 128:
 //
-//   W   K^T T'^T         -> W^T (double buffered)                 (a4)
+//   W   K^T T'^T         -> W^T                                   (a4)
 //   U   V^T T''^T        -> U^T                                   (a4)
 //   VN  U^T - S^T W^T    -> v_new^T (S^T as a bf16 TMEM operand)  (a5)
 //   DS  S^T += v~^T K    -> state update, v~ = e^{G_L-G} v_new    (a5)
@@ -31,12 +31,16 @@
 //   1      chain MMA issuer (one thread: U, VN, DS) and TMEM owner;
 //   2-5    prep: one thread issues W of the next chunk as soon as its tiles
 //          and T' have landed; the warpgroup turns W^T into the bf16 -W^T
-//          operand, running ahead of the state scan;
+//          operand, running ahead of the state scan, then scales the chunk's
+//          Q rows by scale e^G in place for O;
 //   6-9    state: v_new and v~ operands; key blocks 0-1 of the state passes;
 //   10-13  output: key blocks 2-3 of each state pass (the S^T operand, the
 //          alpha scaling, ht); then reads o = scale e^{G} (S^T Q^T) +
 //          P v_new, transposes it through shared memory, stores bf16 rows;
 //   14     output MMA issuer (one thread: O, PV).
+//
+// With Params::hs set (the backward's state pass, no o) the state passes also
+// store the fp32 state each chunk starts from, and o is not written.
 //
 // Every wait is bounded: after kTimeoutNs a CTA records kStatusTimeout in the
 // status word, raises a shared abort flag so the other roles stop too, drains
