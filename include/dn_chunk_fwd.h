@@ -121,7 +121,8 @@ typedef enum {
  * call: the per-chunk WY inverse T and causal scores of every chunk in
  * parallel ([WY] §2.3-§2.4), then the sequential state scan and output
  * ([CGDR] §3.2-§3.3).  Other shapes and chunk sizes launch one CUDA-core
- * kernel.
+ * kernel; for DN_BF16 its state products (K S, Q S, the state update) are
+ * TF32 tensor-core tiles with fp32 accumulation, within the bf16 bound.
  */
 dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,
