@@ -7,7 +7,8 @@
 // The WY kernel (dn_wy.cu) has already written T' = T diag(beta e^G),
 // T'' = T diag(beta) and P = tril(scale QK^T . D) of every chunk to the
 // workspace.  One persistent CTA per (sequence, value head, 128-column value
-// tile) then walks the sequence's 64-token chunks in order.  The fp32 state
+// tile; after a placement lead of CTAs that exit at once, see tc_launch) then
+// walks the sequence's 64-token chunks in order.  The fp32 state
 // lives in tensor memory, transposed (lane = value column v, column = key
 // index d), for the whole sequence.  Every contraction is a tcgen05 MMA with
 // M = 128:
@@ -55,13 +56,14 @@
 #include "dn_tmap.h"
 #include "tc_ptx.cuh"
 
-// Optional per-chunk event trace of CTA 0 (SM clock), compiled in only with
-// -DDN_TRACE for profiling builds; the default build contains no trace code.
+// Optional per-chunk event trace of the grid's last CTA (SM clock), compiled
+// in only with -DDN_TRACE for profiling builds; the default build contains no
+// trace code.
 #ifdef DN_TRACE
 __device__ unsigned long long g_dn_trace[16][1024][16];  // [warp][chunk][event]
 #define DN_TRACE_EV(ev, c)                                                    \
     do {                                                                      \
-        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (c) < 1024)         \
+        if (blockIdx.x + 1 == gridDim.x && (threadIdx.x & 31) == 0 && (c) < 1024) \
             g_dn_trace[threadIdx.x >> 5][(c)][(ev)] = clock64();              \
     } while (0)
 extern "C" __attribute__((visibility("default"))) int dn_trace_dump(void *dst) {
@@ -83,6 +85,7 @@ constexpr int DK = 128;
 constexpr int BVT = 128;       // value columns per CTA
 constexpr int NS = 3;          // pipeline stages of K/Q/V tiles
 constexpr int NTHREADS = 480;
+constexpr int kLeadCtas = 12;  // placement lead of the scan grid (tc_launch)
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
@@ -219,10 +222,17 @@ struct Unit {
     int n, h, hk, v0, nc;
 };
 
+// Units of a launch: one per (sequence, value head, value-column tile).
+__device__ __forceinline__ unsigned unit_count(const Params &p) {
+    return (unsigned)p.N * (unsigned)p.Nv * (unsigned)(p.dv / BVT);
+}
+
+// The unit of this CTA; the grid's first gridDim.x - unit_count(p) CTAs are
+// the placement lead (see tc_launch) and have none.
 __device__ __forceinline__ Unit unit_of(const Params &p) {
     Unit u;
     const int nvt = p.dv / BVT;
-    const int idx = blockIdx.x;
+    const int idx = (int)(blockIdx.x - (gridDim.x - unit_count(p)));
     const int vt = idx % nvt;
     u.h = (idx / nvt) % p.Nv;
     u.n = idx / (nvt * p.Nv);
@@ -850,6 +860,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
 __global__ void __maxnreg__(128)
 tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ CUtensorMap mV, const __grid_constant__ Params p) {
+    if (blockIdx.x + unit_count(p) < gridDim.x) return;  // placement lead: no unit
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     Ctx x;
@@ -955,7 +966,25 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
-    tc_fwd<<<(unsigned)grid, NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);
+    // Placement lead.  One scan CTA fills an SM (its shared memory), and the
+    // block scheduler hands a grid's first CTAs to the same SMs every launch:
+    // on GB300 the first 12 go to four SMs of the second die and to the first
+    // TPC of four GPCs, where a scan CTA measured up to 10 % slower than on
+    // the SMs filled next (82-86 against 74-77 us on B = 4, H = 16, T = 2048).
+    // The scan lasts as long as its slowest CTA, so when the grid leaves room
+    // on the GPU it leads with kLeadCtas CTAs that exit at once and the units
+    // go to the CTAs after them (116.3 against 119.5 us per forward, A/B on
+    // one GPU).  Results do not depend on where a unit runs.
+    static int sms_cache[64];  // 0: not looked up yet
+    int dev = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+    if (sms <= 0) {
+        if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+        if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+    }
+    const long long lead = (grid + kLeadCtas <= sms) ? kLeadCtas : 0;
+    tc_fwd<<<(unsigned)(grid + lead), NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);
     *name = "wy_fwd+tc_fwd";
     return cudaGetLastError();
 }
