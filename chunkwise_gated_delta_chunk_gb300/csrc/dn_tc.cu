@@ -50,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "dn_chunk.cuh"
 #include "dn_internal.h"
 #include "dn_tc.h"
@@ -975,13 +977,13 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     // on the GPU it leads with kLeadCtas CTAs that exit at once and the units
     // go to the CTAs after them (116.3 against 119.5 us per forward, A/B on
     // one GPU).  Results do not depend on where a unit runs.
-    static int sms_cache[64];  // 0: not looked up yet
+    static std::atomic<int> sms_cache[64];  // 0: not looked up yet (calls may come from several threads)
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev] : 0;
+    int sms = (dev >= 0 && dev < 64) ? sms_cache[dev].load(std::memory_order_relaxed) : 0;
     if (sms <= 0) {
         if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-        if (dev >= 0 && dev < 64) sms_cache[dev] = sms;
+        if (dev >= 0 && dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
     }
     const long long lead = (grid + kLeadCtas <= sms) ? kLeadCtas : 0;
     tc_fwd<<<(unsigned)(grid + lead), NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);

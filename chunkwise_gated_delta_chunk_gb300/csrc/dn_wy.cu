@@ -32,6 +32,8 @@
 // Waits are bounded: a wait that runs out records kStatusTimeout in the status
 // word, the CTA skips the rest and drains its own TMA / MMA work before it
 // frees its tensor memory.
+#include <atomic>
+
 #include "dn_wy_item.cuh"
 
 namespace dn {
@@ -87,10 +89,10 @@ cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap 
     // one resident wave of CTAs (per device and instantiation, looked up
     // once); on 2048 items (B = 4, H = 16, T = 2048) it measured 1.5 us
     // faster per forward than one CTA per item
-    static int wave_cache[64][2];  // 0: not looked up yet
+    static std::atomic<int> wave_cache[64][2];  // 0: not looked up yet (calls may come from several threads)
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    int wave = (dev >= 0 && dev < 64) ? wave_cache[dev][qkn] : 0;
+    int wave = (dev >= 0 && dev < 64) ? wave_cache[dev][qkn].load(std::memory_order_relaxed) : 0;
     if (wave <= 0) {
         // CTAs per SM: the launch bound, or fewer if shared memory runs out
         // (the occupancy query reports fewer under the default carveout)
@@ -104,7 +106,7 @@ cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap 
         int per_sm = smem_sm / (int)(smem + (uint32_t)reserved);
         if (per_sm > kWyCtasPerSm) per_sm = kWyCtasPerSm;
         wave = sms * (per_sm > 0 ? per_sm : 1);
-        if (dev >= 0 && dev < 64) wave_cache[dev][qkn] = wave;
+        if (dev >= 0 && dev < 64) wave_cache[dev][qkn].store(wave, std::memory_order_relaxed);
     }
     const unsigned grid = (unsigned)(items < wave ? items : wave);
     if (qkn)
