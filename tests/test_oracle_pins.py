@@ -8,6 +8,8 @@ Pages: [WY] "flash-linear-attention ä¸­ DeltaNet çš„åˆ†å—å¹¶è¡ŒåŒ–WY è¡¨ç¤ºæ¨å
 [CGDR] "01 Â· æ•°å­¦åŸç†:ChunkGatedDeltaRule åœ¨ç®—ä»€ä¹ˆ".
 """
 import math
+import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -204,6 +206,39 @@ def test_single_token_by_hand():
                              t_([[[[1.0, 0.0], [0.0, 4.0]]]]), None, 1.0)
     assert np.allclose(ht[0, 0], [[0.75, 1.0], [0.0, 2.0]], atol=1e-15, rtol=0)
     assert np.allclose(o[0, 0, 0], [0.75, 3.0], atol=1e-15, rtol=0)
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(path):
+    """`name: values` lines of a worked-example fixture (fractions allowed)."""
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                name, vals = line.split(":", 1)
+                rec[name.strip()] = [float(Fraction(x)) for x in vals.split()]
+    return rec
+
+
+@pytest.mark.parametrize("name", sorted(f for f in os.listdir(GOLDEN) if f.endswith(".txt")))
+def test_golden_worked_examples(name):
+    """Hand-derived worked examples (exact fractions, derivation in each
+    fixture) against the token recurrence and the chunk form."""
+    rec = _read_golden(os.path.join(GOLDEN, name))
+    dk, dv = (int(x) for x in rec["dims"])
+    T = len(rec["beta"])
+    t_ = lambda x, *shape: torch.tensor(x, dtype=torch.float64).reshape(*shape)
+    args = (t_(rec["q"], 1, T, 1, dk), t_(rec["k"], 1, T, 1, dk), t_(rec["v"], 1, T, 1, dv),
+            t_(rec["beta"], 1, T, 1), t_([math.log(d) for d in rec["decay"]], 1, T, 1),
+            t_(rec["h0"], 1, 1, dk, dv), None, rec["scale"][0])
+    want_o, want_ht = np.array(rec["o"]).reshape(T, dv), np.array(rec["ht"]).reshape(dk, dv)
+    runs = [oracle.recurrent(*args)] + [oracle.chunked(*args, chunk=c) for c in (1, 2, 64)]
+    for o, ht in runs:
+        assert np.abs(o[0, :, 0] - want_o).max() < 1e-14
+        assert np.abs(ht[0, 0] - want_ht).max() < 1e-14
 
 
 def test_linearity():
