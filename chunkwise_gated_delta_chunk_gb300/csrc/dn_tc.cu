@@ -975,8 +975,8 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     // the SMs filled next (82-86 against 74-77 us on B = 4, H = 16, T = 2048).
     // The scan lasts as long as its slowest CTA, so when the grid leaves room
     // on the GPU it leads with kLeadCtas CTAs that exit at once and the units
-    // go to the CTAs after them (116.3 against 119.5 us per forward, A/B on
-    // one GPU).  Results do not depend on where a unit runs.
+    // go to the CTAs after them (A/B of two builds on one GPU: 118.7 against
+    // 122.2 us per forward).  Results do not depend on where a unit runs.
     static std::atomic<int> sms_cache[64];  // 0: not looked up yet (calls may come from several threads)
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
