@@ -245,7 +245,7 @@ def reference_arm(args, inp, wl_name, rank, world):
     line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=steps, warmup=warm,
                 ms_per_step=1e3 * sec / steps, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
-                config=config_of(wl_name, inp, l2="n/a (CPU)"),
+                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2="n/a (CPU)"), mode=args.mode),
                 cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
                                   sample=sample),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))

@@ -73,13 +73,14 @@ DN_EXPORT size_t dn_chunk_fwd_workspace_bytes(int n_seqs, int B, int T, int Nk, 
     return workspace_bytes((long long)B * T, n_seqs, Nv, dk, dv, dtype, chunk);
 }
 
-DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
-                                 const float *beta, const float *g, const float *h0,
-                                 const int64_t *cu_seqlens, int n_seqs,
-                                 int B, int T, int Nk, int Nv, int dk, int dv,
-                                 dn_dtype dtype, float scale, unsigned flags, int chunk,
-                                 void *o, float *ht, void *workspace, size_t workspace_bytes_,
-                                 dn_stream_t stream) {
+namespace dn {
+
+// Checks of dn_chunk_fwd's arguments other than the workspace (also run by
+// dn_chunk_fwd_noalloc before it looks at sizes).  DN_OK: the call can run.
+dn_status chunk_fwd_check_args(const void *q, const void *k, const void *v, const float *beta,
+                               const float *g, const float *h0, const int64_t *cu_seqlens, int n_seqs,
+                               int B, int T, int Nk, int Nv, int dk, int dv, dn_dtype dtype,
+                               float scale, unsigned flags, int chunk, const void *o, const float *ht) {
     // ---- arguments that are wrong whatever is built ----------------------
     if (dtype != DN_BF16 && dtype != DN_F32) return DN_ERR_INVALID_ARG;
     if (n_seqs < 0 || B < 0 || T < 0 || Nk <= 0 || Nv <= 0 || dk <= 0 || dv <= 0)
@@ -98,7 +99,23 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     if (!chunk_ok(chunk)) return DN_ERR_UNSUPPORTED;
     if (!dim_ok(dk) || !dim_ok(dv)) return DN_ERR_UNSUPPORTED;
     if (dtype == DN_F32 && dk > 128) return DN_ERR_UNSUPPORTED;
+    return DN_OK;
+}
+
+}  // namespace dn
+
+DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
+                                 const float *beta, const float *g, const float *h0,
+                                 const int64_t *cu_seqlens, int n_seqs,
+                                 int B, int T, int Nk, int Nv, int dk, int dv,
+                                 dn_dtype dtype, float scale, unsigned flags, int chunk,
+                                 void *o, float *ht, void *workspace, size_t workspace_bytes_,
+                                 dn_stream_t stream) {
+    const dn_status args = dn::chunk_fwd_check_args(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv,
+                                                    dk, dv, dtype, scale, flags, chunk, o, ht);
+    if (args != DN_OK) return args;
     if (n_seqs == 0) return DN_OK;
+    const long long tokens = (long long)B * T;
     const size_t ws_need = workspace_bytes(tokens, n_seqs, Nv, dk, dv, dtype, chunk);
     if (ws_need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes_ < ws_need))
         return DN_ERR_INVALID_ARG;

@@ -47,13 +47,6 @@
 #include "dn_simt_common.cuh"
 #include "dn_tc.h"
 
-#ifdef DN_TRACE
-__device__ unsigned long long g_bwd_ph[64][16];
-extern "C" __attribute__((visibility("default"))) int dn_trace_dump_bwd(void *dst) {
-    return (int)cudaMemcpyFromSymbol(dst, g_bwd_ph, sizeof(g_bwd_ph));
-}
-#endif
-
 namespace dn {
 namespace {
 
@@ -635,7 +628,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         const int L = (eos - t0) < C ? (int)(eos - t0) : C;
         __syncthreads();  // the previous (later) chunk is done with every buffer
 
-        DN_PHASE(g_bwd_ph, pc, 0);
         // ---- load --------------------------------------------------------
         // K, Q rows and the state: asynchronous copies, in flight while V and
         // dO are converted.  On the tensor-core path this chunk's were issued
@@ -675,7 +667,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             cp_async_wait_all();
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 1);
         // ---- gate prefix sum (warp 0); <S, dS'> partials (every warp) ----
         if (warp == 0) {
             float a = sG[lane], b = sG[lane + 32];
@@ -722,7 +713,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 2);
         // ---- -(K K^T . D) (strictly lower) and P (lower) ------------------
         // (dk = 128 at compile time on the tensor-core path: the k loop unrolls)
         simt::kq_products<NT>(sK, sQ, ldkq, MMA ? 128 : dk, L, tid, [&](int i, int j, float kk, float qk) {
@@ -737,11 +727,9 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         });
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 3);
         // ---- T = (I - A)^-1, A_im = beta_i sM0_im (blocked; sVn, written
         // later, is its scratch) ---------------------------------------------
         simt::solve_T_blocked<NT>(sM0, LDC, sBeta, sM1, LDC, sVn, L, tid);
-        DN_PHASE(g_bwd_ph, pc, 4);
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         if constexpr (MMA) {
@@ -795,7 +783,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 5);
         // ---- Vn = T diag(beta) U ------------------------------------------
         if constexpr (MMA) {
             if (tid < C) sDGam[tid] = p.scale * sQSdO[tid];  // dR's row sums are added to it
@@ -817,7 +804,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 6);
         // ---- dVn = diag(dec) K dS' + P^T dO; e_i --------------------------
         if constexpr (MMA) {
             tcp::mma_dvn(bc, warp, lane);
@@ -834,7 +820,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 7);
         // ---- dR = T^T dVn; dv = diag(beta) dR ------------------------------
         if constexpr (MMA) {
             tcp::mma_dr(bc, warp, lane, p.dvv + (t0 * Nv + h) * (long long)dv + v0, (long long)Nv * dv);
@@ -864,7 +849,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 8);
         // ---- dA, dP and E (row i per warp, columns j = lane, lane + 32) ----
         if constexpr (MMA) {
             tcp::mma_e(bc, warp, lane);
@@ -909,7 +893,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 9);
         // ---- warp 0: dbeta, dG and dg ------------------------------------
         if (warp == 0) {
             float dG[2], db[2];
@@ -1035,7 +1018,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_bwd_ph, pc, 10);
         // ---- dS = e^{G_L} dS' + scale Q^T diag(e^G) dO - K^T diag(beta e^G) dR
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of dS
         if constexpr (MMA) {
@@ -1080,7 +1062,6 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                 }
             }
         }
-        DN_PHASE(g_bwd_ph, pc, 11);
     }
 
     __syncthreads();

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dn_chunk_fwd.h"
+
 namespace dn {
 
 constexpr int kChunk = 64;  // C: tokens per chunk of the tensor-core path; tile size of both paths
@@ -50,6 +52,15 @@ size_t simt_smem_bytes(int dk, bool bf16);
 // chunks in reverse.  dk <= 128.
 cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);
 size_t bwd_smem_bytes(int dk, bool bf16, bool mma);  // mma: the tensor-core instantiation
+
+// Host checks of dn_chunk_fwd's arguments other than the workspace, in the
+// order that entry point applies them: DN_ERR_INVALID_ARG for arguments that
+// are wrong whatever is built, then DN_ERR_UNSUPPORTED for valid shapes no
+// kernel takes; DN_OK otherwise.  Touches no device state.
+dn_status chunk_fwd_check_args(const void *q, const void *k, const void *v, const float *beta,
+                               const float *g, const float *h0, const int64_t *cu_seqlens, int n_seqs,
+                               int B, int T, int Nk, int Nv, int dk, int dv, dn_dtype dtype,
+                               float scale, unsigned flags, int chunk, const void *o, const float *ht);
 
 // Token-serial kernel (decode / short sequences): any supported shape.
 cudaError_t recurrent_launch(const Params &p, bool bf16, cudaStream_t stream, const char **name);

@@ -10,8 +10,14 @@
 // inputs and outputs only; the T' | T'' slots the tensor-core path keeps
 // between its two kernels live in g_noalloc_scratch below.
 //
-// The array is kNoAllocScratchBytes (64 MiB) of device memory that every GPU
-// on which this library's code is loaded holds until the process exits.
+// The array is kNoAllocScratchBytes (64 MiB) of device memory.  The device
+// copy of this file's module is made when the module is first used on a GPU:
+// with CUDA's default lazy module loading that is the first
+// dn_chunk_fwd_noalloc call on that GPU (its symbol lookup), which therefore
+// reserves the 64 MiB and can fail with DN_ERR_CUDA if the device memory is
+// already taken.  Callers make one call at set-up time, before they commit
+// the rest of the device memory; later calls reserve nothing more, and the
+// array is held until the process exits.
 // Nothing in it has to start at zero: every slot a call reads was written by
 // the same call.  All calls share it, so two calls whose kernels overlap on
 // the GPU (different streams, or different host threads on one device) race
@@ -19,6 +25,7 @@
 #include <mutex>
 
 #include "dn_chunk_fwd.h"
+#include "dn_internal.h"
 
 #define DN_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -61,6 +68,11 @@ DN_EXPORT dn_status dn_chunk_fwd_noalloc(const void *q, const void *k, const voi
                                          int B, int T, int Nk, int Nv, int dk, int dv,
                                          dn_dtype dtype, float scale, unsigned flags, int chunk,
                                          void *o, float *ht, dn_stream_t stream) {
+    // the same argument checks as dn_chunk_fwd first, so a bad argument is
+    // reported as such whatever the sizes
+    const dn_status args = dn::chunk_fwd_check_args(q, k, v, beta, g, h0, cu_seqlens, n_seqs, B, T, Nk, Nv,
+                                                    dk, dv, dtype, scale, flags, chunk, o, ht);
+    if (args != DN_OK) return args;
     const size_t need = dn_chunk_fwd_workspace_bytes(n_seqs, B, T, Nk, Nv, dk, dv, dtype, chunk);
     if (need > kNoAllocScratchBytes) return DN_ERR_UNSUPPORTED;
     void *ws = nullptr;

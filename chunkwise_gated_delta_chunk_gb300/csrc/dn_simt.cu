@@ -38,13 +38,6 @@
 #include "dn_internal.h"
 #include "dn_simt_common.cuh"
 
-#ifdef DN_TRACE
-__device__ unsigned long long g_simt_ph[64][16];
-extern "C" __attribute__((visibility("default"))) int dn_trace_dump_simt(void *dst) {
-    return (int)cudaMemcpyFromSymbol(dst, g_simt_ph, sizeof(g_simt_ph));
-}
-#endif
-
 namespace dn {
 namespace {
 
@@ -200,7 +193,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             }
         }
 
-        DN_PHASE(g_simt_ph, ci, 0);
         // ---- load the chunk (K and Q rows asynchronously, beside V) --------
         simt::load_rows_async<Tin, NT>(sK, k, t0, L, Nk, hk, dk, tid);
         simt::load_rows_async<Tin, NT>(sQ, q, t0, L, Nk, hk, dk, tid);
@@ -215,7 +207,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         simt::cp_async_wait_all();
         __syncthreads();
 
-        DN_PHASE(g_simt_ph, ci, 1);
         // ---- a1: gate prefix sum ----------------------------------------
         if (warp == 0) {
             float a = sG[lane], b = sG[lane + 32];
@@ -255,7 +246,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_simt_ph, ci, 2);
         // ---- a2: A (strictly lower) and P (lower incl. diagonal) ---------
         simt::kq_products<NT>(sK, sQ, ldkq, dk, L, tid, [&](int i, int j, float kk, float qk) {
             float a = 0.0f, pv = 0.0f;
@@ -269,12 +259,10 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         });
         __syncthreads();
 
-        DN_PHASE(g_simt_ph, ci, 3);
         // ---- a3: T = (I - A)^-1, blocked over 16 x 16 blocks ----------------
         // (sVn, written only in a5, is the solve's scratch)
         simt::solve_T_blocked<NT>(sA, LDC, nullptr, sT, LDC, sVn, L, tid);
 
-        DN_PHASE(g_simt_ph, ci, 4);
         // ---- a4/a5: R = diag(beta)(V - diag(e^G) K S_in); also Q S_in -----
         // thread: RP rows from i0; columns cg + 8 x (x < 4).  RP = 2 covers
         // 64 rows, RP = 1 the first 32 (enough for chunks of up to 32 tokens)
@@ -355,7 +343,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_simt_ph, ci, 5);
         // ---- a5: v_new = T R (row i per warp, lane = column) ---------------
         const int c = lane;
         {
@@ -380,7 +367,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
         }
         __syncthreads();
 
-        DN_PHASE(g_simt_ph, ci, 6);
         // ---- a6: o = scale e^G (Q S_in) + P v_new ------------------------
         if (want_o) {
             float acc[8];
@@ -403,7 +389,6 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
             }
         }
 
-        DN_PHASE(g_simt_ph, ci, 7);
         // ---- a5: S_out = e^{G_L} S_in + sum_i e^{G_L-G_i} k_i v_new_i^T ----
         // thread: columns 2 cp, 2 cp + 1; rows d0 .. d0 + 7 of S
         if constexpr (MMA) {

@@ -11,20 +11,6 @@
 
 #include "dn_internal.h"
 
-// Optional per-chunk phase stamps of CTA 0 (SM clock), compiled in only with
-// -DDN_TRACE for profiling builds; the default build contains no trace code.
-#ifdef DN_TRACE
-#define DN_PHASE(arr, ci, k)                                                  \
-    do {                                                                      \
-        if (blockIdx.x == 0 && threadIdx.x == 0 && (ci) < 64)                 \
-            (arr)[(ci)][(k)] = clock64();                                     \
-    } while (0)
-#else
-#define DN_PHASE(arr, ci, k) \
-    do {                     \
-    } while (0)
-#endif
-
 namespace dn {
 namespace simt {
 

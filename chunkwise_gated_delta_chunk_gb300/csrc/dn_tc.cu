@@ -58,25 +58,6 @@
 #include "dn_tmap.h"
 #include "tc_ptx.cuh"
 
-// Optional per-chunk event trace of the grid's last CTA (SM clock), compiled
-// in only with -DDN_TRACE for profiling builds; the default build contains no
-// trace code.
-#ifdef DN_TRACE
-__device__ unsigned long long g_dn_trace[16][1024][16];  // [warp][chunk][event]
-#define DN_TRACE_EV(ev, c)                                                    \
-    do {                                                                      \
-        if (blockIdx.x + 1 == gridDim.x && (threadIdx.x & 31) == 0 && (c) < 1024) \
-            g_dn_trace[threadIdx.x >> 5][(c)][(ev)] = clock64();              \
-    } while (0)
-extern "C" __attribute__((visibility("default"))) int dn_trace_dump(void *dst) {
-    return (int)cudaMemcpyFromSymbol(dst, g_dn_trace, sizeof(g_dn_trace));
-}
-#else
-#define DN_TRACE_EV(ev, c) \
-    do {                   \
-    } while (0)
-#endif
-
 namespace dn {
 namespace {
 
@@ -161,11 +142,7 @@ __device__ __forceinline__ float *scal(const Ctx &x, int s) {
 __device__ __noinline__ bool wait_slow(const Ctx &x, uint32_t b, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-#ifdef DN_WAIT_HINT
-        if (mbar_try_wait_sleep(b, parity, DN_WAIT_HINT)) return true;
-#else
         if (mbar_try_wait(b, parity)) return true;
-#endif
         if ((it & 31u) == 0) {
             if (*x.abort_flag) return false;
             if (globaltimer() - t0 > kTimeoutNs) {
@@ -290,7 +267,6 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
             chunk_norms_load(cs, static_cast<const uint8_t *>(p.ws) +
                                      ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n)) * kSlotBytes, lane);
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
-        DN_TRACE_EV(0, c);
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         if (lane == 0) {
             const uint32_t fb = bar(x, B_FULL + s);
@@ -304,11 +280,9 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
             tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
         }
         armed = c;
-        DN_TRACE_EV(2, c);
         chunk_scalars_store(p, cs, scal(x, s), lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
-        DN_TRACE_EV(1, c);
     }
 }
 
@@ -379,13 +353,11 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
         // this thread, so in order)
         if (!wait(x, bar(x, B_WSM_FULL), par)) break;
         if (!wait(x, bar(x, B_S_FULL), par)) break;
-        DN_TRACE_EV(2, c);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_ts(av, tm + TM_SB + 64 * t + kk * 8, sdesc(x.base + OFF_WT + kk * 2048, 8192, 1024), ID_VN, 1);
         mma_commit(bar(x, B_V_FULL));
-        DN_TRACE_EV(0, c);
         // U of the next chunk into the other acc_v buffer, whose last readers
         // (DS / PV of chunk c - 1) are done; PV of c - 1 also freed the P
         // buffer of chunk c + 1
@@ -404,7 +376,6 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
         for (int kk = 0; kk < 4; ++kk)
             mma_ts(tm + TM_S, av + 32 + kk * 8, sdesc(st + kk * 2048, 16384, 1024), ID_DS, 1);
         mma_commit(bar(x, B_S_UPD));
-        DN_TRACE_EV(1, c);
         // U of the next chunk, behind DS in the tensor pipe: issued while
         // v_new was converted it slowed that conversion more than it gains
         if (c + 1 < u.nc) {
@@ -416,7 +387,6 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
             load_ring(x, p, u, 1, c + 2);
             loaded[1] = c + 2;
         }
-        DN_TRACE_EV(3, c);
     }
     // every MMA issued by this thread completes before tensor memory is
     // freed, and the last ring copies it issued land before shared memory
@@ -556,21 +526,18 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         // then acc_s *= alpha(c+1), which DS(c+1) waits for (VSM_FULL).
         const bool last = c + 1 == u.nc;
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
-        DN_TRACE_EV(4, c);
         tc_fence_after();
         state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
-            DN_TRACE_EV(5, c);
             const int s1 = (c + 1) % NS;
             if (bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1))) break;
             state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 2);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_VSM_FULL));
-            DN_TRACE_EV(6, c);
         }
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
         tc_fence_after();
@@ -592,7 +559,6 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         }
         tc_fence_before();
         warp_arrive(bar(x, B_O_EMPTY));
-        DN_TRACE_EV(0, c);
         if (!p.o) continue;
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
@@ -617,7 +583,6 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
             }
             named_bar_sync(2, 128);
         }
-        DN_TRACE_EV(1, c);
     }
 }
 
@@ -661,12 +626,10 @@ __device__ void out_mma_role(const Ctx x, const Unit u, uint32_t tm) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool issue_w_mma(const Ctx &x, uint32_t tm, int c) {
     const bool ok = wait_tiles(x, c, 0);
-    DN_TRACE_EV(8, c);
     if (ok) {
         tc_fence_after();
         issue_w(x, tm, c);
         mma_commit(bar(x, B_WF));
-        DN_TRACE_EV(9, c);
     }
     return ok;
 }
@@ -679,7 +642,6 @@ __device__ __forceinline__ bool issue_w_mma(const Ctx &x, uint32_t tm, int c) {
 __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     const int s = c % NS;
     if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return false;
-    DN_TRACE_EV(10, c);
     const float *sc = scal(x, s);
     const int tid = threadIdx.x - 64;
 #pragma unroll
@@ -699,7 +661,6 @@ __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     }
     fence_proxy_async_smem();
     warp_arrive(bar(x, B_QS + s));
-    DN_TRACE_EV(12, c);
     return true;
 }
 
@@ -713,7 +674,6 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
     if (leader && u.nc > 0) lok = issue_w_mma(x, tm, 0);
     for (int c = 0; c < u.nc; ++c) {
         if (!wwait(x, bar(x, B_WF), c & 1) || !__all_sync(0xffffffffu, lok)) break;
-        DN_TRACE_EV(11, c);
         // W of chunk c is done with its T' buffer: it takes chunk c + 2's
         if (leader && c + 2 < u.nc) {
             load_ring(x, p, u, 0, c + 2);
@@ -722,7 +682,6 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
         // the -W^T buffer is free once the chain's VN of the chunk before has
         // completed
         if (c > 0 && !wwait(x, bar(x, B_V_FULL), (c - 1) & 1)) break;
-        DN_TRACE_EV(0, c);
         tc_fence_after();
         uint32_t r0[32], r1[32];
         tmem_ld32(lb + TM_W, r0);
@@ -745,7 +704,6 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(bar(x, B_WSM_FULL));
-        DN_TRACE_EV(3, c);
         // the next chunk's W, once all four warps have read acc_w (their
         // WSM arrivals)
         if (leader && c + 1 < u.nc) lok = wait(x, bar(x, B_WSM_FULL), c & 1) && issue_w_mma(x, tm, c + 1);
@@ -797,7 +755,6 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         // (D_FULL(c) needs this warpgroup's VSM(c), so the barrier is at most
         // one phase ahead here.)
         if (c > 0 && !wwait(x, bar(x, B_D_FULL), (c - 1) & 1)) return;
-        DN_TRACE_EV(0, c);
         tc_fence_after();
         {
             const float4 *dec4 = reinterpret_cast<const float4 *>(scal(x, s) + SC_DEC);
@@ -830,29 +787,23 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_VSM_FULL));
-            DN_TRACE_EV(1, c);
         }
         warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
         // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
         const bool last = (c + 1 == u.nc);
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
-        DN_TRACE_EV(2, c);
         tc_fence_after();
         state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col(p, u, c + 1, v));
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
-            DN_TRACE_EV(3, c);
         }
-        DN_TRACE_EV(5, c);
         if (last) break;
         const int s1 = (c + 1) % NS;
         if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
-        DN_TRACE_EV(6, c);
         state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 0);
         tmem_wait_st();  // ordered before the next v~ arrive (fence there)
-        DN_TRACE_EV(4, c);
     }
 }
 
@@ -872,7 +823,6 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     x.status = p.status;
     const int warp = threadIdx.x >> 5;
     const Unit u = unit_of(p);
-    DN_TRACE_EV(15, 1023);  // kernel start (per warp)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -936,12 +886,10 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         if ((threadIdx.x & 31) == 0) out_mma_role(x, u, tm);
         __syncwarp();
     }
-    DN_TRACE_EV(13, 1023);  // role done (per warp)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tm, TM_COLS);
-    DN_TRACE_EV(14, 1023);  // kernel end (per warp)
 }
 
 }  // namespace

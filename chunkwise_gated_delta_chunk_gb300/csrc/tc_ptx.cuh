@@ -68,20 +68,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with a suspend-time hint (ns): the warp may sleep until the phase
-// completes or the hint elapses instead of spinning on issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 // ---------------------------------------------------------------- bulk copies
 // One contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global memory into this CTA's shared memory; completion is

@@ -176,16 +176,21 @@ dn_status dn_recurrent_fwd(const void *q, const void *k, const void *v,
  *
  * Same arguments and results as dn_chunk_fwd, without a workspace: the
  * scratch space lives in one fixed device array of this library,
- * DN_NOALLOC_SCRATCH_BYTES long, that each GPU holds from the time the
- * library's code is loaded on it until the process exits.  The call
- * allocates nothing.
- *   - Sizes whose dn_chunk_fwd_workspace_bytes() exceeds
+ * DN_NOALLOC_SCRATCH_BYTES long.  The call allocates nothing itself.
+ *   - Arguments are checked exactly as dn_chunk_fwd checks them, first: a
+ *     bad argument gives DN_ERR_INVALID_ARG (or DN_ERR_UNSUPPORTED for a
+ *     shape no kernel takes) whatever the sizes.
+ *   - Then sizes whose dn_chunk_fwd_workspace_bytes() exceeds
  *     DN_NOALLOC_SCRATCH_BYTES are rejected with DN_ERR_UNSUPPORTED before
- *     anything is launched (64 MiB covers (floor(B*T/64) + n_seqs) * Nv <=
- *     2674, e.g. B = 4, T = 2048, Nv = 16).
+ *     anything is launched.
  *   - The first call with a given device current looks up the array's device
- *     address there (a host query that allocates nothing); make that first
- *     call before any stream capture on that device.
+ *     address there.  Under CUDA's default lazy module loading that lookup
+ *     also loads this part of the library onto the GPU, which is when the
+ *     GPU reserves the array: the first call can therefore fail with
+ *     DN_ERR_CUDA if device memory is already exhausted.  Make that first
+ *     call at set-up time, before committing the rest of the device memory
+ *     and before any stream capture on that device; later calls reserve
+ *     nothing, and the array is held until the process exits.
  *   - Every call uses the same array; its contents on entry do not matter.
  *     Calls whose kernels can overlap on one GPU (other streams, other host
  *     threads) race on it; calls ordered in one stream do not.

@@ -89,6 +89,30 @@ def test_optional_inputs(lib, gate, h0, final):
     check(inp, o, ht, label="gate=%s h0=%s" % (gate, h0))
 
 
+@pytest.mark.parametrize("dv,h0", [(128, False), (128, True), (256, False), (256, True)])
+def test_ungated_long_bf16(lib, dv, h0):
+    """Plain DeltaNet (g = NULL, [WY] §1) in bf16 at T = 8192 on the tensor-core
+    path: without gates the state never forgets, so rounding error is not
+    damped and this is the case closest to the bf16 bound."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = inputs(B=1, T=8192, Nk=2, Nv=2, dk=128, dv=dv, gate=None, h0=h0, seed=320 + dv + h0)
+    o, ht = run_gpu(inp)
+    assert dn.dn_last_kernel().startswith("wy_fwd")
+    res = check(inp, o, ht, label="ungated T=8192 dv=%d h0=%s" % (dv, h0))
+    print("ungated T=8192 dv=%d h0=%s" % (dv, h0), res)
+
+
+def test_ungated_long_varlen_gqa_bf16(lib):
+    """Plain DeltaNet, packed GQA batch with sequences longer than 4096."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = inputs(B=1, Nk=2, Nv=4, dk=128, dv=128, gate=None, h0=True,
+                 lengths=[5000, 1, 8200, 4097, 63], seed=330)
+    o, ht = run_gpu(inp)
+    assert dn.dn_last_kernel().startswith("wy_fwd")
+    res = check(inp, o, ht, label="ungated varlen GQA")
+    print("ungated varlen GQA", res)
+
+
 def test_custom_scale(lib):
     inp = inputs(dk=128, dv=128, seed=301)
     inp["scale"] = 0.37
