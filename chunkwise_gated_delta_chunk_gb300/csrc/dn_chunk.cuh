@@ -38,10 +38,11 @@ __device__ __forceinline__ long long seq_eos(const Params &p, int n) {
     return p.cu ? p.cu[n + 1] : (long long)(n + 1) * p.T;
 }
 
-// Workspace slot of the chunk that starts at token t0 of sequence n.  With
-// non-decreasing offsets, floor(t0 / C) + n is one-to-one over every chunk of
-// every sequence and stays below floor(tokens / C) + N.
-__device__ __forceinline__ long long wy_slot(long long t0, int n) { return t0 / kChunk + n; }
+// Workspace slot of the chunk that starts at token t0 of sequence n, for
+// chunks of `chunk` tokens.  With non-decreasing offsets, floor(t0 / chunk) + n
+// is one-to-one over every chunk of every sequence and stays below
+// floor(tokens / chunk) + N.
+__device__ __forceinline__ long long wy_slot(long long t0, int n, int chunk) { return t0 / chunk + n; }
 
 // Gate scalars of one chunk, per lane (tokens lane and lane + 32).
 struct ChunkScalars {

@@ -228,16 +228,16 @@ __device__ __forceinline__ Unit unit_of(const Params &p) {
         u.bos = (long long)u.n * p.T;
         u.eos = u.bos + p.T;
     }
-    u.nc = (int)((u.eos - u.bos + C - 1) / C);
+    u.nc = (int)((u.eos - u.bos + p.chunk - 1) / p.chunk);
     return u;
 }
 
 // Bulk copy of ring r (0: T', 1: T'', 2: P) of chunk c into buffer c & 1
 // (one thread; the buffer must be free).
 __device__ __forceinline__ void load_ring(const Ctx &x, const Params &p, const Unit &u, int r, int c) {
-    const long long t0 = u.bos + (long long)c * C;
+    const long long t0 = u.bos + (long long)c * p.chunk;
     const uint8_t *slot = static_cast<const uint8_t *>(p.ws) +
-                          ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n)) * kSlotBytes + 8192 * r;
+                          ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes + 8192 * r;
     const uint32_t fb = bar(x, B_TPF + 4 * r + (c & 1));
     mbar_arrive_expect_tx(fb, 8192);
     bulk_load(x.base + OFF_TP + r * 16384 + (c & 1) * 8192, slot, 8192, fb);
@@ -258,14 +258,15 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
             for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c);
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
-        const long long t0 = u.bos + (long long)c * C;
-        const int L = (int)min((long long)C, u.eos - t0);
+        const long long t0 = u.bos + (long long)c * p.chunk;
+        const int L = (int)min((long long)p.chunk, u.eos - t0);
         // the gates (and the WY kernel's inverse q / k norms) come from
         // global memory while the stage is still in use
         ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
         if (p.flags & kQkL2Norm)
             chunk_norms_load(cs, static_cast<const uint8_t *>(p.ws) +
-                                     ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n)) * kSlotBytes, lane);
+                                     ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes,
+                             lane);
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         if (lane == 0) {
@@ -411,7 +412,7 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 // d = 0, rows dv apart), or null when the states are not saved.
 __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, int v) {
     if (!p.hs) return nullptr;
-    const long long slot = wy_slot(u.bos + (long long)c * C, u.n);
+    const long long slot = wy_slot(u.bos + (long long)c * p.chunk, u.n, p.chunk);
     return p.hs + ((size_t)u.h * p.nslots + (size_t)slot) * DK * p.dv + u.v0 + v;
 }
 
@@ -541,8 +542,8 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         }
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
         tc_fence_after();
-        const long long t0 = u.bos + (long long)c * C;
-        const int L = (int)min((long long)C, u.eos - t0);
+        const long long t0 = u.bos + (long long)c * p.chunk;
+        const int L = (int)min((long long)p.chunk, u.eos - t0);
         // the chunk's output column v as packed bf16 pairs (tokens 2k, 2k + 1)
         // (with no o, as in the backward's state pass, only the hand-off)
         uint32_t ob[32];
@@ -894,11 +895,13 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
 
 }  // namespace
 
-bool tc_supported(int dk, int dv, bool bf16) { return bf16 && dk == DK && dv % BVT == 0; }
+bool tc_supported(int dk, int dv, bool bf16, int chunk) {
+    return bf16 && dk == DK && dv % BVT == 0 && (chunk == 16 || chunk == 32 || chunk == C);
+}
 
-size_t tc_workspace_bytes(long long tokens, int N, int Nv) {
-    if (tokens <= 0 || N <= 0) return 0;
-    return (size_t)(tokens / C + N) * (size_t)Nv * kSlotBytes;
+size_t tc_workspace_bytes(long long tokens, int N, int Nv, int chunk) {
+    if (tokens <= 0 || N <= 0 || chunk <= 0) return 0;
+    return (size_t)(tokens / chunk + N) * (size_t)Nv * kSlotBytes;
 }
 
 cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {

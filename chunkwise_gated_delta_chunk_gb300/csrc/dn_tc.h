@@ -8,9 +8,11 @@
 
 namespace dn {
 
-bool tc_supported(int dk, int dv, bool bf16);
+// chunk: tokens per chunk (16, 32 or 64; a chunk occupies the first `chunk`
+// rows of the kernels' 64-row tiles).
+bool tc_supported(int dk, int dv, bool bf16, int chunk);
 // Workspace bytes the tensor-core path needs (0 for no tokens).
-size_t tc_workspace_bytes(long long tokens, int N, int Nv);
+size_t tc_workspace_bytes(long long tokens, int N, int Nv, int chunk);
 cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name);
 cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream);
 

@@ -320,15 +320,15 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
     int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (wy_slot(seq_bos(p, mid), mid) <= slot) lo = mid; else hi = mid - 1;
+        if (wy_slot(seq_bos(p, mid), mid, p.chunk) <= slot) lo = mid; else hi = mid - 1;
     }
     const int n = lo;
     const long long bos = seq_bos(p, n), eos = seq_eos(p, n);
     if (bos < 0 || eos < bos || eos > p.tokens) return true;  // the scan kernel reports it
-    const long long c = slot - wy_slot(bos, n);
-    const long long t0 = bos + c * C;
+    const long long c = slot - wy_slot(bos, n, p.chunk);
+    const long long t0 = bos + c * p.chunk;
     if (c < 0 || t0 >= eos) return true;  // a slot no chunk maps to
-    const int L = (int)min((long long)C, eos - t0);
+    const int L = (int)min((long long)p.chunk, eos - t0);
     const int hk = h / (p.Nv / p.Nk);
     const uint32_t par = g.it & 1;
     ++g.it;

@@ -99,7 +99,8 @@ def test_invalid_arguments_rejected_on_host(clib, over, code):
 
 
 def test_workspace_size(clib):
-    """One 24.5 KB slot per (floor(tokens/64) + N) x Nv on the tensor-core path, none elsewhere."""
+    """One 24.5 KB slot per (floor(tokens/C) + N) x Nv on the tensor-core path (C the chunk
+    length), none elsewhere."""
     ws = clib.dn_chunk_fwd_workspace_bytes
     assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 25088
     assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 25088
@@ -107,7 +108,9 @@ def test_workspace_size(clib):
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
     assert ws(0, 0, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0
-    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 32) == 0     # chunk 32: CUDA-core path
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 32) == (2 * 64 // 32 + 2) * 2 * 25088
+    assert ws(1, 1, 100, 2, 2, 128, 128, dn.DN_BF16, 16) == (100 // 16 + 1) * 2 * 25088
+    assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 32) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_BF16, 48) == 0     # rejected chunk size
 
 

@@ -61,6 +61,43 @@ def test_chunk_sizes(lib, chunk, dtype, dk, dv):
     check(inp, o, ht, label="C=%d varlen" % chunk)
 
 
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_chunk_sizes_tensor_core_path(lib, chunk):
+    """bf16 with dk = 128 runs C = 16 and 32 on the tensor-core kernels (a chunk
+    fills the first C rows of their 64-row tiles): extreme gates, many short
+    packed sequences, in-kernel q / k normalisation, and dv = 256."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    cases = []
+    inp = inputs(B=2, T=150, dk=128, dv=128, seed=470 + chunk)
+    inp["g"] = torch.full_like(inp["g"], -30.0)
+    cases.append(("g=-30", inp))
+    inp = inputs(B=2, T=150, dk=128, dv=128, seed=471 + chunk)
+    inp["g"] = torch.zeros_like(inp["g"])
+    inp["beta"] = torch.ones_like(inp["beta"])
+    cases.append(("g=0 beta=1", inp))
+    cases.append(("many short", inputs(B=1, Nk=2, Nv=4, dk=128, dv=128, seed=472 + chunk,
+                                       lengths=[16, 15, 17, 1, 0, 33, 31, 64, 65, 2, 130])))
+    cases.append(("qk l2norm", inputs(B=2, T=140, dk=128, dv=128, seed=473 + chunk, raw_qk=True)))
+    cases.append(("dv=256 no gate", inputs(B=1, T=200, dk=128, dv=256, gate=None, seed=474 + chunk)))
+    for label, inp in cases:
+        o, ht = run_gpu(inp, chunk=chunk)
+        assert dn.dn_last_kernel().startswith("wy_fwd"), dn.dn_last_kernel()
+        check(inp, o, ht, label="C=%d %s" % (chunk, label))
+
+
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_chunk_sizes_headline_full_size(lib, chunk):
+    """The headline shapes (B = 4, H = 16, T = 2048, d = 128) at C = 16 and 32,
+    on sampled (sequence, head) units, in the launch configuration the
+    benchmark times with --chunk."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    inp = workloads.workload_inputs("gdn_bf16_b4_h16_t2048_d128")
+    o, ht = run_gpu(inp, chunk=chunk)
+    assert dn.dn_last_kernel().startswith("wy_fwd"), dn.dn_last_kernel()
+    res = check(inp, o, ht, units=[0, 21, 63], label="headline C=%d" % chunk)
+    print("headline C=%d" % chunk, res)
+
+
 def test_chunk_sizes_agree(lib):
     """The same inputs at C = 16, 32 and 64 agree with each other to the
     rounding of the two paths (the chunk form is exact, [WY] §6)."""
