@@ -76,5 +76,41 @@ def build(force: bool = False, extra: list[str] | None = None) -> str:
     return LIB
 
 
+# Translation units that change in the failure-path test build.
+STALL_SOURCES = ("dn_api.cu", "dn_tc.cu", "dn_wy.cu")
+STALL_LIB = os.path.join(BUILD, "stall", "libdnchunk_stall.so")
+
+
+def build_stall_variant() -> str:
+    """Build the failure-path test variant of the library (never the product
+    library): dn_api.cu, dn_tc.cu and dn_wy.cu compiled with -DDN_TEST_STALL
+    (2 ms wait limit, the dn_test_stall_next hook), linked with the other
+    objects of the regular build, into ``_build/stall/libdnchunk_stall.so``."""
+    build()
+    out = os.path.dirname(STALL_LIB)
+    os.makedirs(out, exist_ok=True)
+    stall_srcs = [os.path.join(CSRC, f) for f in STALL_SOURCES]
+
+    def one(src: str) -> str:
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc()] + NVCC_FLAGS + ["-DDN_TEST_STALL", "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s" % (src, r.stderr))
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(stall_srcs)) as ex:
+        objs = list(ex.map(one, stall_srcs))
+    objs += [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources()
+             if os.path.basename(s) not in STALL_SOURCES]
+    tmp = STALL_LIB + ".tmp%d" % os.getpid()
+    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s" % r.stderr)
+    os.replace(tmp, STALL_LIB)
+    return STALL_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv))

@@ -25,6 +25,12 @@ unsigned *g_status_ptr[kMaxDevices];
 
 thread_local const char *t_last_kernel = "";
 
+#ifdef DN_TEST_STALL
+// The failure-path test build's hook: the next dn_chunk_fwd call on this
+// thread makes one bounded wait run out (kStallScan / kStallWy).
+thread_local unsigned t_test_stall = 0;
+#endif
+
 // Device address of g_dn_status on the current device (looked up once per
 // device; the lookup is a host call that allocates nothing).
 cudaError_t status_ptr(unsigned **out) {
@@ -130,6 +136,10 @@ DN_EXPORT dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
     p.nslots = tokens / chunk + n_seqs;
     p.chunk = chunk;
     p.flags = flags;
+#ifdef DN_TEST_STALL
+    p.test_stall = t_test_stall;
+    t_test_stall = 0;
+#endif
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;
 
     const char *name = "";
@@ -281,3 +291,9 @@ DN_EXPORT const char *dn_status_str(dn_status status) {
 }
 
 DN_EXPORT const char *dn_last_kernel(void) { return t_last_kernel; }
+
+#ifdef DN_TEST_STALL
+// Exported only by the failure-path test build (-DDN_TEST_STALL), never by
+// the library's own build: arm a stall for the next dn_chunk_fwd call.
+DN_EXPORT void dn_test_stall_next(unsigned mode) { t_test_stall = mode; }
+#endif

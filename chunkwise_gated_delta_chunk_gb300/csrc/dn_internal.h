@@ -17,6 +17,21 @@ constexpr unsigned kStatusBadSeq = 2u;    // cu_seqlens out of order / out of ra
 // Option bits of Params::flags (the public DN_ flags of the same value).
 constexpr unsigned kQkL2Norm = 1u;        // q and k rows divided by max(||x||_2, 1e-12)
 
+// Limit of every bounded mbarrier wait of the tensor-core kernels.  A build
+// for the failure-path test (-DDN_TEST_STALL) shortens it, so that a wait
+// that runs out costs milliseconds, not seconds.
+#ifdef DN_TEST_STALL
+constexpr unsigned long long kWaitLimitNs = 2000000ull;     // 2 ms
+#else
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+#endif
+
+// Params::test_stall in a -DDN_TEST_STALL build: the call makes one wait run
+// out on purpose (1: the scan kernel's first stage never completes; 2: the
+// first item of one WY worker expects more TMA bytes than arrive).  Always 0
+// in the library's own build, which contains none of this code.
+constexpr unsigned kStallScan = 1u, kStallWy = 2u;
+
 struct Params {
     const void *q, *k, *v;     // [tokens, Nk, dk], [tokens, Nk, dk], [tokens, Nv, dv]
     const float *beta, *g;     // [tokens, Nv]; g may be null
@@ -32,6 +47,7 @@ struct Params {
     long long nslots;          // floor(tokens / C) + N
     int chunk;                 // chunk length: 64 (both paths) or 16 / 32 (CUDA-core path)
     unsigned flags;            // kQkL2Norm
+    unsigned test_stall;       // 0, or kStallScan / kStallWy in a -DDN_TEST_STALL build
     // backward (dn_chunk_bwd) only; null elsewhere
     float *hs;                 // [Nv][nslots][dk][dv]: state before each 64-token chunk (slot t0/64 + n)
     const void *dout;          // [tokens, Nv, dv] gradient of o (dtype of q)

@@ -69,7 +69,7 @@ constexpr int BVT = 128;       // value columns per CTA
 constexpr int NS = 3;          // pipeline stages of K/Q/V tiles
 constexpr int NTHREADS = 480;
 constexpr int kLeadCtas = 12;  // placement lead of the scan grid (tc_launch)
-constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint64_t kTimeoutNs = kWaitLimitNs;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
 constexpr uint32_t STAGE_BYTES = 49152;  // K0 Q0 K1 Q1 V0 V1, 8 KB each
@@ -283,6 +283,11 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         armed = c;
         chunk_scalars_store(p, cs, scal(x, s), lane);
         __syncwarp();
+#ifdef DN_TEST_STALL
+        // failure-path test: the first stage's second arrival never comes, so
+        // every wait on it runs out (its TMA bytes still land)
+        if (p.test_stall == kStallScan && c == 0) continue;
+#endif
         if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
     }
 }

@@ -48,7 +48,7 @@ using namespace ptx;
 
 constexpr int C = kChunk;  // 64
 constexpr int NT = 128;
-constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint64_t kTimeoutNs = kWaitLimitNs;
 
 // Shared memory (offsets from a 1024-byte aligned base).  The tile region is
 // free once the MMA has read it and then holds A / T and the solve scratch.
@@ -337,7 +337,14 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
     if (warp == 0) {
         if (lane == 0) {
             *okf = 1;
-            mbar_arrive_expect_tx(b_tma, 32768);
+            uint32_t tx = 32768;
+#ifdef DN_TEST_STALL
+            // failure-path test: the first item of worker 0 expects 16 bytes
+            // more than its four copies bring, so its wait runs out after the
+            // copies have landed
+            if (p.test_stall == kStallWy && blockIdx.x == 0 && g.it == 1) tx += 16;
+#endif
+            mbar_arrive_expect_tx(b_tma, tx);
             tma_load_3d(g.base + OFF_K, mK, b_tma, 0, hk, (int)t0);
             tma_load_3d(g.base + OFF_K + 8192, mQ, b_tma, 0, hk, (int)t0);
             tma_load_3d(g.base + OFF_K + 16384, mK, b_tma, 64, hk, (int)t0);
