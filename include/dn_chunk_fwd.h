@@ -100,9 +100,10 @@ typedef enum {
  *   scale       multiplies q in the output; scale <= 0 selects 1/sqrt(dk).
  *   flags       0 or DN_QK_L2NORM (q and k rows normalised in the kernels).
  *   chunk       chunk length C: 16, 32 or 64 ([WY] §5 chunk_size; the result
- *               is the same up to rounding, [WY] §6).  64 runs the tensor-core
- *               path where it applies; 16 and 32 run the CUDA-core kernel.
- *               Other values: DN_ERR_UNSUPPORTED.
+ *               is the same up to rounding, [WY] §6).  The tensor-core path
+ *               takes all three (a chunk fills the first C rows of its 64-row
+ *               tiles, so a step costs about the same at every C and C = 64
+ *               is the fastest); other values: DN_ERR_UNSUPPORTED.
  *   o           [B, T, Nv, dv]  dtype       output, written for every token of
  *                                           every sequence (rounded to nearest
  *                                           even from fp32 for DN_BF16).
@@ -117,12 +118,23 @@ typedef enum {
  *
  * Returns DN_OK once the work is enqueued; DN_ERR_INVALID_ARG also when the
  * workspace is missing, misaligned or too small.  The tensor-core path
- * (bf16, dk = 128, dv a multiple of 128, chunk 64) launches two kernels per
- * call: the per-chunk WY inverse T and causal scores of every chunk in
- * parallel ([WY] §2.3-§2.4), then the sequential state scan and output
- * ([CGDR] §3.2-§3.3).  Other shapes and chunk sizes launch one CUDA-core
- * kernel; for DN_BF16 its state products (K S, Q S, the state update) are
- * TF32 tensor-core tiles with fp32 accumulation, within the bf16 bound.
+ * (bf16, dk = 128, dv a multiple of 128) launches two kernels per call: the
+ * per-chunk WY inverse T and causal scores of every chunk in parallel
+ * ([WY] §2.3-§2.4), then the sequential state scan and output ([CGDR]
+ * §3.2-§3.3).  Other shapes launch one CUDA-core kernel; for DN_BF16 its
+ * state products (K S, Q S, the state update) are TF32 tensor-core tiles with
+ * fp32 accumulation, within the bf16 bound.
+ *
+ * Why a workspace.  The per-chunk work that needs no state (the inverse T,
+ * the scores P) runs for all chunks at once in the first kernel; only the
+ * scan is sequential.  The two kernels hand over three 64 x 64 bf16 matrices
+ * per chunk and value head through the workspace (mostly through L2 between
+ * the two launches).  A single kernel that formed T beside the scan put that
+ * work back on the scan's serial path and measured slower (158 against about
+ * 120 us per forward at B = 4, H = 16, T = 2048, d = 128).  So the call takes
+ * the caller's workspace instead of allocating one (dn_chunk_fwd_noalloc
+ * below uses a fixed array of the library instead), plus the flags and chunk
+ * arguments of the options it implements.
  */
 dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
                        const float *beta, const float *g, const float *h0,
@@ -135,7 +147,8 @@ dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
 /*
  * dn_chunk_fwd_workspace_bytes -- bytes of workspace dn_chunk_fwd needs for
  * these sizes (same meaning as there).  For the tensor-core path it is
- * (floor(B*T / 64) + n_seqs) * Nv * 25088: one slot per chunk and value head
+ * (floor(B*T / C) + n_seqs) * Nv * 25088 (C the chunk length): one slot per
+ * chunk and value head
  * holding three bf16 64 x 64 matrices of the chunk, T diag(beta e^G) and
  * T diag(beta) of its WY representation ([WY] §2.4) and its causal score
  * matrix tril(scale QK^T . D) ([CGDR] §3.2), then the chunk's 64 key and 64
