@@ -42,7 +42,8 @@ __device__ __forceinline__ long long seq_eos(const Params &p, int n) {
 // chunks of `chunk` tokens.  With non-decreasing offsets, floor(t0 / chunk) + n
 // is one-to-one over every chunk of every sequence and stays below
 // floor(tokens / chunk) + N.
-__device__ __forceinline__ long long wy_slot(long long t0, int n, int chunk) { return t0 / chunk + n; }
+// (chunk is a power of two on every path that has slots.)
+__device__ __forceinline__ long long wy_slot(long long t0, int n, int chunk) { return (t0 >> (__ffs(chunk) - 1)) + n; }
 
 // Gate scalars of one chunk, per lane (tokens lane and lane + 32).
 struct ChunkScalars {
@@ -52,20 +53,31 @@ struct ChunkScalars {
     int L;
 };
 
-// Loads and prefix-sums the gates of the chunk [t0, t0 + L) of value head h
-// (one warp).  Tokens past L get beta = 0 and g = 0, so they write nothing
-// and decay nothing.
-__device__ __forceinline__ ChunkScalars chunk_scalars_load(const Params &p, int h, long long t0, int L, int lane) {
-    ChunkScalars r;
-    float ga = 0.f, gb = 0.f, ba = 0.f, bb = 0.f;
+// The raw gates and betas of a chunk's tokens lane and lane + 32 (one warp),
+// loaded ahead of their use.  Tokens past L get beta = 0 and g = 0, so they
+// write nothing and decay nothing.
+struct ChunkGates {
+    float ga, gb, ba, bb;
+};
+
+__device__ __forceinline__ ChunkGates chunk_gates_load(const Params &p, int h, long long t0, int L, int lane) {
+    ChunkGates r{0.f, 0.f, 0.f, 0.f};
     if (lane < L) {
-        ba = p.beta[(t0 + lane) * p.Nv + h];
-        if (p.g) ga = p.g[(t0 + lane) * p.Nv + h];
+        r.ba = p.beta[(t0 + lane) * p.Nv + h];
+        if (p.g) r.ga = p.g[(t0 + lane) * p.Nv + h];
     }
     if (lane + 32 < L) {
-        bb = p.beta[(t0 + lane + 32) * p.Nv + h];
-        if (p.g) gb = p.g[(t0 + lane + 32) * p.Nv + h];
+        r.bb = p.beta[(t0 + lane + 32) * p.Nv + h];
+        if (p.g) r.gb = p.g[(t0 + lane + 32) * p.Nv + h];
     }
+    return r;
+}
+
+// Prefix-sums the gates of the chunk [t0, t0 + L) (one warp).
+__device__ __forceinline__ ChunkScalars chunk_scalars_from(const ChunkGates &in, int L, int lane) {
+    ChunkScalars r;
+    float ga = in.ga, gb = in.gb;
+    const float ba = in.ba, bb = in.bb;
     // inclusive prefix sums G_i = g_0 + ... + g_i
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -133,6 +145,12 @@ __device__ __forceinline__ void chunk_scalars_store(const Params &p, const Chunk
         sc[SC_L] = __int_as_float(r.L);
         sc[SC_FACT] = (r.span <= kSpanMax) ? 1.f : 0.f;
     }
+}
+
+// Loads and prefix-sums the gates of the chunk [t0, t0 + L) of value head h
+// (one warp).
+__device__ __forceinline__ ChunkScalars chunk_scalars_load(const Params &p, int h, long long t0, int L, int lane) {
+    return chunk_scalars_from(chunk_gates_load(p, h, t0, L, lane), L, lane);
 }
 
 // Gate scalars of the chunk [t0, t0 + L) of value head h, computed by one

@@ -62,9 +62,19 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     ptx::tc_fence_after();
     g.tm = *reinterpret_cast<volatile uint32_t *>(gb + wy::OFF_BAR + 16);
 
-    const long long items = p.nslots * p.Nv;
-    for (long long item = blockIdx.x; item < items; item += gridDim.x)
-        if (!wy::item<QKN>(g, &mK, &mQ, p, item / p.Nv, (int)(item % p.Nv))) break;
+    // items (< 2^31, checked at launch) in steps of the grid; each item's
+    // gates are loaded during the item before
+    const unsigned items = (unsigned)(p.nslots * p.Nv), nv = (unsigned)p.Nv;
+    ChunkGates gates{0.f, 0.f, 0.f, 0.f};
+    if (threadIdx.x < 32 && blockIdx.x < items)
+        gates = wy::item_gates(p, blockIdx.x / nv, (int)(blockIdx.x % nv), threadIdx.x);
+    for (unsigned it = blockIdx.x; it < items; it += gridDim.x) {
+        const unsigned nx = it + gridDim.x;
+        const wy::ItemLoc loc = wy::locate(p, it / nv);
+        if (!wy::item<QKN>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
+                           nx < items ? (long long)(nx / nv) : -1, (int)(nx % nv)))
+            break;
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if (threadIdx.x < 32) {

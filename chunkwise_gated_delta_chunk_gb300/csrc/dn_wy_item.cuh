@@ -305,30 +305,62 @@ __device__ __forceinline__ void group_init(const Group &g) {
     }
 }
 
-// The item of workspace slot `slot` and value head h.  Returns false when a
-// wait ran out (the worker must stop).
+// Where the chunk of workspace slot `slot` lies: sequence n, first token t0
+// and length L.  valid is false for a slot no chunk maps to and for a
+// malformed sequence (which the scan kernel reports).
+struct ItemLoc {
+    long long t0;
+    int n, L;
+    bool valid;
+};
+
+__device__ __forceinline__ ItemLoc locate(const Params &p, long long slot) {
+    ItemLoc r{0, 0, 0, false};
+    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (wy_slot(seq_bos(p, mid), mid, p.chunk) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const long long bos = seq_bos(p, lo), eos = seq_eos(p, lo);
+    if (bos < 0 || eos < bos || eos > p.tokens) return r;
+    const long long c = slot - wy_slot(bos, lo, p.chunk);
+    const long long t0 = bos + c * p.chunk;
+    if (c < 0 || t0 >= eos) return r;
+    r.t0 = t0;
+    r.n = lo;
+    r.L = (int)min((long long)p.chunk, eos - t0);
+    r.valid = true;
+    return r;
+}
+
+// Warp 0: the gates of the item of slot `slot`, value head h (zero where no
+// chunk maps to the slot).
+__device__ __forceinline__ ChunkGates item_gates(const Params &p, long long slot, int h, int lane) {
+    const ItemLoc l = locate(p, slot);
+    if (!l.valid) return ChunkGates{0.f, 0.f, 0.f, 0.f};
+    return chunk_gates_load(p, h, l.t0, l.L, lane);
+}
+
+// The item of workspace slot `slot` and value head h, located at `loc`.
+// Warp 0 enters with the item's gates in `gates` (loaded ahead) and leaves
+// with those of the worker's next item (slot next_slot < 0: none; value head
+// next_h), whose loads then overlap the rest of this item.  Returns false
+// when a wait ran out (the worker must stop).
 template <bool QKN>
 __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, const Params &p, long long slot,
-                     int h) {
+                     int h, const ItemLoc &loc, ChunkGates &gates, long long next_slot, int next_h) {
     const int warp = g.tid >> 5, lane = g.tid & 31;
     const uint32_t b_tma = g.base + OFF_BAR, b_mma = g.base + OFF_BAR + 8;
     volatile int *okf = reinterpret_cast<volatile int *>(g.gb + OFF_BAR + 20);
     float *sc = reinterpret_cast<float *>(g.gb + OFF_SC);
     float *sA = reinterpret_cast<float *>(g.gb + OFF_K);
     float *scr = reinterpret_cast<float *>(g.gb + OFF_SCR);
-    // ---- which chunk: slot -> (sequence n, chunk c) ------------------
-    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (wy_slot(seq_bos(p, mid), mid, p.chunk) <= slot) lo = mid; else hi = mid - 1;
+    if (!loc.valid) {
+        if (warp == 0 && next_slot >= 0) gates = item_gates(p, next_slot, next_h, lane);
+        return true;
     }
-    const int n = lo;
-    const long long bos = seq_bos(p, n), eos = seq_eos(p, n);
-    if (bos < 0 || eos < bos || eos > p.tokens) return true;  // the scan kernel reports it
-    const long long c = slot - wy_slot(bos, n, p.chunk);
-    const long long t0 = bos + c * p.chunk;
-    if (c < 0 || t0 >= eos) return true;  // a slot no chunk maps to
-    const int L = (int)min((long long)p.chunk, eos - t0);
+    const long long t0 = loc.t0;
+    const int L = loc.L;
     const int hk = h / (p.Nv / p.Nk);
     const uint32_t par = g.it & 1;
     ++g.it;
@@ -350,7 +382,9 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
             tma_load_3d(g.base + OFF_K + 16384, mK, b_tma, 64, hk, (int)t0);
             tma_load_3d(g.base + OFF_K + 24576, mQ, b_tma, 64, hk, (int)t0);
         }
-        chunk_scalars(p, h, t0, L, sc, lane);
+        chunk_scalars_store(p, chunk_scalars_from(gates, L, lane), sc, lane);
+        // the next item's gates: their loads run under this item's work
+        if (next_slot >= 0) gates = item_gates(p, next_slot, next_h, lane);
         __syncwarp();
         if (lane == 0) {
             bool ok = wait_bounded(b_tma, par);
