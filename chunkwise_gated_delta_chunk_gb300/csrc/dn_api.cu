@@ -60,15 +60,15 @@ static_assert(DN_QK_L2NORM == dn::kQkL2Norm, "public and internal flag bits agre
 // tensor-core path keeps T' | T'' of every chunk there between its two kernels.
 bool chunk_ok(int chunk) { return chunk == 16 || chunk == 32 || chunk == dn::kChunk; }
 
-// The tensor-core path takes bf16, dk = 128 and dv a multiple of 128, at every
-// chunk length; everything else runs on the CUDA-core kernel.
+// The tensor-core path takes bf16, dk = 128 or 256 and dv a multiple of 128,
+// at every chunk length; everything else runs on the CUDA-core kernel.
 bool use_tc(long long tokens, int dk, int dv, dn_dtype dtype, int chunk) {
     return tokens > 0 && dn::tc_supported(dk, dv, dtype == DN_BF16, chunk);
 }
 
 size_t workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype, int chunk) {
     if (!use_tc(tokens, dk, dv, dtype, chunk)) return 0;
-    return dn::tc_workspace_bytes(tokens, n_seqs, Nv, chunk);
+    return dn::tc_workspace_bytes(tokens, n_seqs, Nv, dk, chunk);
 }
 
 }  // namespace
@@ -202,7 +202,7 @@ size_t bwd_states_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv) {
 
 size_t bwd_workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype) {
     size_t b = bwd_states_bytes(tokens, n_seqs, Nv, dk, dv);
-    if (use_tc(tokens, dk, dv, dtype, dn::kChunk)) b += dn::tc_workspace_bytes(tokens, n_seqs, Nv, dn::kChunk);
+    if (use_tc(tokens, dk, dv, dtype, dn::kChunk)) b += dn::tc_workspace_bytes(tokens, n_seqs, Nv, dk, dn::kChunk);
     return b;
 }
 

@@ -1155,7 +1155,7 @@ cudaError_t bwd_launch(const Params &p, bool bf16, cudaStream_t stream, const ch
     f.o = nullptr;
     f.ht = nullptr;
     f.chunk = kChunk;
-    const bool tc = p.tokens > 0 && tc_supported(p.dk, p.dv, bf16, kChunk);
+    const bool tc = p.tokens > 0 && p.dk == 128 && tc_supported(p.dk, p.dv, bf16, kChunk);
     if (tc && !p.ws) return cudaErrorInvalidValue;
     const char *fname = "";
     if ((err = tc ? tc_launch(f, stream, &fname) : simt_launch(f, bf16, false, stream, &fname)) != cudaSuccess) return err;

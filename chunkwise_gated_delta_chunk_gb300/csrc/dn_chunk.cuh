@@ -19,16 +19,23 @@ constexpr int SC_G = 0, SC_BETA = 64, SC_BEG = 128, SC_DEC = 192, SC_OSC = 256, 
 constexpr int SCAL_FLOATS = 512;
 constexpr float kSpanMax = 80.f;
 
-// Bytes of one workspace slot: T' = T diag(beta e^G), T'' = T diag(beta) and
-// P = tril(scale QK^T . D), each a 64 x 64 bf16 matrix stored as the
-// 128-byte-swizzled K-major image the MMAs read (row i at 128 i, 16-byte
-// chunk c at (c ^ (i & 7)) * 16), in that order; then, with kQkL2Norm, the
-// fp32 factors 1 / max(||k_i||, 1e-12) and 1 / max(||q_i||, 1e-12) of the
-// chunk's 64 rows (the WY kernel folds them into T' and P; the scan kernel
-// folds them into its per-token factors).
+// One workspace slot of the tensor-core path holds a chunk's per-chunk
+// operands for one value head, each a bf16 matrix stored as the
+// 128-byte-swizzled image the MMAs read (row i at 128 i, 16-byte chunk c at
+// (c ^ (i & 7)) * 16):
+//   dk = 128: T' = T diag(beta e^G) (64 x 64), then T'' and P;
+//   dk = 256: -W^T = -(T' K)^T (256 rows d x 64 tokens), then T'' and P;
+// with T'' = T diag(beta) and P = tril(scale QK^T . D) (64 x 64 each); then,
+// with kQkL2Norm, the fp32 factors 1 / max(||k_i||, 1e-12) and
+// 1 / max(||q_i||, 1e-12) of the chunk's 64 rows (the WY kernel folds them
+// into T', W and P; the scan kernel folds them into its per-token factors).
 constexpr uint32_t kImageBytes = 8192;
-constexpr uint32_t kSlotNormOff = 3 * kImageBytes;  // 64 key factors, then 64 query factors
-constexpr uint32_t kSlotBytes = kSlotNormOff + 2 * 64 * 4;
+__host__ __device__ constexpr uint32_t slot_tu_off(int dk) { return dk == 256 ? 32768u : kImageBytes; }
+__host__ __device__ constexpr uint32_t slot_p_off(int dk) { return slot_tu_off(dk) + kImageBytes; }
+__host__ __device__ constexpr uint32_t slot_norm_off(int dk) { return slot_p_off(dk) + kImageBytes; }
+__host__ __device__ constexpr uint32_t slot_bytes(int dk) { return slot_norm_off(dk) + 2 * 64 * 4; }
+constexpr uint32_t kSlotNormOff = slot_norm_off(128);  // 64 key factors, then 64 query factors
+constexpr uint32_t kSlotBytes = slot_bytes(128);
 
 __device__ __forceinline__ long long seq_bos(const Params &p, int n) {
     return p.cu ? p.cu[n] : (long long)n * p.T;
@@ -109,10 +116,10 @@ __device__ __forceinline__ ChunkScalars chunk_scalars_from(const ChunkGates &in,
     return r;
 }
 
-// The chunk's inverse key and query norms from its workspace slot (written
-// by the WY kernel), for the lane's two tokens.
-__device__ __forceinline__ void chunk_norms_load(ChunkScalars &r, const uint8_t *slot, int lane) {
-    const float *f = reinterpret_cast<const float *>(slot + kSlotNormOff);
+// The chunk's inverse key and query norms from the factors in its workspace
+// slot (written by the WY kernel), for the lane's two tokens.
+__device__ __forceinline__ void chunk_norms_load(ChunkScalars &r, const uint8_t *norms, int lane) {
+    const float *f = reinterpret_cast<const float *>(norms);
     r.ka = f[lane];
     r.kb = f[lane + 32];
     r.qa = f[64 + lane];

@@ -57,11 +57,13 @@
 #include "dn_tc.h"
 #include "dn_tmap.h"
 #include "tc_ptx.cuh"
+#include "dn_tc_sync.cuh"
 
 namespace dn {
 namespace {
 
 using namespace ptx;
+using namespace tcs;
 
 constexpr int C = kChunk;      // 64
 constexpr int DK = 128;
@@ -69,7 +71,6 @@ constexpr int BVT = 128;       // value columns per CTA
 constexpr int NS = 3;          // pipeline stages of K/Q/V tiles
 constexpr int NTHREADS = 480;
 constexpr int kLeadCtas = 12;  // placement lead of the scan grid (tc_launch)
-constexpr uint64_t kTimeoutNs = kWaitLimitNs;
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
 constexpr uint32_t STAGE_BYTES = 49152;  // K0 Q0 K1 Q1 V0 V1, 8 KB each
@@ -126,74 +127,9 @@ constexpr uint32_t ID_O = idesc_bf16(128, 64, 0, 0);    // A TMEM, B K-major (Q 
 constexpr uint32_t ID_DS = idesc_bf16(128, 128, 0, 1);  // A TMEM, B MN-major (K rows)
 constexpr uint32_t ID_PV = idesc_bf16(128, 64, 0, 0);   // A TMEM, B K-major (P rows)
 
-struct Ctx {
-    uint32_t base;     // shared address of the aligned base
-    uint8_t *gbase;    // generic pointer to the same
-    volatile int *abort_flag;
-    unsigned *status;
-};
-
 __device__ __forceinline__ uint32_t bar(const Ctx &x, int i) { return x.base + OFF_BAR + 8u * i; }
 __device__ __forceinline__ float *scal(const Ctx &x, int s) {
     return reinterpret_cast<float *>(x.gbase + OFF_SCAL + s * SCAL_FLOATS * 4);
-}
-
-// Bounded wait.  Returns false once the CTA is aborting.
-__device__ __noinline__ bool wait_slow(const Ctx &x, uint32_t b, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(b, parity)) return true;
-        if ((it & 31u) == 0) {
-            if (*x.abort_flag) return false;
-            if (globaltimer() - t0 > kTimeoutNs) {
-                *x.abort_flag = 1;
-                atomicOr(x.status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ bool wait(const Ctx &x, uint32_t b, uint32_t parity) {
-    if (mbar_try_wait(b, parity)) return true;
-    return wait_slow(x, b, parity);
-}
-
-// Wait that ignores the abort flag (used while draining); bounded by time.
-__device__ __noinline__ void wait_drain(uint32_t b, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(b, parity))
-        if (globaltimer() - t0 > kTimeoutNs) return;
-}
-
-// Warp-uniform wait: every lane gets the same answer, so lanes never diverge
-// around the .sync.aligned tcgen05 instructions and warp syncs that follow.
-__device__ __forceinline__ bool wwait(const Ctx &x, uint32_t b, uint32_t parity) {
-    const bool ok = wait(x, b, parity);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// OR of `pred` over the `n` threads of named barrier `id` (also a barrier).
-__device__ __forceinline__ bool bar_red_or(uint32_t id, uint32_t n, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
-    return tmem + ((uint32_t)((warp & 3) * 32) << 16);
-}
-
-__device__ __forceinline__ void warp_arrive(uint32_t b) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(b);
 }
 
 struct Unit {
@@ -265,7 +201,8 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
         if (p.flags & kQkL2Norm)
             chunk_norms_load(cs, static_cast<const uint8_t *>(p.ws) +
-                                     ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes,
+                                     ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes +
+                                     kSlotNormOff,
                              lane);
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
@@ -901,15 +838,16 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
 }  // namespace
 
 bool tc_supported(int dk, int dv, bool bf16, int chunk) {
-    return bf16 && dk == DK && dv % BVT == 0 && (chunk == 16 || chunk == 32 || chunk == C);
+    return bf16 && (dk == DK || dk == 256) && dv % BVT == 0 && (chunk == 16 || chunk == 32 || chunk == C);
 }
 
-size_t tc_workspace_bytes(long long tokens, int N, int Nv, int chunk) {
+size_t tc_workspace_bytes(long long tokens, int N, int Nv, int dk, int chunk) {
     if (tokens <= 0 || N <= 0 || chunk <= 0) return 0;
-    return (size_t)(tokens / chunk + N) * (size_t)Nv * kSlotBytes;
+    return (size_t)(tokens / chunk + N) * (size_t)Nv * slot_bytes(dk);
 }
 
 cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
+    if (p.dk == 256) return tc_wide_launch(p, stream, name);
     CUtensorMap mK, mQ, mV;
     const uint64_t tokens = (uint64_t)p.tokens;
     if (!make_tmap_rows_heads_d(&mK, p.k, tokens, p.Nk, DK, 64, C) ||

@@ -40,27 +40,31 @@ namespace dn {
 namespace {
 
 // QKN: in-kernel q / k normalisation (kQkL2Norm); a template parameter so
-// that the plain instantiation carries none of its registers.
-constexpr int kWyCtasPerSm = 6;  // launch bound: 80 registers x 128 threads x 6 fit the register file
+// that the plain instantiation carries none of its registers.  CTAs per SM:
+// dk = 128: 6 (80 registers x 128 threads x 6 fit the register file, 36 KB
+// of shared memory each); dk = 256: 3 (67 KB of shared memory each).
+template <int DKW>
+constexpr int wy_ctas_per_sm() { return DKW == 128 ? 6 : 3; }
 
-template <bool QKN>
-__global__ void __launch_bounds__(wy::NT, kWyCtasPerSm)
+template <int DKW, bool QKN>
+__global__ void __launch_bounds__(wy::NT, wy_ctas_per_sm<DKW>())
 wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ Params p) {
+    using Y = wy::Lay<DKW>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gb = smem_raw + (base - raw);
     wy::Group g{base, gb, 0u, 1u, (int)threadIdx.x, 0u};
-    wy::group_init(g);
+    wy::group_init<DKW>(g);
     if (threadIdx.x < 32) {
-        ptx::tmem_alloc(base + wy::OFF_BAR + 16, wy::TM_COLS);
+        ptx::tmem_alloc(base + Y::OFF_BAR + 16, Y::TM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    g.tm = *reinterpret_cast<volatile uint32_t *>(gb + wy::OFF_BAR + 16);
+    g.tm = *reinterpret_cast<volatile uint32_t *>(gb + Y::OFF_BAR + 16);
 
     // items (< 2^31, checked at launch) in steps of the grid; each item's
     // gates are loaded during the item before
@@ -71,34 +75,31 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     for (unsigned it = blockIdx.x; it < items; it += gridDim.x) {
         const unsigned nx = it + gridDim.x;
         const wy::ItemLoc loc = wy::locate(p, it / nv);
-        if (!wy::item<QKN>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
-                           nx < items ? (long long)(nx / nv) : -1, (int)(nx % nv)))
+        if (!wy::item<DKW, QKN>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
+                                nx < items ? (long long)(nx / nv) : -1, (int)(nx % nv)))
             break;
     }
     ptx::tc_fence_before();
     __syncthreads();
     if (threadIdx.x < 32) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(g.tm, wy::TM_COLS);
+        ptx::tmem_dealloc(g.tm, Y::TM_COLS);
     }
 }
 
-}  // namespace
-
-cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
-    const long long items = p.nslots * p.Nv;
-    if (items <= 0) return cudaSuccess;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const uint32_t smem = wy::GROUP_BYTES + 1024;
+template <int DKW>
+cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream,
+                         unsigned items) {
+    const uint32_t smem = wy::Lay<DKW>::GROUP_BYTES + 1024;
     const bool qkn = (p.flags & kQkL2Norm) != 0;
-    const void *kern = qkn ? (const void *)wy_fwd<true> : (const void *)wy_fwd<false>;
+    const void *kern = qkn ? (const void *)wy_fwd<DKW, true> : (const void *)wy_fwd<DKW, false>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
-    // one resident wave of CTAs (per device and instantiation, looked up
-    // once); on 2048 items (B = 4, H = 16, T = 2048) it measured 1.5 us
-    // faster per forward than one CTA per item
+    // one resident wave of CTAs (per device, head size and instantiation,
+    // looked up once); on 2048 items (B = 4, H = 16, T = 2048, dk = 128) it
+    // measured 1.5 us faster per forward than one CTA per item
     static std::atomic<int> wave_cache[64][2];  // 0: not looked up yet (calls may come from several threads)
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
@@ -114,16 +115,27 @@ cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap 
         if ((err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
             return err;
         int per_sm = smem_sm / (int)(smem + (uint32_t)reserved);
-        if (per_sm > kWyCtasPerSm) per_sm = kWyCtasPerSm;
+        if (per_sm > wy_ctas_per_sm<DKW>()) per_sm = wy_ctas_per_sm<DKW>();
         wave = sms * (per_sm > 0 ? per_sm : 1);
         if (dev >= 0 && dev < 64) wave_cache[dev][qkn].store(wave, std::memory_order_relaxed);
     }
-    const unsigned grid = (unsigned)(items < wave ? items : wave);
+    const unsigned grid = items < (unsigned)wave ? items : (unsigned)wave;
     if (qkn)
-        wy_fwd<true><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+        wy_fwd<DKW, true><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
     else
-        wy_fwd<false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+        wy_fwd<DKW, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
+    const long long items = p.nslots * p.Nv;
+    if (items <= 0) return cudaSuccess;
+    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (p.dk == 128) return wy_launch_dk<128>(p, mK, mQ, stream, (unsigned)items);
+    if (p.dk == 256) return wy_launch_dk<256>(p, mK, mQ, stream, (unsigned)items);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace dn

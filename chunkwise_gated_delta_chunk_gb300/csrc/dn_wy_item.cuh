@@ -50,20 +50,41 @@ constexpr int C = kChunk;  // 64
 constexpr int NT = 128;
 constexpr uint64_t kTimeoutNs = kWaitLimitNs;
 
-// Shared memory (offsets from a 1024-byte aligned base).  The tile region is
-// free once the MMA has read it and then holds A / T and the solve scratch.
-constexpr uint32_t OFF_K = 0;                    // K0 Q0 K1 Q1 (8 KB each): column halves of K and Q
-constexpr int LDA = 68;                          // fp32 row stride of A / T (aliases the tiles)
-constexpr uint32_t OFF_SCR = 64 * LDA * 4;       // solve scratch (aliases the tiles)
-constexpr uint32_t OFF_SC = 32768;               // gate scalars
-constexpr uint32_t OFF_NRM = OFF_SC + SCAL_FLOATS * 4;  // 64 inverse key norms, 64 inverse query norms
-constexpr uint32_t OFF_BAR = OFF_NRM + 512;
-constexpr uint32_t SMEM_USED = OFF_BAR + 32;     // 2 mbarriers, TMEM base, flag
-constexpr uint32_t GROUP_BYTES = (SMEM_USED + 1023u) & ~1023u;  // one worker's region, 1024-aligned
-static_assert(kSlotNormOff == 3 * kImageBytes && kImageBytes == 8192, "slot = T' | T'' | P | norms");
+// Shared memory of a worker (offsets from a 1024-byte aligned base): the K
+// and Q tiles as 64-column quarters K0 Q0 K1 Q1 .. (8 KB each, so that K_q
+// and Q_q form the 128 rows of one MMA operand), then the gate scalars, the
+// inverse norms and the barriers.  Once the [K; Q] K^T MMA has read the tiles,
+// A / T (fp32, row stride LDA, 16-row block rows RS floats apart) and the
+// solve scratch (groups of three 16 x 16 blocks, XRS floats apart) reuse
+// them: for dk = 128 the whole tile region, for dk = 256 only the Q quarters,
+// since the K tile is read again by the W MMA.  For dk = 256 the bf16 T'
+// image that MMA reads then takes the first Q quarter (OFF_TPI).
+constexpr int LDA = 68;              // fp32 row stride of A / T
+constexpr int SLD = 20, SBLK = 16 * SLD;  // scratch blocks: fp32, row stride SLD
+template <int DKW>
+struct Lay {
+    static_assert(DKW == 128 || DKW == 256, "key head size");
+    static constexpr uint32_t TILE_BYTES = 2u * 64u * DKW * 2u;
+    static constexpr uint32_t OFF_A = DKW == 128 ? 0u : 8192u;
+    static constexpr int RS = DKW == 128 ? 16 * LDA : 4096;
+    static constexpr uint32_t OFF_SCR = DKW == 128 ? 64u * LDA * 4u : 8192u + 16u * LDA * 4u;
+    static constexpr int XRS = DKW == 128 ? 3 * SBLK : 4096;
+    static constexpr uint32_t OFF_TPI = 8192;
+    static constexpr uint32_t OFF_SC = TILE_BYTES;
+    static constexpr uint32_t OFF_NRM = OFF_SC + SCAL_FLOATS * 4;  // 64 inverse key norms, 64 inverse query norms
+    static constexpr uint32_t OFF_BAR = OFF_NRM + 512;
+    static constexpr uint32_t SMEM_USED = OFF_BAR + 32;             // 2 mbarriers, TMEM base, flag, W mbarrier
+    static constexpr uint32_t GROUP_BYTES = (SMEM_USED + 1023u) & ~1023u;  // one worker's region
+    // [K; Q] K^T in columns 0-63; for dk = 256, W^T (two 128-row halves of
+    // d) in columns 0-63 and 64-127 after it
+    static constexpr uint32_t TM_COLS = DKW == 128 ? 64 : 128;
+};
+static_assert(kImageBytes == 8192 && slot_norm_off(128) == 3 * kImageBytes &&
+                  slot_norm_off(256) == 32768 + 2 * kImageBytes,
+              "slot = T' or -W^T | T'' | P | norms");
 
-constexpr uint32_t TM_COLS = 64;
 constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);  // A, B K-major
+constexpr uint32_t ID_W = idesc_bf16(128, 64, 1, 0);   // A MN-major (K^T), B K-major (T' rows)
 
 __device__ bool wait_bounded(uint32_t b, uint32_t parity) {
     const uint64_t t0 = globaltimer();
@@ -141,20 +162,22 @@ __device__ __forceinline__ void tile_store(float *Cb, int ldc, int n0, const flo
     Cb[(g + 8) * ldc + n0 + 2 * t + 1] = acc[3];
 }
 
-// Scratch blocks of the solve (fp32, row stride SLD), after A in the tile
-// region.
-constexpr int SLD = 20, SBLK = 16 * SLD;
+// Scratch blocks of the solve.
 enum { XN10, XN20, XN21, XN30, XN31, XN32, XP20, XS31, XS30, XCOUNT };
-static_assert(OFF_SCR + XCOUNT * SBLK * 4 <= OFF_SC, "the solve scratch fits in the tile region");
+static_assert(Lay<128>::OFF_SCR + XCOUNT * SBLK * 4 <= Lay<128>::OFF_SC, "the solve scratch fits in the tiles");
+static_assert(16 * LDA * 4 + 3 * SBLK * 4 <= 8192 && (XCOUNT + 2) / 3 <= 3,
+              "dk = 256: 16 rows of A / T and three scratch blocks fit in each of Q0-Q2");
 
-// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A in sA (row stride
-// LDA); 128 threads.  With A_D the four 16 x 16 diagonal blocks and A_O the
+// In-place T = (I - A)^-1 for the 64 x 64 strictly lower A at sA (row stride
+// LDA, block row b at sA + b RS); scratch block k at scr + (k / 3) XRS +
+// (k % 3) SBLK; 128 threads.  With A_D the four 16 x 16 diagonal blocks and A_O the
 // rest, I - A = (I - A_D)(I - N) with N = (I - A_D)^-1 A_O strictly block
 // lower, so N^4 = 0 and
 //     T = (I + N + N^2 + N^3) T_D,   T_D = (I - A_D)^-1,   N_ij = T_ii A_ij.
 // The diagonal blocks are inverted by forward substitution in fp32 (warp pw
 // owns block pw, lane l the column l % 16); the block products are TF32
 // tensor-core tiles with fp32 accumulation, in four barrier-separated phases.
+template <int RS, int XRS>
 __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane, uint32_t bid) {
     {
         // x = column `col` of (I - A_bb)^-1:  x_r = [r == col] + sum_{m < r} A[r][m] x_m.
@@ -164,7 +187,7 @@ __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane,
         float xv[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const float4 *ar = reinterpret_cast<const float4 *>(sA + (o + r) * LDA + o);
+            const float4 *ar = reinterpret_cast<const float4 *>(sA + pw * RS + r * LDA + o);
             float p4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int q4 = 0; q4 < (r + 3) / 4; ++q4) {
@@ -179,12 +202,12 @@ __device__ __forceinline__ void solve_T(float *sA, float *scr, int pw, int lane,
         __syncwarp();
         if (lane < 16) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sA[(o + r) * LDA + o + col] = xv[r];
+            for (int r = 0; r < 16; ++r) sA[pw * RS + r * LDA + o + col] = xv[r];
         }
     }
     named_bar_sync(bid, 128);
-    auto blkA = [&](int i, int j) { return sA + 16 * i * LDA + 16 * j; };
-    auto blkX = [&](int k) { return scr + k * SBLK; };
+    auto blkA = [&](int i, int j) { return sA + i * RS + 16 * j; };
+    auto blkX = [&](int k) { return scr + (k / 3) * XRS + (k % 3) * SBLK; };
     // phase 1: N_ij = T_ii A_ij, six blocks x two column halves (3 per warp)
     {
         float acc[3][4];
@@ -297,10 +320,12 @@ struct Group {
 };
 
 // Barrier setup of a worker (its thread 0); the caller synchronises after.
+template <int DKW>
 __device__ __forceinline__ void group_init(const Group &g) {
     if (g.tid == 0) {
-        mbar_init(g.base + OFF_BAR, 1);
-        mbar_init(g.base + OFF_BAR + 8, 1);
+        mbar_init(g.base + Lay<DKW>::OFF_BAR, 1);
+        mbar_init(g.base + Lay<DKW>::OFF_BAR + 8, 1);
+        mbar_init(g.base + Lay<DKW>::OFF_BAR + 24, 1);
         fence_barrier_init();
     }
 }
@@ -341,20 +366,81 @@ __device__ __forceinline__ ChunkGates item_gates(const Params &p, long long slot
     return chunk_gates_load(p, h, l.t0, l.L, lane);
 }
 
+// dk = 256: W^T = K^T T'^T, with the K tile quarters read MN-major and the T'
+// image at OFF_TPI (written by threads 0-63 just before) read K-major, into
+// TMEM columns 0-63 (d = 0..127) and 64-127 (d = 128..255); then -W^T row d
+// (the thread's TMEM lane in each half, 64 tokens) is rounded to bf16 and
+// stored to the slot.  Returns false when the MMA's wait ran out.
+template <int DKW>
+__device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
+    using Y = Lay<DKW>;
+    const uint32_t b_w = g.base + Y::OFF_BAR + 24;
+    volatile int *okf = reinterpret_cast<volatile int *>(g.gb + Y::OFF_BAR + 20);
+    fence_proxy_async_smem();  // the T' image is read through the async proxy
+    tc_fence_before();
+    named_bar_sync(g.bid, NT);
+    if (g.tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ss(g.tm + 64 * hh, sdesc(g.base + 32768 * hh + kk * 2048, 16384, 1024),
+                       sdesc(g.base + Y::OFF_TPI + kk * 32, 16, 1024), ID_W, kk != 0);
+        mma_commit(b_w);
+        if (!wait_bounded(b_w, par)) {
+            wait_bounded(b_w, par);  // drain: the MMA still reads shared memory
+            *okf = 0;
+            atomicOr(p.status, kStatusTimeout);
+        }
+    }
+    tc_fence_before();
+    named_bar_sync(g.bid, NT);
+    tc_fence_after();
+    if (*okf == 0) return false;
+    const int warp = g.tid >> 5;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r0[32], r1[32];
+        const uint32_t ta = g.tm + ((uint32_t)(32 * warp) << 16) + 64 * hh;
+        tmem_ld32(ta, r0);
+        tmem_ld32(ta + 32, r1);
+        tmem_wait_ld_dep(r0);
+        tmem_ld_dep(r1);
+        uint32_t pk[2][16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            pk[0][k] = pack_bf16(-__uint_as_float(r0[2 * k]), -__uint_as_float(r0[2 * k + 1]));
+            pk[1][k] = pack_bf16(-__uint_as_float(r1[2 * k]), -__uint_as_float(r1[2 * k + 1]));
+        }
+        store_image_row(img, g.tid + 128 * hh, 0, pk[0]);
+        store_image_row(img, g.tid + 128 * hh, 1, pk[1]);
+    }
+    return true;
+}
+
 // The item of workspace slot `slot` and value head h, located at `loc`.
 // Warp 0 enters with the item's gates in `gates` (loaded ahead) and leaves
 // with those of the worker's next item (slot next_slot < 0: none; value head
 // next_h), whose loads then overlap the rest of this item.  Returns false
 // when a wait ran out (the worker must stop).
-template <bool QKN>
+//
+// dk = 256 adds a step 6: the bf16 T' image goes to shared memory, one MMA
+// chain computes W^T = K^T T'^T into tensor memory (two 128-row halves of d),
+// and the threads store -W^T (row d = TMEM lane) to the slot, so that the
+// scan kernel needs neither T' nor tensor memory for W.
+template <int DKW, bool QKN>
 __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, const Params &p, long long slot,
                      int h, const ItemLoc &loc, ChunkGates &gates, long long next_slot, int next_h) {
+    using Y = Lay<DKW>;
+    constexpr int NQ = DKW / 64;  // 64-column quarters of a K / Q row
     const int warp = g.tid >> 5, lane = g.tid & 31;
-    const uint32_t b_tma = g.base + OFF_BAR, b_mma = g.base + OFF_BAR + 8;
-    volatile int *okf = reinterpret_cast<volatile int *>(g.gb + OFF_BAR + 20);
-    float *sc = reinterpret_cast<float *>(g.gb + OFF_SC);
-    float *sA = reinterpret_cast<float *>(g.gb + OFF_K);
-    float *scr = reinterpret_cast<float *>(g.gb + OFF_SCR);
+    const uint32_t b_tma = g.base + Y::OFF_BAR, b_mma = g.base + Y::OFF_BAR + 8;
+    volatile int *okf = reinterpret_cast<volatile int *>(g.gb + Y::OFF_BAR + 20);
+    float *sc = reinterpret_cast<float *>(g.gb + Y::OFF_SC);
+    float *sA = reinterpret_cast<float *>(g.gb + Y::OFF_A);
+    float *scr = reinterpret_cast<float *>(g.gb + Y::OFF_SCR);
+    auto arow = [&](int i) { return sA + (i >> 4) * Y::RS + (i & 15) * LDA; };  // row i of A / T
     if (!loc.valid) {
         if (warp == 0 && next_slot >= 0) gates = item_gates(p, next_slot, next_h, lane);
         return true;
@@ -364,23 +450,24 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
     const int hk = h / (p.Nv / p.Nk);
     const uint32_t par = g.it & 1;
     ++g.it;
-    uint8_t *img = static_cast<uint8_t *>(p.ws) + ((size_t)h * p.nslots + slot) * kSlotBytes;
+    uint8_t *img = static_cast<uint8_t *>(p.ws) + ((size_t)h * p.nslots + slot) * slot_bytes(DKW);
 
     if (warp == 0) {
         if (lane == 0) {
             *okf = 1;
-            uint32_t tx = 32768;
+            uint32_t tx = Y::TILE_BYTES;
 #ifdef DN_TEST_STALL
             // failure-path test: the first item of worker 0 expects 16 bytes
-            // more than its four copies bring, so its wait runs out after the
+            // more than its copies bring, so its wait runs out after the
             // copies have landed
             if (p.test_stall == kStallWy && blockIdx.x == 0 && g.it == 1) tx += 16;
 #endif
             mbar_arrive_expect_tx(b_tma, tx);
-            tma_load_3d(g.base + OFF_K, mK, b_tma, 0, hk, (int)t0);
-            tma_load_3d(g.base + OFF_K + 8192, mQ, b_tma, 0, hk, (int)t0);
-            tma_load_3d(g.base + OFF_K + 16384, mK, b_tma, 64, hk, (int)t0);
-            tma_load_3d(g.base + OFF_K + 24576, mQ, b_tma, 64, hk, (int)t0);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                tma_load_3d(g.base + 16384 * q, mK, b_tma, 64 * q, hk, (int)t0);
+                tma_load_3d(g.base + 16384 * q + 8192, mQ, b_tma, 64 * q, hk, (int)t0);
+            }
         }
         chunk_scalars_store(p, chunk_scalars_from(gates, L, lane), sc, lane);
         // the next item's gates: their loads run under this item's work
@@ -391,10 +478,10 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int kb = 0; kb < 2; ++kb)
+                for (int kb = 0; kb < NQ; ++kb)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t a = g.base + OFF_K + kb * 16384 + kk * 32;
+                        const uint32_t a = g.base + kb * 16384 + kk * 32;
                         mma_ss(g.tm, sdesc(a, 16, 1024), sdesc(a, 16, 1024), ID_KQ, (kb | kk) != 0);
                     }
                 mma_commit(b_mma);
@@ -414,19 +501,19 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
     tc_fence_after();
     if (*okf == 0) return false;
 
-    float *nrm = reinterpret_cast<float *>(g.gb + OFF_NRM);
+    float *nrm = reinterpret_cast<float *>(g.gb + Y::OFF_NRM);
     constexpr bool qkn = QKN;
     if (qkn) {
         // 1 / max(||x||, 1e-12) of key row i (threads 0-63) or query row
-        // i (64-127), from the two column halves of the tile.  The sum
-        // of squares does not depend on the order of the row's 16-byte
-        // chunks, so the swizzle is ignored; each lane starts at chunk
-        // (i & 7) so that eight lanes of a phase hit eight bank groups.
+        // i (64-127), from the quarters of the tile.  The sum of squares
+        // does not depend on the order of the row's 16-byte chunks, so the
+        // swizzle is ignored; each lane starts at chunk (i & 7) so that
+        // eight lanes of a phase hit eight bank groups.
         const int i = g.tid & 63;
-        const uint8_t *row = g.gb + OFF_K + (g.tid < 64 ? 0 : 8192) + i * 128;
+        const uint8_t *row = g.gb + (g.tid < 64 ? 0 : 8192) + i * 128;
         float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
+        for (int hb = 0; hb < NQ; ++hb)
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
                 const uint4 w = *reinterpret_cast<const uint4 *>(row + hb * 16384 + (((cc + i) & 7) << 4));
@@ -440,7 +527,7 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
             }
         const float rn = rsqrtf(fmaxf(ss0 + ss1, 1e-24f));
         nrm[g.tid] = rn;
-        reinterpret_cast<float *>(img + kSlotNormOff)[g.tid] = rn;
+        reinterpret_cast<float *>(img + slot_norm_off(DKW))[g.tid] = rn;
         // T' = T diag(beta e^G / ||k||)
         if (g.tid < 64) sc[SC_BEG + i] *= rn;
         named_bar_sync(g.bid, NT);
@@ -507,40 +594,54 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
             }
             if (rowA) {
+                float *ar = arow(i);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)
-                    *reinterpret_cast<float4 *>(sA + i * LDA + 32 * hf + 4 * q4) =
+                    *reinterpret_cast<float4 *>(ar + 32 * hf + 4 * q4) =
                         make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3]);
             } else {
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(val[2 * k], val[2 * k + 1]);
-                store_image_row(img + 16384, i, hf, pk);
+                store_image_row(img + slot_p_off(DKW), i, hf, pk);
             }
         }
     }
     tc_fence_before();
     named_bar_sync(g.bid, NT);
-    solve_T(sA, scr, warp, lane, g.bid);
+    solve_T<Y::RS, Y::XRS>(sA, scr, warp, lane, g.bid);
     {
         // T' = T diag(beta e^G) (threads 0-63), T'' = T diag(beta) (64-127)
         const int i = g.tid & 63;
         const bool tp = g.tid < 64;
-        const float *trow = sA + i * LDA;
+        const float *trow = arow(i);
         const float *cs = sc + (tp ? SC_BEG : SC_BETA);
+        uint32_t pk[2][16];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            uint32_t pk[16];
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
                 const float4 a = *reinterpret_cast<const float4 *>(trow + 32 * hf + 4 * q4);
                 const float4 cc = *reinterpret_cast<const float4 *>(cs + 32 * hf + 4 * q4);
-                pk[2 * q4] = pack_bf16(a.x * cc.x, a.y * cc.y);
-                pk[2 * q4 + 1] = pack_bf16(a.z * cc.z, a.w * cc.w);
+                pk[hf][2 * q4] = pack_bf16(a.x * cc.x, a.y * cc.y);
+                pk[hf][2 * q4 + 1] = pack_bf16(a.z * cc.z, a.w * cc.w);
             }
-            store_image_row(img + (tp ? 0 : 8192), i, hf, pk);
+            if (DKW == 128 || !tp) store_image_row(img + (tp ? 0 : slot_tu_off(DKW)), i, hf, pk[hf]);
+        }
+        if (DKW == 256) {
+            // T' into shared memory once every row of T has been read
+            named_bar_sync(g.bid, NT);
+            if (tp) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        st_shared_v4(g.base + Y::OFF_TPI + sw128(i, 4 * hf + ch), pk[hf][4 * ch], pk[hf][4 * ch + 1],
+                                     pk[hf][4 * ch + 2], pk[hf][4 * ch + 3]);
+            }
         }
     }
+    if (DKW == 256 && !w_step<DKW>(g, p, img, par)) return false;
     // A / T and the scratch are read; the next item's TMA rewrites them
     fence_proxy_async_smem();
     tc_fence_before();

@@ -98,6 +98,49 @@ def test_chunk_sizes_headline_full_size(lib, chunk):
     print("headline C=%d" % chunk, res)
 
 
+@pytest.mark.parametrize("case", ["gated_h0", "varlen_gqa", "ungated", "chunk16", "chunk32",
+                                  "qk_l2norm", "dv256"])
+def test_wide_heads_tensor_core_path(lib, case):
+    """dk = 256 (bf16) runs on the tensor-core kernels, with -W^T formed by
+    the WY kernel: several chunks and a ragged tail, a varlen GQA batch with
+    empty and length-1 sequences, no gates, the shorter chunks, in-kernel q / k
+    normalisation and two value tiles per head."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    chunk = {"chunk16": 16, "chunk32": 32}.get(case, 64)
+    if case == "varlen_gqa":
+        inp = inputs(B=1, Nk=2, Nv=4, dk=256, dv=128, lengths=[1, 0, 65, 200, 64, 130], seed=520)
+    elif case == "ungated":
+        inp = inputs(B=2, T=300, dk=256, dv=128, gate=None, seed=521)
+    elif case == "qk_l2norm":
+        inp = inputs(B=2, T=150, dk=256, dv=128, seed=522, raw_qk=True)
+    elif case == "dv256":
+        inp = inputs(B=2, T=190, dk=256, dv=256, seed=523)
+    else:
+        inp = inputs(B=2, T=200, dk=256, dv=128, seed=524 + chunk)
+    o, ht = run_gpu(inp, chunk=chunk)
+    assert dn.dn_last_kernel() == "wy_fwd+tc_wide_fwd", dn.dn_last_kernel()
+    check(inp, o, ht, label="wide %s" % case)
+
+
+def test_wide_heads_state_carry(lib):
+    """dk = 256: a second call from the first call's ht equals one call on the
+    whole sequence."""
+    inp = inputs(B=2, T=300, dk=256, dv=128, seed=525)
+    o, ht = run_gpu(inp)
+    cut = 100
+    p1, p2 = dict(inp), dict(inp)
+    for key in ("q", "k", "v", "beta", "g"):
+        p1[key] = inp[key][:, :cut].contiguous()
+        p2[key] = inp[key][:, cut:].contiguous()
+    o1, h1 = run_gpu(p1)
+    p2["h0"] = h1.cpu()
+    o2, h2 = run_gpu(p2)
+    both = torch.cat([o1, o2], dim=1).float()
+    tol = TOL[torch.bfloat16]
+    assert (both - o.float()).abs().max().item() <= tol["max_abs"]
+    assert (h2 - ht).abs().max().item() <= tol["max_abs"]
+
+
 def test_chunk_sizes_agree(lib):
     """The same inputs at C = 16, 32 and 64 agree with each other to the
     rounding of the two paths (the chunk form is exact, [WY] §6)."""
@@ -298,6 +341,9 @@ def test_workload_full_size(lib, name):
         Nv = inp["v"].shape[2]
         nl, ns = int(np.argmax(lens)), int(np.argmin(lens))
         units = [nl * Nv, nl * Nv + Nv - 1, ns * Nv + 1]
+    if name.startswith("gdn_wide"):
+        import chunkwise_gated_delta_chunk_gb300 as dn
+        assert dn.dn_last_kernel() == "wy_fwd+tc_wide_fwd", dn.dn_last_kernel()
     res = check(inp, o, ht, units=units, label=name)
     # every output of every unit is finite
     assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
