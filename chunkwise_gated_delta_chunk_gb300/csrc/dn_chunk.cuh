@@ -24,7 +24,8 @@ constexpr float kSpanMax = 80.f;
 // 128-byte-swizzled image the MMAs read (row i at 128 i, 16-byte chunk c at
 // (c ^ (i & 7)) * 16):
 //   dk = 128: T' = T diag(beta e^G) (64 x 64), then T'' and P;
-//   dk = 256: -W^T = -(T' K)^T (256 rows d x 64 tokens), then T'' and P;
+//   dk = 256: -W = -T' K (64 x 256, as four 64-column quarters of 8 KB),
+//             then T'' and P;
 // with T'' = T diag(beta) and P = tril(scale QK^T . D) (64 x 64 each); then,
 // with kQkL2Norm, the fp32 factors 1 / max(||k_i||, 1e-12) and
 // 1 / max(||q_i||, 1e-12) of the chunk's 64 rows (the WY kernel folds them

@@ -9,40 +9,43 @@
 // 128 x 256 floats: transposed in tensor memory (lane = value column v,
 // column = key index d) it takes 256 of the SM's 512 columns, and its bf16
 // image (the A operand of VN and O) another 128.  That leaves no room for W,
-// so the WY kernel (dn_wy.cu) forms -W^T = -(T' K)^T per chunk and writes it
-// to the workspace beside T'' and P; this kernel reads it as an MMA operand.
-// One persistent CTA per unit walks the sequence's chunks in order; every
-// contraction is a tcgen05 MMA with M = 128:
+// so the WY kernel (dn_wy.cu) forms -W = -T' K per chunk and writes it to the
+// workspace beside T'' and P.  One persistent CTA per unit walks the
+// sequence's chunks in order; every contraction is a tcgen05 MMA with
+// M = 128, and VN and O, which share their A operand, run as one:
 //
-//   U   V^T T''^T             -> acc_v = U^T                          (a4)
-//   VN  acc_v += S^T (-W^T)   -> v_new^T (S^T: the bf16 TMEM image)   (a5)
-//   O   S^T Q~^T              -> acc_o, Q~ = diag(scale e^G) Q        (a6)
-//   DS  acc_s += v~^T K       -> state update, v~ = e^{G_L-G} v_new   (a5)
-//   PV  acc_o += v_new^T P^T  -> intra-chunk output                   (a6)
+//   U    [V^T T''^T | 0]            -> [acc_v | acc_o] = [U^T | 0]       (a4)
+//   VNO  += S^T [-W^T | Q~^T]       -> [v_new^T | inter-chunk output]    (a5, a6)
+//   DS   acc_s += v~^T K            -> state update, v~ = e^{G_L-G} v_new (a5)
+//   PV   acc_o += v_new^T P^T       -> intra-chunk output                (a6)
 //
-// Tensor memory: acc_s (256 columns), the bf16 S^T image (128), acc_v (64)
-// and acc_o (64), each single: one MMA issuer thread issues all five MMAs of
-// a chunk in the order above, so the in-order tensor pipe has finished O(c),
-// which reads the S^T image, when DS(c) completes, and the state pass may
-// then overwrite the image; U(c+1) waits for PV(c) before it refills acc_v.
+// with Q~ = diag(scale e^G) Q.  acc_v (64 columns) and acc_o (64) are
+// adjacent, so U and VNO are N = 128 MMAs on the same accumulator: U's B
+// operand is T'' followed by 64 zero rows, VNO's is -W followed by Q~, which
+// is why each buffer of the -W and Q tiles interleaves their 64-column
+// quarters (W0 Q0 W1 Q1 ..).  U and VNO are ordered by the tensor pipe (same
+// accumulator and shape); every other dependency between MMAs goes through a
+// commit and an mbarrier.
 //
-// Shared memory holds one chunk's K (32 KB), V (16 KB), T'' and P (8 KB
-// each), and two chunks' Q and -W^T (2 x 32 KB each): every buffer has its
-// own full / empty mbarrier pair, the loader refills it as soon as its last
-// reader (an MMA, through a commit) releases it, and the two-deep ones are
-// those whose release comes latest in a chunk relative to their next use.
+// Shared memory holds two chunks' interleaved -W / Q tiles (2 x 64 KB) and
+// one chunk's K (32 KB), V (16 KB), T'' and P (8 KB each): every buffer has
+// its own full / empty mbarriers, and its loader refills it as soon as its
+// last reader (an MMA, through a commit) releases it.
 //
-// Warp roles (14 warps):
-//   0      loader: gate scalars (two-deep ring), TMA for K, Q, V, bulk copies
-//          of -W^T, T'' and P;
-//   1      MMA issuer (one thread) and TMEM owner;
-//   2-5    prep: Q rows scaled by scale e^G in place; key blocks 0-2 of
-//          each state pass;
-//   6-9    state: v_new / v~ operands from acc_v; key blocks 3-5;
-//   10-13  output: key blocks 6-7; then o from acc_o, transposed through
-//          shared memory and stored as 16-byte bf16 rows.
+// Warp roles (15 warps):
+//   0      loader: gate scalars (two-deep ring, gates fetched a chunk ahead),
+//          TMA for K and V, bulk copies of T'' and P;
+//   1      MMA issuer (one thread: U, VNO, DS, PV) and TMEM owner;
+//   2-5    prep: Q rows scaled by scale e^G in place (a chunk ahead); key
+//          blocks 0-3 of each state pass;
+//   6-9    state: v_new / v~ operands from acc_v; key blocks 4-7;
+//   10-13  output: o from acc_o (released at once, since the next U writes
+//          it), transposed through shared memory and stored as 16-byte bf16
+//          rows;
+//   14     loader of the -W / Q tiles (one thread), up to two chunks ahead.
 // A state pass turns acc_s into the next chunk's bf16 image (or ht after the
-// last chunk), then scales acc_s by the next chunk's alpha = e^{G_L}.
+// last chunk).  acc_s holds the state divided by a running product of the
+// chunk decays, so the decay of each chunk needs no pass over it (see SC_A).
 //
 // Every wait is bounded (dn_tc_sync.cuh): a wait that runs out records
 // kStatusTimeout, raises the CTA's abort flag, and every role drains its own
@@ -50,8 +53,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
-
-#include <atomic>
 
 #include "dn_chunk.cuh"
 #include "dn_internal.h"
@@ -69,44 +70,45 @@ using namespace tcs;
 constexpr int C = kChunk;  // 64-row tiles
 constexpr int DK = 256;
 constexpr int BVT = 128;  // value columns per CTA
-constexpr int NTHREADS = 448;
+constexpr int NTHREADS = 480;
 constexpr uint32_t SLOT = slot_bytes(DK);
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
-constexpr uint32_t OFF_K = 0;                    // K: 4 quarters of 64 columns, 8 KB each
-constexpr uint32_t OFF_Q = OFF_K + 32768;        // Q: 2 buffers x 4 quarters
-constexpr uint32_t OFF_WT = OFF_Q + 65536;       // -W^T: 2 buffers x 256 rows x 128 B
-constexpr uint32_t OFF_V = OFF_WT + 65536;       // V: 2 halves of 64 value columns
-constexpr uint32_t OFF_TU = OFF_V + 16384;       // T''
-constexpr uint32_t OFF_PR = OFF_TU + 8192;       // P
-constexpr uint32_t OFF_SCAL = OFF_PR + 8192;     // 2 x SCAL_FLOATS floats
+constexpr uint32_t QW_BYTES = 65536;               // one buffer: W0 Q0 W1 Q1 W2 Q2 W3 Q3, 8 KB each
+constexpr uint32_t OFF_QW = 0;                     // 2 buffers
+constexpr uint32_t OFF_K = OFF_QW + 2 * QW_BYTES;  // K: 4 quarters of 64 columns, 8 KB each
+constexpr uint32_t OFF_V = OFF_K + 32768;          // V: 2 halves of 64 value columns
+constexpr uint32_t OFF_TU = OFF_V + 16384;         // T''
+constexpr uint32_t OFF_ZERO = OFF_TU + 8192;       // 64 zero rows: U's B operand continues here
+constexpr uint32_t OFF_PR = OFF_ZERO + 8192;       // P
+constexpr uint32_t OFF_SCAL = OFF_PR + 8192;       // 2 x SCAL_FLOATS floats
 constexpr uint32_t OFF_OST = OFF_SCAL + 2 * SCAL_FLOATS * 4;  // output staging, 32 x 256 B
 constexpr uint32_t OFF_BAR = OFF_OST + 8192;
-constexpr int NBARS = 32;
+constexpr int NBARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;  // TMEM base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // alignment slack
 
-static_assert(OFF_Q % 1024 == 0 && OFF_WT % 1024 == 0 && OFF_V % 1024 == 0 && OFF_TU % 1024 == 0 &&
+static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_TU % 1024 == 0 && OFF_ZERO == OFF_TU + 8192 &&
                   OFF_PR % 1024 == 0,
               "swizzled operands need 1024-byte alignment");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KB of shared memory per CTA");
-static_assert(SLOT % 16 == 0 && slot_tu_off(DK) == 32768, "slot = -W^T | T'' | P | norms");
+static_assert(SLOT % 16 == 0 && slot_tu_off(DK) == 32768, "slot = -W | T'' | P | norms");
 
 // Barrier indices.  Buffer barriers: FULL = copy landed (tx bytes + the
-// loader's arrive), EMPTY = last reader done (an MMA commit).
+// loader's arrive), EMPTY = last reader done (an MMA commit).  Two-deep
+// buffers have one of each per buffer (chunk c uses buffer c & 1).
 enum {
     B_KF = 0, B_KE,
-    B_QF, B_QE = B_QF + 2,      // 2 each (buffer c & 1)
-    B_WF = B_QE + 2, B_WE = B_WF + 2,
-    B_VF = B_WE + 2, B_VE,
+    B_WF, B_QF = B_WF + 2, B_QWE = B_QF + 2,  // 2 each
+    B_VF = B_QWE + 2, B_VE,
     B_TUF, B_TUE,
     B_PF, B_PE,
-    B_SCF, B_SCE = B_SCF + 2,   // 2 each: scalars landed (loader) / read (12 warps)
-    B_QS = B_SCE + 2,           // Q(c) scaled (prep)
-    B_S_FULL,                   // bf16 S^T image of the chunk written (12 warps)
-    B_VN,                       // VN(c) done (commit)
-    B_VSM,                      // v_new / v~ operands (state) + acc_s scaled by alpha(c) (12 warps)
+    B_SCF, B_SCE = B_SCF + 2,   // 2 each: scalars landed (loader) / read (8 warps)
+    B_QS = B_SCE + 2,           // 2: Q of the buffer's chunk scaled (prep)
+    B_S_FULL = B_QS + 2,        // bf16 S^T image of the chunk written (8 warps)
+    B_VN,                       // VNO(c) done (commit)
+    B_VSM,                      // v_new / v~ operands (state) + the state pass before the chunk (12 warps)
     B_S_UPD,                    // DS(c), and every MMA before it, done (commit)
     B_D_FULL,                   // PV(c) done: acc_o complete, acc_v free (commit)
     B_O_EMPTY,                  // acc_o read (output)
@@ -115,18 +117,35 @@ enum {
 };
 static_assert(B_COUNT <= NBARS, "barrier space");
 
-// Tensor memory columns.
+// Tensor memory columns: acc_v and acc_o adjacent, one N = 128 accumulator
+// for U and VNO.
 constexpr uint32_t TM_S = 0, TM_SB = 256, TM_V = 384, TM_O = 448, TM_COLS = 512;
+static_assert(TM_O == TM_V + 64, "acc_o follows acc_v");
 
 // Instruction descriptors.
-constexpr uint32_t ID_U = idesc_bf16(128, 64, 1, 0);    // A MN-major (V^T), B K-major (T'' rows)
-constexpr uint32_t ID_VN = idesc_bf16(128, 64, 0, 1);   // A TMEM, B MN-major (-W^T rows d)
-constexpr uint32_t ID_O = idesc_bf16(128, 64, 0, 0);    // A TMEM, B K-major (Q rows)
-constexpr uint32_t ID_DS = idesc_bf16(128, 256, 0, 1);  // A TMEM, B MN-major (K rows)
-constexpr uint32_t ID_PV = idesc_bf16(128, 64, 0, 0);   // A TMEM, B K-major (P rows)
+constexpr uint32_t ID_U = idesc_bf16(128, 128, 1, 0);    // A MN-major (V^T), B K-major ([T''; 0] rows)
+constexpr uint32_t ID_VNO = idesc_bf16(128, 128, 0, 0);  // A TMEM, B K-major ([-W; Q~] rows)
+constexpr uint32_t ID_DS = idesc_bf16(128, 256, 0, 1);   // A TMEM, B MN-major (K rows)
+constexpr uint32_t ID_PV = idesc_bf16(128, 64, 0, 0);    // A TMEM, B K-major (P rows)
 
 // Key blocks (32 columns of acc_s) of each state pass, per warpgroup.
-constexpr int kPrepB0 = 0, kPrepNB = 3, kStateB0 = 3, kStateNB = 3, kOutB0 = 6, kOutNB = 2;
+constexpr int kPrepB0 = 0, kStateB0 = 4, kPassNB = 4;
+
+// The state in tensor memory is kept unscaled: acc_s holds S_c / A_c, where
+// A_c is the product of the decays alpha = e^{G_L} of the chunks since the
+// last renormalisation.  A chunk whose decay keeps alpha_c A_c within
+// [2^-40, 2^40] needs no pass over acc_s: A_{c+1} = alpha_c A_c, and v~ is
+// divided by A_{c+1} before DS accumulates it.  Otherwise (a renormalising
+// chunk: strong decay, or alpha = 0) acc_s is scaled by alpha_c A_c before
+// DS(c) and A_{c+1} = 1.  The bf16 image is A_c (S_c / A_c) and ht =
+// A (S / A), so VN, O and ht see S itself.  Extra scalars per chunk (the
+// loader tracks A):
+constexpr int SC_A = 452;   // A_c
+constexpr int SC_RN = 453;  // 1: renormalise before DS(c)
+constexpr int SC_RS = 454;  // alpha_c A_c, the renormalising scale
+constexpr int SC_AN = 455;  // A_{c+1} (SC_DEC already carries 1 / A_{c+1})
+static_assert(SC_A > SC_FACT && SC_AN < SCAL_FLOATS, "free scalar slots");
+constexpr float kAMin = 9.094947e-13f, kAMax = 1.0995116e12f;  // 2^-40, 2^40
 
 __device__ __forceinline__ uint32_t bar(const Ctx &x, int i) { return x.base + OFF_BAR + 8u * i; }
 __device__ __forceinline__ float *scal(const Ctx &x, int c) {
@@ -169,19 +188,19 @@ __device__ __forceinline__ const uint8_t *slot_of(const Params &p, const Unit &u
 }
 
 // ---------------------------------------------------------------------------
-// Loader warp.  Per chunk: the gate scalars (whole warp), then (lane 0) the
-// copies in the order their buffers free up in the previous chunk: V and T''
-// (after U), -W^T and Q (two-deep: after VN / O of the chunk two back), K
-// (after DS), P (after PV).  last[] records the last chunk loaded into each
-// buffer kind, for the drain at exit.
+// Loaders.  Warp 0: per chunk the gate scalars (whole warp), then (lane 0)
+// the single-buffered copies in the order their buffers free up in the
+// previous chunk: V and T'' (after U), K (after DS), P (after PV).  Warp 14
+// (one thread): the -W and Q tiles of each chunk into its two-deep buffer,
+// as soon as VNO of the chunk two back has released it.  last[] records the
+// last chunk loaded into each buffer kind, for the drain at exit.
 // ---------------------------------------------------------------------------
-enum { LV, LTU, LW, LQ, LK, LP, LCOUNT };
+enum { LV, LTU, LK, LP, LQW, LCOUNT };
 
 __device__ bool load_chunk(const Ctx &x, const Unit &u, int c, long long t0, const uint8_t *slot,
-                           const CUtensorMap *mK, const CUtensorMap *mQ, const CUtensorMap *mV,
-                           int (&last)[LCOUNT]) {
-    const int tt = (int)t0, b = c & 1;
-    const uint32_t p1 = (c & 1) ^ 1, p2 = ((c >> 1) & 1) ^ 1;  // free-wait parities: single, two-deep
+                           const CUtensorMap *mK, const CUtensorMap *mV, int (&last)[LCOUNT]) {
+    const int tt = (int)t0;
+    const uint32_t p1 = (c & 1) ^ 1;  // free-wait parity of a single buffer
     if (!wait(x, bar(x, B_VE), p1)) return false;
     mbar_arrive_expect_tx(bar(x, B_VF), 16384);
     tma_load_3d(x.base + OFF_V, mV, bar(x, B_VF), u.v0, u.h, tt);
@@ -191,15 +210,6 @@ __device__ bool load_chunk(const Ctx &x, const Unit &u, int c, long long t0, con
     mbar_arrive_expect_tx(bar(x, B_TUF), kImageBytes);
     bulk_load(x.base + OFF_TU, slot + slot_tu_off(DK), kImageBytes, bar(x, B_TUF));
     last[LTU] = c;
-    if (!wait(x, bar(x, B_WE + b), p2)) return false;
-    mbar_arrive_expect_tx(bar(x, B_WF + b), 32768);
-    bulk_load(x.base + OFF_WT + 32768 * b, slot, 32768, bar(x, B_WF + b));
-    last[LW] = c;
-    if (!wait(x, bar(x, B_QE + b), p2)) return false;
-    mbar_arrive_expect_tx(bar(x, B_QF + b), 32768);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_3d(x.base + OFF_Q + 32768 * b + 8192 * q, mQ, bar(x, B_QF + b), 64 * q, u.hk, tt);
-    last[LQ] = c;
     if (!wait(x, bar(x, B_KE), p1)) return false;
     mbar_arrive_expect_tx(bar(x, B_KF), 32768);
 #pragma unroll
@@ -212,52 +222,118 @@ __device__ bool load_chunk(const Ctx &x, const Unit &u, int c, long long t0, con
     return true;
 }
 
+// The raw gates of chunk c and, with kQkL2Norm, its inverse key / query
+// norms from the WY kernel's slot, for the lane's two tokens.
+struct ChunkInputs {
+    ChunkGates gates;
+    float ka, kb, qa, qb;
+};
+
+__device__ __forceinline__ ChunkInputs chunk_inputs_load(const Params &p, const Unit &u, int c, int lane) {
+    ChunkInputs r;
+    const long long t0 = u.bos + (long long)c * p.chunk;
+    r.gates = chunk_gates_load(p, u.h, t0, (int)min((long long)p.chunk, u.eos - t0), lane);
+    r.ka = r.kb = r.qa = r.qb = 1.f;
+    if (p.flags & kQkL2Norm) {
+        const float *f = reinterpret_cast<const float *>(slot_of(p, u, c) + slot_norm_off(DK));
+        r.ka = f[lane];
+        r.kb = f[lane + 32];
+        r.qa = f[64 + lane];
+        r.qb = f[64 + lane + 32];
+    }
+    return r;
+}
+
 __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
-                            const CUtensorMap *mQ, const CUtensorMap *mV, int (&last)[LCOUNT]) {
+                            const CUtensorMap *mV, int (&last)[LCOUNT]) {
     const int lane = threadIdx.x & 31;
+    // each chunk's gates (and norms) are loaded one iteration ahead, so that
+    // their latency hides under the previous chunk's waits
+    ChunkInputs next{};
+    if (u.nc > 0) next = chunk_inputs_load(p, u, 0, lane);
+    float A = 1.f;  // A_c, the same in every lane
     for (int c = 0; c < u.nc; ++c) {
         const long long t0 = u.bos + (long long)c * p.chunk;
         const int L = (int)min((long long)p.chunk, u.eos - t0);
-        const uint8_t *slot = slot_of(p, u, c);
-        // the gates (and the WY kernel's inverse q / k norms) come from
-        // global memory while the scalar buffer is still in use
-        ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
-        if (p.flags & kQkL2Norm) chunk_norms_load(cs, slot + slot_norm_off(DK), lane);
+        const ChunkInputs in = next;
+        if (c + 1 < u.nc) next = chunk_inputs_load(p, u, c + 1, lane);
+        ChunkScalars cs = chunk_scalars_from(in.gates, L, lane);
+        const float rs = __expf(cs.GL) * A;
+        const bool rn = !(rs >= kAMin && rs <= kAMax);
+        const float an = rn ? 1.f : rs;
+        const float inv_an = 1.f / an;
+        cs.ka = in.ka * inv_an;  // rides on e^{G_L - G_i}: v~ / A_{c+1}
+        cs.kb = in.kb * inv_an;
+        cs.qa = in.qa;
+        cs.qb = in.qb;
         if (!wwait(x, bar(x, B_SCE + (c & 1)), ((c >> 1) & 1) ^ 1)) return;
-        chunk_scalars_store(p, cs, scal(x, c), lane);
+        float *sc = scal(x, c);
+        chunk_scalars_store(p, cs, sc, lane);
+        if (lane == 0) {
+            sc[SC_A] = A;
+            sc[SC_RN] = rn ? 1.f : 0.f;
+            sc[SC_RS] = rs;
+            sc[SC_AN] = an;
+        }
+        A = an;
         __syncwarp();
         bool ok = true;
         if (lane == 0) {
             mbar_arrive(bar(x, B_SCF + (c & 1)));
-            ok = load_chunk(x, u, c, t0, slot, mK, mQ, mV, last);
+            ok = load_chunk(x, u, c, t0, slot_of(p, u, c), mK, mV, last);
         }
         if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return;
     }
 }
 
+// One thread: -W (four 8 KB quarters, bulk copies from the slot) and Q (TMA)
+// of chunk c into the odd and even 8 KB slots of buffer c & 1.
+__device__ void qw_loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mQ,
+                               int (&last)[LCOUNT]) {
+    for (int c = 0; c < u.nc; ++c) {
+        const int b = c & 1;
+        if (!wait(x, bar(x, B_QWE + b), ((c >> 1) & 1) ^ 1)) return;
+        const uint32_t buf = x.base + OFF_QW + QW_BYTES * b;
+        const uint8_t *slot = slot_of(p, u, c);
+        mbar_arrive_expect_tx(bar(x, B_WF + b), 32768);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bulk_load(buf + 16384 * q, slot + 8192 * q, 8192, bar(x, B_WF + b));
+        mbar_arrive_expect_tx(bar(x, B_QF + b), 32768);
+        const int tt = (int)(u.bos + (long long)c * p.chunk);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tma_load_3d(buf + 16384 * q + 8192, mQ, bar(x, B_QF + b), 64 * q, u.hk, tt);
+        last[LQW] = c;
+    }
+}
+
 // Waits (ignoring the abort flag) for the last copies into each buffer to
 // land, so none writes shared memory after the CTA has left (lane 0 of the
-// loader).
-__device__ void loader_drain(const Ctx &x, const int (&last)[LCOUNT]) {
-    const int single[4][2] = {{LV, B_VF}, {LTU, B_TUF}, {LK, B_KF}, {LP, B_PF}};
-    for (int i = 0; i < 4; ++i)
-        if (last[single[i][0]] >= 0) wait_drain(bar(x, single[i][1]), last[single[i][0]] & 1);
-    const int twodeep[2][2] = {{LW, B_WF}, {LQ, B_QF}};
-    for (int i = 0; i < 2; ++i)
-        for (int k = last[twodeep[i][0]] - 1; k <= last[twodeep[i][0]]; ++k)
-            if (k >= 0) wait_drain(bar(x, twodeep[i][1] + (k & 1)), (k >> 1) & 1);
+// loader warps).
+__device__ void loader_drain(const Ctx &x, const int (&last)[LCOUNT], bool qw) {
+    if (!qw) {
+        const int single[4][2] = {{LV, B_VF}, {LTU, B_TUF}, {LK, B_KF}, {LP, B_PF}};
+        for (int i = 0; i < 4; ++i)
+            if (last[single[i][0]] >= 0) wait_drain(bar(x, single[i][1]), last[single[i][0]] & 1);
+        return;
+    }
+    for (int k = last[LQW] - 1; k <= last[LQW]; ++k)
+        if (k >= 0) {
+            wait_drain(bar(x, B_WF + (k & 1)), (k >> 1) & 1);
+            wait_drain(bar(x, B_QF + (k & 1)), (k >> 1) & 1);
+        }
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread): per chunk U, VN, O, DS, PV, in that order.  Each
+// MMA issuer (one thread): per chunk U, VNO, DS, PV, in that order.  Each
 // buffer is released by a commit after its last reading MMA.
 // ---------------------------------------------------------------------------
 __device__ void mma_role(const Ctx x, const Unit u, uint32_t tm) {
     for (int c = 0; c < u.nc; ++c) {
         const int b = c & 1;
         const uint32_t par = c & 1, par2 = (c >> 1) & 1;
-        // U(c) into acc_v, free once PV(c - 1) is done
-        if (c > 0 && !wait(x, bar(x, B_D_FULL), par ^ 1)) break;
+        // U(c) into [acc_v | acc_o]: acc_v is free once PV(c - 1) is done,
+        // acc_o once the output warpgroup has read it
+        if (c > 0 && !(wait(x, bar(x, B_D_FULL), par ^ 1) && wait(x, bar(x, B_O_EMPTY), par ^ 1))) break;
         if (!(wait(x, bar(x, B_VF), par) && wait(x, bar(x, B_TUF), par))) break;
         tc_fence_after();
 #pragma unroll
@@ -266,24 +342,17 @@ __device__ void mma_role(const Ctx x, const Unit u, uint32_t tm) {
                    ID_U, kk != 0);
         mma_commit(bar(x, B_VE));
         mma_commit(bar(x, B_TUE));
-        // VN(c): v_new^T = U^T + S^T (-W^T)
-        if (!(wait(x, bar(x, B_WF + b), par2) && wait(x, bar(x, B_S_FULL), par))) break;
+        // VNO(c): [acc_v | acc_o] += S^T [-W^T | Q~^T]
+        if (!(wait(x, bar(x, B_WF + b), par2) && wait(x, bar(x, B_QS + b), par2) &&
+              wait(x, bar(x, B_S_FULL), par)))
+            break;
         tc_fence_after();
-        const uint32_t wt = x.base + OFF_WT + 32768 * b;
+        const uint32_t qw = x.base + OFF_QW + QW_BYTES * b;
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk)
-            mma_ts(tm + TM_V, tm + TM_SB + kk * 8, sdesc(wt + kk * 2048, 8192, 1024), ID_VN, 1);
+            mma_ts(tm + TM_V, tm + TM_SB + kk * 8, sdesc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), ID_VNO, 1);
         mma_commit(bar(x, B_VN));
-        mma_commit(bar(x, B_WE + b));
-        // O(c) = S^T Q~^T into acc_o, read by the output warpgroup for c - 1
-        if (!(wait(x, bar(x, B_QS), par) && wait(x, bar(x, B_O_EMPTY), par ^ 1))) break;
-        tc_fence_after();
-        const uint32_t qb = x.base + OFF_Q + 32768 * b;
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-            mma_ts(tm + TM_O, tm + TM_SB + kk * 8, sdesc(qb + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), ID_O,
-                   kk != 0);
-        mma_commit(bar(x, B_QE + b));
+        mma_commit(bar(x, B_QWE + b));
         // DS(c): acc_s (scaled by alpha(c)) += v~^T K
         if (!(wait(x, bar(x, B_VSM), par) && wait(x, bar(x, B_KF), par))) break;
         tc_fence_after();
@@ -334,54 +403,6 @@ __device__ __forceinline__ void state_init(const Params &p, uint32_t lb, size_t 
     }
 }
 
-// After DS(c): the bf16 image of the state chunk c + 1 starts from, or, after
-// the last chunk, ht = acc_s.  All NB TMEM loads are in flight before the one
-// wait.
-template <int NB>
-__device__ __forceinline__ void state_convert(const Params &p, uint32_t lb, size_t hb, bool last, int b0) {
-    uint32_t r[NB][32];
-#pragma unroll
-    for (int e = 0; e < NB; ++e) tmem_ld32(lb + TM_S + 32 * (b0 + e), r[e]);
-    tmem_wait_ld_dep(r[0]);
-#pragma unroll
-    for (int e = 1; e < NB; ++e) tmem_ld_dep(r[e]);
-#pragma unroll
-    for (int e = 0; e < NB; ++e) {
-        const int blk = b0 + e;
-        if (!last) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k)
-                pk[k] = pack_bf16(__uint_as_float(r[e][2 * k]), __uint_as_float(r[e][2 * k + 1]));
-            tmem_st16(lb + TM_SB + 16 * blk, pk);
-        } else if (p.ht) {
-            float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                *hp = __uint_as_float(r[e][k]);
-                hp += p.dv;
-            }
-        }
-    }
-}
-
-// acc_s *= alpha(c + 1) before DS(c + 1).
-template <int NB>
-__device__ __forceinline__ void state_scale(uint32_t lb, float alpha, int b0) {
-    uint32_t r[NB][32];
-#pragma unroll
-    for (int e = 0; e < NB; ++e) tmem_ld32(lb + TM_S + 32 * (b0 + e), r[e]);
-    tmem_wait_ld_dep(r[0]);
-#pragma unroll
-    for (int e = 1; e < NB; ++e) tmem_ld_dep(r[e]);
-#pragma unroll
-    for (int e = 0; e < NB; ++e) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) r[e][k] = __float_as_uint(alpha * __uint_as_float(r[e][k]));
-        tmem_st32(lb + TM_S + 32 * (b0 + e), r[e]);
-    }
-}
-
 // Hand-off after TMEM stores: the stores are complete and ordered before the
 // MMAs that the arrival releases.
 __device__ __forceinline__ void st_arrive(uint32_t b) {
@@ -390,8 +411,58 @@ __device__ __forceinline__ void st_arrive(uint32_t b) {
     warp_arrive(b);
 }
 
+// After DS(c), key blocks [b0, b0 + kPassNB), two at a time: the bf16
+// image of S_{c+1} = A_{c+1} acc_s (then S_FULL, which VNO(c + 1) waits
+// for), and for a renormalising chunk c + 1 acc_s *= alpha_{c+1} A_{c+1}
+// (before VSM, which DS(c + 1) waits for); after the last chunk, ht =
+// A_{c+1} acc_s.  sn: the scalars of chunk c + 1 (those of chunk c after the
+// last chunk).
+__device__ __forceinline__ void state_pass(const Ctx &x, const Params &p, uint32_t lb, size_t hb, bool last,
+                                           int b0, const float *sn) {
+    const float a = last ? sn[SC_AN] : sn[SC_A];
+    const bool rn = !last && sn[SC_RN] != 0.f;
+    const float rs = sn[SC_RS];
+#pragma unroll 1
+    for (int e0 = 0; e0 < kPassNB; e0 += 2) {
+        uint32_t r[2][32];
+        tmem_ld32(lb + TM_S + 32 * (b0 + e0), r[0]);
+        tmem_ld32(lb + TM_S + 32 * (b0 + e0 + 1), r[1]);
+        tmem_wait_ld_dep(r[0]);
+        tmem_ld_dep(r[1]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int blk = b0 + e0 + e;
+            if (last) {
+                if (p.ht) {
+                    float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        *hp = a * __uint_as_float(r[e][k]);
+                        hp += p.dv;
+                    }
+                }
+                continue;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                pk[k] = pack_bf16(a * __uint_as_float(r[e][2 * k]), a * __uint_as_float(r[e][2 * k + 1]));
+            tmem_st16(lb + TM_SB + 16 * blk, pk);
+            if (rn) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) r[e][k] = __float_as_uint(rs * __uint_as_float(r[e][k]));
+                tmem_st32(lb + TM_S + 32 * blk, r[e]);
+            }
+        }
+    }
+    if (last) return;
+    st_arrive(bar(x, B_S_FULL));
+    warp_arrive(bar(x, B_VSM));
+}
+
 // ---------------------------------------------------------------------------
-// Prep warpgroup: Q rows scaled in place, key blocks 0-2 of the state.
+// Prep warpgroup: Q rows scaled in place a chunk ahead, key blocks 0-2 of
+// the state.
 // ---------------------------------------------------------------------------
 // Q row i *= scale e^{G_i} (bf16) for chunk c, so that O and PV share one
 // accumulator: o_i = S^T (scale e^{G_i} q_i) + sum_j P_ij v_new_j.  Each step
@@ -403,12 +474,12 @@ __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     if (!wwait(x, bar(x, B_QF + b), (c >> 1) & 1) || !wwait(x, bar(x, B_SCF + b), (c >> 1) & 1)) return false;
     const float *sc = scal(x, c);
     const int tid = threadIdx.x - 64;
-    uint8_t *qt = x.gbase + OFF_Q + 32768 * b;
+    uint8_t *qt = x.gbase + OFF_QW + QW_BYTES * b + 8192;  // quarter q at qt + 16384 q
 #pragma unroll 4
     for (int it = 0; it < 16; ++it) {
         const int k = tid + 128 * it, quarter = k >> 9, r = (k >> 3) & 63, ch = k & 7;
         const float f = sc[SC_OSC + r];
-        uint4 *qp = reinterpret_cast<uint4 *>(qt + 8192 * quarter + 128 * r + 16 * ch);
+        uint4 *qp = reinterpret_cast<uint4 *>(qt + 16384 * quarter + 128 * r + 16 * ch);
         const uint4 q = *qp;
         uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -419,7 +490,7 @@ __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
         *qp = make_uint4(w[0], w[1], w[2], w[3]);
     }
     fence_proxy_async_smem();
-    warp_arrive(bar(x, B_QS));
+    warp_arrive(bar(x, B_QS + b));
     return true;
 }
 
@@ -429,22 +500,19 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
     const uint32_t lb = lane_base(tm, warp);
     const size_t hb = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;
     if (u.nc == 0 || !scale_q(x, 0)) return;
-    state_init<kPrepNB>(p, lb, hb, scal(x, 0)[SC_ALPHA], kPrepB0);
+    state_init<kPassNB>(p, lb, hb, scal(x, 0)[SC_RN] != 0.f ? scal(x, 0)[SC_RS] : 1.f, kPrepB0);
     st_arrive(bar(x, B_S_FULL));
     warp_arrive(bar(x, B_VSM));
     warp_arrive(bar(x, B_SCE + 0));
     for (int c = 0; c < u.nc; ++c) {
         const bool last = c + 1 == u.nc;
+        // Q~ of the next chunk, which VNO(c + 1) reads, while this chunk's
+        // VNO and DS run
+        if (!last && !scale_q(x, c + 1)) return;
         if (!wwait(x, bar(x, B_S_UPD), c & 1)) return;
         tc_fence_after();
-        state_convert<kPrepNB>(p, lb, hb, last, kPrepB0);
+        state_pass(x, p, lb, hb, last, kPrepB0, scal(x, last ? c : c + 1));
         if (last) break;
-        st_arrive(bar(x, B_S_FULL));
-        // Q~ of the next chunk, which O(c + 1) waits for, then the scaling
-        // of this warpgroup's blocks, which DS(c + 1) waits for
-        if (!scale_q(x, c + 1)) return;
-        state_scale<kPrepNB>(lb, scal(x, c + 1)[SC_ALPHA], kPrepB0);
-        st_arrive(bar(x, B_VSM));
         warp_arrive(bar(x, B_SCE + ((c + 1) & 1)));
     }
 }
@@ -463,7 +531,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         return;
     }
     if (!wwait(x, bar(x, B_SCF + 0), 0)) return;
-    state_init<kStateNB>(p, lb, hb, scal(x, 0)[SC_ALPHA], kStateB0);
+    state_init<kPassNB>(p, lb, hb, scal(x, 0)[SC_RN] != 0.f ? scal(x, 0)[SC_RS] : 1.f, kStateB0);
     st_arrive(bar(x, B_S_FULL));
     warp_arrive(bar(x, B_VSM));
     for (int c = 0; c < u.nc; ++c) {
@@ -504,25 +572,23 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
             st_arrive(bar(x, B_VSM));
         }
         warp_arrive(bar(x, B_SCE + (c & 1)));  // done with this chunk's scalars
-        // ---- state: the next chunk's bf16 image, then acc_s *= alpha ----
+        // ---- state: the next chunk's bf16 image (key blocks 4-7) ---------
         const bool last = c + 1 == u.nc;
+        if (!last && !wwait(x, bar(x, B_SCF + ((c + 1) & 1)), ((c + 1) >> 1) & 1)) return;
         if (!wwait(x, bar(x, B_S_UPD), c & 1)) return;
         tc_fence_after();
-        state_convert<kStateNB>(p, lb, hb, last, kStateB0);
+        state_pass(x, p, lb, hb, last, kStateB0, scal(x, last ? c : c + 1));
         if (last) break;
-        st_arrive(bar(x, B_S_FULL));
-        if (!wwait(x, bar(x, B_SCF + ((c + 1) & 1)), ((c + 1) >> 1) & 1)) return;
-        state_scale<kStateNB>(lb, scal(x, c + 1)[SC_ALPHA], kStateB0);
-        st_arrive(bar(x, B_VSM));
     }
 }
 
 // ---------------------------------------------------------------------------
-// Output warpgroup: key blocks 6-7 of the state, then o[i][v] =
-// (S^T Q~^T + v_new^T P^T)[v][i] for value column v = this thread's TMEM
-// lane, chunk by chunk once PV is done.  Every exit is taken by the whole
-// warpgroup together (bar_red_or), so no warp is left waiting at one of its
-// named barriers.
+// Output warpgroup: o[i][v] = (S^T Q~^T + v_new^T P^T)[v][i] for value column
+// v = this thread's TMEM lane, chunk by chunk once PV is done.  acc_o is read
+// and released first (it is the next chunk's U accumulator too), then
+// transposed through shared memory and stored.  Every exit is taken by the
+// whole warpgroup together (bar_red_or), so no warp is left waiting at one of
+// its named barriers.
 // ---------------------------------------------------------------------------
 __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
@@ -532,29 +598,9 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     const uint32_t buf = x.base + OFF_OST;
     const uint8_t *gbuf = x.gbase + OFF_OST;
     const long long rstride = (long long)p.Nv * p.dv * 2;  // bytes between tokens
-    const size_t hb = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;
-    if (u.nc == 0) return;
-    if (bar_red_or(2, 128, !wwait(x, bar(x, B_SCF + 0), 0))) return;
-    state_init<kOutNB>(p, lb, hb, scal(x, 0)[SC_ALPHA], kOutB0);
-    st_arrive(bar(x, B_S_FULL));
-    warp_arrive(bar(x, B_VSM));
-    warp_arrive(bar(x, B_SCE + 0));
     for (int c = 0; c < u.nc; ++c) {
-        const bool last = c + 1 == u.nc;
-        if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
-        tc_fence_after();
-        state_convert<kOutNB>(p, lb, hb, last, kOutB0);
-        if (!last) {
-            st_arrive(bar(x, B_S_FULL));
-            if (bar_red_or(2, 128, !wwait(x, bar(x, B_SCF + ((c + 1) & 1)), ((c + 1) >> 1) & 1))) break;
-            state_scale<kOutNB>(lb, scal(x, c + 1)[SC_ALPHA], kOutB0);
-            st_arrive(bar(x, B_VSM));
-            warp_arrive(bar(x, B_SCE + ((c + 1) & 1)));
-        }
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
         tc_fence_after();
-        const long long t0 = u.bos + (long long)c * p.chunk;
-        const int L = (int)min((long long)p.chunk, u.eos - t0);
         // the chunk's output column v as packed bf16 pairs (tokens 2k, 2k + 1)
         uint32_t ob[32];
 #pragma unroll
@@ -570,6 +616,8 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         warp_arrive(bar(x, B_O_EMPTY));
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
+        const long long t0 = u.bos + (long long)c * p.chunk;
+        const int L = (int)min((long long)p.chunk, u.eos - t0);
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -609,15 +657,15 @@ tc_wide_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUte
     const Unit u = unit_of(p);
 
     if (threadIdx.x == 0) {
-        const int ones[] = {B_KF, B_KE, B_QF, B_QF + 1, B_QE, B_QE + 1, B_WF, B_WF + 1, B_WE, B_WE + 1,
-                            B_VF, B_VE, B_TUF, B_TUE, B_PF, B_PE, B_SCF, B_SCF + 1, B_VN, B_S_UPD,
-                            B_D_FULL, B_DRAIN};
+        const int ones[] = {B_KF, B_KE, B_WF, B_WF + 1, B_QF, B_QF + 1, B_QWE, B_QWE + 1, B_VF, B_VE,
+                            B_TUF, B_TUE, B_PF, B_PE, B_SCF, B_SCF + 1, B_VN, B_S_UPD, B_D_FULL, B_DRAIN};
         for (int b : ones) mbar_init(bar(x, b), 1);
-        mbar_init(bar(x, B_SCE), 12);
-        mbar_init(bar(x, B_SCE + 1), 12);
+        mbar_init(bar(x, B_SCE), 8);      // prep and state warpgroups
+        mbar_init(bar(x, B_SCE + 1), 8);
         mbar_init(bar(x, B_QS), 4);
-        mbar_init(bar(x, B_S_FULL), 12);  // prep, state and output warpgroups
-        mbar_init(bar(x, B_VSM), 16);     // the same twelve (alpha) + state (v_new, v~)
+        mbar_init(bar(x, B_QS + 1), 4);
+        mbar_init(bar(x, B_S_FULL), 8);   // prep and state warpgroups, half the state each
+        mbar_init(bar(x, B_VSM), 12);     // the same eight (state pass) + state (v_new, v~)
         mbar_init(bar(x, B_O_EMPTY), 4);
         *x.abort_flag = 0;
         fence_barrier_init();
@@ -631,17 +679,23 @@ tc_wide_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUte
         prefetch_tmap(&mQ);
         prefetch_tmap(&mV);
     }
+    // the 64 zero rows of U's B operand
+    for (int i = threadIdx.x; i < 8192 / 16; i += NTHREADS)
+        *reinterpret_cast<uint4 *>(x.gbase + OFF_ZERO + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *reinterpret_cast<volatile uint32_t *>(x.gbase + OFF_MISC);
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 14) {
         int last[LCOUNT];
         for (int i = 0; i < LCOUNT; ++i) last[i] = -1;
-        loader_role(x, p, u, &mK, &mQ, &mV, last);
-        if ((threadIdx.x & 31) == 0) loader_drain(x, last);
+        if (warp == 0)
+            loader_role(x, p, u, &mK, &mV, last);
+        else if ((threadIdx.x & 31) == 0)
+            qw_loader_role(x, p, u, &mQ, last);
+        if ((threadIdx.x & 31) == 0) loader_drain(x, last, warp == 14);
         __syncwarp();
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0 && u.nc > 0) mma_role(x, u, tm);
@@ -671,7 +725,7 @@ cudaError_t tc_wide_launch(const Params &p, cudaStream_t stream, const char **na
     const long long grid = (long long)p.N * p.Nv * (p.dv / BVT);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    // -W^T, T'' and P of every chunk first (all chunks in parallel), then the scan
+    // -W, T'' and P of every chunk first (all chunks in parallel), then the scan
     cudaError_t err = wy_launch(p, mK, mQ, stream);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(tc_wide_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);

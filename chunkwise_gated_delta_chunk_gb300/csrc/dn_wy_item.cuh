@@ -73,18 +73,18 @@ struct Lay {
     static constexpr uint32_t OFF_SC = TILE_BYTES;
     static constexpr uint32_t OFF_NRM = OFF_SC + SCAL_FLOATS * 4;  // 64 inverse key norms, 64 inverse query norms
     static constexpr uint32_t OFF_BAR = OFF_NRM + 512;
-    static constexpr uint32_t SMEM_USED = OFF_BAR + 32;             // 2 mbarriers, TMEM base, flag, W mbarrier
+    static constexpr uint32_t SMEM_USED = OFF_BAR + 40;             // 2 mbarriers, TMEM base, flag, 2 W mbarriers
     static constexpr uint32_t GROUP_BYTES = (SMEM_USED + 1023u) & ~1023u;  // one worker's region
-    // [K; Q] K^T in columns 0-63; for dk = 256, W^T (two 128-row halves of
-    // d) in columns 0-63 and 64-127 after it
+    // [K; Q] K^T in columns 0-63; for dk = 256, then W, one 128-column half
+    // of d at a time
     static constexpr uint32_t TM_COLS = DKW == 128 ? 64 : 128;
 };
 static_assert(kImageBytes == 8192 && slot_norm_off(128) == 3 * kImageBytes &&
                   slot_norm_off(256) == 32768 + 2 * kImageBytes,
-              "slot = T' or -W^T | T'' | P | norms");
+              "slot = T' or -W | T'' | P | norms");
 
 constexpr uint32_t ID_KQ = idesc_bf16(128, 64, 0, 0);  // A, B K-major
-constexpr uint32_t ID_W = idesc_bf16(128, 64, 1, 0);   // A MN-major (K^T), B K-major (T' rows)
+constexpr uint32_t ID_WK = idesc_bf16(128, 128, 0, 1); // A K-major (T' rows), B MN-major (K rows)
 
 __device__ bool wait_bounded(uint32_t b, uint32_t parity) {
     const uint64_t t0 = globaltimer();
@@ -326,6 +326,7 @@ __device__ __forceinline__ void group_init(const Group &g) {
         mbar_init(g.base + Lay<DKW>::OFF_BAR, 1);
         mbar_init(g.base + Lay<DKW>::OFF_BAR + 8, 1);
         mbar_init(g.base + Lay<DKW>::OFF_BAR + 24, 1);
+        mbar_init(g.base + Lay<DKW>::OFF_BAR + 32, 1);
         fence_barrier_init();
     }
 }
@@ -366,55 +367,57 @@ __device__ __forceinline__ ChunkGates item_gates(const Params &p, long long slot
     return chunk_gates_load(p, h, l.t0, l.L, lane);
 }
 
-// dk = 256: W^T = K^T T'^T, with the K tile quarters read MN-major and the T'
-// image at OFF_TPI (written by threads 0-63 just before) read K-major, into
-// TMEM columns 0-63 (d = 0..127) and 64-127 (d = 128..255); then -W^T row d
-// (the thread's TMEM lane in each half, 64 tokens) is rounded to bf16 and
-// stored to the slot.  Returns false when the MMA's wait ran out.
+// dk = 256: -W = -T' K as the bf16 K-major image the scan kernel reads (four
+// 64-column quarters of 64 rows x 128 B, swizzled like the other images), in
+// two 128-column halves of d.  Each half is one MMA chain with M = 128: A is
+// the T' image at OFF_TPI (written by threads 0-63 just before) followed by
+// 64 rows the result ignores, B the K tile quarters read MN-major; TMEM lane
+// i < 64 then holds row i of W.  Returns false when a wait ran out.
 template <int DKW>
 __device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
     using Y = Lay<DKW>;
-    const uint32_t b_w = g.base + Y::OFF_BAR + 24;
     volatile int *okf = reinterpret_cast<volatile int *>(g.gb + Y::OFF_BAR + 20);
+    const int warp = g.tid >> 5, i = g.tid;
     fence_proxy_async_smem();  // the T' image is read through the async proxy
-    tc_fence_before();
-    named_bar_sync(g.bid, NT);
-    if (g.tid == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t b_w = g.base + Y::OFF_BAR + 24 + 8 * hh;
+        tc_fence_before();
+        named_bar_sync(g.bid, NT);  // T' written / the previous half read
+        if (g.tid == 0) {
+            tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_ss(g.tm + 64 * hh, sdesc(g.base + 32768 * hh + kk * 2048, 16384, 1024),
-                       sdesc(g.base + Y::OFF_TPI + kk * 32, 16, 1024), ID_W, kk != 0);
-        mma_commit(b_w);
-        if (!wait_bounded(b_w, par)) {
-            wait_bounded(b_w, par);  // drain: the MMA still reads shared memory
-            *okf = 0;
-            atomicOr(p.status, kStatusTimeout);
+                mma_ss(g.tm, sdesc(g.base + Y::OFF_TPI + kk * 32, 16, 1024),
+                       sdesc(g.base + 32768 * hh + kk * 2048, 16384, 1024), ID_WK, kk != 0);
+            mma_commit(b_w);
+            if (!wait_bounded(b_w, par)) {
+                wait_bounded(b_w, par);  // drain: the MMA still reads shared memory
+                *okf = 0;
+                atomicOr(p.status, kStatusTimeout);
+            }
         }
-    }
-    tc_fence_before();
-    named_bar_sync(g.bid, NT);
-    tc_fence_after();
-    if (*okf == 0) return false;
-    const int warp = g.tid >> 5;
+        tc_fence_before();
+        named_bar_sync(g.bid, NT);
+        tc_fence_after();
+        if (*okf == 0) return false;
+        if (warp < 2) {
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {  // 32 columns of d at a time
+                uint32_t r[32], pk[16];
+                tmem_ld32(g.tm + ((uint32_t)(32 * warp) << 16) + 32 * cb, r);
+                tmem_wait_ld_dep(r);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t r0[32], r1[32];
-        const uint32_t ta = g.tm + ((uint32_t)(32 * warp) << 16) + 64 * hh;
-        tmem_ld32(ta, r0);
-        tmem_ld32(ta + 32, r1);
-        tmem_wait_ld_dep(r0);
-        tmem_ld_dep(r1);
-        uint32_t pk[2][16];
+                for (int k = 0; k < 16; ++k)
+                    pk[k] = pack_bf16(-__uint_as_float(r[2 * k]), -__uint_as_float(r[2 * k + 1]));
+                // d = 128 hh + 32 cb + 8 ch + e: quarter 2 hh + cb / 2, 16-byte chunk 4 (cb & 1) + ch
+                uint8_t *q = img + 8192 * (2 * hh + (cb >> 1)) + i * 128;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            pk[0][k] = pack_bf16(-__uint_as_float(r0[2 * k]), -__uint_as_float(r0[2 * k + 1]));
-            pk[1][k] = pack_bf16(-__uint_as_float(r1[2 * k]), -__uint_as_float(r1[2 * k + 1]));
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4 *>(q + (((4 * (cb & 1) + ch) ^ (i & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            }
         }
-        store_image_row(img, g.tid + 128 * hh, 0, pk[0]);
-        store_image_row(img, g.tid + 128 * hh, 1, pk[1]);
     }
     return true;
 }
@@ -425,10 +428,10 @@ __device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
 // next_h), whose loads then overlap the rest of this item.  Returns false
 // when a wait ran out (the worker must stop).
 //
-// dk = 256 adds a step 6: the bf16 T' image goes to shared memory, one MMA
-// chain computes W^T = K^T T'^T into tensor memory (two 128-row halves of d),
-// and the threads store -W^T (row d = TMEM lane) to the slot, so that the
-// scan kernel needs neither T' nor tensor memory for W.
+// dk = 256 adds a step 6: the bf16 T' image goes to shared memory, MMAs
+// compute W = T' K into tensor memory (two 128-column halves of d), and
+// threads 0-63 store row i of -W to the slot, so that the scan kernel needs
+// neither T' nor tensor memory for W.
 template <int DKW, bool QKN>
 __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, const Params &p, long long slot,
                      int h, const ItemLoc &loc, ChunkGates &gates, long long next_slot, int next_h) {

@@ -200,21 +200,38 @@ def test_custom_scale(lib):
     check(inp, o, ht, label="scale")
 
 
-def test_extreme_gates(lib):
-    """Very strong decay (e^g ~ 1e-13 per token), no decay, and beta = 1."""
-    inp = inputs(dk=128, dv=128, seed=302, T=150)
+@pytest.mark.parametrize("dk", [128, 256])
+def test_extreme_gates(lib, dk):
+    """Very strong decay (e^g ~ 1e-13 per token), no decay, and beta = 1;
+    for dk = 256 also a weak decay over many chunks, which the wide kernel
+    carries as a running product (renormalised when it leaves [2^-40, 2^40])."""
+    inp = inputs(dk=dk, dv=128, seed=302, T=150)
     inp["g"] = torch.full_like(inp["g"], -30.0)
     o, ht = run_gpu(inp)
     check(inp, o, ht, label="g=-30")
-    inp = inputs(dk=128, dv=128, seed=303, T=150)
+    inp = inputs(dk=dk, dv=128, seed=303, T=150)
     inp["g"] = torch.zeros_like(inp["g"])
     inp["beta"] = torch.ones_like(inp["beta"])
     o, ht = run_gpu(inp)
     check(inp, o, ht, label="g=0 beta=1")
-    inp = inputs(dk=128, dv=128, seed=304, T=150)
+    inp = inputs(dk=dk, dv=128, seed=304, T=150)
     inp["g"] = -torch.rand(inp["g"].shape, generator=torch.Generator().manual_seed(9)) * 4.0
     o, ht = run_gpu(inp)
     check(inp, o, ht, label="g~U(-4,0)")
+    if dk == 256:
+        # e^{G_L} ~ e^-0.6 per chunk: the product crosses 2^-40 after ~45 chunks
+        inp = inputs(B=1, dk=dk, dv=128, seed=305, T=64 * 120 + 17)
+        inp["g"] = torch.full_like(inp["g"], -0.01)
+        o, ht = run_gpu(inp)
+        check(inp, o, ht, label="g=-0.01 long")
+        # strong and weak chunks alternating
+        inp = inputs(B=1, dk=dk, dv=128, seed=306, T=64 * 12)
+        g = torch.full_like(inp["g"], -0.02)
+        g[:, 64 * 3:64 * 4] = -2.0
+        g[:, 64 * 7:64 * 8] = -30.0
+        inp["g"] = g
+        o, ht = run_gpu(inp)
+        check(inp, o, ht, label="g mixed")
 
 
 def test_state_carry(lib):
@@ -325,6 +342,7 @@ SAMPLES = {
     "gdn_gqa_varlen_bf16_n8_nk8_nv32_d128": "longest_shortest",
     "gdn_long_bf16_b1_h32_t32768_d128": [0, 31],
     "gdn_wide_bf16_b8_h8_t8192_d256": [0, 63],
+    "gdn_wide_bf16_b2_h8_t8192_d256": [5],
     "gdn_decode_bf16_b64_h16_t1_d128": None,
     "gdn_l2norm_bf16_b4_h16_t2048_d128": [0, 33, 63],
 }

@@ -62,6 +62,10 @@ WORKLOADS = {
                  dv=128, dtype=torch.bfloat16, gate_mu=5.0, h0=False, seed=4),
         Workload("gdn_wide_bf16_b8_h8_t8192_d256", B=8, T=8192, Nk=8, Nv=8, dk=256, dv=256,
                  dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=5),
+        # the wide-head shapes at a quarter of the batch (profiling case: its
+        # inputs still exceed L2)
+        Workload("gdn_wide_bf16_b2_h8_t8192_d256", B=2, T=8192, Nk=8, Nv=8, dk=256, dv=256,
+                 dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=8),
         # one decoding step of 64 sequences: the state comes in and goes out
         Workload("gdn_decode_bf16_b64_h16_t1_d128", B=64, T=1, Nk=16, Nv=16, dk=128, dv=128,
                  dtype=torch.bfloat16, gate_mu=3.0, h0=True, seed=6),
