@@ -155,6 +155,46 @@ __device__ __forceinline__ void chunk_scalars_store(const Params &p, const Chunk
     }
 }
 
+// The scan kernels keep the state in tensor memory unscaled: acc_s holds
+// S_c / A_c, where A_c is the product of the decays alpha = e^{G_L} of the
+// chunks since the last renormalisation.  A chunk whose decay keeps
+// alpha_c A_c within [2^-40, 2^40] needs no pass over acc_s: A_{c+1} =
+// alpha_c A_c, and v~ is divided by A_{c+1} before DS accumulates it (the
+// factor rides on e^{G_L - G_i}).  Otherwise (strong decay, or alpha = 0) the
+// chunk renormalises: acc_s is scaled by alpha_c A_c before DS(c) and
+// A_{c+1} = 1.  The bf16 image of the state is A_c acc_s and ht =
+// A acc_s, so every product sees S itself.  The loader tracks A; the scalar
+// block of chunk c then also holds:
+constexpr int SC_A = 452;   // A_c
+constexpr int SC_RN = 453;  // 1: renormalise before DS(c)
+constexpr int SC_RS = 454;  // alpha_c A_c, the renormalising scale
+constexpr int SC_AN = 455;  // A_{c+1}
+static_assert(SC_A > SC_FACT && SC_AN < SCAL_FLOATS, "free scalar slots");
+constexpr float kAMin = 0x1p-40f, kAMax = 0x1p40f;
+
+struct ChunkDecay {
+    float A, rs, an;
+    bool rn;
+};
+
+// The decay bookkeeping of a chunk whose G at its last token is GL, entered
+// with A = A_c (every lane computes the same).
+__device__ __forceinline__ ChunkDecay chunk_decay(float GL, float A) {
+    ChunkDecay d;
+    d.A = A;
+    d.rs = __expf(GL) * A;
+    d.rn = !(d.rs >= kAMin && d.rs <= kAMax);
+    d.an = d.rn ? 1.f : d.rs;
+    return d;
+}
+
+__device__ __forceinline__ void chunk_decay_store(float *sc, const ChunkDecay &d) {
+    sc[SC_A] = d.A;
+    sc[SC_RN] = d.rn ? 1.f : 0.f;
+    sc[SC_RS] = d.rs;
+    sc[SC_AN] = d.an;
+}
+
 // Loads and prefix-sums the gates of the chunk [t0, t0 + L) of value head h
 // (one warp).
 __device__ __forceinline__ ChunkScalars chunk_scalars_load(const Params &p, int h, long long t0, int L, int lane) {

@@ -35,10 +35,14 @@
 //          operand, running ahead of the state scan, then scales the chunk's
 //          Q rows by scale e^G in place for O;
 //   6-9    state: v_new and v~ operands; key blocks 0-1 of the state passes;
-//   10-13  output: key blocks 2-3 of each state pass (the S^T operand, the
-//          alpha scaling, ht); then reads o = scale e^{G} (S^T Q^T) +
-//          P v_new, transposes it through shared memory, stores bf16 rows;
+//   10-13  output: key blocks 2-3 of each state pass (the S^T operand or
+//          ht); then reads o = scale e^{G} (S^T Q^T) + P v_new, transposes
+//          it through shared memory, stores bf16 rows;
 //   14     output MMA issuer (one thread: O, PV).
+//
+// acc_s holds the state divided by a running product of the chunk decays
+// (chunk_decay in dn_chunk.cuh), so a chunk's decay needs no pass over the
+// state: the state passes multiply by the product where they read it out.
 //
 // With Params::hs set (the backward's state pass, no o) the state passes also
 // store the fp32 state each chunk starts from, and o is not written.
@@ -192,6 +196,7 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
     if (lane == 0)
         for (int c = 0; c < min(u.nc, 2); ++c)
             for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c);
+    float A = 1.f;  // running decay product A_c (chunk_decay), the same in every lane
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const long long t0 = u.bos + (long long)c * p.chunk;
@@ -204,6 +209,10 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
                                      ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes +
                                      kSlotNormOff,
                              lane);
+        const ChunkDecay dec = chunk_decay(cs.GL, A);
+        A = dec.an;
+        cs.ka /= dec.an;  // rides on e^{G_L - G_i}: v~ / A_{c+1}
+        cs.kb /= dec.an;
         if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
         const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
         if (lane == 0) {
@@ -219,6 +228,7 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         }
         armed = c;
         chunk_scalars_store(p, cs, scal(x, s), lane);
+        if (lane == 0) chunk_decay_store(scal(x, s), dec);
         __syncwarp();
 #ifdef DN_TEST_STALL
         // failure-path test: the first stage's second arrival never comes, so
@@ -349,7 +359,8 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 // chain.  `lb` is the thread's TMEM lane base; `hb` its element of h0 / ht at
 // key index 0 (row stride dv).
 // ---------------------------------------------------------------------------
-// acc_s = alpha_0 h0^T and SB[0] = bf16(h0^T), blocks [b0, b1).
+// acc_s = s0 h0^T and SB[0] = bf16(h0^T), blocks [b0, b1), with s0 =
+// alpha_0 when chunk 0 renormalises and 1 otherwise (chunk_decay: A_0 = 1).
 // Column of this lane's value column v in the saved state of chunk c (row
 // d = 0, rows dv apart), or null when the states are not saved.
 __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, int v) {
@@ -358,7 +369,7 @@ __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, 
     return p.hs + ((size_t)u.h * p.nslots + (size_t)slot) * DK * p.dv + u.v0 + v;
 }
 
-__device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, size_t hb, float alpha, int b0,
+__device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, size_t hb, float s0, int b0,
                                                   int b1, float *hsd) {
     uint32_t r[32], pk[16];
     for (int blk = b0; blk < b1; ++blk) {
@@ -381,16 +392,17 @@ __device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, 
         for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
         tmem_st16(lb + TM_SB + 16 * blk, pk);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(alpha * f[k]);
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(s0 * f[k]);
         tmem_st32(lb + TM_S + 32 * blk, r);
     }
 }
 
-// After DS(c): SB[(c+1) & 1] = bf16(acc_s) (and, with hsd, the fp32 state
-// chunk c + 1 starts from), or for the last chunk ht = acc_s.  Key blocks b0
-// and b0 + 1: both TMEM loads are in flight before the one wait.
+// After DS(c), key blocks b0 and b0 + 1: SB[(c+1) & 1] = bf16(a acc_s) with
+// a = A_{c+1} (and, with hsd, the fp32 state chunk c + 1 starts from); or for
+// the last chunk ht = a acc_s with a = A_{nc} (chunk_decay).  Both TMEM
+// loads are in flight before the one wait.
 __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t lb, size_t hb, int c, bool last,
-                                                     int b0, float *hsd) {
+                                                     int b0, float *hsd, float a) {
     uint32_t r[2][32];
     tmem_ld32(lb + TM_S + 32 * b0, r[0]);
     tmem_ld32(lb + TM_S + 32 * (b0 + 1), r[1]);
@@ -403,13 +415,13 @@ __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t l
             uint32_t pk[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k)
-                pk[k] = pack_bf16(__uint_as_float(r[e][2 * k]), __uint_as_float(r[e][2 * k + 1]));
+                pk[k] = pack_bf16(a * __uint_as_float(r[e][2 * k]), a * __uint_as_float(r[e][2 * k + 1]));
             tmem_st16(lb + TM_SB + 64 * ((c + 1) & 1) + 16 * blk, pk);
             if (hsd) {
                 float *dp = hsd + (size_t)(32 * blk) * p.dv;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    *dp = __uint_as_float(r[e][k]);
+                    *dp = a * __uint_as_float(r[e][k]);
                     dp += p.dv;
                 }
             }
@@ -417,15 +429,16 @@ __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t l
             float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-                *hp = __uint_as_float(r[e][k]);
+                *hp = a * __uint_as_float(r[e][k]);
                 hp += p.dv;
             }
         }
     }
 }
 
-// acc_s *= alpha(c+1) before DS(c+1), key blocks b0 and b0 + 1.
-__device__ __forceinline__ void state_scale_blocks(uint32_t lb, float alpha, int b0) {
+// A renormalising chunk c + 1 (chunk_decay): acc_s *= rs = alpha_{c+1}
+// A_{c+1} before DS(c+1), key blocks b0 and b0 + 1.
+__device__ __noinline__ void state_renorm_blocks(uint32_t lb, float rs, int b0) {
     uint32_t r[2][32];
     tmem_ld32(lb + TM_S + 32 * b0, r[0]);
     tmem_ld32(lb + TM_S + 32 * (b0 + 1), r[1]);
@@ -434,7 +447,7 @@ __device__ __forceinline__ void state_scale_blocks(uint32_t lb, float alpha, int
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[e][k] = __float_as_uint(alpha * __uint_as_float(r[e][k]));
+        for (int k = 0; k < 32; ++k) r[e][k] = __float_as_uint(rs * __uint_as_float(r[e][k]));
         tmem_st32(lb + TM_S + 32 * (b0 + e), r[e]);
     }
 }
@@ -455,7 +468,8 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     if (u.nc > 0) {
         // blocks 2-3 of the initial state; then acc_s is ready for DS(0)
         if (!bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + 0), 0))) {
-            state_init_blocks(p, lb, hb, scal(x, 0)[SC_ALPHA], 2, 4, hs_col(p, u, 0, v));
+            const float *s0 = scal(x, 0);
+            state_init_blocks(p, lb, hb, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, 2, 4, hs_col(p, u, 0, v));
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
@@ -465,21 +479,21 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     for (int c = 0; c < u.nc; ++c) {
         // Every exit is taken by the whole warpgroup together (bar_red_or), so
         // no warp is left waiting at one of its named barriers.
-        // Blocks 2-3 of the state: the S^T operand of chunk c + 1 (or ht),
-        // then acc_s *= alpha(c+1), which DS(c+1) waits for (VSM_FULL).
+        // Blocks 2-3 of the state: the S^T operand of chunk c + 1 (or ht);
+        // acc_s is then ready for DS(c+1) (VSM_FULL).
         const bool last = c + 1 == u.nc;
+        const int s1 = (c + 1) % NS;
+        if (!last && bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1))) break;
+        const float *sn = scal(x, last ? c % NS : s1);
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
         tc_fence_after();
-        state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col(p, u, c + 1, v));
+        state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col(p, u, c + 1, v),
+                             last ? sn[SC_AN] : sn[SC_A]);
+        if (!last && sn[SC_RN] != 0.f) state_renorm_blocks(lb, sn[SC_RS], 2);
         if (!last) {
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
-            const int s1 = (c + 1) % NS;
-            if (bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1))) break;
-            state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 2);
-            tmem_wait_st();
-            tc_fence_before();
             warp_arrive(bar(x, B_VSM_FULL));
         }
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_D_FULL), c & 1))) break;
@@ -678,10 +692,11 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
             for (int d = 0; d < DK; ++d) p.ht[sbase + (size_t)d * dv] = p.h0 ? p.h0[sbase + (size_t)d * dv] : 0.f;
         return;
     }
-    // initial state: acc_s = alpha_0 h0^T, SB = bf16(h0^T) (blocks 0-1 here,
+    // initial state: acc_s = s0 h0^T, SB = bf16(h0^T) (blocks 0-1 here,
     // 2-3 in the output warpgroup)
     if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
-    state_init_blocks(p, lb, sbase, scal(x, 0)[SC_ALPHA], 0, 2, hs_col(p, u, 0, v));
+    const float *s0 = scal(x, 0);
+    state_init_blocks(p, lb, sbase, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, 0, 2, hs_col(p, u, 0, v));
     tmem_wait_st();
     tc_fence_before();
     warp_arrive(bar(x, B_S_FULL));
@@ -732,21 +747,20 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
             warp_arrive(bar(x, B_VSM_FULL));
         }
         warp_arrive(bar(x, B_EMPTY + s));  // done with this chunk's scalars
-        // ---- state: S_in(c+1) operand, then pre-scale by alpha(c+1) ------
+        // ---- state: S_in(c+1) operand (blocks 0-1) -----------------------
         const bool last = (c + 1 == u.nc);
+        const int s1 = (c + 1) % NS;
+        if (!last && !wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
+        const float *sn = scal(x, last ? s : s1);
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         tc_fence_after();
-        state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col(p, u, c + 1, v));
-        if (!last) {
-            tmem_wait_st();
-            tc_fence_before();
-            warp_arrive(bar(x, B_S_FULL));
-        }
+        state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col(p, u, c + 1, v),
+                             last ? sn[SC_AN] : sn[SC_A]);
         if (last) break;
-        const int s1 = (c + 1) % NS;
-        if (!wwait(x, bar(x, B_FULL + s1), ((c + 1) / NS) & 1)) return;
-        state_scale_blocks(lb, scal(x, s1)[SC_ALPHA], 0);
-        tmem_wait_st();  // ordered before the next v~ arrive (fence there)
+        if (sn[SC_RN] != 0.f) state_renorm_blocks(lb, sn[SC_RS], 0);
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(bar(x, B_S_FULL));
     }
 }
 

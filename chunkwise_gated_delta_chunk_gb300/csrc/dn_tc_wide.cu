@@ -45,7 +45,8 @@
 //   14     loader of the -W / Q tiles (one thread), up to two chunks ahead.
 // A state pass turns acc_s into the next chunk's bf16 image (or ht after the
 // last chunk).  acc_s holds the state divided by a running product of the
-// chunk decays, so the decay of each chunk needs no pass over it (see SC_A).
+// chunk decays, so the decay of each chunk needs no pass over it (see
+// chunk_decay in dn_chunk.cuh).
 //
 // Every wait is bounded (dn_tc_sync.cuh): a wait that runs out records
 // kStatusTimeout, raises the CTA's abort flag, and every role drains its own
@@ -131,21 +132,7 @@ constexpr uint32_t ID_PV = idesc_bf16(128, 64, 0, 0);    // A TMEM, B K-major (P
 // Key blocks (32 columns of acc_s) of each state pass, per warpgroup.
 constexpr int kPrepB0 = 0, kStateB0 = 4, kPassNB = 4;
 
-// The state in tensor memory is kept unscaled: acc_s holds S_c / A_c, where
-// A_c is the product of the decays alpha = e^{G_L} of the chunks since the
-// last renormalisation.  A chunk whose decay keeps alpha_c A_c within
-// [2^-40, 2^40] needs no pass over acc_s: A_{c+1} = alpha_c A_c, and v~ is
-// divided by A_{c+1} before DS accumulates it.  Otherwise (a renormalising
-// chunk: strong decay, or alpha = 0) acc_s is scaled by alpha_c A_c before
-// DS(c) and A_{c+1} = 1.  The bf16 image is A_c (S_c / A_c) and ht =
-// A (S / A), so VN, O and ht see S itself.  Extra scalars per chunk (the
-// loader tracks A):
-constexpr int SC_A = 452;   // A_c
-constexpr int SC_RN = 453;  // 1: renormalise before DS(c)
-constexpr int SC_RS = 454;  // alpha_c A_c, the renormalising scale
-constexpr int SC_AN = 455;  // A_{c+1} (SC_DEC already carries 1 / A_{c+1})
-static_assert(SC_A > SC_FACT && SC_AN < SCAL_FLOATS, "free scalar slots");
-constexpr float kAMin = 9.094947e-13f, kAMax = 1.0995116e12f;  // 2^-40, 2^40
+
 
 __device__ __forceinline__ uint32_t bar(const Ctx &x, int i) { return x.base + OFF_BAR + 8u * i; }
 __device__ __forceinline__ float *scal(const Ctx &x, int c) {
@@ -258,10 +245,8 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         const ChunkInputs in = next;
         if (c + 1 < u.nc) next = chunk_inputs_load(p, u, c + 1, lane);
         ChunkScalars cs = chunk_scalars_from(in.gates, L, lane);
-        const float rs = __expf(cs.GL) * A;
-        const bool rn = !(rs >= kAMin && rs <= kAMax);
-        const float an = rn ? 1.f : rs;
-        const float inv_an = 1.f / an;
+        const ChunkDecay dec = chunk_decay(cs.GL, A);
+        const float inv_an = 1.f / dec.an;
         cs.ka = in.ka * inv_an;  // rides on e^{G_L - G_i}: v~ / A_{c+1}
         cs.kb = in.kb * inv_an;
         cs.qa = in.qa;
@@ -269,13 +254,8 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         if (!wwait(x, bar(x, B_SCE + (c & 1)), ((c >> 1) & 1) ^ 1)) return;
         float *sc = scal(x, c);
         chunk_scalars_store(p, cs, sc, lane);
-        if (lane == 0) {
-            sc[SC_A] = A;
-            sc[SC_RN] = rn ? 1.f : 0.f;
-            sc[SC_RS] = rs;
-            sc[SC_AN] = an;
-        }
-        A = an;
+        if (lane == 0) chunk_decay_store(sc, dec);
+        A = dec.an;
         __syncwarp();
         bool ok = true;
         if (lane == 0) {
