@@ -118,18 +118,18 @@ typedef enum {
  *
  * Returns DN_OK once the work is enqueued; DN_ERR_INVALID_ARG also when the
  * workspace is missing, misaligned or too small.  The tensor-core path
- * (bf16, dk = 128, dv a multiple of 128) launches two kernels per call: the
- * per-chunk WY inverse T and causal scores of every chunk in parallel
- * ([WY] §2.3-§2.4), then the sequential state scan and output ([CGDR]
- * §3.2-§3.3).  Other shapes launch one CUDA-core kernel; for DN_BF16 its
+ * (bf16, dk = 128 or 256, dv a multiple of 128) launches two kernels per
+ * call: the per-chunk WY inverse T and causal scores of every chunk in
+ * parallel ([WY] §2.3-§2.4), then the sequential state scan and output
+ * ([CGDR] §3.2-§3.3).  Other shapes launch one CUDA-core kernel; for DN_BF16 its
  * state products (K S, Q S, the state update) are TF32 tensor-core tiles with
  * fp32 accumulation, within the bf16 bound.
  *
  * Why a workspace.  The per-chunk work that needs no state (the inverse T,
  * the scores P) runs for all chunks at once in the first kernel; only the
- * scan is sequential.  The two kernels hand over three 64 x 64 bf16 matrices
- * per chunk and value head through the workspace (mostly through L2 between
- * the two launches).  A single kernel that formed T beside the scan put that
+ * scan is sequential.  The two kernels hand over three bf16 matrices per
+ * chunk and value head through the workspace (mostly through L2 between the
+ * two launches).  A single kernel that formed T beside the scan put that
  * work back on the scan's serial path and measured slower (158 against about
  * 120 us per forward at B = 4, H = 16, T = 2048, d = 128).  So the call takes
  * the caller's workspace instead of allocating one (dn_chunk_fwd_noalloc
@@ -147,12 +147,14 @@ dn_status dn_chunk_fwd(const void *q, const void *k, const void *v,
 /*
  * dn_chunk_fwd_workspace_bytes -- bytes of workspace dn_chunk_fwd needs for
  * these sizes (same meaning as there).  For the tensor-core path it is
- * (floor(B*T / C) + n_seqs) * Nv * 25088 (C the chunk length): one slot per
- * chunk and value head
- * holding three bf16 64 x 64 matrices of the chunk, T diag(beta e^G) and
- * T diag(beta) of its WY representation ([WY] §2.4) and its causal score
- * matrix tril(scale QK^T . D) ([CGDR] §3.2), then the chunk's 64 key and 64
- * query inverse norms (fp32; written only with DN_QK_L2NORM).  The size does
+ * (floor(B*T / C) + n_seqs) * Nv * S (C the chunk length): one slot of S
+ * bytes per chunk and value head holding bf16 matrices of the chunk --
+ * T diag(beta e^G) (64 x 64; for dk = 256 instead -W = -T diag(beta e^G) K,
+ * 64 x 256) and T diag(beta) (64 x 64) of its WY representation ([WY] §2.4)
+ * and its causal score matrix tril(scale QK^T . D) (64 x 64, [CGDR] §3.2) --
+ * then the chunk's 64 key and 64 query inverse norms (fp32; written only
+ * with DN_QK_L2NORM).  S = 25088 for dk = 128 and 49664 for dk = 256.  The
+ * size does
  * not depend on the flags.  Returns 0 when no workspace is
  * needed, and for sizes dn_chunk_fwd would reject.  Host-only; no CUDA call.
  */

@@ -99,11 +99,15 @@ def test_invalid_arguments_rejected_on_host(clib, over, code):
 
 
 def test_workspace_size(clib):
-    """One 24.5 KB slot per (floor(tokens/C) + N) x Nv on the tensor-core path (C the chunk
-    length), none elsewhere."""
+    """One slot per (floor(tokens/C) + N) x Nv on the tensor-core path (C the chunk
+    length; 25088 bytes for dk = 128, 49664 for dk = 256, which holds -W), none
+    elsewhere."""
     ws = clib.dn_chunk_fwd_workspace_bytes
     assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16, 64) == (4 * 2048 // 64 + 4) * 16 * 25088
     assert ws(3, 1, 300, 2, 8, 128, 256, dn.DN_BF16, 64) == (300 // 64 + 3) * 8 * 25088
+    assert ws(8, 8, 8192, 8, 8, 256, 256, dn.DN_BF16, 64) == (8 * 8192 // 64 + 8) * 8 * 49664
+    assert ws(2, 2, 100, 2, 4, 256, 128, dn.DN_BF16, 32) == (2 * 100 // 32 + 2) * 4 * 49664
+    assert ws(2, 2, 64, 2, 4, 256, 64, dn.DN_BF16, 64) == 0      # dv not a multiple of 128
     assert ws(2, 2, 64, 2, 4, 64, 64, dn.DN_BF16, 64) == 0       # CUDA-core path
     assert ws(2, 2, 64, 2, 2, 128, 128, dn.DN_F32, 64) == 0      # fp32: CUDA-core path
     assert ws(2, 2, 0, 2, 2, 128, 128, dn.DN_BF16, 64) == 0      # no tokens
