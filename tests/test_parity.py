@@ -122,6 +122,29 @@ def test_wide_heads_tensor_core_path(lib, case):
     check(inp, o, ht, label="wide %s" % case)
 
 
+@pytest.mark.parametrize("case", ["chunk16", "chunk32", "ungated", "qk_l2norm", "varlen_gqa"])
+def test_wide_heads_full_size(lib, case):
+    """The wide-head shapes (B = 8, H = 8, T = 8192, d = 256) in the modes of
+    the smaller tests: the shorter chunks, no gates, in-kernel q / k
+    normalisation, and a varlen GQA batch with long and short sequences; on
+    sampled (sequence, head) units."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    chunk = {"chunk16": 16, "chunk32": 32}.get(case, 64)
+    if case == "varlen_gqa":
+        inp = workloads.make_inputs(1, 0, 4, 8, 256, 256, gate_mu=3.0, h0=True, seed=530,
+                                    lengths=[8192, 1, 3000, 64, 12289, 0, 700, 4097])
+        units = [4 * 8 + 0, 4 * 8 + 7, 1 * 8 + 3, 2 * 8 + 5]
+    else:
+        inp = workloads.make_inputs(8, 8192, 8, 8, 256, 256, gate_mu=None if case == "ungated" else 3.0,
+                                    h0=True, seed=531, raw_qk=case == "qk_l2norm")
+        units = [0, 37, 63]
+    o, ht = run_gpu(inp, chunk=chunk)
+    assert dn.dn_last_kernel() == "wy_fwd+tc_wide_fwd", dn.dn_last_kernel()
+    res = check(inp, o, ht, units=units, label="wide full %s" % case)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
+    print("wide full", case, res)
+
+
 def test_wide_heads_state_carry(lib):
     """dk = 256: a second call from the first call's ht equals one call on the
     whole sequence."""
