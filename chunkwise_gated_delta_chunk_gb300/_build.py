@@ -77,13 +77,13 @@ def build(force: bool = False, extra: list[str] | None = None) -> str:
 
 
 # Translation units that change in the failure-path test build.
-STALL_SOURCES = ("dn_api.cu", "dn_tc.cu", "dn_wy.cu")
+STALL_SOURCES = ("dn_api.cu", "dn_tc.cu", "dn_tc_wide.cu", "dn_wy.cu")
 STALL_LIB = os.path.join(BUILD, "stall", "libdnchunk_stall.so")
 
 
 def build_stall_variant() -> str:
     """Build the failure-path test variant of the library (never the product
-    library): dn_api.cu, dn_tc.cu and dn_wy.cu compiled with -DDN_TEST_STALL
+    library): dn_api.cu, dn_tc.cu, dn_tc_wide.cu and dn_wy.cu compiled with -DDN_TEST_STALL
     (2 ms wait limit, the dn_test_stall_next hook), linked with the other
     objects of the regular build, into ``_build/stall/libdnchunk_stall.so``."""
     build()

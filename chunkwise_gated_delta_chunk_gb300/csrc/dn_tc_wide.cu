@@ -259,7 +259,12 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         __syncwarp();
         bool ok = true;
         if (lane == 0) {
-            mbar_arrive(bar(x, B_SCF + (c & 1)));
+#ifdef DN_TEST_STALL
+            // failure-path test: the first chunk's scalars are never
+            // announced, so every wait on them runs out (the copies land)
+            if (!(p.test_stall == kStallScan && c == 0))
+#endif
+                mbar_arrive(bar(x, B_SCF + (c & 1)));
             ok = load_chunk(x, u, c, t0, slot_of(p, u, c), mK, mV, last);
         }
         if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return;

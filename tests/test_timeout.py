@@ -9,7 +9,9 @@ These tests use the failure-path build of the library (compiled with
 -DDN_TEST_STALL into _build/stall/, never the library's own build): its wait
 limit is 2 ms and it has a hook, dn_test_stall_next, that makes one wait of
 the next call run out
-  1: the scan kernel's first stage never receives its second arrival;
+  1: the scan kernel's first chunk never becomes ready (dk = 128: its first
+     stage never receives its second arrival; dk = 256: its gate scalars are
+     never announced);
   2: the WY kernel's first item on one CTA expects 16 bytes more than its
      copies bring.
 In both cases the bytes that were requested still land before the kernel
@@ -47,9 +49,9 @@ def stall_build():
         dn._lib = saved
 
 
-@pytest.mark.parametrize("mode,where", [(1, "scan"), (2, "wy")])
-def test_wait_runs_out_then_next_call_is_clean(mode, where):
-    inp = workloads.make_inputs(2, 200, 2, 2, 128, 128, gate_mu=3.0, h0=True, seed=600 + mode)
+@pytest.mark.parametrize("mode,where,dk", [(1, "scan", 128), (2, "wy", 128), (1, "scan", 256), (2, "wy", 256)])
+def test_wait_runs_out_then_next_call_is_clean(mode, where, dk):
+    inp = workloads.make_inputs(2, 200, 2, 2, dk, 128, gate_mu=3.0, h0=True, seed=600 + mode + dk)
     d = workloads.to_device(inp, "cuda")
     with stall_build() as (dn, lib):
         def call():
@@ -59,7 +61,7 @@ def test_wait_runs_out_then_next_call_is_clean(mode, where):
 
         o_ref, ht_ref, st = call()
         assert st == dn.DN_OK, dn.dn_status_str(st)
-        assert dn.dn_last_kernel() == "wy_fwd+tc_fwd"
+        assert dn.dn_last_kernel() == ("wy_fwd+tc_fwd" if dk == 128 else "wy_fwd+tc_wide_fwd")
         lib.dn_test_stall_next(mode)
         _, _, st = call()
         assert st == dn.DN_ERR_TIMEOUT, (where, dn.dn_status_str(st))
