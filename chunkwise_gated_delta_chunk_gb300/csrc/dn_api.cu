@@ -200,9 +200,17 @@ size_t bwd_states_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv) {
     return (size_t)(tokens / dn::kChunk + n_seqs) * (size_t)Nv * (size_t)dk * (size_t)dv * 4u;
 }
 
+// Where the backward's forward pass runs on the tensor cores, its WY slots
+// follow the states, then the fp32 matrices that WY kernel also keeps for the
+// reverse walk (Params::wyx): three 64 x 64 per chunk and value head.
+size_t bwd_wyx_bytes(long long tokens, int n_seqs, int Nv) {
+    return (size_t)(tokens / dn::kChunk + n_seqs) * (size_t)Nv * 3u * 64u * 64u * 4u;
+}
+
 size_t bwd_workspace_bytes(long long tokens, int n_seqs, int Nv, int dk, int dv, dn_dtype dtype) {
     size_t b = bwd_states_bytes(tokens, n_seqs, Nv, dk, dv);
-    if (use_tc(tokens, dk, dv, dtype, dn::kChunk)) b += dn::tc_workspace_bytes(tokens, n_seqs, Nv, dk, dn::kChunk);
+    if (use_tc(tokens, dk, dv, dtype, dn::kChunk))
+        b += dn::tc_workspace_bytes(tokens, n_seqs, Nv, dk, dn::kChunk) + bwd_wyx_bytes(tokens, n_seqs, Nv);
     return b;
 }
 
@@ -252,8 +260,11 @@ DN_EXPORT dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
     p.chunk = dn::kChunk;
     p.flags = flags;
     p.hs = static_cast<float *>(workspace);
-    if (use_tc(tokens, dk, dv, dtype, dn::kChunk))
+    if (use_tc(tokens, dk, dv, dtype, dn::kChunk)) {
         p.ws = static_cast<uint8_t *>(workspace) + bwd_states_bytes(tokens, n_seqs, Nv, dk, dv);
+        p.wyx = reinterpret_cast<float *>(static_cast<uint8_t *>(p.ws) +
+                                          dn::tc_workspace_bytes(tokens, n_seqs, Nv, dk, dn::kChunk));
+    }
     p.dout = d_o; p.dht = d_ht;
     p.dq = d_q; p.dkk = d_k; p.dvv = d_v; p.dbeta = d_beta; p.dg = d_g; p.dh0 = d_h0;
     if (status_ptr(&p.status) != cudaSuccess) return DN_ERR_CUDA;

@@ -164,6 +164,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // every committed group but the latest one has landed
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
 // The tensor-core phases (their own strides).
 namespace tcp {
@@ -634,6 +635,15 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         // one chunk ahead (K, Q) and during the previous chunk's dS update
         // (the state); the next chunk's K and Q go out now.
         if constexpr (MMA) {
+            // the chunk's -(K K^T . D), P and T, which the forward pass's WY
+            // kernel kept (Params::wyx): in flight until they are needed
+            const float *wx = p.wyx + ((size_t)h * p.nslots + (size_t)(t0 / C + n)) * 3 * 4096;
+            for (int idx = tid; idx < 3 * 64 * 16; idx += NT) {
+                const int mtx = idx >> 10, rr = (idx >> 4) & 63, c4 = idx & 15;
+                float *dst = (mtx == 0 ? sM0 : (mtx == 1 ? sM2 : sM1)) + rr * LDC + 4 * c4;
+                cp_async16(dst, wx + mtx * 4096 + rr * 64 + 4 * c4);
+            }
+            cp_async_commit();
             sK = (ci & 1) ? sK1 : sK0;
             sQ = (ci & 1) ? sQ1 : sQ0;
             bc.K = reinterpret_cast<const __nv_bfloat16 *>(sK);
@@ -662,6 +672,8 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         bc.L = L;
         if (MMA && ci > 0)
+            cp_async_wait_prev2();  // not the matrices above, nor the next chunk's K, Q
+        else if (MMA)
             cp_async_wait_prev();
         else
             cp_async_wait_all();
@@ -713,23 +725,31 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         }
         __syncthreads();
 
-        // ---- -(K K^T . D) (strictly lower) and P (lower) ------------------
-        // (dk = 128 at compile time on the tensor-core path: the k loop unrolls)
-        simt::kq_products<NT>(sK, sQ, ldkq, MMA ? 128 : dk, L, tid, [&](int i, int j, float kk, float qk) {
-            float a = 0.0f, pv = 0.0f;
-            if (i < L && j <= i) {
-                const float D = expf(sG[i] - sG[j]) * sRK[j];
-                if (j < i) a = -kk * D * sRK[i];
-                pv = p.scale * qk * D * sRQ[i];
-            }
-            sM0[i * LDC + j] = a;
-            sM2[i * LDC + j] = pv;
-        });
-        __syncthreads();
+        if constexpr (MMA) {
+            // -(K K^T . D), P and T have landed
+            if (ci > 0)
+                cp_async_wait_prev();
+            else
+                cp_async_wait_all();
+            __syncthreads();
+        } else {
+            // ---- -(K K^T . D) (strictly lower) and P (lower) --------------
+            simt::kq_products<NT>(sK, sQ, ldkq, dk, L, tid, [&](int i, int j, float kk, float qk) {
+                float a = 0.0f, pv = 0.0f;
+                if (i < L && j <= i) {
+                    const float D = expf(sG[i] - sG[j]) * sRK[j];
+                    if (j < i) a = -kk * D * sRK[i];
+                    pv = p.scale * qk * D * sRQ[i];
+                }
+                sM0[i * LDC + j] = a;
+                sM2[i * LDC + j] = pv;
+            });
+            __syncthreads();
 
-        // ---- T = (I - A)^-1, A_im = beta_i sM0_im (blocked; sVn, written
-        // later, is its scratch) ---------------------------------------------
-        simt::solve_T_blocked<NT>(sM0, LDC, sBeta, sM1, LDC, sVn, L, tid);
+            // ---- T = (I - A)^-1, A_im = beta_i sM0_im (blocked; sVn,
+            // written later, is its scratch) ---------------------------------
+            simt::solve_T_blocked<NT>(sM0, LDC, sBeta, sM1, LDC, sVn, L, tid);
+        }
         // ---- K S, Q S (.dO), K dS'; U = V - e^G K S ------------------------
         // thread: rows i0, i0 + 1; columns cg + 8 x (x < 4)
         if constexpr (MMA) {

@@ -55,6 +55,10 @@ struct Params {
     float *dq, *dkk, *dvv;     // [tokens, Nk, dk], [tokens, Nk, dk], [tokens, Nv, dv]
     float *dbeta, *dg;         // [tokens, Nv]; dg may be null
     float *dh0;                // [N, Nv, dk, dv] or null
+    // [Nv][nslots][3][64][64] fp32 per chunk: -(K K^T . D) (strictly lower),
+    // P (lower) and T = (I - A)^-1, written by the WY kernel in the backward's
+    // forward pass (dk = 128 tensor-core path) for the reverse walk; else null
+    float *wyx;
 };
 
 // CUDA-core kernel: any supported shape.  `bf16` selects bf16 q/k/v/o, else

@@ -46,7 +46,9 @@ namespace {
 template <int DKW>
 constexpr int wy_ctas_per_sm() { return DKW == 128 ? 6 : 3; }
 
-template <int DKW, bool QKN>
+// BWD (dk = 128, the backward's forward pass): also keep the fp32 rows of
+// -(K K^T . D), P and T in Params::wyx for the backward's reverse walk.
+template <int DKW, bool QKN, bool BWD>
 __global__ void __launch_bounds__(wy::NT, wy_ctas_per_sm<DKW>())
 wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ Params p) {
@@ -75,7 +77,7 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     for (unsigned it = blockIdx.x; it < items; it += gridDim.x) {
         const unsigned nx = it + gridDim.x;
         const wy::ItemLoc loc = wy::locate(p, it / nv);
-        if (!wy::item<DKW, QKN>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
+        if (!wy::item<DKW, QKN, BWD>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
                                 nx < items ? (long long)(nx / nv) : -1, (int)(nx % nv)))
             break;
     }
@@ -92,7 +94,9 @@ cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorM
                          unsigned items) {
     const uint32_t smem = wy::Lay<DKW>::GROUP_BYTES + 1024;
     const bool qkn = (p.flags & kQkL2Norm) != 0;
-    const void *kern = qkn ? (const void *)wy_fwd<DKW, true> : (const void *)wy_fwd<DKW, false>;
+    const bool bwd = DKW == 128 && p.wyx != nullptr;
+    const void *kern = qkn ? (bwd ? (const void *)wy_fwd<DKW, true, DKW == 128> : (const void *)wy_fwd<DKW, true, false>)
+                           : (bwd ? (const void *)wy_fwd<DKW, false, DKW == 128> : (const void *)wy_fwd<DKW, false, false>);
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
@@ -100,10 +104,11 @@ cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorM
     // one resident wave of CTAs (per device, head size and instantiation,
     // looked up once); on 2048 items (B = 4, H = 16, T = 2048, dk = 128) it
     // measured 1.5 us faster per forward than one CTA per item
-    static std::atomic<int> wave_cache[64][2];  // 0: not looked up yet (calls may come from several threads)
+    static std::atomic<int> wave_cache[64][4];  // 0: not looked up yet (calls may come from several threads)
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    int wave = (dev >= 0 && dev < 64) ? wave_cache[dev][qkn].load(std::memory_order_relaxed) : 0;
+    const int ci = 2 * (int)qkn + (int)bwd;
+    int wave = (dev >= 0 && dev < 64) ? wave_cache[dev][ci].load(std::memory_order_relaxed) : 0;
     if (wave <= 0) {
         // CTAs per SM: the launch bound, or fewer if shared memory runs out
         // (the occupancy query reports fewer under the default carveout)
@@ -117,13 +122,17 @@ cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorM
         int per_sm = smem_sm / (int)(smem + (uint32_t)reserved);
         if (per_sm > wy_ctas_per_sm<DKW>()) per_sm = wy_ctas_per_sm<DKW>();
         wave = sms * (per_sm > 0 ? per_sm : 1);
-        if (dev >= 0 && dev < 64) wave_cache[dev][qkn].store(wave, std::memory_order_relaxed);
+        if (dev >= 0 && dev < 64) wave_cache[dev][ci].store(wave, std::memory_order_relaxed);
     }
     const unsigned grid = items < (unsigned)wave ? items : (unsigned)wave;
-    if (qkn)
-        wy_fwd<DKW, true><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+    if (qkn && bwd)
+        wy_fwd<DKW, true, DKW == 128><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+    else if (qkn)
+        wy_fwd<DKW, true, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+    else if (bwd)
+        wy_fwd<DKW, false, DKW == 128><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
     else
-        wy_fwd<DKW, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+        wy_fwd<DKW, false, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
     return cudaGetLastError();
 }
 

@@ -432,7 +432,7 @@ __device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
 // compute W = T' K into tensor memory (two 128-column halves of d), and
 // threads 0-63 store row i of -W to the slot, so that the scan kernel needs
 // neither T' nor tensor memory for W.
-template <int DKW, bool QKN>
+template <int DKW, bool QKN, bool BWD>
 __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, const Params &p, long long slot,
                      int h, const ItemLoc &loc, ChunkGates &gates, long long next_slot, int next_h) {
     using Y = Lay<DKW>;
@@ -544,8 +544,13 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
         // A_ij = -beta_i e^{G_i - G_j} (K K^T)_ij for j < i;
         // P_ij = scale e^{G_i - G_j} (Q K^T)_ij for j <= i
         // with kQkL2Norm: times 1/||k_i|| or 1/||q_i||, and 1/||k_j|| per column
-        const float ri = (rowA ? -sc[SC_BETA + i] : p.scale) * (qkn ? nrm[row] : 1.f);
+        // (BWD: the rows of A are formed without beta_i, as -(K K^T . D),
+        // which the backward keeps; A_ij = beta_i times that)
+        const float ri = (rowA ? (BWD ? -1.f : -sc[SC_BETA + i]) : p.scale) * (qkn ? nrm[row] : 1.f);
         const float ai = ri * sc[SC_AF + i];
+        const bool live = i < loc.L;  // BWD: rows past the chunk are stored as zero
+        float *wx = BWD ? p.wyx + ((size_t)h * p.nslots + (size_t)slot) * 3 * 4096 + (rowA ? 0 : 4096) + i * 64
+                        : nullptr;
         const int jmax = rowA ? i - 1 : i;
         const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
         uint32_t r[32];
@@ -596,6 +601,19 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 const int j = 32 * hf + jj;
                 val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
             }
+            if (BWD) {
+                // -(K K^T . D) or P row i, fp32, for the backward
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    *reinterpret_cast<float4 *>(wx + 32 * hf + 4 * q4) =
+                        live ? make_float4(val[4 * q4], val[4 * q4 + 1], val[4 * q4 + 2], val[4 * q4 + 3])
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (rowA) {
+                    const float bi = sc[SC_BETA + i];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) val[jj] *= bi;
+                }
+            }
             if (rowA) {
                 float *ar = arow(i);
 #pragma unroll
@@ -619,6 +637,14 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
         const bool tp = g.tid < 64;
         const float *trow = arow(i);
         const float *cs = sc + (tp ? SC_BEG : SC_BETA);
+        if (BWD && tp) {
+            // T row i, fp32, for the backward (rows past the chunk: the
+            // identity's, as A is zero there)
+            float *wt = p.wyx + ((size_t)h * p.nslots + (size_t)slot) * 3 * 4096 + 8192 + i * 64;
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4)
+                *reinterpret_cast<float4 *>(wt + 4 * q4) = *reinterpret_cast<const float4 *>(trow + 4 * q4);
+        }
         uint32_t pk[2][16];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {

@@ -270,10 +270,13 @@ dn_status dn_chunk_bwd(const void *q, const void *k, const void *v,
 /*
  * dn_chunk_bwd_workspace_bytes -- bytes of workspace dn_chunk_bwd needs:
  * (floor(B*T / 64) + n_seqs) * Nv * dk * dv * 4 (one fp32 state per chunk and
- * value head), plus dn_chunk_fwd_workspace_bytes() of the same sizes at
- * chunk 64 where the backward's forward pass runs on the tensor cores (bf16,
- * dk = 128, dv a multiple of 128).  0 for sizes dn_chunk_bwd would reject.
- * Host-only.
+ * value head), plus, where the backward's forward pass runs on the tensor
+ * cores (bf16, dk = 128, dv a multiple of 128), dn_chunk_fwd_workspace_bytes()
+ * of the same sizes at chunk 64 and (floor(B*T / 64) + n_seqs) * Nv * 49152:
+ * three fp32 64 x 64 matrices per chunk and value head (-(K K^T . D), the
+ * scores P and the WY inverse T), which that forward pass keeps so that the
+ * reverse walk need not form them again for every value tile.  0 for sizes
+ * dn_chunk_bwd would reject.  Host-only.
  */
 size_t dn_chunk_bwd_workspace_bytes(int n_seqs, int B, int T, int Nk, int Nv, int dk, int dv,
                                     dn_dtype dtype);

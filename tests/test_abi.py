@@ -200,7 +200,7 @@ def test_bwd_workspace_bytes(clib):
     WY slots where that forward runs on the tensor cores; 0 for rejected sizes."""
     ws = clib.dn_chunk_bwd_workspace_bytes
     slots = 4 * 2048 // 64 + 4
-    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16) == slots * 16 * (128 * 128 * 4 + 25088)
+    assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_BF16) == slots * 16 * (128 * 128 * 4 + 25088 + 3 * 64 * 64 * 4)
     assert ws(4, 4, 2048, 16, 16, 128, 128, dn.DN_F32) == slots * 16 * 128 * 128 * 4
     assert ws(4, 4, 2048, 16, 16, 64, 128, dn.DN_BF16) == slots * 16 * 64 * 128 * 4
     assert ws(3, 1, 300, 2, 8, 64, 32, dn.DN_F32) == (300 // 64 + 3) * 8 * 64 * 32 * 4
