@@ -188,23 +188,62 @@ __device__ __forceinline__ void load_ring(const Ctx &x, const Params &p, const U
 // chunks' T', T'' and P images (later ones are fetched by their readers as
 // soon as a ring buffer frees up).  armed is the last chunk whose stage was
 // armed.
+//
+// The kernel is launched as a programmatic dependent of the WY kernel, so
+// it can start while that kernel's last CTAs finish: the first stage's
+// copies (q, k, v: inputs) go out first, and the workspace slots are read
+// only after grid_dep_wait, here and in the two other threads that refill
+// the rings.
 // ---------------------------------------------------------------------------
 __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
                             const CUtensorMap *mQ, const CUtensorMap *mV, int &armed) {
     const int lane = threadIdx.x & 31;
     armed = -1;
-    if (lane == 0)
-        for (int c = 0; c < min(u.nc, 2); ++c)
-            for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c);
     float A = 1.f;  // running decay product A_c (chunk_decay), the same in every lane
     for (int c = 0; c < u.nc; ++c) {
         const int s = c % NS;
         const long long t0 = u.bos + (long long)c * p.chunk;
         const int L = (int)min((long long)p.chunk, u.eos - t0);
+        // the stage's copies: once every reader of its previous chunk is done
+        auto arm = [&]() -> bool {
+            if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return false;
+            const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
+            if (lane == 0) {
+                const uint32_t fb = bar(x, B_FULL + s);
+                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                const int tt = (int)t0;
+                tma_load_3d(st + 0, mK, fb, 0, u.hk, tt);
+                tma_load_3d(st + 8192, mQ, fb, 0, u.hk, tt);
+                tma_load_3d(st + 16384, mK, fb, 64, u.hk, tt);
+                tma_load_3d(st + 24576, mQ, fb, 64, u.hk, tt);
+                tma_load_3d(st + 32768, mV, fb, u.v0, u.h, tt);
+                tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
+            }
+            armed = c;
+            return true;
+        };
+        // the WY kernel's slots of the first two chunks, once that kernel
+        // has completed (issued even when arming failed: their readers drain
+        // them)
+        auto rings = [&]() {
+            grid_dep_wait();
+            if (lane == 0)
+                for (int c2 = 0; c2 < min(u.nc, 2); ++c2)
+                    for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c2);
+        };
+        const bool qkn = (p.flags & kQkL2Norm) != 0;
+        // the first NS stages are free from the start: their copies go out
+        // before the gates are loaded
+        if (c < NS) {
+            const bool ok = arm();
+            // with normalisation chunk 0's scalars need its slot (the norms)
+            if (c == 0 && (qkn || !ok)) rings();
+            if (!ok) return;
+        }
         // the gates (and the WY kernel's inverse q / k norms) come from
         // global memory while the stage is still in use
         ChunkScalars cs = chunk_scalars_load(p, u.h, t0, L, lane);
-        if (p.flags & kQkL2Norm)
+        if (qkn)
             chunk_norms_load(cs, static_cast<const uint8_t *>(p.ws) +
                                      ((size_t)u.h * p.nslots + (size_t)wy_slot(t0, u.n, p.chunk)) * kSlotBytes +
                                      kSlotNormOff,
@@ -213,29 +252,22 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
         A = dec.an;
         cs.ka /= dec.an;  // rides on e^{G_L - G_i}: v~ / A_{c+1}
         cs.kb /= dec.an;
-        if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return;
-        const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
-        if (lane == 0) {
-            const uint32_t fb = bar(x, B_FULL + s);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            const int tt = (int)t0;
-            tma_load_3d(st + 0, mK, fb, 0, u.hk, tt);
-            tma_load_3d(st + 8192, mQ, fb, 0, u.hk, tt);
-            tma_load_3d(st + 16384, mK, fb, 64, u.hk, tt);
-            tma_load_3d(st + 24576, mQ, fb, 64, u.hk, tt);
-            tma_load_3d(st + 32768, mV, fb, u.v0, u.h, tt);
-            tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
-        }
-        armed = c;
+        if (c >= NS && !arm()) return;
         chunk_scalars_store(p, cs, scal(x, s), lane);
         if (lane == 0) chunk_decay_store(scal(x, s), dec);
         __syncwarp();
 #ifdef DN_TEST_STALL
         // failure-path test: the first stage's second arrival never comes, so
         // every wait on it runs out (its TMA bytes still land)
-        if (p.test_stall == kStallScan && c == 0) continue;
+        const bool skip = p.test_stall == kStallScan && c == 0;
+#else
+        const bool skip = false;
 #endif
-        if (lane == 0) mbar_arrive(bar(x, B_FULL + s));
+        if (lane == 0 && !skip) mbar_arrive(bar(x, B_FULL + s));
+        // without normalisation chunk 0's stage (tiles and scalars) is out
+        // before the wait for the WY kernel, so that the initial state and
+        // everything else that needs no slot can proceed
+        if (c == 0 && !qkn) rings();
     }
 }
 
@@ -290,6 +322,7 @@ __device__ __forceinline__ bool wait_tiles(const Ctx &x, int c, int ring) {
 __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     int loaded[3];  // last chunk whose T'' / P copy was issued (index 1, 2)
     loaded[1] = loaded[2] = min(u.nc, 2) - 1;
+    grid_dep_wait();  // this thread refills the T'' and P rings from the workspace
     int c = 0;
     if (wait_tiles(x, 0, 1)) {
         tc_fence_after();
@@ -359,8 +392,12 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 // chain.  `lb` is the thread's TMEM lane base; `hb` its element of h0 / ht at
 // key index 0 (row stride dv).
 // ---------------------------------------------------------------------------
-// acc_s = s0 h0^T and SB[0] = bf16(h0^T), blocks [b0, b1), with s0 =
+// The initial state, key blocks b0 and b0 + 1: f = the lane's h0 rows (zero
+// without h0), then SB[0] = bf16(h0^T) (and, with hsd, the fp32 state chunk 0
+// starts from), and once chunk 0's scalars are out acc_s = s0 h0^T, with s0 =
 // alpha_0 when chunk 0 renormalises and 1 otherwise (chunk_decay: A_0 = 1).
+// The loads go out before the wait for the scalars, so that their latency
+// overlaps the first stage's copies.
 // Column of this lane's value column v in the saved state of chunk c (row
 // d = 0, rows dv apart), or null when the states are not saved.
 __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, int v) {
@@ -369,31 +406,39 @@ __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, 
     return p.hs + ((size_t)u.h * p.nslots + (size_t)slot) * DK * p.dv + u.v0 + v;
 }
 
-__device__ __forceinline__ void state_init_blocks(const Params &p, uint32_t lb, size_t hb, float s0, int b0,
-                                                  int b1, float *hsd) {
-    uint32_t r[32], pk[16];
-    for (int blk = b0; blk < b1; ++blk) {
-        float f[32];
-        const float *hp = p.h0 ? p.h0 + hb + (size_t)(32 * blk) * p.dv : nullptr;
+__device__ __forceinline__ void state_init_load(const Params &p, size_t hb, int b0, float (&f)[2][32]) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            f[k] = hp ? *hp : 0.f;
-            if (hp) hp += p.dv;
-        }
+    for (int e = 0; e < 2; ++e) {
+        const float *hp = p.h0 ? p.h0 + hb + (size_t)(32 * (b0 + e)) * p.dv : nullptr;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) f[e][k] = hp ? hp[(size_t)k * p.dv] : 0.f;
+    }
+}
+
+__device__ __forceinline__ void state_init_sb(const Params &p, uint32_t lb, int b0, const float (&f)[2][32],
+                                              float *hsd) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int blk = b0 + e;
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[e][2 * k], f[e][2 * k + 1]);
+        tmem_st16(lb + TM_SB + 16 * blk, pk);
         if (hsd) {
             float *dp = hsd + (size_t)(32 * blk) * p.dv;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                *dp = f[k];
-                dp += p.dv;
-            }
+            for (int k = 0; k < 32; ++k) dp[(size_t)k * p.dv] = f[e][k];
         }
+    }
+}
+
+__device__ __forceinline__ void state_init_s(uint32_t lb, int b0, float s0, const float (&f)[2][32]) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(f[2 * k], f[2 * k + 1]);
-        tmem_st16(lb + TM_SB + 16 * blk, pk);
+    for (int e = 0; e < 2; ++e) {
+        uint32_t r[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(s0 * f[k]);
-        tmem_st32(lb + TM_S + 32 * blk, r);
+        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(s0 * f[e][k]);
+        tmem_st32(lb + TM_S + 32 * (b0 + e), r);
     }
 }
 
@@ -467,9 +512,12 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
     const size_t hb = ((size_t)u.n * p.Nv + u.h) * DK * p.dv + u.v0 + v;  // h0 / ht of this lane
     if (u.nc > 0) {
         // blocks 2-3 of the initial state; then acc_s is ready for DS(0)
+        float f[2][32];
+        state_init_load(p, hb, 2, f);
+        state_init_sb(p, lb, 2, f, hs_col(p, u, 0, v));
         if (!bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + 0), 0))) {
             const float *s0 = scal(x, 0);
-            state_init_blocks(p, lb, hb, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, 2, 4, hs_col(p, u, 0, v));
+            state_init_s(lb, 2, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, f);
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(bar(x, B_S_FULL));
@@ -628,6 +676,7 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
     const uint32_t lb = lane_base(tm, warp);
     int loaded = min(u.nc, 2) - 1;  // last chunk whose T' copy was issued
     bool lok = true;                // the leader's own waits
+    if (leader) grid_dep_wait();    // it refills the T' ring from the workspace
     if (leader && u.nc > 0) lok = issue_w_mma(x, tm, 0);
     for (int c = 0; c < u.nc; ++c) {
         if (!wwait(x, bar(x, B_WF), c & 1) || !__all_sync(0xffffffffu, lok)) break;
@@ -694,9 +743,14 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
     }
     // initial state: acc_s = s0 h0^T, SB = bf16(h0^T) (blocks 0-1 here,
     // 2-3 in the output warpgroup)
-    if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
-    const float *s0 = scal(x, 0);
-    state_init_blocks(p, lb, sbase, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, 0, 2, hs_col(p, u, 0, v));
+    {
+        float f[2][32];
+        state_init_load(p, sbase, 0, f);
+        state_init_sb(p, lb, 0, f, hs_col(p, u, 0, v));
+        if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
+        const float *s0 = scal(x, 0);
+        state_init_s(lb, 0, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, f);
+    }
     tmem_wait_st();
     tc_fence_before();
     warp_arrive(bar(x, B_S_FULL));
@@ -894,7 +948,19 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
         if (dev >= 0 && dev < 64) sms_cache[dev].store(sms, std::memory_order_relaxed);
     }
     const long long lead = (grid + kLeadCtas <= sms) ? kLeadCtas : 0;
-    tc_fwd<<<(unsigned)(grid + lead), NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);
+    // a programmatic dependent of the WY kernel: its launch and its CTAs'
+    // set-up, h0 loads and first tile copies overlap the end of that kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(grid + lead));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, tc_fwd, mK, mQ, mV, p)) != cudaSuccess) return err;
     *name = "wy_fwd+tc_fwd";
     return cudaGetLastError();
 }

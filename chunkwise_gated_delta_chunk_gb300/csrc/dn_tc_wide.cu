@@ -180,7 +180,10 @@ __device__ __forceinline__ const uint8_t *slot_of(const Params &p, const Unit &u
 // previous chunk: V and T'' (after U), K (after DS), P (after PV).  Warp 14
 // (one thread): the -W and Q tiles of each chunk into its two-deep buffer,
 // as soon as VNO of the chunk two back has released it.  last[] records the
-// last chunk loaded into each buffer kind, for the drain at exit.
+// last chunk loaded into each buffer kind, for the drain at exit.  The kernel
+// is launched as a programmatic dependent of the WY kernel, so it may start
+// while that kernel's last CTAs finish: copies of the inputs (V, K, Q) go out
+// at once, the slots' -W, T'', P and norms only after grid_dep_wait.
 // ---------------------------------------------------------------------------
 enum { LV, LTU, LK, LP, LQW, LCOUNT };
 
@@ -193,6 +196,9 @@ __device__ bool load_chunk(const Ctx &x, const Unit &u, int c, long long t0, con
     tma_load_3d(x.base + OFF_V, mV, bar(x, B_VF), u.v0, u.h, tt);
     tma_load_3d(x.base + OFF_V + 8192, mV, bar(x, B_VF), u.v0 + 64, u.h, tt);
     last[LV] = c;
+    // the WY kernel's slots only once that kernel has completed (the scan
+    // is its programmatic dependent)
+    if (c == 0) grid_dep_wait();
     if (!wait(x, bar(x, B_TUE), p1)) return false;
     mbar_arrive_expect_tx(bar(x, B_TUF), kImageBytes);
     bulk_load(x.base + OFF_TU, slot + slot_tu_off(DK), kImageBytes, bar(x, B_TUF));
@@ -237,6 +243,7 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
     // each chunk's gates (and norms) are loaded one iteration ahead, so that
     // their latency hides under the previous chunk's waits
     ChunkInputs next{};
+    if (p.flags & kQkL2Norm) grid_dep_wait();  // the norms come from the slots
     if (u.nc > 0) next = chunk_inputs_load(p, u, 0, lane);
     float A = 1.f;  // A_c, the same in every lane
     for (int c = 0; c < u.nc; ++c) {
@@ -280,13 +287,14 @@ __device__ void qw_loader_role(const Ctx x, const Params &p, const Unit u, const
         if (!wait(x, bar(x, B_QWE + b), ((c >> 1) & 1) ^ 1)) return;
         const uint32_t buf = x.base + OFF_QW + QW_BYTES * b;
         const uint8_t *slot = slot_of(p, u, c);
-        mbar_arrive_expect_tx(bar(x, B_WF + b), 32768);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) bulk_load(buf + 16384 * q, slot + 8192 * q, 8192, bar(x, B_WF + b));
         mbar_arrive_expect_tx(bar(x, B_QF + b), 32768);
         const int tt = (int)(u.bos + (long long)c * p.chunk);
 #pragma unroll
         for (int q = 0; q < 4; ++q) tma_load_3d(buf + 16384 * q + 8192, mQ, bar(x, B_QF + b), 64 * q, u.hk, tt);
+        if (c == 0) grid_dep_wait();  // -W comes from the WY kernel's slots
+        mbar_arrive_expect_tx(bar(x, B_WF + b), 32768);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) bulk_load(buf + 16384 * q, slot + 8192 * q, 8192, bar(x, B_WF + b));
         last[LQW] = c;
     }
 }
@@ -715,7 +723,19 @@ cudaError_t tc_wide_launch(const Params &p, cudaStream_t stream, const char **na
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(tc_wide_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
-    tc_wide_fwd<<<(unsigned)grid, NTHREADS, SMEM_ALLOC, stream>>>(mK, mQ, mV, p);
+    // a programmatic dependent of the WY kernel (its loaders wait for that
+    // kernel before they read the slots)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, tc_wide_fwd, mK, mQ, mV, p)) != cudaSuccess) return err;
     *name = "wy_fwd+tc_wide_fwd";
     return cudaGetLastError();
 }

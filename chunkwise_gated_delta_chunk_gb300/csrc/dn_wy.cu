@@ -87,6 +87,9 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         ptx::tc_fence_after();
         ptx::tmem_dealloc(g.tm, Y::TM_COLS);
     }
+    // the scan kernel may start: it reads this grid's slots only after
+    // waiting for its completion
+    ptx::grid_dep_launch();
 }
 
 template <int DKW>

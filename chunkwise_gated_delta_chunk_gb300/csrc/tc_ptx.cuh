@@ -19,6 +19,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Programmatic dependent launch.  grid_dep_launch: this CTA lets the next
+// kernel of the stream (launched with programmatic stream serialisation)
+// start once every CTA of this grid has said so or exited.  grid_dep_wait:
+// the calling thread waits until the grids this one depends on have completed
+// and their memory operations are visible to it (at once when there are none).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
