@@ -40,9 +40,11 @@ E2E_NOTE = ("every step copies its inputs from pinned host memory to the device,
             "and copies the results back to pinned host memory; steps run as a three-stage "
             "pipeline (copy-in stream, compute stream, copy-out stream; double-buffered), timed "
             "from the first copy in to the last copy out")
-L2_NOTE = ("flushed before every timed step, outside the step's events: a 256 MiB write, then a "
-           "256 MiB read of another buffer so the written lines are back in HBM and L2 holds "
-           "only clean unrelated lines")
+# The same string in both arms' config, so that the two lines name one
+# workload and one timing rule (the reference arm runs on host cores).
+L2_NOTE = ("GPU arm: L2 flushed before every timed step, outside the step's events: a 256 MiB "
+           "write, then a 256 MiB read of another buffer so the written lines are back in HBM "
+           "and L2 holds only clean unrelated lines; reference arm: host cores, no device cache")
 
 
 class L2Flush:
@@ -245,7 +247,7 @@ def reference_arm(args, inp, wl_name, rank, world):
     line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=steps, warmup=warm,
                 ms_per_step=1e3 * sec / steps, higher_is_better=True, scaling="weak",
                 vs_baseline=None, dtype="f64", data="synthetic", impl="reference",
-                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2="n/a (CPU)"), mode=args.mode),
+                config=dict(config_of(wl_name, inp, chunk=args.chunk, l2=L2_NOTE), mode=args.mode),
                 cpu_baseline=dict(value=value, unit=UNIT, cores=cores, kind="oracle",
                                   sample=sample),
                 e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
