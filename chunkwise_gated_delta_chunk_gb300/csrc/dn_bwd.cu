@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include "dn_internal.h"
+#include "dn_order.cuh"
 #include "dn_simt_common.cuh"
 #include "dn_tc.h"
 
@@ -520,13 +521,13 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
     const int nvt = (dv + BV - 1) / BV;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vt = blockIdx.x % nvt;
     const int h = (blockIdx.x / nvt) % Nv;
-    const int n = blockIdx.x / (nvt * Nv);
+    const int n = seq_of_rank(p, blockIdx.x / (nvt * Nv), lane);  // longest sequences first
     const int hk = h / (Nv / Nk);
     const int v0 = vt * BV;
     const int bvw = min(BV, dv - v0);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = lane;  // value column of the C x BV tiles in the row-per-warp loops
     const int SLD = st_ld(dk);
 

@@ -7,6 +7,7 @@
 #pragma once
 
 #include "dn_internal.h"
+#include "dn_order.cuh"
 
 namespace dn {
 

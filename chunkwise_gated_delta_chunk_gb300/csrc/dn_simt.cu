@@ -36,6 +36,7 @@
 #include <type_traits>
 
 #include "dn_internal.h"
+#include "dn_order.cuh"
 #include "dn_simt_common.cuh"
 
 namespace dn {
@@ -120,13 +121,13 @@ __global__ void __launch_bounds__(NT) simt_fwd(Params p) {
     const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
     const int nvt = (dv + BV - 1) / BV;
     const int unit = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vt = unit % nvt;
     const int h = (unit / nvt) % Nv;
-    const int n = unit / (nvt * Nv);
+    const int n = seq_of_rank(p, unit / (nvt * Nv), lane);  // longest sequences first
     const int hk = h / (Nv / Nk);
     const int v0 = vt * BV;
     const int bvw = min(BV, dv - v0);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const Layout lay = layout<Tin>(dk);
     Tin *sK = reinterpret_cast<Tin *>(smem + lay.k);

@@ -154,32 +154,6 @@ __device__ __forceinline__ int unit_rank(const Params &p) {
     return idx / ((p.dv / BVT) * p.Nv);
 }
 
-// With offsets (sequences of different lengths) the units run longest
-// sequence first: when they outnumber the SMs, the block scheduler hands the
-// later units to SMs as earlier ones finish, and starting the longest walks
-// first shortens the launch (a longest-processing-time order).  One warp, up
-// to kSortSeqs sequences (else the rank is the sequence); ties go by index.
-// Every warp of the CTA works it out for itself.
-constexpr int kSortSeqs = 64;
-__device__ __forceinline__ int seq_of_rank(const Params &p, int r, int lane) {
-    if (!p.cu || p.N <= 1 || p.N > kSortSeqs) return r;
-    auto len = [&](int m) -> int {
-        const long long l = m < p.N ? p.cu[m + 1] - p.cu[m] : -1;
-        return (int)max(min(l, (long long)INT_MAX), (long long)-1);
-    };
-    const int la = len(lane), lb = len(lane + 32);
-    int ra = 0, rb = 0;  // ranks of sequences lane and lane + 32
-    for (int j = 0; j < p.N; ++j) {
-        const int lj = __shfl_sync(0xffffffffu, j < 32 ? la : lb, j & 31);
-        ra += (lj > la) || (lj == la && j < lane);
-        rb += (lj > lb) || (lj == lb && j < lane + 32);
-    }
-    int n = -1;
-    if (lane < p.N && ra == r) n = lane;
-    if (lane + 32 < p.N && rb == r) n = lane + 32;
-    return __reduce_max_sync(0xffffffffu, n);
-}
-
 // The unit of this CTA, whose sequence is n (seq_of_rank of unit_rank).
 __device__ __forceinline__ Unit unit_of(const Params &p, int n) {
     Unit u;

@@ -151,7 +151,7 @@ __device__ __forceinline__ Unit unit_of(const Params &p) {
     const int idx = (int)blockIdx.x;
     const int vt = idx % nvt;
     u.h = (idx / nvt) % p.Nv;
-    u.n = idx / (nvt * p.Nv);
+    u.n = seq_of_rank(p, idx / (nvt * p.Nv), threadIdx.x & 31);  // longest sequences first
     u.hk = u.h / (p.Nv / p.Nk);
     u.v0 = vt * BVT;
     if (p.cu) {
