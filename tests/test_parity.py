@@ -389,3 +389,18 @@ def test_workload_full_size(lib, name):
     # every output of every unit is finite
     assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
     print(name, res)
+
+
+@pytest.mark.parametrize("nseq", [64, 65])
+def test_many_sequences_longest_first(lib, nseq):
+    """Packed batches at and just past the number of sequences the kernels order
+    longest first (64; beyond it units run in sequence order): random lengths,
+    empty ones included, on the tensor-core forward and the backward's walk."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    rng = np.random.default_rng(800 + nseq)
+    lengths = [int(x) for x in rng.integers(0, 260, size=nseq)]
+    lengths[3] = 0
+    inp = inputs(B=1, Nk=1, Nv=2, dk=128, dv=128, lengths=lengths, seed=810 + nseq)
+    o, ht = run_gpu(inp)
+    assert dn.dn_last_kernel() == "wy_fwd+tc_fwd", dn.dn_last_kernel()
+    check(inp, o, ht, label="%d sequences" % nseq)
