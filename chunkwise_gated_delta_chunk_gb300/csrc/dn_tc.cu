@@ -202,6 +202,7 @@ __device__ __forceinline__ void load_ring(const Ctx &x, const Params &p, const U
 // only after grid_dep_wait, here and in the two other threads that refill
 // the rings.
 // ---------------------------------------------------------------------------
+template <bool QKN>
 __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
                             const CUtensorMap *mQ, const CUtensorMap *mV, int &armed) {
     const int lane = threadIdx.x & 31;
@@ -238,7 +239,7 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
                 for (int c2 = 0; c2 < min(u.nc, 2); ++c2)
                     for (int r = 0; r < 3; ++r) load_ring(x, p, u, r, c2);
         };
-        const bool qkn = (p.flags & kQkL2Norm) != 0;
+        constexpr bool qkn = QKN;
         // the first NS stages are free from the start: their copies go out
         // before the gates are loaded
         if (c < NS) {
@@ -406,9 +407,11 @@ __device__ void mma_role(const Ctx x, const Params &p, const Unit u, uint32_t tm
 // The loads go out before the wait for the scalars, so that their latency
 // overlaps the first stage's copies.
 // Column of this lane's value column v in the saved state of chunk c (row
-// d = 0, rows dv apart), or null when the states are not saved.
+// d = 0, rows dv apart), or null when the states are not saved (HS: the
+// backward's state pass).
+template <bool HS>
 __device__ __forceinline__ float *hs_col(const Params &p, const Unit &u, int c, int v) {
-    if (!p.hs) return nullptr;
+    if (!HS) return nullptr;
     const long long slot = wy_slot(u.bos + (long long)c * p.chunk, u.n, p.chunk);
     return p.hs + ((size_t)u.h * p.nslots + (size_t)slot) * DK * p.dv + u.v0 + v;
 }
@@ -508,6 +511,7 @@ __device__ __noinline__ void state_renorm_blocks(uint32_t lb, float rs, int b0) 
 // Output warpgroup: o[i][v] = (S^T Q~^T + v_new^T P^T)[v][i] for value column
 // v = this thread's TMEM lane, chunk by chunk once O and PV are done.
 // ---------------------------------------------------------------------------
+template <bool HS>
 __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
     const int v = 32 * (warp & 3) + (threadIdx.x & 31);
@@ -521,7 +525,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         // blocks 2-3 of the initial state; then acc_s is ready for DS(0)
         float f[2][32];
         state_init_load(p, hb, 2, f);
-        state_init_sb(p, lb, 2, f, hs_col(p, u, 0, v));
+        state_init_sb(p, lb, 2, f, hs_col<HS>(p, u, 0, v));
         if (!bar_red_or(2, 128, !wwait(x, bar(x, B_FULL + 0), 0))) {
             const float *s0 = scal(x, 0);
             state_init_s(lb, 2, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, f);
@@ -542,7 +546,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         const float *sn = scal(x, last ? c % NS : s1);
         if (bar_red_or(2, 128, !wwait(x, bar(x, B_S_UPD), c & 1))) break;
         tc_fence_after();
-        state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col(p, u, c + 1, v),
+        state_convert_blocks(p, lb, hb, c, last, 2, last ? nullptr : hs_col<HS>(p, u, c + 1, v),
                              last ? sn[SC_AN] : sn[SC_A]);
         if (!last && sn[SC_RN] != 0.f) state_renorm_blocks(lb, sn[SC_RS], 2);
         if (!last) {
@@ -558,7 +562,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         // the chunk's output column v as packed bf16 pairs (tokens 2k, 2k + 1)
         // (with no o, as in the backward's state pass, only the hand-off)
         uint32_t ob[32];
-        if (p.o) {
+        if (!HS) {
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t ra[32];
@@ -571,7 +575,7 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         }
         tc_fence_before();
         warp_arrive(bar(x, B_O_EMPTY));
-        if (!p.o) continue;
+        if (HS) continue;
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
@@ -736,6 +740,7 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
 // ---------------------------------------------------------------------------
 // State warpgroup: v_new operands, fp32 state, ht.
 // ---------------------------------------------------------------------------
+template <bool HS>
 __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t tm) {
     const int warp = threadIdx.x >> 5;
     const int v = 32 * (warp & 3) + (threadIdx.x & 31);  // value column = TMEM lane
@@ -753,7 +758,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
     {
         float f[2][32];
         state_init_load(p, sbase, 0, f);
-        state_init_sb(p, lb, 0, f, hs_col(p, u, 0, v));
+        state_init_sb(p, lb, 0, f, hs_col<HS>(p, u, 0, v));
         if (!wwait(x, bar(x, B_FULL + 0), 0)) return;
         const float *s0 = scal(x, 0);
         state_init_s(lb, 0, s0[SC_RN] != 0.f ? s0[SC_RS] : 1.f, f);
@@ -815,7 +820,7 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
         const float *sn = scal(x, last ? s : s1);
         if (!wwait(x, bar(x, B_S_UPD), par)) return;
         tc_fence_after();
-        state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col(p, u, c + 1, v),
+        state_convert_blocks(p, lb, sbase, c, last, 0, last ? nullptr : hs_col<HS>(p, u, c + 1, v),
                              last ? sn[SC_AN] : sn[SC_A]);
         if (last) break;
         if (sn[SC_RN] != 0.f) state_renorm_blocks(lb, sn[SC_RS], 0);
@@ -828,6 +833,10 @@ __device__ void state_role(const Ctx x, const Params &p, const Unit u, uint32_t 
 // ---------------------------------------------------------------------------
 // Output warpgroup: o = scale e^{G_i} (S^T Q^T)[v][i] + (v_new^T P^T)[v][i].
 // ---------------------------------------------------------------------------
+// HS: the backward's state pass (p.hs set, no o); QKN: in-kernel q / k
+// normalisation.  Template parameters, so that the forward's instance
+// carries neither path's code.
+template <bool HS, bool QKN>
 __global__ void __maxnreg__(128)
 tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ CUtensorMap mV, const __grid_constant__ Params p) {
@@ -884,7 +893,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
 
     if (warp == 0) {
         int armed = -1;
-        loader_role(x, p, u, &mK, &mQ, &mV, armed);
+        loader_role<QKN>(x, p, u, &mK, &mQ, &mV, armed);
         // drain: the last NS armed stages must have landed before exit (the
         // ring copies are drained by the roles that issued them)
         if ((threadIdx.x & 31) == 0)
@@ -897,9 +906,9 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     } else if (warp < 6) {
         prep_role(x, p, u, tm);
     } else if (warp < 10) {
-        state_role(x, p, u, tm);
+        state_role<HS>(x, p, u, tm);
     } else if (warp < 14) {
-        output_role(x, p, u, tm);
+        output_role<HS>(x, p, u, tm);
     } else {
         if ((threadIdx.x & 31) == 0) out_mma_role(x, u, tm);
         __syncwarp();
@@ -935,7 +944,13 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     // T', T'' and P of every chunk first (all chunks in parallel), then the scan
     cudaError_t err = wy_launch(p, mK, mQ, stream);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    // the backward's state pass saves the states and writes no o; the
+    // forward writes o
+    const bool hs = p.hs != nullptr, qkn = (p.flags & kQkL2Norm) != 0;
+    if (hs != (p.o == nullptr)) return cudaErrorInvalidValue;
+    const void *kern = hs ? (qkn ? (const void *)tc_fwd<true, true> : (const void *)tc_fwd<true, false>)
+                          : (qkn ? (const void *)tc_fwd<false, true> : (const void *)tc_fwd<false, false>);
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
     // Placement lead.  One scan CTA fills an SM (its shared memory), and the
     // block scheduler hands a grid's first CTAs to the same SMs every launch:
@@ -967,7 +982,9 @@ cudaError_t tc_launch(const Params &p, cudaStream_t stream, const char **name) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, tc_fwd, mK, mQ, mV, p)) != cudaSuccess) return err;
+    void *args[] = {const_cast<CUtensorMap *>(&mK), const_cast<CUtensorMap *>(&mQ), const_cast<CUtensorMap *>(&mV),
+                    const_cast<Params *>(&p)};
+    if ((err = cudaLaunchKernelExC(&cfg, kern, args)) != cudaSuccess) return err;
     *name = "wy_fwd+tc_fwd";
     return cudaGetLastError();
 }

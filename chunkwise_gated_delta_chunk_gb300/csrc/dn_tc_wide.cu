@@ -222,12 +222,13 @@ struct ChunkInputs {
     float ka, kb, qa, qb;
 };
 
+template <bool QKN>
 __device__ __forceinline__ ChunkInputs chunk_inputs_load(const Params &p, const Unit &u, int c, int lane) {
     ChunkInputs r;
     const long long t0 = u.bos + (long long)c * p.chunk;
     r.gates = chunk_gates_load(p, u.h, t0, (int)min((long long)p.chunk, u.eos - t0), lane);
     r.ka = r.kb = r.qa = r.qb = 1.f;
-    if (p.flags & kQkL2Norm) {
+    if (QKN) {
         const float *f = reinterpret_cast<const float *>(slot_of(p, u, c) + slot_norm_off(DK));
         r.ka = f[lane];
         r.kb = f[lane + 32];
@@ -237,20 +238,21 @@ __device__ __forceinline__ ChunkInputs chunk_inputs_load(const Params &p, const 
     return r;
 }
 
+template <bool QKN>
 __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CUtensorMap *mK,
                             const CUtensorMap *mV, int (&last)[LCOUNT]) {
     const int lane = threadIdx.x & 31;
     // each chunk's gates (and norms) are loaded one iteration ahead, so that
     // their latency hides under the previous chunk's waits
     ChunkInputs next{};
-    if (p.flags & kQkL2Norm) grid_dep_wait();  // the norms come from the slots
-    if (u.nc > 0) next = chunk_inputs_load(p, u, 0, lane);
+    if (QKN) grid_dep_wait();  // the norms come from the slots
+    if (u.nc > 0) next = chunk_inputs_load<QKN>(p, u, 0, lane);
     float A = 1.f;  // A_c, the same in every lane
     for (int c = 0; c < u.nc; ++c) {
         const long long t0 = u.bos + (long long)c * p.chunk;
         const int L = (int)min((long long)p.chunk, u.eos - t0);
         const ChunkInputs in = next;
-        if (c + 1 < u.nc) next = chunk_inputs_load(p, u, c + 1, lane);
+        if (c + 1 < u.nc) next = chunk_inputs_load<QKN>(p, u, c + 1, lane);
         ChunkScalars cs = chunk_scalars_from(in.gates, L, lane);
         const ChunkDecay dec = chunk_decay(cs.GL, A);
         const float inv_an = 1.f / dec.an;
@@ -636,6 +638,9 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
 }
 
 // ---------------------------------------------------------------------------
+// QKN: in-kernel q / k normalisation (a template parameter, so that the plain
+// instance carries none of its code).
+template <bool QKN>
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_wide_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
             const __grid_constant__ CUtensorMap mV, const __grid_constant__ Params p) {
@@ -685,7 +690,7 @@ tc_wide_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUte
         int last[LCOUNT];
         for (int i = 0; i < LCOUNT; ++i) last[i] = -1;
         if (warp == 0)
-            loader_role(x, p, u, &mK, &mV, last);
+            loader_role<QKN>(x, p, u, &mK, &mV, last);
         else if ((threadIdx.x & 31) == 0)
             qw_loader_role(x, p, u, &mQ, last);
         if ((threadIdx.x & 31) == 0) loader_drain(x, last, warp == 14);
@@ -721,7 +726,8 @@ cudaError_t tc_wide_launch(const Params &p, cudaStream_t stream, const char **na
     // -W, T'' and P of every chunk first (all chunks in parallel), then the scan
     cudaError_t err = wy_launch(p, mK, mQ, stream);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tc_wide_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
+    const void *kern = (p.flags & kQkL2Norm) ? (const void *)tc_wide_fwd<true> : (const void *)tc_wide_fwd<false>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_ALLOC);
     if (err != cudaSuccess) return err;
     // a programmatic dependent of the WY kernel (its loaders wait for that
     // kernel before they read the slots)
@@ -735,7 +741,9 @@ cudaError_t tc_wide_launch(const Params &p, cudaStream_t stream, const char **na
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, tc_wide_fwd, mK, mQ, mV, p)) != cudaSuccess) return err;
+    void *args[] = {const_cast<CUtensorMap *>(&mK), const_cast<CUtensorMap *>(&mQ), const_cast<CUtensorMap *>(&mV),
+                    const_cast<Params *>(&p)};
+    if ((err = cudaLaunchKernelExC(&cfg, kern, args)) != cudaSuccess) return err;
     *name = "wy_fwd+tc_wide_fwd";
     return cudaGetLastError();
 }
