@@ -452,12 +452,32 @@ __device__ __forceinline__ void state_init_s(uint32_t lb, int b0, float s0, cons
     }
 }
 
+// The last chunk's ht = a acc_s, key blocks b0 and b0 + 1 (out of line: run once).
+__device__ __noinline__ void state_write_ht(const Params &p, uint32_t lb, size_t hb, int b0, float a) {
+    if (!p.ht) return;
+    for (int e = 0; e < 2; ++e) {
+        uint32_t r[32];
+        tmem_ld32(lb + TM_S + 32 * (b0 + e), r);
+        tmem_wait_ld_dep(r);
+        float *hp = p.ht + hb + (size_t)(32 * (b0 + e)) * p.dv;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            *hp = a * __uint_as_float(r[k]);
+            hp += p.dv;
+        }
+    }
+}
+
 // After DS(c), key blocks b0 and b0 + 1: SB[(c+1) & 1] = bf16(a acc_s) with
 // a = A_{c+1} (and, with hsd, the fp32 state chunk c + 1 starts from); or for
-// the last chunk ht = a acc_s with a = A_{nc} (chunk_decay).  Both TMEM
-// loads are in flight before the one wait.
+// the last chunk ht = a acc_s with a = A_{nc} (chunk_decay), out of line.
+// Both TMEM loads are in flight before the one wait.
 __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t lb, size_t hb, int c, bool last,
                                                      int b0, float *hsd, float a) {
+    if (last) {
+        state_write_ht(p, lb, hb, b0, a);
+        return;
+    }
     uint32_t r[2][32];
     tmem_ld32(lb + TM_S + 32 * b0, r[0]);
     tmem_ld32(lb + TM_S + 32 * (b0 + 1), r[1]);
@@ -479,13 +499,6 @@ __device__ __forceinline__ void state_convert_blocks(const Params &p, uint32_t l
                     *dp = a * __uint_as_float(r[e][k]);
                     dp += p.dv;
                 }
-            }
-        } else if (p.ht) {
-            float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                *hp = a * __uint_as_float(r[e][k]);
-                hp += p.dv;
             }
         }
     }
@@ -578,12 +591,15 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         if (HS) continue;
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
+        // (loops here and in the prep warpgroup are left rolled where they
+        // are off the chain: the scan measured faster with a smaller
+        // instruction footprint)
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const uint32_t w = ob[16 * hf + k];
+                const uint32_t w = hf ? ob[16 + k] : ob[k];
                 asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + (2 * k) * 256 + 2 * v),
                              "h"((uint16_t)(w & 0xffffu)));
                 asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + (2 * k + 1) * 256 + 2 * v),
@@ -660,7 +676,7 @@ __device__ __forceinline__ bool scale_q(const Ctx &x, int c) {
     if (!wwait(x, bar(x, B_FULL + s), (c / NS) & 1)) return false;
     const float *sc = scal(x, s);
     const int tid = threadIdx.x - 64;
-#pragma unroll
+#pragma unroll 2
     for (int it = 0; it < 8; ++it) {
         const int k = tid + 128 * it, half = k >> 9, r = (k >> 3) & 63, ch = k & 7;
         const float f = sc[SC_OSC + r];
@@ -705,7 +721,7 @@ __device__ void prep_role(const Ctx x, const Params &p, const Unit u, uint32_t t
         tmem_ld32(lb + TM_W + 32, r1);
         tmem_wait_ld_dep(r0);
         tmem_wait_ld_dep(r1);
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {

@@ -406,6 +406,22 @@ __device__ __forceinline__ void st_arrive(uint32_t b) {
     warp_arrive(b);
 }
 
+// ht = a acc_s for key blocks [b0, b0 + kPassNB) (out of line: run once).
+__device__ __noinline__ void state_pass_ht(const Params &p, uint32_t lb, size_t hb, int b0, float a) {
+    if (!p.ht) return;
+    for (int e = 0; e < kPassNB; ++e) {
+        uint32_t r[32];
+        tmem_ld32(lb + TM_S + 32 * (b0 + e), r);
+        tmem_wait_ld_dep(r);
+        float *hp = p.ht + hb + (size_t)(32 * (b0 + e)) * p.dv;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            *hp = a * __uint_as_float(r[k]);
+            hp += p.dv;
+        }
+    }
+}
+
 // After DS(c), key blocks [b0, b0 + kPassNB), two at a time: the bf16
 // image of S_{c+1} = A_{c+1} acc_s (then S_FULL, which VNO(c + 1) waits
 // for), and for a renormalising chunk c + 1 acc_s *= alpha_{c+1} A_{c+1}
@@ -415,6 +431,10 @@ __device__ __forceinline__ void st_arrive(uint32_t b) {
 __device__ __forceinline__ void state_pass(const Ctx &x, const Params &p, uint32_t lb, size_t hb, bool last,
                                            int b0, const float *sn) {
     const float a = last ? sn[SC_AN] : sn[SC_A];
+    if (last) {
+        state_pass_ht(p, lb, hb, b0, a);
+        return;
+    }
     const bool rn = !last && sn[SC_RN] != 0.f;
     const float rs = sn[SC_RS];
 #pragma unroll 1
@@ -427,17 +447,6 @@ __device__ __forceinline__ void state_pass(const Ctx &x, const Params &p, uint32
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int blk = b0 + e0 + e;
-            if (last) {
-                if (p.ht) {
-                    float *hp = p.ht + hb + (size_t)(32 * blk) * p.dv;
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        *hp = a * __uint_as_float(r[e][k]);
-                        hp += p.dv;
-                    }
-                }
-                continue;
-            }
             uint32_t pk[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k)
@@ -450,7 +459,6 @@ __device__ __forceinline__ void state_pass(const Ctx &x, const Params &p, uint32
             }
         }
     }
-    if (last) return;
     st_arrive(bar(x, B_S_FULL));
     warp_arrive(bar(x, B_VSM));
 }
@@ -611,14 +619,16 @@ __device__ void output_role(const Ctx x, const Params &p, const Unit u, uint32_t
         warp_arrive(bar(x, B_O_EMPTY));
         // transpose through shared memory, 32 tokens x 128 value columns
         // (256-byte rows) at a time, then 16-byte stores of whole rows i < L
+        // (a rolled loop: the scan measured faster with a smaller
+        // instruction footprint)
         const long long t0 = u.bos + (long long)c * p.chunk;
         const int L = (int)min((long long)p.chunk, u.eos - t0);
         uint8_t *obase = static_cast<uint8_t *>(p.o) + ((t0 * p.Nv + u.h) * (long long)p.dv + u.v0) * 2;
-#pragma unroll
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const uint32_t w = ob[16 * hf + k];
+                const uint32_t w = hf ? ob[16 + k] : ob[k];
                 asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + (2 * k) * 256 + 2 * v),
                              "h"((uint16_t)(w & 0xffffu)));
                 asm volatile("st.shared.b16 [%0], %1;" ::"r"(buf + (2 * k + 1) * 256 + 2 * v),
