@@ -73,7 +73,7 @@ struct Strides {
 __host__ __device__ inline int st_ld(int dk) { return dk + 4; }
 
 struct Layout {
-    size_t k, q, k2, q2, s, ds, m0, m1, m2, u, dO, ks, vn, dv, kds, sc, end;
+    size_t k, q, k2, q2, s, ds, m0, m1, m2, u, dO, ks, vn, dv, kds, stg, sc, end;
 };
 
 // Per-row scalars (C floats each) at Layout::sc.
@@ -101,6 +101,9 @@ __host__ __device__ inline Layout layout(int dk) {
     L.vn = off; off += align16(size_t(C) * LDV * 4);
     L.dv = off; off += align16(size_t(C) * LDV * 4);
     L.kds = off; off += align16(size_t(C) * LDV * 4);
+    // tensor-core path: the next chunk's V and dO tiles (raw) and its beta and
+    // g, copied in while this chunk is worked on
+    L.stg = off; off += MMA ? align16(2 * size_t(C) * BV * sizeof(Tin) + 2 * size_t(C) * 4) : 0;
     L.sc = off; off += size_t(R_COUNT) * C * 4 + 64;  // + G_L, block partial sums
     L.end = off;
     return L;
@@ -549,6 +552,11 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     float *sdV = reinterpret_cast<float *>(smem + lay.dv);   // dVn, then dR
     float *sKdS = reinterpret_cast<float *>(smem + lay.kds);
     float *sc = reinterpret_cast<float *>(smem + lay.sc);
+    // staged V, dO (C x BV, raw) and beta, g (C) of the chunk to come
+    Tin *const sVst = reinterpret_cast<Tin *>(smem + lay.stg);
+    Tin *const sdOst = sVst + C * BV;
+    float *const sBst = reinterpret_cast<float *>(sdOst + C * BV);
+    float *const sGst = sBst + C;
     float *sG = sc + R_G * C, *sEG = sc + R_EG * C, *sDec = sc + R_DEC * C, *sBeta = sc + R_BETA * C;
     float *sQSdO = sc + R_QSDO * C, *sDBU = sc + R_DBU * C, *sDGam = sc + R_DGAM * C;
     float *sE = sc + R_E * C, *sRowE = sc + R_ROWE * C, *sDBA = sc + R_DBA * C;
@@ -618,9 +626,28 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
                 sSt[cc * SLD + d] = 0.0f;
         }
     };
+    // tensor-core path (bf16, dv a multiple of 128, so every tile is BV
+    // columns wide): chunk cj's V and dO rows, beta and g into the staging
+    // buffer (rows past its length are not read)
+    auto stage_vdo = [&](long long cj) {
+        const long long tj = bos + cj * C;
+        const int Lj = (eos - tj) < C ? (int)(eos - tj) : C;
+        constexpr int PARTS = BV * sizeof(Tin) / 16;  // 16-byte pieces of a tile row
+        for (int idx = tid; idx < Lj * PARTS; idx += NT) {
+            const int i = idx / PARTS, part = idx - i * PARTS;
+            const long long off = ((tj + i) * Nv + h) * (long long)dv + v0 + part * (16 / sizeof(Tin));
+            cp_async16(sVst + i * BV + part * (16 / sizeof(Tin)), v + off);
+            cp_async16(sdOst + i * BV + part * (16 / sizeof(Tin)), dout + off);
+        }
+        if (tid < Lj) {
+            cp_async4(sBst + tid, p.beta + (tj + tid) * Nv + h);
+            if (p.g) cp_async4(sGst + tid, p.g + (tj + tid) * Nv + h);
+        }
+    };
     if (MMA && nch > 0) {
         load_kq(nch - 1, ((nch - 1) & 1) ? sK1 : sK0, ((nch - 1) & 1) ? sQ1 : sQ0);
         load_hs(nch - 1);
+        stage_vdo(nch - 1);
         cp_async_commit();
     }
     for (long long ci = nch - 1; ci >= 0; --ci) {
@@ -657,28 +684,47 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
             load_kq(ci, sK, sQ);
             load_hs(ci);
         }
-        for (int idx = tid; idx < C * BV; idx += NT) {
-            const int i = idx / BV, cc = idx - i * BV;
-            const bool in = i < L && cc < bvw;
-            const long long off = ((t0 + i) * Nv + h) * (long long)dv + v0 + cc;
-            sU[i * LDV + cc] = in ? to_f(v[off]) : 0.0f;
-            sdO[i * LDV + cc] = in ? to_f(dout[off]) : 0.0f;
-        }
-        if (tid < C) {
-            sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
-            sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
-            if (MMA) {  // row sums the tensor-core phases add into
-                sQSdO[tid] = sE[tid] = sRowE[tid] = sDBA[tid] = sDBU[tid] = sColE[tid] = 0.0f;
-            }
-        }
-        bc.L = L;
         if (MMA && ci > 0)
             cp_async_wait_prev2();  // not the matrices above, nor the next chunk's K, Q
         else if (MMA)
             cp_async_wait_prev();
         else
             cp_async_wait_all();
+        if constexpr (MMA) {
+            // V, dO, beta and g were staged while the chunk before was worked on
+            __syncthreads();
+            for (int idx = tid; idx < C * BV; idx += NT) {
+                const int i = idx / BV, cc = idx - i * BV;
+                const bool in = i < L;
+                sU[i * LDV + cc] = in ? to_f(sVst[i * BV + cc]) : 0.0f;
+                sdO[i * LDV + cc] = in ? to_f(sdOst[i * BV + cc]) : 0.0f;
+            }
+            if (tid < C) {
+                sBeta[tid] = tid < L ? sBst[tid] : 0.0f;
+                sG[tid] = (tid < L && p.g) ? sGst[tid] : 0.0f;
+                // row sums the tensor-core phases add into
+                sQSdO[tid] = sE[tid] = sRowE[tid] = sDBA[tid] = sDBU[tid] = sColE[tid] = 0.0f;
+            }
+        } else {
+            for (int idx = tid; idx < C * BV; idx += NT) {
+                const int i = idx / BV, cc = idx - i * BV;
+                const bool in = i < L && cc < bvw;
+                const long long off = ((t0 + i) * Nv + h) * (long long)dv + v0 + cc;
+                sU[i * LDV + cc] = in ? to_f(v[off]) : 0.0f;
+                sdO[i * LDV + cc] = in ? to_f(dout[off]) : 0.0f;
+            }
+            if (tid < C) {
+                sBeta[tid] = tid < L ? p.beta[(t0 + tid) * Nv + h] : 0.0f;
+                sG[tid] = (tid < L && p.g) ? p.g[(t0 + tid) * Nv + h] : 0.0f;
+            }
+        }
+        bc.L = L;
         __syncthreads();
+        // the staging buffer is free: the chunk before this one (next in the walk)
+        if (MMA && ci > 0) {
+            stage_vdo(ci - 1);
+            cp_async_commit();
+        }
 
         // ---- gate prefix sum (warp 0); <S, dS'> partials (every warp) ----
         if (warp == 0) {
@@ -727,9 +773,10 @@ __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
         __syncthreads();
 
         if constexpr (MMA) {
-            // -(K K^T . D), P and T have landed
+            // -(K K^T . D), P and T have landed (not the next chunk's K, Q
+            // and staged V, dO)
             if (ci > 0)
-                cp_async_wait_prev();
+                cp_async_wait_prev2();
             else
                 cp_async_wait_all();
             __syncthreads();
