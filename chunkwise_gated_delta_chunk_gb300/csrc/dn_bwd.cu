@@ -522,7 +522,9 @@ template <typename Tin, bool MMA>
 __global__ void __launch_bounds__(NT) simt_bwd(Params p) {
     constexpr int LDC = Strides<MMA>::LDC, LDV = Strides<MMA>::LDV;
     extern __shared__ __align__(16) unsigned char smem[];
-    const int dk = p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
+    // the tensor-core path runs dk = 128 only (bwd_launch): a constant there,
+    // so that the index arithmetic on it needs no division
+    const int dk = MMA ? 128 : p.dk, dv = p.dv, Nk = p.Nk, Nv = p.Nv;
     const int nvt = (dv + BV - 1) / BV;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vt = blockIdx.x % nvt;
