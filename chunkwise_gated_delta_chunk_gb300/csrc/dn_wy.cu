@@ -48,7 +48,9 @@ constexpr int wy_ctas_per_sm() { return DKW == 128 ? 6 : 3; }
 
 // BWD (dk = 128, the backward's forward pass): also keep the fp32 rows of
 // -(K K^T . D), P and T in Params::wyx for the backward's reverse walk.
-template <int DKW, bool QKN, bool BWD>
+// SUB: chunks of 16 or 32 tokens, several per 64-token tile (never with BWD,
+// whose forward pass runs 64-token chunks).
+template <int DKW, bool QKN, bool BWD, bool SUB>
 __global__ void __launch_bounds__(wy::NT, wy_ctas_per_sm<DKW>())
 wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mQ,
        const __grid_constant__ Params p) {
@@ -68,16 +70,16 @@ wy_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     ptx::tc_fence_after();
     g.tm = *reinterpret_cast<volatile uint32_t *>(gb + Y::OFF_BAR + 16);
 
-    // items (< 2^31, checked at launch) in steps of the grid; each item's
-    // gates are loaded during the item before
-    const unsigned items = (unsigned)(p.nslots * p.Nv), nv = (unsigned)p.Nv;
+    // items, one per (64-token tile, value head) (< 2^31, checked at launch),
+    // in steps of the grid; each item's gates are loaded during the item before
+    const unsigned items = (unsigned)(wy::tile_count(p) * p.Nv), nv = (unsigned)p.Nv;
     ChunkGates gates{0.f, 0.f, 0.f, 0.f};
     if (threadIdx.x < 32 && blockIdx.x < items)
         gates = wy::item_gates(p, blockIdx.x / nv, (int)(blockIdx.x % nv), threadIdx.x);
     for (unsigned it = blockIdx.x; it < items; it += gridDim.x) {
         const unsigned nx = it + gridDim.x;
         const wy::ItemLoc loc = wy::locate(p, it / nv);
-        if (!wy::item<DKW, QKN, BWD>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
+        if (!wy::item<DKW, QKN, BWD, SUB>(g, &mK, &mQ, p, it / nv, (int)(it % nv), loc, gates,
                                 nx < items ? (long long)(nx / nv) : -1, (int)(nx % nv)))
             break;
     }
@@ -98,8 +100,12 @@ cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorM
     const uint32_t smem = wy::Lay<DKW>::GROUP_BYTES + 1024;
     const bool qkn = (p.flags & kQkL2Norm) != 0;
     const bool bwd = DKW == 128 && p.wyx != nullptr;
-    const void *kern = qkn ? (bwd ? (const void *)wy_fwd<DKW, true, DKW == 128> : (const void *)wy_fwd<DKW, true, false>)
-                           : (bwd ? (const void *)wy_fwd<DKW, false, DKW == 128> : (const void *)wy_fwd<DKW, false, false>);
+    const bool sub = p.chunk < kChunk;
+    if (bwd && sub) return cudaErrorInvalidValue;
+    const void *kern = qkn ? (bwd ? (const void *)wy_fwd<DKW, true, DKW == 128, false>
+                                  : (sub ? (const void *)wy_fwd<DKW, true, false, true> : (const void *)wy_fwd<DKW, true, false, false>))
+                           : (bwd ? (const void *)wy_fwd<DKW, false, DKW == 128, false>
+                                  : (sub ? (const void *)wy_fwd<DKW, false, false, true> : (const void *)wy_fwd<DKW, false, false, false>));
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
@@ -128,21 +134,15 @@ cudaError_t wy_launch_dk(const Params &p, const CUtensorMap &mK, const CUtensorM
         if (dev >= 0 && dev < 64) wave_cache[dev][ci].store(wave, std::memory_order_relaxed);
     }
     const unsigned grid = items < (unsigned)wave ? items : (unsigned)wave;
-    if (qkn && bwd)
-        wy_fwd<DKW, true, DKW == 128><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
-    else if (qkn)
-        wy_fwd<DKW, true, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
-    else if (bwd)
-        wy_fwd<DKW, false, DKW == 128><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
-    else
-        wy_fwd<DKW, false, false><<<grid, wy::NT, smem, stream>>>(mK, mQ, p);
+    void *args[] = {const_cast<CUtensorMap *>(&mK), const_cast<CUtensorMap *>(&mQ), const_cast<Params *>(&p)};
+    if ((err = cudaLaunchKernel(kern, dim3(grid), dim3(wy::NT), args, smem, stream)) != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t wy_launch(const Params &p, const CUtensorMap &mK, const CUtensorMap &mQ, cudaStream_t stream) {
-    const long long items = p.nslots * p.Nv;
+    const long long items = wy::tile_count(p) * p.Nv;
     if (items <= 0) return cudaSuccess;
     if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (p.dk == 128) return wy_launch_dk<128>(p, mK, mQ, stream, (unsigned)items);

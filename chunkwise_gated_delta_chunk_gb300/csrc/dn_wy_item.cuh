@@ -309,6 +309,35 @@ __device__ __forceinline__ void store_image_row(uint8_t *img, int i, int hf, con
 }
 
 
+// Tiles of several chunks (ch = 16 or 32 tokens).  Tile row i's chunk owns
+// the tile columns from i & ~(ch - 1), all within column half
+// (i & ~(ch - 1)) / 32.  From that half's packed words pk (columns 2k, 2k + 1
+// of the half), in place: the first half of row i mod ch of the chunk's own
+// image (the chunk's ch columns, then zeros).
+__device__ __forceinline__ void sub_row_words(uint32_t (&pk)[16], int i, int ch) {
+    if (ch == 16) {
+        const bool hi = ((i >> 4) & 1) != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pk[k] = hi ? pk[8 + k] : pk[k];
+#pragma unroll
+        for (int k = 8; k < 16; ++k) pk[k] = 0u;
+    }
+}
+
+// Row r of a chunk's image (first half w, second half zero) and the zero rows
+// r + ch, r + 2 ch, ... below the chunk's ch rows.
+__device__ __forceinline__ void store_sub_rows(uint8_t *img, int r, int ch, const uint32_t (&w)[16]) {
+    uint32_t z[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) z[k] = 0u;
+    store_image_row(img, r, 0, w);
+    store_image_row(img, r, 1, z);
+    for (int rr = r + ch; rr < C; rr += ch) {
+        store_image_row(img, rr, 0, z);
+        store_image_row(img, rr, 1, z);
+    }
+}
+
 // One worker: its shared-memory region, TMEM columns and named barrier.
 struct Group {
     uint32_t base;  // shared address of the worker's 1024-aligned region
@@ -331,38 +360,88 @@ __device__ __forceinline__ void group_init(const Group &g) {
     }
 }
 
-// Where the chunk of workspace slot `slot` lies: sequence n, first token t0
-// and length L.  valid is false for a slot no chunk maps to and for a
-// malformed sequence (which the scan kernel reports).
+// Where work tile `tile` lies: sequence n, first token t0 and length L (at
+// most 64).  A tile is 64 tokens of one sequence (tiles numbered like the
+// slots of 64-token chunks, t0 / 64 + n): one chunk of 64 tokens, or two of
+// 32 or four of 16, each with its own workspace slot.  valid is false for a
+// tile number no tokens map to and for a malformed sequence (which the scan
+// kernel reports).
 struct ItemLoc {
     long long t0;
     int n, L;
     bool valid;
 };
 
-__device__ __forceinline__ ItemLoc locate(const Params &p, long long slot) {
+__device__ __forceinline__ ItemLoc locate(const Params &p, long long tile) {
     ItemLoc r{0, 0, 0, false};
-    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n) <= slot
+    int lo = 0, hi = p.N - 1;  // largest n with wy_slot(bos_n, n, 64) <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (wy_slot(seq_bos(p, mid), mid, p.chunk) <= slot) lo = mid; else hi = mid - 1;
+        if (wy_slot(seq_bos(p, mid), mid, C) <= tile) lo = mid; else hi = mid - 1;
     }
     const long long bos = seq_bos(p, lo), eos = seq_eos(p, lo);
     if (bos < 0 || eos < bos || eos > p.tokens) return r;
-    const long long c = slot - wy_slot(bos, lo, p.chunk);
-    const long long t0 = bos + c * p.chunk;
+    const long long c = tile - wy_slot(bos, lo, C);
+    const long long t0 = bos + c * C;
     if (c < 0 || t0 >= eos) return r;
     r.t0 = t0;
     r.n = lo;
-    r.L = (int)min((long long)p.chunk, eos - t0);
+    r.L = (int)min((long long)C, eos - t0);
     r.valid = true;
     return r;
 }
 
-// Warp 0: the gates of the item of slot `slot`, value head h (zero where no
-// chunk maps to the slot).
-__device__ __forceinline__ ChunkGates item_gates(const Params &p, long long slot, int h, int lane) {
-    const ItemLoc l = locate(p, slot);
+// Number of work tiles (a bound: tile numbers no tokens map to are skipped).
+__host__ __device__ inline long long tile_count(const Params &p) { return p.tokens / C + p.N; }
+
+// Warp 0, tiles of several chunks (ch = 16 or 32 tokens each): the scalars
+// the WY item reads (SC_G, SC_BETA, SC_BEG, SC_AF, SC_BF, SC_FACT) with the
+// gate prefix sums restarting at every chunk, so that G_i, and e^{G_i - G_0}
+// with G_0 that of the chunk's first token, are each chunk's own.
+__device__ __forceinline__ void sub_chunk_scalars_store(const ChunkGates &in, int ch, float *sc, int lane) {
+    float ga = in.ga, gb = in.gb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float ta = __shfl_up_sync(0xffffffffu, ga, off);
+        const float tb = __shfl_up_sync(0xffffffffu, gb, off);
+        if (lane >= off && (lane ^ (lane - off)) < ch) {  // the same chunk
+            ga += ta;
+            gb += tb;
+        }
+    }
+    const int first = lane & ~(ch - 1);
+    const float g0a = __shfl_sync(0xffffffffu, ga, first), g0b = __shfl_sync(0xffffffffu, gb, first);
+    float mxa = ga, mna = ga, mxb = gb, mnb = gb;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float xa = __shfl_xor_sync(0xffffffffu, mxa, off), na = __shfl_xor_sync(0xffffffffu, mna, off);
+        const float xb = __shfl_xor_sync(0xffffffffu, mxb, off), nb = __shfl_xor_sync(0xffffffffu, mnb, off);
+        if (off < ch) {  // partners within the same chunk
+            mxa = fmaxf(mxa, xa);
+            mna = fminf(mna, na);
+            mxb = fmaxf(mxb, xb);
+            mnb = fminf(mnb, nb);
+        }
+    }
+    const bool fact = __all_sync(0xffffffffu, mxa - mna <= kSpanMax && mxb - mnb <= kSpanMax);
+    const int ia = lane, ib = lane + 32;
+    sc[SC_G + ia] = ga;
+    sc[SC_G + ib] = gb;
+    sc[SC_BETA + ia] = in.ba;
+    sc[SC_BETA + ib] = in.bb;
+    sc[SC_BEG + ia] = in.ba * __expf(ga);
+    sc[SC_BEG + ib] = in.bb * __expf(gb);
+    sc[SC_AF + ia] = __expf(ga - g0a);
+    sc[SC_AF + ib] = __expf(gb - g0b);
+    sc[SC_BF + ia] = __expf(g0a - ga);
+    sc[SC_BF + ib] = __expf(g0b - gb);
+    if (lane == 0) sc[SC_FACT] = fact ? 1.f : 0.f;
+}
+
+// Warp 0: the gates of the tokens of tile `tile`, value head h (zero where no
+// tokens map to the tile).
+__device__ __forceinline__ ChunkGates item_gates(const Params &p, long long tile, int h, int lane) {
+    const ItemLoc l = locate(p, tile);
     if (!l.valid) return ChunkGates{0.f, 0.f, 0.f, 0.f};
     return chunk_gates_load(p, h, l.t0, l.L, lane);
 }
@@ -373,8 +452,10 @@ __device__ __forceinline__ ChunkGates item_gates(const Params &p, long long slot
 // the T' image at OFF_TPI (written by threads 0-63 just before) followed by
 // 64 rows the result ignores, B the K tile quarters read MN-major; TMEM lane
 // i < 64 then holds row i of W.  Returns false when a wait ran out.
+// Threads 0-63 store row i of -W as row `row` of the image at `img` (null:
+// none), and zero rows row + rs, row + 2 rs, ... below it.
 template <int DKW>
-__device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
+__device__ bool w_step(Group &g, const Params &p, uint8_t *img, int row, int rs, uint32_t par) {
     using Y = Lay<DKW>;
     volatile int *okf = reinterpret_cast<volatile int *>(g.gb + Y::OFF_BAR + 20);
     const int warp = g.tid >> 5, i = g.tid;
@@ -411,11 +492,17 @@ __device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
                 for (int k = 0; k < 16; ++k)
                     pk[k] = pack_bf16(-__uint_as_float(r[2 * k]), -__uint_as_float(r[2 * k + 1]));
                 // d = 128 hh + 32 cb + 8 ch + e: quarter 2 hh + cb / 2, 16-byte chunk 4 (cb & 1) + ch
-                uint8_t *q = img + 8192 * (2 * hh + (cb >> 1)) + i * 128;
+                if (!img) continue;
+                uint8_t *qb = img + 8192 * (2 * hh + (cb >> 1));
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4 *>(q + (((4 * (cb & 1) + ch) ^ (i & 7)) << 4)) =
+                    *reinterpret_cast<uint4 *>(qb + row * 128 + (((4 * (cb & 1) + ch) ^ (row & 7)) << 4)) =
                         make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                for (int rr = row + rs; rr < C; rr += rs)
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        *reinterpret_cast<uint4 *>(qb + rr * 128 + (((4 * (cb & 1) + ch) ^ (rr & 7)) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
@@ -432,7 +519,7 @@ __device__ bool w_step(Group &g, const Params &p, uint8_t *img, uint32_t par) {
 // compute W = T' K into tensor memory (two 128-column halves of d), and
 // threads 0-63 store row i of -W to the slot, so that the scan kernel needs
 // neither T' nor tensor memory for W.
-template <int DKW, bool QKN, bool BWD>
+template <int DKW, bool QKN, bool BWD, bool SUB>
 __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, const Params &p, long long slot,
                      int h, const ItemLoc &loc, ChunkGates &gates, long long next_slot, int next_h) {
     using Y = Lay<DKW>;
@@ -453,7 +540,18 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
     const int hk = h / (p.Nv / p.Nk);
     const uint32_t par = g.it & 1;
     ++g.it;
+    // chunks of ch tokens: one per tile (ch = 64, its slot `slot`) or several
+    // (ch = 16, 32), each with its own slot; img is the single chunk's slot
+    const int ch = SUB ? p.chunk : C;
+    constexpr bool sub = SUB;
     uint8_t *img = static_cast<uint8_t *>(p.ws) + ((size_t)h * p.nslots + slot) * slot_bytes(DKW);
+    // sub: the slot of the chunk that holds tile row i (null past the tile's tokens)
+    auto sub_img = [&](int i) -> uint8_t * {
+        const int c0 = i & ~(ch - 1);
+        if (c0 >= L) return nullptr;
+        const long long s2 = wy_slot(t0 + c0, loc.n, ch);
+        return static_cast<uint8_t *>(p.ws) + ((size_t)h * p.nslots + (size_t)s2) * slot_bytes(DKW);
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -472,7 +570,10 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 tma_load_3d(g.base + 16384 * q + 8192, mQ, b_tma, 64 * q, hk, (int)t0);
             }
         }
-        chunk_scalars_store(p, chunk_scalars_from(gates, L, lane), sc, lane);
+        if (sub)
+            sub_chunk_scalars_store(gates, ch, sc, lane);
+        else
+            chunk_scalars_store(p, chunk_scalars_from(gates, L, lane), sc, lane);
         // the next item's gates: their loads run under this item's work
         if (next_slot >= 0) gates = item_gates(p, next_slot, next_h, lane);
         __syncwarp();
@@ -530,7 +631,14 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
             }
         const float rn = rsqrtf(fmaxf(ss0 + ss1, 1e-24f));
         nrm[g.tid] = rn;
-        reinterpret_cast<float *>(img + slot_norm_off(DKW))[g.tid] = rn;
+        if (!sub) {
+            reinterpret_cast<float *>(img + slot_norm_off(DKW))[g.tid] = rn;
+        } else if (uint8_t *im = sub_img(i)) {
+            // row i mod ch of its chunk's slot; 1 in the rows past the chunk
+            float *nf = reinterpret_cast<float *>(im + slot_norm_off(DKW)) + (g.tid < 64 ? 0 : 64);
+            nf[i & (ch - 1)] = rn;
+            for (int rr = (i & (ch - 1)) + ch; rr < C; rr += ch) nf[rr] = 1.f;
+        }
         // T' = T diag(beta e^G / ||k||)
         if (g.tid < 64) sc[SC_BEG + i] *= rn;
         named_bar_sync(g.bid, NT);
@@ -552,7 +660,8 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
         float *wx = BWD ? p.wyx + ((size_t)h * p.nslots + (size_t)slot) * 3 * 4096 + (rowA ? 0 : 4096) + i * 64
                         : nullptr;
         const int jmax = rowA ? i - 1 : i;
-        const bool fact = sc[SC_FACT] != 0.f;  // uniform over the chunk
+        const int jmin = i & ~(ch - 1);        // the first row of row i's chunk
+        const bool fact = sc[SC_FACT] != 0.f;  // uniform over the tile
         uint32_t r[32];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -577,10 +686,10 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 for (int q4 = 0; q4 < 8; ++q4) {
                     const float4 gg = g4[q4];
                     const int j = 32 * hf + 4 * q4;
-                    dcy[4 * q4] = ri * __expf(j <= jmax ? Gi - gg.x : -INFINITY);
-                    dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax ? Gi - gg.y : -INFINITY);
-                    dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax ? Gi - gg.z : -INFINITY);
-                    dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax ? Gi - gg.w : -INFINITY);
+                    dcy[4 * q4] = ri * __expf(j <= jmax && j >= jmin ? Gi - gg.x : -INFINITY);
+                    dcy[4 * q4 + 1] = ri * __expf(j + 1 <= jmax && j + 1 >= jmin ? Gi - gg.y : -INFINITY);
+                    dcy[4 * q4 + 2] = ri * __expf(j + 2 <= jmax && j + 2 >= jmin ? Gi - gg.z : -INFINITY);
+                    dcy[4 * q4 + 3] = ri * __expf(j + 3 <= jmax && j + 3 >= jmin ? Gi - gg.w : -INFINITY);
                 }
             }
             if (qkn) {
@@ -599,7 +708,7 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
                 const int j = 32 * hf + jj;
-                val[jj] = j <= jmax ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
+                val[jj] = (j <= jmax && j >= jmin) ? dcy[jj] * __uint_as_float(r[jj]) : 0.f;
             }
             if (BWD) {
                 // -(K K^T . D) or P row i, fp32, for the backward
@@ -624,7 +733,14 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(val[2 * k], val[2 * k + 1]);
-                store_image_row(img + slot_p_off(DKW), i, hf, pk);
+                if (!sub) {
+                    store_image_row(img + slot_p_off(DKW), i, hf, pk);
+                } else if (hf == (i >> 5)) {  // the half that holds row i's chunk
+                    if (uint8_t *im = sub_img(i)) {
+                        sub_row_words(pk, i, ch);
+                        store_sub_rows(im + slot_p_off(DKW), i & (ch - 1), ch, pk);
+                    }
+                }
             }
         }
     }
@@ -655,7 +771,19 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
                 pk[hf][2 * q4] = pack_bf16(a.x * cc.x, a.y * cc.y);
                 pk[hf][2 * q4 + 1] = pack_bf16(a.z * cc.z, a.w * cc.w);
             }
-            if (DKW == 128 || !tp) store_image_row(img + (tp ? 0 : slot_tu_off(DKW)), i, hf, pk[hf]);
+            if (DKW == 128 || !tp) {
+                if (!sub) {
+                    store_image_row(img + (tp ? 0 : slot_tu_off(DKW)), i, hf, pk[hf]);
+                } else if (hf == (i >> 5)) {  // the half that holds row i's chunk
+                    if (uint8_t *im = sub_img(i)) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) w[k] = pk[hf][k];
+                        sub_row_words(w, i, ch);
+                        store_sub_rows(im + (tp ? 0 : slot_tu_off(DKW)), i & (ch - 1), ch, w);
+                    }
+                }
+            }
         }
         if (DKW == 256) {
             // T' into shared memory once every row of T has been read
@@ -670,7 +798,11 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
             }
         }
     }
-    if (DKW == 256 && !w_step<DKW>(g, p, img, par)) return false;
+    if (DKW == 256) {
+        // row i of -W goes to row i mod ch of its chunk's slot (threads 0-63)
+        uint8_t *wimg = sub ? sub_img(g.tid & 63) : img;
+        if (!w_step<DKW>(g, p, wimg, sub ? (g.tid & (ch - 1)) : g.tid, sub ? ch : C, par)) return false;
+    }
     // A / T and the scratch are read; the next item's TMA rewrites them
     fence_proxy_async_smem();
     tc_fence_before();
