@@ -86,7 +86,7 @@ constexpr uint32_t OFF_WT = OFF_PR + 2 * 8192;              // -W^T 16 KB
 constexpr uint32_t OFF_SCAL = OFF_WT + 16384;               // NS x 2048 B
 constexpr uint32_t OFF_OST = OFF_SCAL + NS * SCAL_FLOATS * 4;  // output staging, 32 x 256 B
 constexpr uint32_t OFF_BAR = OFF_OST + 8192;
-constexpr int NBARS = 32;
+constexpr int NBARS = 34;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBARS * 8;          // TMEM base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;           // alignment slack
@@ -114,7 +114,8 @@ enum {
     B_DRAIN,
     B_DRAIN2,
     B_DRAIN3,                   // the output issuer's own MMAs
-    B_COUNT
+    B_KF,                       // NS: the stage's K tiles (W reads them before the rest lands)
+    B_COUNT = B_KF + NS
 };
 static_assert(B_COUNT <= NBARS, "barrier space");
 
@@ -217,12 +218,13 @@ __device__ void loader_role(const Ctx x, const Params &p, const Unit u, const CU
             if (!wwait(x, bar(x, B_EMPTY + s), ((c / NS) & 1) ^ 1)) return false;
             const uint32_t st = x.base + OFF_STAGE + s * STAGE_BYTES;
             if (lane == 0) {
-                const uint32_t fb = bar(x, B_FULL + s);
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                const uint32_t fb = bar(x, B_FULL + s), kb = bar(x, B_KF + s);
+                mbar_arrive_expect_tx(kb, 16384);
+                mbar_arrive_expect_tx(fb, STAGE_BYTES - 16384);
                 const int tt = (int)t0;
-                tma_load_3d(st + 0, mK, fb, 0, u.hk, tt);
+                tma_load_3d(st + 0, mK, kb, 0, u.hk, tt);
+                tma_load_3d(st + 16384, mK, kb, 64, u.hk, tt);
                 tma_load_3d(st + 8192, mQ, fb, 0, u.hk, tt);
-                tma_load_3d(st + 16384, mK, fb, 64, u.hk, tt);
                 tma_load_3d(st + 24576, mQ, fb, 64, u.hk, tt);
                 tma_load_3d(st + 32768, mV, fb, u.v0, u.h, tt);
                 tma_load_3d(st + 40960, mV, fb, u.v0 + 64, u.h, tt);
@@ -322,8 +324,9 @@ __device__ __forceinline__ void issue_o(const Ctx &x, uint32_t tm, int c) {
 // T'' and P rings as their buffers free up (W and the T' ring belong to the
 // prep warpgroup).
 // ---------------------------------------------------------------------------
+// (ring 0, T': the W MMA reads only the stage's K tiles)
 __device__ __forceinline__ bool wait_tiles(const Ctx &x, int c, int ring) {
-    return wait(x, bar(x, B_FULL + c % NS), (c / NS) & 1) &&
+    return wait(x, bar(x, (ring == 0 ? B_KF : B_FULL) + c % NS), (c / NS) & 1) &&
            wait(x, bar(x, B_TPF + 4 * ring + (c & 1)), (c >> 1) & 1);
 }
 
@@ -870,6 +873,7 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(x, B_FULL + s), 2);
+            mbar_init(bar(x, B_KF + s), 1);
             mbar_init(bar(x, B_EMPTY + s), 5);
             mbar_init(bar(x, B_QS + s), 4);
         }
@@ -914,7 +918,10 @@ tc_fwd(const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorM
         // ring copies are drained by the roles that issued them)
         if ((threadIdx.x & 31) == 0)
             for (int c = armed - NS + 1; c <= armed; ++c)
-                if (c >= 0) wait_drain(bar(x, B_FULL + c % NS), (c / NS) & 1);
+                if (c >= 0) {
+                    wait_drain(bar(x, B_FULL + c % NS), (c / NS) & 1);
+                    wait_drain(bar(x, B_KF + c % NS), (c / NS) & 1);
+                }
         __syncwarp();
     } else if (warp == 1) {
         if ((threadIdx.x & 31) == 0 && u.nc > 0) mma_role(x, p, u, tm);
