@@ -86,6 +86,26 @@ def test_chunk_sizes_tensor_core_path(lib, chunk):
 
 
 @pytest.mark.parametrize("chunk", [16, 32])
+def test_chunk_sizes_wide_heads(lib, chunk):
+    """dk = dv = 256 at C = 16 and 32 on the wide tensor-core kernels, whose WY
+    items then hold two or four chunks of a 64-token tile: ragged tails, a
+    varlen GQA batch of short sequences, extreme gates, in-kernel q / k
+    normalisation."""
+    import chunkwise_gated_delta_chunk_gb300 as dn
+    cases = [("ragged", inputs(B=2, T=150, dk=256, dv=256, seed=480 + chunk)),
+             ("varlen gqa", inputs(B=1, Nk=1, Nv=2, dk=256, dv=256, seed=481 + chunk,
+                                   lengths=[16, 1, 0, 33, 97, 64, 15])),
+             ("qk l2norm", inputs(B=1, T=140, dk=256, dv=256, seed=482 + chunk, raw_qk=True))]
+    inp = inputs(B=1, T=100, dk=256, dv=256, seed=483 + chunk)
+    inp["g"] = torch.full_like(inp["g"], -30.0)
+    cases.append(("g=-30", inp))
+    for label, inp in cases:
+        o, ht = run_gpu(inp, chunk=chunk)
+        assert dn.dn_last_kernel() == "wy_fwd+tc_wide_fwd", dn.dn_last_kernel()
+        check(inp, o, ht, label="C=%d dk=dv=256 %s" % (chunk, label))
+
+
+@pytest.mark.parametrize("chunk", [16, 32])
 def test_chunk_sizes_headline_full_size(lib, chunk):
     """The headline shapes (B = 4, H = 16, T = 2048, d = 128) at C = 16 and 32,
     on sampled (sequence, head) units, in the launch configuration the
