@@ -753,13 +753,16 @@ __device__ bool item(Group &g, const CUtensorMap *mK, const CUtensorMap *mQ, con
         const bool tp = g.tid < 64;
         const float *trow = arow(i);
         const float *cs = sc + (tp ? SC_BEG : SC_BETA);
-        if (BWD && tp) {
-            // T row i, fp32, for the backward (rows past the chunk: the
-            // identity's, as A is zero there)
-            float *wt = p.wyx + ((size_t)h * p.nslots + (size_t)slot) * 3 * 4096 + 8192 + i * 64;
+        if (BWD) {
+            // T, fp32, for the backward (rows past the chunk: the identity's,
+            // as A is zero there), copied from shared memory by all 128
+            // threads: each warp stores two whole 256-byte rows at a time
+            float *wt = p.wyx + ((size_t)h * p.nslots + (size_t)slot) * 3 * 4096 + 8192;
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4)
-                *reinterpret_cast<float4 *>(wt + 4 * q4) = *reinterpret_cast<const float4 *>(trow + 4 * q4);
+            for (int it = 0; it < 8; ++it) {
+                const int idx = g.tid + 128 * it, rr = idx >> 4, q4 = idx & 15;
+                *reinterpret_cast<float4 *>(wt + rr * 64 + 4 * q4) = *reinterpret_cast<const float4 *>(arow(rr) + 4 * q4);
+            }
         }
         uint32_t pk[2][16];
 #pragma unroll
