@@ -16,7 +16,7 @@
 // ahead of the sequential scan kernel, which then only reads T', T'' and P.
 // 128-thread CTAs (one worker of dn_wy_item.cuh each), 36 KB of shared
 // memory and 64 TMEM columns each, 6 per SM, as many as fit on the GPU at
-// once; each loops over (chunk slot, value head) items, so the TMEM
+// once; each loops over (64-token tile, value head) items, so the TMEM
 // allocation and barrier setup are paid once per CTA, not per item.  Per item:
 //   1. TMA brings the chunk's K and Q (64 x 128 bf16 each, as two
 //      128-byte-swizzled column halves); warp 0 computes the gate scalars;

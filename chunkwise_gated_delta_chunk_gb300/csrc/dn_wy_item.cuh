@@ -1,9 +1,12 @@
 // One WY work item of the chunkwise gated delta rule forward (bf16 q/k,
-// dk = 128): for one chunk and value head, the lower-triangular inverse
-// T = (I - A)^-1 of the chunk's WY representation and the chunk's causal
-// score matrix, written to the chunk's workspace slot as the three bf16 MMA
-// operands T' = T diag(beta e^G) and T'' = T diag(beta) (which give
-// W = T' K and U = T'' V) and P = tril(scale QK^T . D).
+// dk = 128 or 256): for one 64-token tile and value head, the lower-triangular
+// inverse T = (I - A)^-1 of each chunk's WY representation and each chunk's
+// causal score matrix, written to the chunk's workspace slot as the three
+// bf16 MMA operands T' = T diag(beta e^G) and T'' = T diag(beta) (which give
+// W = T' K and U = T'' V) and P = tril(scale QK^T . D).  A tile holds one
+// chunk of 64 tokens, or two of 32 or four of 16: A and P are then block
+// diagonal (each chunk's own block), the solve gives each chunk's T in its
+// block, and each chunk's rows go to its own slot.
 //
 // Sources: [WY]   "flash-linear-attention 中 DeltaNet 的分块并行化WY 表示推导与 Triton 内核实现"
 //                 §2.3 (A = -tril(diag(beta) K K^T, -1), T = (I - A)^-1 by
